@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Throughput of chunked KDA prefill on GB300, one JSON line on stdout.
+
+A step is one kda_chunk_prefill call (prologue when packed, intra-chunk
+kernel, recurrent kernel) over one batch of the workload, inputs resident in
+HBM. ``--impl reference`` times the fp64 CPU oracle instead, on a bounded
+sample of the same workload. Under torchrun every rank runs its own copy of
+the workload on its own GPU (weak scaling, no collective on the data path).
+"""
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kda_inputs as KI  # noqa: E402
+
+METRIC = "KDA prefill tokens/s (T=8192, H=64, D=128) on 1 GB300; % of roofline"
+UNIT = "tokens/s"
+
+# Counted work of the chunked algorithm (dense 16-token tiles, 2 FLOP/MAC).
+FLOPS_INTRA_PER_CHUNK_HEAD = 262144 + 2731     # gated Gram + scores, W, Ut; inversion
+FLOPS_RECUR_PER_CHUNK_HEAD = 1638400           # W S, Qg S, P U, Kd^T U
+BYTES_IN_PER_TOKEN_HEAD = 3 * 256 + 512 + 4    # q, k, v bf16; g fp32; beta fp32
+BYTES_OUT_PER_TOKEN_HEAD = 256                 # o bf16
+STATE_BYTES = 128 * 128 * 4
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=KI.HEADLINE, choices=KI.WORKLOAD_ORDER)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def workload_counts(d, H):
+    lens = d["seqlens"]
+    tokens = sum(lens)
+    chunks = sum((L + 15) // 16 for L in lens)
+    n = len(lens)
+    init = d["initial_state"] is not None
+    intra_bytes = tokens * H * BYTES_IN_PER_TOKEN_HEAD
+    recur_bytes = tokens * H * BYTES_OUT_PER_TOKEN_HEAD + n * H * STATE_BYTES * (1 + int(init))
+    return dict(tokens=tokens, chunk_heads=chunks * H, n_seqs=n,
+                intra_bytes=intra_bytes, recur_bytes=recur_bytes,
+                path_bytes=intra_bytes + recur_bytes,
+                intra_flops=chunks * H * FLOPS_INTRA_PER_CHUNK_HEAD,
+                recur_flops=chunks * H * FLOPS_RECUR_PER_CHUNK_HEAD)
+
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while the timed loops run."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.samples, self.proc, self.thread = [], None, None
+        self.sel = []
+        try:
+            bus = torch.cuda.get_device_properties(device).pci_bus_id
+            dom = torch.cuda.get_device_properties(device).pci_domain_id
+            dv = torch.cuda.get_device_properties(device).pci_device_id
+            self.sel = ["-i", f"{dom:08X}:{bus:02X}:{dv:02X}.0"]
+        except Exception:
+            self.sel = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.sel, f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 7:
+                self.samples.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, reasons = [], None, set()
+        for s in self.samples:
+            try:
+                sm.append(float(s[0]))
+                mx = float(s[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, s[3:]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on this kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "prefill_kda_chunk_gb300", "csrc", rec["source"])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if sha != rec.get("source_sha") or workload not in rec.get("per_launch_bytes", {}):
+        return None
+    return rec["per_launch_bytes"][workload]
+
+
+def run_reference(args, rank, world):
+    """fp64 CPU oracle, bounded sample of the workload per step, rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    w = KI.WORKLOADS[args.workload]
+    d = KI.make_inputs(w)
+    cores = len(os.sched_getaffinity(0))
+    Hs = max(1, min(w.H, 4))
+    sub = {n: d[n][:, :Hs].contiguous() for n in ("q", "k", "v", "g", "beta")}
+    s0 = None if d["initial_state"] is None else d["initial_state"][:, :Hs].contiguous()
+
+    def step():
+        oracle.recurrent(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], initial_state=s0,
+                         cu_seqlens=d["cu_seqlens"], scale=d["scale"], out_tokens=w.T,
+                         threads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    tokens_equiv = w.T * Hs / w.H          # one step covers Hs of the H heads
+    value = args.steps * tokens_equiv / dt
+    sample = f"{Hs} of {w.H} heads, all {w.T} tokens, per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, d),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, d):
+    return {"workload": w.name, "T": w.T, "H": w.H, "D": 128, "n_seqs": len(d["seqlens"]),
+            "initial_state": d["initial_state"] is not None, "seed": w.seed,
+            "gate_mu": w.mu, "l2": "inputs larger than L2, no flush between steps"}
+
+
+def cpu_baseline(w, d):
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    # about 30 core-seconds: ~63 us per token-head per core for the fp64 recurrence
+    Hs = max(1, min(w.H, int(30.0 / (w.T * 63e-6))))
+    sub = {n: d[n][:, :Hs].contiguous() for n in ("q", "k", "v", "g", "beta")}
+    s0 = None if d["initial_state"] is None else d["initial_state"][:, :Hs].contiguous()
+    t0 = time.perf_counter()
+    oracle.recurrent(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], initial_state=s0,
+                     cu_seqlens=d["cu_seqlens"], scale=d["scale"], threads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": w.T * Hs / w.H / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{Hs} of {w.H} heads x {w.T} tokens, {dt:.2f} s wall"}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    import prefill_kda_chunk_gb300 as K
+    from prefill_kda_chunk_gb300 import build as B
+    if rank == 0:
+        B.build()
+    barrier(world)
+    K.lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    w = KI.WORKLOADS[args.workload]
+    d = KI.make_inputs(w)
+    H = w.H
+    cnt = workload_counts(d, H)
+    x = {n: d[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+    s0 = None if d["initial_state"] is None else d["initial_state"].to(dev)
+    cu = d["cu_seqlens"].to(dev) if w.varlen else None
+    out = torch.empty_like(x["v"])
+    fin = torch.empty((cnt["n_seqs"], H, 128, 128), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call(q=x["q"], k=x["k"], v=x["v"], g=x["g"], beta=x["beta"], s0=s0, cu=cu, out=out):
+        K.chunk_prefill(q, k, v, g, beta, initial_state=s0, cu_seqlens=cu, scale=d["scale"],
+                        out=out, final_state=fin)
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    for _ in range(max(args.warmup, 3)):
+        call()
+    K.check_device_error()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    start.record(stream)
+    for i in range(args.steps):
+        K.kda_set_stage_events([e.cuda_event for e in ev[i]])
+        call()
+    end.record(stream)
+    K.kda_set_stage_events(None)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    K.check_device_error()
+    ms = max_over_ranks(start.elapsed_time(end), world)
+    clk = clocks.stop()
+    intra_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    recur_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+
+    # end to end: pinned host inputs copied in, result copied out, every step
+    e2e = None
+    if not args.no_e2e:
+        hin = {n: d[n].pin_memory() for n in ("q", "k", "v", "g", "beta")}
+        hs0 = None if s0 is None else d["initial_state"].pin_memory()
+        hcu = d["cu_seqlens"].pin_memory() if w.varlen else None
+        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hfin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+        dbuf = {n: torch.empty_like(x[n]) for n in x}
+        ds0 = None if s0 is None else torch.empty_like(s0)
+        dcu = None if cu is None else torch.empty_like(cu)
+        h2d = sum(t.numel() * t.element_size() for t in hin.values())
+        h2d += 0 if hs0 is None else hs0.numel() * 4
+        h2d += 0 if hcu is None else hcu.numel() * 4
+        d2h = hout.numel() * 2 + hfin.numel() * 4
+
+        def e2e_step():
+            for n in dbuf:
+                dbuf[n].copy_(hin[n], non_blocking=True)
+            if ds0 is not None:
+                ds0.copy_(hs0, non_blocking=True)
+            if dcu is not None:
+                dcu.copy_(hcu, non_blocking=True)
+            call(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], ds0, dcu, out)
+            hout.copy_(out, non_blocking=True)
+            hfin.copy_(fin, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(3, min(args.steps, 20))
+        es.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        K.check_device_error()
+        ems = max_over_ranks(es.elapsed_time(ee), world)
+        e2e = {"value": world * cnt["tokens"] * e2e_steps / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    if rank != 0:
+        return
+    hbm, tf, peak_src = load_peaks()
+    sec = ms / 1e3 / args.steps
+    value = world * cnt["tokens"] * args.steps / (ms / 1e3)
+
+    kernels = {
+        "kda_intra_chunk_kernel": {
+            "ms": intra_ms, "bound": "hbm", "alg_bytes": cnt["intra_bytes"],
+            "alg_flops": cnt["intra_flops"],
+            "achieved_gbs": cnt["intra_bytes"] / (intra_ms / 1e3) / 1e9,
+            "frac": cnt["intra_bytes"] / (intra_ms / 1e3) / 1e9 / hbm},
+        "kda_recurrent_kernel": {
+            "ms": recur_ms, "bound": "tensor", "alg_bytes": cnt["recur_bytes"],
+            "alg_flops": cnt["recur_flops"],
+            "achieved_tflops": cnt["recur_flops"] / (recur_ms / 1e3) / 1e12,
+            "frac": cnt["recur_flops"] / (recur_ms / 1e3) / 1e12 / tf},
+    }
+    dom = max(kernels, key=lambda k: kernels[k]["ms"])
+    kd = kernels[dom]
+    if kd["bound"] == "hbm":
+        roof = {"bound": "hbm", "achieved": kd["achieved_gbs"], "peak": hbm, "unit": "GB/s",
+                "frac": kd["frac"]}
+    else:
+        roof = {"bound": "tensor", "achieved": kd["achieved_tflops"], "peak": tf,
+                "unit": "TFLOP/s", "frac": kd["frac"]}
+    roof.update({"kernel": dom, "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)"
+                 if peak_src == "measured" else "fallback",
+                 "traffic": traffic_for(dom, w.name)})
+    # the whole call against the slower of the two bounds of the counted work
+    t_hbm = cnt["path_bytes"] / (hbm * 1e9)
+    t_tc = (cnt["intra_flops"] + cnt["recur_flops"]) / (tf * 1e12)
+    path_roof = {"bound": "hbm" if t_hbm >= t_tc else "tensor", "roofline_us": 1e6 * max(t_hbm, t_tc),
+                 "measured_us": 1e6 * sec, "frac": max(t_hbm, t_tc) / sec,
+                 "alg_bytes": cnt["path_bytes"],
+                 "alg_flops": cnt["intra_flops"] + cnt["recur_flops"],
+                 "achieved_gbs": cnt["path_bytes"] / sec / 1e9}
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_of(w, d), "roofline": roof, "path_roofline": path_roof,
+            "kernels": kernels, "gpu_launches": args.steps * (2 + int(w.varlen)),
+            "clocks": clk, "e2e": e2e}
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, d)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,148 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) chunked prefill for Kimi Delta
+ * Attention (KDA).
+ *
+ * The operation. KDA keeps one fixed-size recurrent state per (sequence,
+ * head) in place of a growing key-value cache, and every token updates it
+ * ("Kimi K3 開源基礎設施", section "FlashKDA"; "Kimi K3 的三個系統設計",
+ * section "第一個設計"). The update is the gated delta rule with a decay per
+ * key channel:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(exp(g_t)) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * with S a K x V fp32 matrix (row = key channel). Prefill computes it in
+ * 16-token chunks with two kernels of different parallelism, a
+ * token-parallel intra-chunk kernel and a recurrent inter-chunk kernel
+ * ("Kimi K3 的三個系統設計", section "為什麼 FlashKDA 選擇 16-token chunks"),
+ * over fixed-length or packed variable-length batches with K = V = 128
+ * ("MoonEP / FlashKDA / AgentENV" release note, section "MoE通信とアテンション").
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers must be CUDA device memory (or
+ *     managed memory) on the CURRENT device; the caller owns them. The
+ *     library never frees them and holds none of them after the stream work
+ *     the call enqueued has finished.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). All work is enqueued on it; no entry point but
+ *     kda_last_device_error() blocks the host.
+ *   - Errors found from the arguments alone are returned before anything
+ *     is enqueued and leave every output untouched.
+ */
+#ifndef KDA_GB300_H
+#define KDA_GB300_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL_ARG = -1,          /* a required pointer is NULL */
+    KDA_ERR_BAD_SHAPE = -2,         /* B, T, H, N inconsistent or out of range */
+    KDA_ERR_UNSUPPORTED_DIM = -3,   /* K or V is not 128 */
+    KDA_ERR_MISALIGNED = -4,        /* a pointer breaks the alignment rule below */
+    KDA_ERR_BAD_CU_SEQLENS = -5,    /* (device) cu_seqlens not 0..T nondecreasing */
+    KDA_ERR_CUDA = -6,              /* a CUDA runtime call failed */
+    KDA_ERR_DEVICE_TIMEOUT = -7,    /* (device) a bounded wait inside a kernel ran out */
+    KDA_ERR_NO_DEVICE_SUPPORT = -8, /* current device is not sm_103 */
+    KDA_ERR_ALIAS = -9,             /* out or final_state overlaps an input */
+    KDA_ERR_GATE_RANGE = -10,       /* (device) a chunk's summed log decay left [-80, 80] */
+    KDA_ERR_CAPTURE = -11,          /* workspace must grow while the stream is capturing */
+    KDA_ERR_WRONG_DEVICE = -12,     /* a buffer or the stream belongs to another device */
+    KDA_ERR_NOT_DEVICE_MEMORY = -13 /* a pointer is not CUDA device (or managed) memory */
+} kda_status;
+
+/*
+ * kda_chunk_prefill -- chunked KDA prefill over a batch of sequences.
+ *
+ * Layout (all row-major, tokens of all sequences packed back to back):
+ *   q, k      device, bf16  [B*T, H, K]   (the method expects L2-normalised rows)
+ *   v         device, bf16  [B*T, H, V]
+ *   g         device, fp32  [B*T, H, K]   per-token log decay (<= 0), NOT cumulated
+ *   beta      device, fp32  [B*T, H]      in (0, 1)
+ *   initial_state device, fp32 [N, H, K, V] or NULL (= zero state);
+ *             element [n,h,i,j] is S[key i][value j]
+ *   cu_seqlens device, int32 [N+1] or NULL. NULL: N = B sequences of T tokens
+ *             each. Non-NULL: B must be 1, sequence n holds tokens
+ *             [cu[n], cu[n+1]); cu[0] = 0, cu[N] = T, nondecreasing (empty
+ *             sequences allowed). Checked on the device: a violation makes
+ *             the kernels skip all work and kda_last_device_error() report
+ *             KDA_ERR_BAD_CU_SEQLENS.
+ *   B, T, H, K, V, N  sizes; K = V = 128 only; H >= 1; T >= 0; N >= 1;
+ *             B*T*H*128 < 2^40.
+ *   scale     multiplies o (1/sqrt(K) is the usual choice).
+ *   out       device, bf16 [B*T, H, V], written for every token.
+ *             With zero tokens (B*T == 0) q, k, v, g, beta and out may be NULL.
+ *   final_state device, fp32 [N, H, K, V] or NULL (= not written); may equal
+ *             initial_state (updated in place).
+ *   stream    cudaStream_t as void*.
+ *
+ * Alignment: q, k, v, g, out, initial_state, final_state 16-byte aligned;
+ * beta and cu_seqlens 4-byte aligned.
+ *
+ * Precondition of the factored exponentials: within every 16-token chunk
+ * the per-channel cumulative log decay stays in [-80, 80]; outside it the
+ * device flags KDA_ERR_GATE_RANGE (results then unspecified).
+ *
+ * Workspace: the library keeps one scratch buffer per (device, stream),
+ * grown stream-ordered (cudaMallocAsync / cudaFreeAsync) when a call needs
+ * more (about 17 KB per chunk-head). Concurrent calls on different streams
+ * therefore never share scratch. Growing is refused with KDA_ERR_CAPTURE
+ * while the stream is being captured into a graph: make one call of the
+ * largest size before capturing. kda_workspace_release() frees them.
+ *
+ * Returns KDA_OK once the work is enqueued, or a synchronous error. Errors
+ * found on the device are reported by kda_last_device_error().
+ */
+KDA_API kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, const float *initial_state,
+                             const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
+                             int64_t K, int64_t V, int64_t N, float scale, void *out,
+                             float *final_state, void *stream);
+
+/* Static text for a status code (never NULL). */
+KDA_API const char *kda_status_string(kda_status status);
+
+/*
+ * Synchronises `stream`, then returns and clears the first error a kernel
+ * of this library recorded on the current device since the last call
+ * (KDA_OK if none). Device errors are sticky per device, not per stream.
+ */
+KDA_API kda_status kda_last_device_error(void *stream);
+
+/*
+ * Frees every cached workspace buffer of the current device after
+ * synchronising the device. Safe to call at any time no call of this
+ * library is in flight on the device.
+ */
+KDA_API kda_status kda_workspace_release(void);
+
+/* Workspace bytes a call with these sizes needs (0 on bad sizes). Host only. */
+KDA_API int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, int has_cu_seqlens);
+
+/*
+ * Measurement hook. With n == 3, every later kda_chunk_prefill() call on this
+ * host thread records events[0] on its stream just before the intra-chunk
+ * kernel, events[1] between the intra-chunk and the recurrent kernel, and
+ * events[2] after the recurrent kernel (the events are cudaEvent_t handles
+ * owned by the caller). n == 0 turns it off. Any other n: KDA_ERR_BAD_SHAPE.
+ */
+KDA_API kda_status kda_set_stage_events(void *const *events, int n);
+
+/* Library build string: version and target architecture. Host only. */
+KDA_API const char *kda_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_GB300_H */

@@ -1,0 +1,23 @@
+"""Chunked prefill for Kimi Delta Attention on GB300 (sm_103a).
+
+The compute lives in hand-written CUDA kernels behind the C ABI of
+include/kda.h (libkda_gb300.so, built in-tree by ``build.build()``); this
+package is its thin Python binding.
+"""
+from ._binding import (  # noqa: F401
+    STATUS,
+    STATUS_CODE,
+    KdaError,
+    check_device_error,
+    chunk_prefill,
+    kda_build_info,
+    kda_chunk_prefill,
+    kda_last_device_error,
+    kda_set_stage_events,
+    kda_status_string,
+    kda_workspace_bytes,
+    kda_workspace_release,
+    lib,
+)
+
+__version__ = "0.1.0"

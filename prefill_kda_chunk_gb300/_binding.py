@@ -1,0 +1,177 @@
+"""ctypes binding of libkda_gb300.so (include/kda.h).
+
+Argument marshalling only: every step of the prefill runs in the library's
+CUDA kernels. PyTorch supplies device memory and the current stream. There
+is no fallback: if the library is missing or the device is not sm_103, calls
+raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libkda_gb300.so")
+
+STATUS = {
+    0: "KDA_OK", -1: "KDA_ERR_NULL_ARG", -2: "KDA_ERR_BAD_SHAPE", -3: "KDA_ERR_UNSUPPORTED_DIM",
+    -4: "KDA_ERR_MISALIGNED", -5: "KDA_ERR_BAD_CU_SEQLENS", -6: "KDA_ERR_CUDA",
+    -7: "KDA_ERR_DEVICE_TIMEOUT", -8: "KDA_ERR_NO_DEVICE_SUPPORT", -9: "KDA_ERR_ALIAS",
+    -10: "KDA_ERR_GATE_RANGE", -11: "KDA_ERR_CAPTURE", -12: "KDA_ERR_WRONG_DEVICE",
+    -13: "KDA_ERR_NOT_DEVICE_MEMORY",
+}
+STATUS_CODE = {v: k for k, v in STATUS.items()}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        self.name = STATUS.get(code, str(code))
+        super().__init__(f"{where}: {self.name} ({kda_status_string(code)})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load the library (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(
+                    f"{LIB_PATH} is missing; build it with "
+                    "`python -m prefill_kda_chunk_gb300.build`")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+            L.kda_chunk_prefill.restype = ctypes.c_int
+            L.kda_chunk_prefill.argtypes = [vp] * 7 + [i64] * 6 + [f32, vp, vp, vp]
+            L.kda_status_string.restype = ctypes.c_char_p
+            L.kda_status_string.argtypes = [ctypes.c_int]
+            L.kda_last_device_error.restype = ctypes.c_int
+            L.kda_last_device_error.argtypes = [vp]
+            L.kda_workspace_release.restype = ctypes.c_int
+            L.kda_workspace_release.argtypes = []
+            L.kda_workspace_bytes.restype = i64
+            L.kda_workspace_bytes.argtypes = [i64, i64, i64, i64, ctypes.c_int]
+            L.kda_set_stage_events.restype = ctypes.c_int
+            L.kda_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+            L.kda_build_info.restype = ctypes.c_char_p
+            L.kda_build_info.argtypes = []
+            _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------ raw C calls
+
+def kda_chunk_prefill(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V, N, scale,
+                      out, final_state, stream) -> int:
+    """The C entry point, pointers as ints (0 = NULL). Returns the status."""
+    return lib().kda_chunk_prefill(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V, N,
+                                   scale, out, final_state, stream)
+
+
+def kda_status_string(code: int) -> str:
+    return lib().kda_status_string(int(code)).decode()
+
+
+def kda_last_device_error(stream=0) -> int:
+    return lib().kda_last_device_error(stream)
+
+
+def kda_workspace_release() -> int:
+    return lib().kda_workspace_release()
+
+
+def kda_workspace_bytes(B, T, H, N, has_cu_seqlens) -> int:
+    return lib().kda_workspace_bytes(B, T, H, N, int(bool(has_cu_seqlens)))
+
+
+def kda_set_stage_events(events) -> int:
+    """events: three cudaEvent_t handles (ints), or None/[] to turn timing off."""
+    if not events:
+        return lib().kda_set_stage_events(None, 0)
+    arr = (ctypes.c_void_p * len(events))(*events)
+    return lib().kda_set_stage_events(arr, len(events))
+
+
+def kda_build_info() -> str:
+    return lib().kda_build_info().decode()
+
+
+# ------------------------------------------------------------ torch front
+
+def _ptr(t):
+    return 0 if t is None else t.data_ptr()
+
+
+def chunk_prefill(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None, out=None,
+                  final_state=None, output_final_state=True, stream=None):
+    """Chunked KDA prefill on the current CUDA device.
+
+    q, k, v: bf16 [T, H, 128] (packed or one sequence) or [B, T, H, 128];
+    g: fp32 like q; beta: fp32 [..., H]; initial_state: fp32 [N, H, 128, 128]
+    or None; cu_seqlens: int32 [N+1] on the device or None. Returns
+    (o, final_state) with o bf16 like v and final_state fp32 [N, H, 128, 128]
+    (None if output_final_state is False and final_state is None).
+    """
+    import torch
+
+    if q.dim() == 4:
+        B, T, H, K = q.shape
+    elif q.dim() == 3:
+        B, (T, H, K) = 1, q.shape
+    else:
+        raise ValueError("q must be [T, H, K] or [B, T, H, K]")
+    V = v.shape[-1]
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("cu_seqlens needs B == 1")
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("g", g, torch.float32),
+                        ("beta", beta, torch.float32)):
+        if t.dtype != dt:
+            raise ValueError(f"{name} must be {dt}")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:-1] != q.shape[:-1]:
+        raise ValueError("q, k, g must share a shape and v must match it but for the last dim")
+    if tuple(beta.shape) != tuple(q.shape[:-1]):
+        raise ValueError("beta must be q.shape[:-1]")
+    if initial_state is not None:
+        if initial_state.dtype != torch.float32 or not initial_state.is_contiguous():
+            raise ValueError("initial_state must be a contiguous fp32 tensor")
+        if tuple(initial_state.shape) != (N, H, K, V):
+            raise ValueError(f"initial_state must be [{N}, {H}, {K}, {V}]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(K)
+    if out is None:
+        out = torch.empty_like(v)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = kda_chunk_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
+                           _ptr(cu_seqlens), B, T, H, K, V, N, float(scale), _ptr(out),
+                           _ptr(final_state), stream)
+    if rc != 0:
+        raise KdaError(rc, "kda_chunk_prefill")
+    return out, final_state
+
+
+def check_device_error(stream=None):
+    """Synchronise the stream and raise if a kernel recorded an error."""
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream().cuda_stream
+    rc = kda_last_device_error(stream)
+    if rc != 0:
+        raise KdaError(rc, "device")

@@ -1,0 +1,52 @@
+// Host-side interface between the C ABI (kda_api.cu) and the kernel
+// translation units. Nothing here is exported from the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+// Where each sequence's tokens and chunks are. Fixed-length batches
+// (cu == nullptr) hold N sequences of `seq_len` tokens each; packed batches
+// use cu_seqlens and the per-sequence chunk offsets the prologue writes.
+struct ChunkGeometry {
+    const int32_t *cu;         // [N+1] or nullptr
+    const int32_t *chunk_off;  // [N+1] (packed) or nullptr
+    const int *call_flags;     // per-call flag word (packed only)
+    int64_t seq_len;           // fixed: tokens per sequence; packed: total tokens
+    int32_t n_seqs;
+    int32_t n_heads;
+    int32_t chunks_per_seq;    // fixed only
+};
+
+struct IntraParams {
+    const void *q, *k, *v;     // bf16 [tokens, H, 128]
+    const float *g;            // [tokens, H, 128]
+    const float *beta;         // [tokens, H]
+    uint8_t *rec;              // chunk records [chunks, H, kRecBytes]
+    int *err;                  // sticky per-device error word
+    ChunkGeometry geo;
+};
+
+struct RecurParams {
+    const uint8_t *rec;
+    const float *s0;           // [N, H, 128, 128] or nullptr
+    void *out;                 // bf16 [tokens, H, 128]
+    float *s_final;            // [N, H, 128, 128] or nullptr
+    float scale;
+    int *err;
+    ChunkGeometry geo;
+};
+
+// Per-device, once: raise the dynamic shared-memory limits of the kernels.
+cudaError_t configure_intra();
+cudaError_t configure_recurrent();
+
+cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t total_tokens,
+                                   int32_t *chunk_off, int *call_flags, int *err,
+                                   cudaStream_t stream);
+cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStream_t stream);
+cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,332 @@
+// Token-parallel half of chunked KDA prefill: the packed-batch prologue and
+// the intra-chunk kernel.
+//
+// The intra-chunk kernel does, for every 16-token chunk of every head and
+// independently of every other chunk ("Kimi K3 的三個系統設計", section
+// "為什麼 FlashKDA 選擇 16-token chunks": the token-parallel kernel, the
+// 16x16 inversion, the MMA-shaped tiles), with G_r = sum_{u<=r} g_u the
+// chunk-local cumulative log decay (per key channel):
+//
+//   A[r,i] = beta_r sum_c k_rc k_ic exp(G_rc - G_ic)   (i < r), as the MMA
+//            (K * exp(G)) (K * exp(-G))^T, then masked and row-scaled by beta
+//   P[r,i] = sum_c q_rc k_ic exp(G_rc - G_ic)           (i <= r), likewise
+//   Tm     = (I + A)^{-1} by forward substitution (unit lower triangular)
+//   W      = Tm diag(beta) (K * exp(G)),   Ut = Tm diag(beta) V
+//
+// and stores, per (chunk, head), the record the recurrent kernel consumes:
+// -W, Q*exp(G), K*exp(G_last - G), P, exp(G_last) and Ut^T. Rows past the
+// end of a sequence are zero (their k, v, q, beta and g are taken as 0).
+
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+namespace {
+
+constexpr int kIntraWarps = 4;
+
+struct IntraWarpSmem {
+    uint8_t kg[4096];   // K*exp(G), swizzled
+    uint8_t kn[4096];   // K*exp(-G), swizzled; later stages -W
+    uint8_t qg[4096];   // Q*exp(G), swizzled
+    uint8_t v[4096];    // V, swizzled
+    float a[16 * 17];   // masked, beta-scaled A
+    float t[16 * 17];   // (I + A)^{-1}
+};
+
+__device__ __forceinline__ bool locate_chunk(const ChunkGeometry &geo, int64_t c, int &n,
+                                             int64_t &t0, int &L) {
+    if (geo.cu == nullptr) {
+        const int64_t cps = geo.chunks_per_seq;
+        n = static_cast<int>(c / cps);
+        if (n >= geo.n_seqs) return false;
+        const int64_t i = c - static_cast<int64_t>(n) * cps;
+        t0 = static_cast<int64_t>(n) * geo.seq_len + 16 * i;
+        const int64_t rem = geo.seq_len - 16 * i;
+        L = static_cast<int>(rem < 16 ? rem : 16);
+        return true;
+    }
+    const int32_t *off = geo.chunk_off;
+    if (c >= off[geo.n_seqs]) return false;
+    int lo = 0, hi = geo.n_seqs;  // off[lo] <= c < off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= c) lo = mid; else hi = mid;
+    }
+    n = lo;
+    t0 = static_cast<int64_t>(geo.cu[n]) + 16 * (c - off[n]);
+    const int64_t rem = static_cast<int64_t>(geo.cu[n + 1]) - t0;
+    L = static_cast<int>(rem < 16 ? rem : 16);
+    return true;
+}
+
+__global__ void __launch_bounds__(kIntraWarps * 32)
+kda_intra_chunk_kernel(IntraParams p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
+    const ChunkGeometry &geo = p.geo;
+    const int H = geo.n_heads;
+    const int h = blockIdx.y * kIntraWarps + warp;
+    if (h >= H) return;
+    if (geo.cu != nullptr && (*geo.call_flags & kErrBadCu)) return;
+    int n, L;
+    int64_t t0;
+    if (!locate_chunk(geo, blockIdx.x, n, t0, L)) return;
+    (void)n;
+
+    IntraWarpSmem &sm = reinterpret_cast<IntraWarpSmem *>(smem_raw)[warp];
+    const int64_t row = static_cast<int64_t>(H) * kDim;
+    const int64_t base = (t0 * H + h) * kDim + 4 * lane;
+    uint8_t *rec = p.rec + (static_cast<int64_t>(blockIdx.x) * H + h) * kRecBytes;
+
+    // ---- chunk-local cumulative log decay; lane owns channels 4*lane..+3
+    float G[16][4];
+    float run[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        float4 gg = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < L) gg = __ldcs(reinterpret_cast<const float4 *>(p.g + base + r * row));
+        run[0] += gg.x; run[1] += gg.y; run[2] += gg.z; run[3] += gg.w;
+        G[r][0] = run[0]; G[r][1] = run[1]; G[r][2] = run[2]; G[r][3] = run[3];
+    }
+    bool bad = false;
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) bad |= !(fabsf(G[r][e]) <= 80.f);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, kErrGate);
+
+    const float beta_l = (lane < L) ? __ldg(p.beta + (t0 + lane) * H + h) : 0.f;
+
+    // ---- gated operand tiles
+    const __nv_bfloat16 *qp = static_cast<const __nv_bfloat16 *>(p.q);
+    const __nv_bfloat16 *kp = static_cast<const __nv_bfloat16 *>(p.k);
+    const __nv_bfloat16 *vp = static_cast<const __nv_bfloat16 *>(p.v);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        uint2 qq = make_uint2(0u, 0u), kk = make_uint2(0u, 0u), vv = make_uint2(0u, 0u);
+        if (r < L) {
+            qq = __ldcs(reinterpret_cast<const uint2 *>(qp + base + r * row));
+            kk = __ldcs(reinterpret_cast<const uint2 *>(kp + base + r * row));
+            vv = __ldcs(reinterpret_cast<const uint2 *>(vp + base + r * row));
+        }
+        const float2 q01 = unpack_bf16(qq.x), q23 = unpack_bf16(qq.y);
+        const float2 k01 = unpack_bf16(kk.x), k23 = unpack_bf16(kk.y);
+        const float kv[4] = {k01.x, k01.y, k23.x, k23.y};
+        const float qv[4] = {q01.x, q01.y, q23.x, q23.y};
+        float kg[4], kn[4], qg[4], kd[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float eg = __expf(G[r][e]);
+            const float en = __expf(-G[r][e]);
+            const float ed = __expf(run[e] - G[r][e]);
+            kg[e] = kv[e] * eg;
+            kn[e] = kv[e] * en;
+            qg[e] = qv[e] * eg;
+            kd[e] = kv[e] * ed;
+        }
+        const int off = swz(r, 4 * lane);
+        const uint2 ukg = make_uint2(pack_bf16(kg[0], kg[1]), pack_bf16(kg[2], kg[3]));
+        const uint2 ukn = make_uint2(pack_bf16(kn[0], kn[1]), pack_bf16(kn[2], kn[3]));
+        const uint2 uqg = make_uint2(pack_bf16(qg[0], qg[1]), pack_bf16(qg[2], qg[3]));
+        const uint2 ukd = make_uint2(pack_bf16(kd[0], kd[1]), pack_bf16(kd[2], kd[3]));
+        *reinterpret_cast<uint2 *>(sm.kg + off) = ukg;
+        *reinterpret_cast<uint2 *>(sm.kn + off) = ukn;
+        *reinterpret_cast<uint2 *>(sm.qg + off) = uqg;
+        *reinterpret_cast<uint2 *>(sm.v + off) = vv;
+        *reinterpret_cast<uint2 *>(rec + kRecQg + off) = uqg;
+        *reinterpret_cast<uint2 *>(rec + kRecKd + off) = ukd;
+    }
+    *reinterpret_cast<float4 *>(rec + kRecGamma + 16 * lane) =
+        make_float4(__expf(run[0]), __expf(run[1]), __expf(run[2]), __expf(run[3]));
+    __syncwarp();
+
+    // ---- A_raw = (K e^G)(K e^-G)^T and P_raw = (Q e^G)(K e^-G)^T, 16x16 each
+    const uint32_t s_kg = smem_u32(sm.kg), s_kn = smem_u32(sm.kn), s_qg = smem_u32(sm.qg);
+    const uint32_t s_v = smem_u32(sm.v);
+    float accA[2][4] = {}, accP[2][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t aK[4], aQ[4], b[4];
+        const int ra = (quad & 1) * 8 + (lane & 7), ca = (2 * kk + (quad >> 1)) * 8;
+        ldsm_x4(s_kg + swz(ra, ca), aK[0], aK[1], aK[2], aK[3]);
+        ldsm_x4(s_qg + swz(ra, ca), aQ[0], aQ[1], aQ[2], aQ[3]);
+        const int rb = (quad >> 1) * 8 + (lane & 7), cb = (2 * kk + (quad & 1)) * 8;
+        ldsm_x4(s_kn + swz(rb, cb), b[0], b[1], b[2], b[3]);
+        mma16816(accA[0], aK, b[0], b[1]);
+        mma16816(accA[1], aK, b[2], b[3]);
+        mma16816(accP[0], aQ, b[0], b[1]);
+        mma16816(accP[1], aQ, b[2], b[3]);
+    }
+
+    // ---- masks, beta rows; P goes to the record, A to shared memory
+    const float beta_r0 = __shfl_sync(0xffffffffu, beta_l, gid);
+    const float beta_r1 = __shfl_sync(0xffffffffu, beta_l, gid + 8);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+            const int r = gid + 8 * hf;
+            const int i = 8 * nt + 2 * tig;
+            const float br = hf ? beta_r1 : beta_r0;
+            const float a0 = (i < r) ? br * accA[nt][2 * hf] : 0.f;
+            const float a1 = (i + 1 < r) ? br * accA[nt][2 * hf + 1] : 0.f;
+            sm.a[r * 17 + i] = a0;
+            sm.a[r * 17 + i + 1] = a1;
+            const float p0 = (i <= r) ? accP[nt][2 * hf] : 0.f;
+            const float p1 = (i + 1 <= r) ? accP[nt][2 * hf + 1] : 0.f;
+            *reinterpret_cast<uint32_t *>(rec + kRecP + (r * 16 + i) * 2) = pack_bf16(p0, p1);
+        }
+    }
+    __syncwarp();
+
+    // ---- Tm = (I + A)^{-1}: lane j (< 16) solves column j by forward substitution
+    {
+        const int j = lane & 15;
+        float tc[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float s = (r == j) ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 0; i < r; ++i) s = fmaf(-sm.a[r * 17 + i], tc[i], s);
+            tc[r] = s;
+        }
+        if (lane < 16) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sm.t[r * 17 + j] = tc[r];
+        }
+    }
+    __syncwarp();
+
+    // ---- A fragments of Tm diag(beta) (bf16)
+    uint32_t aT[4];
+    {
+        const int c0 = 2 * tig, c1 = 2 * tig + 8;
+        const float b0 = __shfl_sync(0xffffffffu, beta_l, c0);
+        const float b1 = __shfl_sync(0xffffffffu, beta_l, c0 + 1);
+        const float b2 = __shfl_sync(0xffffffffu, beta_l, c1);
+        const float b3 = __shfl_sync(0xffffffffu, beta_l, c1 + 1);
+        aT[0] = pack_bf16(sm.t[gid * 17 + c0] * b0, sm.t[gid * 17 + c0 + 1] * b1);
+        aT[1] = pack_bf16(sm.t[(gid + 8) * 17 + c0] * b0, sm.t[(gid + 8) * 17 + c0 + 1] * b1);
+        aT[2] = pack_bf16(sm.t[gid * 17 + c1] * b2, sm.t[gid * 17 + c1 + 1] * b3);
+        aT[3] = pack_bf16(sm.t[(gid + 8) * 17 + c1] * b2, sm.t[(gid + 8) * 17 + c1 + 1] * b3);
+    }
+
+    // ---- W = Tm diag(beta) (K e^G): stage -W (bf16, swizzled) in sm.kn
+#pragma unroll
+    for (int jp = 0; jp < 8; ++jp) {
+        uint32_t b[4];
+        const int rk = (quad & 1) * 8 + (lane & 7), ck = (2 * jp + (quad >> 1)) * 8;
+        ldsm_x4_t(s_kg + swz(rk, ck), b[0], b[1], b[2], b[3]);
+        float w0[4] = {}, w1[4] = {};
+        mma16816(w0, aT, b[0], b[1]);
+        mma16816(w1, aT, b[2], b[3]);
+        const int c0 = 16 * jp + 2 * tig, c1 = c0 + 8;
+        *reinterpret_cast<uint32_t *>(sm.kn + swz(gid, c0)) = pack_bf16(-w0[0], -w0[1]);
+        *reinterpret_cast<uint32_t *>(sm.kn + swz(gid + 8, c0)) = pack_bf16(-w0[2], -w0[3]);
+        *reinterpret_cast<uint32_t *>(sm.kn + swz(gid, c1)) = pack_bf16(-w1[0], -w1[1]);
+        *reinterpret_cast<uint32_t *>(sm.kn + swz(gid + 8, c1)) = pack_bf16(-w1[2], -w1[3]);
+    }
+
+    // ---- Ut^T = V^T (Tm diag(beta))^T, M = value channel, N = token
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        uint32_t a[4];
+        const int ri = (quad >> 1) * 8 + (lane & 7), cv = 16 * mt + (quad & 1) * 8;
+        ldsm_x4_t(s_v + swz(ri, cv), a[0], a[1], a[2], a[3]);
+        float u0[4] = {}, u1[4] = {};
+        mma16816(u0, a, aT[0], aT[2]);  // tokens 0..7
+        mma16816(u1, a, aT[1], aT[3]);  // tokens 8..15
+        const int vr = 16 * mt + gid, tk = 2 * tig;
+        *reinterpret_cast<uint32_t *>(rec + kRecUt + (vr * 16 + tk) * 2) = pack_bf16(u0[0], u0[1]);
+        *reinterpret_cast<uint32_t *>(rec + kRecUt + ((vr + 8) * 16 + tk) * 2) = pack_bf16(u0[2], u0[3]);
+        *reinterpret_cast<uint32_t *>(rec + kRecUt + (vr * 16 + tk + 8) * 2) = pack_bf16(u1[0], u1[1]);
+        *reinterpret_cast<uint32_t *>(rec + kRecUt + ((vr + 8) * 16 + tk + 8) * 2) =
+            pack_bf16(u1[2], u1[3]);
+    }
+    __syncwarp();
+
+    // ---- copy the staged -W tile out (same swizzled layout), 16 B per lane
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int idx = (it * 32 + lane) * 16;
+        *reinterpret_cast<uint4 *>(rec + kRecW + idx) = *reinterpret_cast<const uint4 *>(sm.kn + idx);
+    }
+}
+
+// Validates cu_seqlens and writes each sequence's first chunk index
+// (exclusive prefix sum of ceil(len/16)). One CTA of 1024 threads.
+__global__ void __launch_bounds__(1024)
+kda_varlen_prologue_kernel(const int32_t *cu, int32_t n_seqs, int64_t total, int32_t *chunk_off,
+                           int *call_flags, int *err) {
+    __shared__ int warp_sums[32];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (tid == 0) { s_bad = 0; chunk_off[0] = 0; }
+    __syncthreads();
+    int running = 0;
+    for (int base = 0; base < n_seqs; base += 1024) {
+        const int i = base + tid;
+        int cnt = 0;
+        if (i < n_seqs) {
+            const int64_t a = cu[i], b = cu[i + 1];
+            bool bad = (b < a) || (i == 0 && a != 0) || (i == n_seqs - 1 && b != total);
+            if (bad) s_bad = 1;
+            else cnt = static_cast<int>((b - a + 15) / 16);
+        }
+        int x = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[wid] = x;
+        __syncthreads();
+        if (wid == 0) {
+            int w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const int incl = x + (wid > 0 ? warp_sums[wid - 1] : 0);
+        if (i < n_seqs) chunk_off[i + 1] = running + incl;
+        running += warp_sums[31];
+        __syncthreads();
+    }
+    if (tid == 0) {
+        *call_flags = s_bad ? kErrBadCu : 0;
+        if (s_bad) atomicOr(err, kErrBadCu);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t total_tokens,
+                                   int32_t *chunk_off, int *call_flags, int *err,
+                                   cudaStream_t stream) {
+    kda_varlen_prologue_kernel<<<1, 1024, 0, stream>>>(cu, n_seqs, total_tokens, chunk_off,
+                                                       call_flags, err);
+    return cudaGetLastError();
+}
+
+cudaError_t configure_intra() {
+    return cudaFuncSetAttribute(kda_intra_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kIntraWarps * static_cast<int>(sizeof(IntraWarpSmem)));
+}
+
+cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStream_t stream) {
+    if (max_chunks <= 0) return cudaSuccess;
+    const int smem = kIntraWarps * static_cast<int>(sizeof(IntraWarpSmem));
+    dim3 grid(static_cast<unsigned>(max_chunks),
+              static_cast<unsigned>((p.geo.n_heads + kIntraWarps - 1) / kIntraWarps));
+    kda_intra_chunk_kernel<<<grid, kIntraWarps * 32, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

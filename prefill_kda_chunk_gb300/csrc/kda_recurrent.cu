@@ -1,0 +1,261 @@
+// Recurrent half of chunked KDA prefill: the inter-chunk kernel.
+//
+// For one (sequence, head, slice of BV value channels) a CTA walks the
+// sequence's chunks in order ("Kimi K3 的三個系統設計", section
+// "為什麼 FlashKDA 選擇 16-token chunks": the recurrent-propagation kernel),
+// with S (K x V, fp32) the state entering the chunk:
+//
+//   U   = Ut - W S                                   (16 x BV)
+//   o_r = scale ( (q_r * exp(G_r))^T S + sum_{i<=r} P[r,i] U_i )
+//   S  <- Diag(exp(G_last)) S + (K * exp(G_last - G))^T U
+//
+// The state lives in registers as S^T fragments of the warp MMA (each
+// consumer warp owns 16 value channels x all 128 key channels), which is at
+// the same time the A operand of S^T W^T (the transposed U product) and the
+// accumulator of the state update. A producer warp streams each chunk's
+// record into a ring of shared-memory stages with bulk async copies,
+// completion tracked by mbarriers; every wait is bounded and a timeout is
+// recorded in the device error word instead of hanging.
+
+#include "kda_device.cuh"
+#include "kda_internal.h"
+
+namespace kda {
+
+namespace {
+
+constexpr int kStages = 4;
+
+template <int BV>
+struct RecurLayout {
+    static constexpr int kWarps = BV / 16;          // consumer warps
+    static constexpr int kSlices = kDim / BV;
+    static constexpr int kStageBytes = kRecUt + BV * 32;  // W, Qg, Kd, P, gamma + Ut^T slice
+    static constexpr int kOStage = kStages * kStageBytes;   // per-warp o staging, 512 B each
+    static constexpr int kBars = kOStage + kWarps * 512;
+    static constexpr int kSmem = kBars + 2 * kStages * 8;
+};
+
+template <int BV>
+__global__ void __launch_bounds__((BV / 16 + 1) * 32)
+kda_recurrent_kernel(RecurParams p) {
+    using Lay = RecurLayout<BV>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
+    const ChunkGeometry &geo = p.geo;
+    const int H = geo.n_heads;
+    const int s = blockIdx.x % Lay::kSlices;
+    const int h = (blockIdx.x / Lay::kSlices) % H;
+    const int n = blockIdx.x / (Lay::kSlices * H);
+
+    const uint32_t bar_full = smem_u32(smem + Lay::kBars);
+    const uint32_t bar_empty = bar_full + kStages * 8;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, Lay::kWarps);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (geo.cu != nullptr && (*geo.call_flags & kErrBadCu)) return;
+
+    int64_t tb, te, chunk0;
+    if (geo.cu == nullptr) {
+        tb = static_cast<int64_t>(n) * geo.seq_len;
+        te = tb + geo.seq_len;
+        chunk0 = static_cast<int64_t>(n) * geo.chunks_per_seq;
+    } else {
+        tb = geo.cu[n];
+        te = geo.cu[n + 1];
+        chunk0 = geo.chunk_off[n];
+    }
+    const int nck = static_cast<int>((te - tb + 15) / 16);
+    const uint8_t *rec0 = p.rec + (chunk0 * H + h) * static_cast<int64_t>(kRecBytes);
+    const uint32_t stage0 = smem_u32(smem);
+
+    if (warp == Lay::kWarps) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            for (int i = 0; i < nck; ++i) {
+                const int st = i % kStages;
+                if (i >= kStages &&
+                    !mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1)) {
+                    atomicOr(p.err, kErrTimeout);
+                    break;
+                }
+                const uint8_t *src = rec0 + static_cast<int64_t>(i) * H * kRecBytes;
+                const uint32_t dst = stage0 + st * Lay::kStageBytes;
+                mbar_arrive_expect_tx(bar_full + 8 * st, Lay::kStageBytes);
+                bulk_g2s(dst, src, kRecUt, bar_full + 8 * st);
+                bulk_g2s(dst + kRecUt, src + kRecUt + s * BV * 32, BV * 32, bar_full + 8 * st);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int vw = 16 * warp;          // first value channel of this warp within the slice
+    const int v0 = s * BV + vw;        // ... within the head
+    float acc[16][4];                  // S^T fragments: rows = value, cols = key
+    const int64_t sbase = (static_cast<int64_t>(n) * H + h) * kDim * kDim;
+    if (p.s0 != nullptr) {
+        const float *S0 = p.s0 + sbase;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int key = 8 * j + 2 * tig;
+            acc[j][0] = S0[key * kDim + v0 + gid];
+            acc[j][1] = S0[(key + 1) * kDim + v0 + gid];
+            acc[j][2] = S0[key * kDim + v0 + gid + 8];
+            acc[j][3] = S0[(key + 1) * kDim + v0 + gid + 8];
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
+    }
+
+    uint8_t *so = smem + Lay::kOStage + warp * 512;   // [16 tok][16 val] bf16
+    __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(p.out);
+
+    for (int i = 0; i < nck; ++i) {
+        const int st = i % kStages;
+        if (!mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
+            atomicOr(p.err, kErrTimeout);
+            break;
+        }
+        const uint8_t *stg = smem + st * Lay::kStageBytes;
+        const uint32_t sw = stage0 + st * Lay::kStageBytes;
+
+        // S^T as bf16 A fragments, one per 16-key step
+        uint32_t aS[8][4];
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            aS[kk][0] = pack_bf16(acc[2 * kk][0], acc[2 * kk][1]);
+            aS[kk][1] = pack_bf16(acc[2 * kk][2], acc[2 * kk][3]);
+            aS[kk][2] = pack_bf16(acc[2 * kk + 1][0], acc[2 * kk + 1][1]);
+            aS[kk][3] = pack_bf16(acc[2 * kk + 1][2], acc[2 * kk + 1][3]);
+        }
+
+        // U^T = Ut^T - S^T W^T and (Q e^G S)^T = S^T Qg^T; two partial sums each
+        float uT[2][2][4], oT[2][2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int tk = 8 * nt + 2 * tig;
+            const float2 u01 = unpack_bf16(
+                *reinterpret_cast<const uint32_t *>(stg + kRecUt + ((vw + gid) * 16 + tk) * 2));
+            const float2 u23 = unpack_bf16(*reinterpret_cast<const uint32_t *>(
+                stg + kRecUt + ((vw + gid + 8) * 16 + tk) * 2));
+            uT[nt][0][0] = u01.x; uT[nt][0][1] = u01.y; uT[nt][0][2] = u23.x; uT[nt][0][3] = u23.y;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) { uT[nt][1][e] = 0.f; oT[nt][0][e] = 0.f; oT[nt][1][e] = 0.f; }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t bw[4], bq[4];
+            const int rb = (quad >> 1) * 8 + (lane & 7), cb = 16 * kk + (quad & 1) * 8;
+            ldsm_x4(sw + kRecW + swz(rb, cb), bw[0], bw[1], bw[2], bw[3]);
+            ldsm_x4(sw + kRecQg + swz(rb, cb), bq[0], bq[1], bq[2], bq[3]);
+            mma16816(uT[0][kk & 1], aS[kk], bw[0], bw[1]);
+            mma16816(uT[1][kk & 1], aS[kk], bw[2], bw[3]);
+            mma16816(oT[0][kk & 1], aS[kk], bq[0], bq[1]);
+            mma16816(oT[1][kk & 1], aS[kk], bq[2], bq[3]);
+        }
+        float u[2][4], o[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                u[nt][e] = uT[nt][0][e] + uT[nt][1][e];
+                o[nt][e] = oT[nt][0][e] + oT[nt][1][e];
+            }
+
+        // U^T as bf16 A fragments (M = value, K = token)
+        uint32_t aU[4];
+        aU[0] = pack_bf16(u[0][0], u[0][1]);
+        aU[1] = pack_bf16(u[0][2], u[0][3]);
+        aU[2] = pack_bf16(u[1][0], u[1][1]);
+        aU[3] = pack_bf16(u[1][2], u[1][3]);
+
+        // o^T += U^T P^T
+        {
+            uint32_t bp[4];
+            const int rp = (quad >> 1) * 8 + (lane & 7);
+            ldsm_x4(sw + kRecP + rp * 32 + (quad & 1) * 16, bp[0], bp[1], bp[2], bp[3]);
+            mma16816(o[0], aU, bp[0], bp[1]);
+            mma16816(o[1], aU, bp[2], bp[3]);
+        }
+
+        // o: stage [token][value] in shared memory, then 16-byte row stores
+        const int64_t t0 = tb + 16 * i;
+        const int L = static_cast<int>((te - t0) < 16 ? (te - t0) : 16);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int tk = 8 * nt + 2 * tig;
+            __nv_bfloat16 *so16 = reinterpret_cast<__nv_bfloat16 *>(so);
+            so16[tk * 16 + gid] = __float2bfloat16_rn(p.scale * o[nt][0]);
+            so16[(tk + 1) * 16 + gid] = __float2bfloat16_rn(p.scale * o[nt][1]);
+            so16[tk * 16 + gid + 8] = __float2bfloat16_rn(p.scale * o[nt][2]);
+            so16[(tk + 1) * 16 + gid + 8] = __float2bfloat16_rn(p.scale * o[nt][3]);
+        }
+        __syncwarp();
+        {
+            const int tok = lane >> 1, hf = lane & 1;
+            if (tok < L) {
+                const uint4 val = *reinterpret_cast<const uint4 *>(so + tok * 32 + hf * 16);
+                *reinterpret_cast<uint4 *>(outp + ((t0 + tok) * H + h) * kDim + v0 + hf * 8) = val;
+            }
+        }
+
+        // S^T <- S^T Diag(gamma) + U^T Kd
+        const float *gam = reinterpret_cast<const float *>(stg + kRecGamma);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float2 gm = *reinterpret_cast<const float2 *>(gam + 8 * j + 2 * tig);
+            acc[j][0] *= gm.x; acc[j][1] *= gm.y; acc[j][2] *= gm.x; acc[j][3] *= gm.y;
+        }
+#pragma unroll
+        for (int jp = 0; jp < 8; ++jp) {
+            uint32_t b[4];
+            const int rk = (quad & 1) * 8 + (lane & 7), ck = 16 * jp + (quad >> 1) * 8;
+            ldsm_x4_t(sw + kRecKd + swz(rk, ck), b[0], b[1], b[2], b[3]);
+            mma16816(acc[2 * jp], aU, b[0], b[1]);
+            mma16816(acc[2 * jp + 1], aU, b[2], b[3]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+    }
+
+    if (p.s_final != nullptr) {
+        float *SF = p.s_final + sbase;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int key = 8 * j + 2 * tig;
+            SF[key * kDim + v0 + gid] = acc[j][0];
+            SF[(key + 1) * kDim + v0 + gid] = acc[j][1];
+            SF[key * kDim + v0 + gid + 8] = acc[j][2];
+            SF[(key + 1) * kDim + v0 + gid + 8] = acc[j][3];
+        }
+    }
+}
+
+constexpr int kBV = 64;
+
+}  // namespace
+
+cudaError_t configure_recurrent() {
+    return cudaFuncSetAttribute(kda_recurrent_kernel<kBV>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                RecurLayout<kBV>::kSmem);
+}
+
+cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream) {
+    using Lay = RecurLayout<kBV>;
+    const int64_t ctas = static_cast<int64_t>(p.geo.n_seqs) * p.geo.n_heads * Lay::kSlices;
+    if (ctas <= 0) return cudaSuccess;
+    kda_recurrent_kernel<kBV><<<static_cast<unsigned>(ctas), (Lay::kWarps + 1) * 32, Lay::kSmem,
+                                stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

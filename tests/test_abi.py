@@ -1,0 +1,80 @@
+"""The C ABI without a GPU: the library loads, exports what include/kda.h
+declares, and rejects bad arguments before touching the device."""
+import os
+import re
+
+import pytest
+
+import prefill_kda_chunk_gb300 as K
+from prefill_kda_chunk_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return K.lib()
+
+
+def declared_symbols():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"KDA_API\s+[\w\s\*]*?\b(kda_\w+)\s*\(", text)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert "kda_chunk_prefill" in names and len(names) >= 6
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in K.STATUS.items():
+        s = K.kda_status_string(code)
+        assert s and s != "unknown status", name
+    assert K.kda_status_string(12345) == "unknown status"
+
+
+def test_workspace_bytes(lib):
+    # 512 chunks x 64 heads x 17408 B + the flag block
+    assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 512 * 64 * 17408
+    assert K.kda_workspace_bytes(1, 8192, 64, 16, 1) == 256 + 256 + ((8192 + 15 * 16) // 16) * 64 * 17408
+    assert K.kda_workspace_bytes(1, 8192, 64, 2, 0) == 0      # N != B without cu_seqlens
+    assert K.kda_workspace_bytes(2, 100, 0, 2, 0) == 0        # H < 1
+
+
+A = 1 << 20  # an aligned fake address; validation fails before any dereference
+
+
+def call(**kw):
+    args = dict(q=A, k=A + 0x100000, v=A + 0x200000, g=A + 0x300000, beta=A + 0x400000,
+                initial_state=0, cu_seqlens=0, B=1, T=16, H=1, K=128, V=128, N=1, scale=1.0,
+                out=A + 0x500000, final_state=0, stream=0)
+    args.update(kw)
+    return K.kda_chunk_prefill(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), "KDA_ERR_NULL_ARG"),
+    (dict(out=0), "KDA_ERR_NULL_ARG"),
+    (dict(K=64), "KDA_ERR_UNSUPPORTED_DIM"),
+    (dict(V=256), "KDA_ERR_UNSUPPORTED_DIM"),
+    (dict(H=0), "KDA_ERR_BAD_SHAPE"),
+    (dict(T=-1), "KDA_ERR_BAD_SHAPE"),
+    (dict(N=2), "KDA_ERR_BAD_SHAPE"),
+    (dict(B=2, N=2, cu_seqlens=A + 0x600000), "KDA_ERR_BAD_SHAPE"),
+    (dict(q=A + 2), "KDA_ERR_MISALIGNED"),
+    (dict(g=A + 0x300004), "KDA_ERR_MISALIGNED"),
+    (dict(beta=A + 0x400002), "KDA_ERR_MISALIGNED"),
+    (dict(out=A), "KDA_ERR_ALIAS"),
+    (dict(out=A + 0x300000 + 4096), "KDA_ERR_ALIAS"),
+    (dict(final_state=A + 0x200000), "KDA_ERR_ALIAS"),
+    (dict(initial_state=A + 0x700000, final_state=A + 0x700000 + 4096), "KDA_ERR_ALIAS"),
+])
+def test_host_validation_rejects(lib, kw, code):
+    assert call(**kw) == K.STATUS_CODE[code]

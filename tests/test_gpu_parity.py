@@ -1,0 +1,261 @@
+"""CUDA path against the fp64 oracle, through the C ABI.
+
+Bar (per tensor, per case): relative L2 error <= 1e-2 and max abs error
+<= 2e-2 * max|ref|, for o (bf16) and final_state (fp32) separately.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs as KI
+import prefill_kda_chunk_gb300 as K
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+MAX_ABS = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from prefill_kda_chunk_gb300 import build
+    build.build()
+    K.lib()
+
+
+def to_dev(d):
+    dev = {}
+    for key in ("q", "k", "v", "g", "beta"):
+        dev[key] = d[key].cuda().contiguous()
+    dev["initial_state"] = None if d["initial_state"] is None else d["initial_state"].cuda()
+    dev["cu_seqlens"] = d["cu_seqlens"].cuda()
+    return dev
+
+
+def run_gpu(d, packed=True, canary=True, **kw):
+    x = to_dev(d)
+    N = len(d["seqlens"])
+    out = torch.empty_like(x["v"])
+    fin = torch.empty((N, x["q"].shape[1], 128, 128), dtype=torch.float32, device="cuda")
+    if canary:
+        out.fill_(float("nan"))
+        fin.fill_(float("nan"))
+    o, f = K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                           initial_state=x["initial_state"],
+                           cu_seqlens=x["cu_seqlens"] if packed else None,
+                           scale=d["scale"], out=out, final_state=fin, **kw)
+    K.check_device_error()
+    return o, f
+
+
+def run_oracle(d, out_tokens=None):
+    import oracle
+    return oracle.recurrent(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                            initial_state=d["initial_state"], cu_seqlens=d["cu_seqlens"],
+                            scale=d["scale"], out_tokens=out_tokens)
+
+
+def errs(x, ref):
+    x = x.detach().double().cpu().numpy()
+    assert np.isfinite(x).all(), "non-finite values (an output element was not written?)"
+    rel = np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300)
+    mx = np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-300)
+    return rel, mx
+
+
+def assert_parity(o, f, o_ref, f_ref, tag=""):
+    for name, x, r in (("o", o, o_ref), ("final_state", f, f_ref)):
+        rel, mx = errs(x, r)
+        assert rel <= REL_L2 and mx <= MAX_ABS, f"{tag} {name}: rel_l2={rel:.3e} max={mx:.3e}"
+
+
+# ------------------------------------------------ the five workloads
+
+@pytest.mark.parametrize("name", ["tiny_T64_H1", "fixed_T8192_H64", "fixed_T8192_H96",
+                                  "varlen16_T8192_H64"])
+def test_workload_parity(name):
+    d = KI.make_inputs(KI.WORKLOADS[name])
+    o, f = run_gpu(d, packed=KI.WORKLOADS[name].varlen)
+    o_ref, f_ref = run_oracle(d)
+    assert_parity(o, f, o_ref, f_ref, name)
+
+
+def test_long_context_parity():
+    """T=131072, H=32: o on the first 8192 tokens, final state after all of them."""
+    d = KI.make_inputs(KI.WORKLOADS["long_T131072_H32"])
+    o, f = run_gpu(d, packed=False)
+    o_ref, f_ref = run_oracle(d, out_tokens=8192)
+    assert_parity(o[:8192], f, o_ref, f_ref, "long")
+
+
+# ------------------------------------------------ ragged and degenerate
+
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 31, 33, 100])
+@pytest.mark.parametrize("init", [False, True])
+def test_single_sequence_lengths(T, init):
+    d = KI.make_case([T], H=2, seed=100 + T, init_state=init)
+    o, f = run_gpu(d, packed=False)
+    assert_parity(o, f, *run_oracle(d), f"T={T}")
+
+
+def test_varlen_ragged_with_empty_sequences():
+    d = KI.make_case([1, 0, 15, 16, 17, 100, 3, 0], H=3, seed=7, init_state=True)
+    o, f = run_gpu(d, packed=True)
+    assert_parity(o, f, *run_oracle(d), "ragged")
+
+
+def test_fixed_batch_of_sequences():
+    """B sequences of T tokens without cu_seqlens ([B, T, H, K] layout)."""
+    Bn, T, H = 3, 37, 2
+    d = KI.make_case([T] * Bn, H=H, seed=8, init_state=True)
+    x = to_dev(d)
+    q, k, v, g = (x[n].view(Bn, T, H, 128) for n in ("q", "k", "v", "g"))
+    beta = x["beta"].view(Bn, T, H)
+    o, f = K.chunk_prefill(q, k, v, g, beta, initial_state=x["initial_state"], scale=d["scale"])
+    K.check_device_error()
+    assert_parity(o.view(Bn * T, H, 128), f, *run_oracle(d), "batch")
+
+
+def test_zero_tokens_copies_state():
+    d = KI.make_case([0, 0], H=2, seed=9, init_state=True)
+    x = to_dev(d)
+    o, f = K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                           initial_state=x["initial_state"], cu_seqlens=x["cu_seqlens"])
+    K.check_device_error()
+    assert torch.equal(f, x["initial_state"])
+
+
+def test_packed_equals_separate_calls_bitwise():
+    d = KI.make_case([40, 7, 64, 19], H=2, seed=10, init_state=True)
+    o, f = run_gpu(d, packed=True)
+    cu = d["cu_seqlens"].tolist()
+    for i in range(len(cu) - 1):
+        a, b = cu[i], cu[i + 1]
+        di = dict(q=d["q"][a:b], k=d["k"][a:b], v=d["v"][a:b], g=d["g"][a:b],
+                  beta=d["beta"][a:b], initial_state=d["initial_state"][i:i + 1],
+                  cu_seqlens=torch.tensor([0, b - a], dtype=torch.int32), seqlens=[b - a],
+                  scale=d["scale"])
+        oi, fi = run_gpu(di, packed=False)
+        assert torch.equal(o[a:b], oi)
+        assert torch.equal(f[i:i + 1], fi)
+
+
+def test_split_call_equals_one_call():
+    """State passing: prefill [0, T1) then [T1, T) from its final state."""
+    d = KI.make_case([96], H=2, seed=11, init_state=True)
+    o, f = run_gpu(d, packed=False)
+    o_ref, f_ref = run_oracle(d)
+    T1 = 48
+    x = to_dev(d)
+    s = slice(0, T1), slice(T1, 96)
+    oa, fa = K.chunk_prefill(*(x[n][s[0]] for n in ("q", "k", "v", "g", "beta")),
+                             initial_state=x["initial_state"], scale=d["scale"])
+    ob, fb = K.chunk_prefill(*(x[n][s[1]].contiguous() for n in ("q", "k", "v", "g", "beta")),
+                             initial_state=fa, scale=d["scale"])
+    K.check_device_error()
+    assert_parity(torch.cat([oa, ob]), fb, o_ref, f_ref, "split")
+    # chunk boundaries coincide (48 = 3 x 16), so the two paths are bitwise equal
+    assert torch.equal(torch.cat([oa, ob]), o) and torch.equal(fb, f)
+
+
+def test_in_place_state_and_no_final_state():
+    d = KI.make_case([50], H=2, seed=12, init_state=True)
+    o_ref, f_ref = run_oracle(d)
+    x = to_dev(d)
+    st = x["initial_state"].clone()
+    o, f = K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], initial_state=st,
+                           final_state=st, scale=d["scale"])
+    K.check_device_error()
+    assert f.data_ptr() == st.data_ptr()
+    assert_parity(o, st, o_ref, f_ref, "in-place")
+    o2, f2 = K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                             initial_state=x["initial_state"], output_final_state=False,
+                             scale=d["scale"])
+    K.check_device_error()
+    assert f2 is None and torch.equal(o2, o)
+
+
+def test_deterministic():
+    d = KI.make_case([300], H=4, seed=13, init_state=True)
+    o1, f1 = run_gpu(d, packed=False)
+    o2, f2 = run_gpu(d, packed=False)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+def test_strong_decay_and_extreme_beta():
+    """Decay close to the precondition bound and beta at the ends of (0, 1)."""
+    d = KI.make_case([64], H=2, seed=14, init_state=True)
+    d["g"] = torch.full_like(d["g"], -4.5)          # 16 * 4.5 = 72 < 80 per chunk
+    d["beta"][::2] = 1.0
+    d["beta"][1::2] = 1e-4
+    o, f = run_gpu(d, packed=False)
+    assert_parity(o, f, *run_oracle(d), "strong-decay")
+
+
+def test_scale_argument():
+    d = KI.make_case([40], H=1, seed=15)
+    d["scale"] = 0.37
+    o, f = run_gpu(d, packed=False)
+    assert_parity(o, f, *run_oracle(d), "scale")
+
+
+# ------------------------------------------------ device-side errors
+
+def test_bad_cu_seqlens_reported_and_outputs_untouched():
+    d = KI.make_case([20, 30], H=1, seed=16)
+    x = to_dev(d)
+    bad = torch.tensor([0, 35, 30], dtype=torch.int32, device="cuda")  # decreasing, end != T
+    out = torch.full_like(x["v"], 7.0)
+    fin = torch.full((2, 1, 128, 128), 7.0, device="cuda")
+    K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], cu_seqlens=bad, out=out,
+                    final_state=fin)
+    rc = K.kda_last_device_error(torch.cuda.current_stream().cuda_stream)
+    assert rc == K.STATUS_CODE["KDA_ERR_BAD_CU_SEQLENS"]
+    assert bool((out == 7.0).all()) and bool((fin == 7.0).all())
+    # the context is still usable and the flag was cleared
+    o, f = run_gpu(d, packed=True)
+    assert_parity(o, f, *run_oracle(d), "after-error")
+
+
+def test_gate_range_flagged():
+    d = KI.make_case([32], H=1, seed=17)
+    x = to_dev(d)
+    x["g"].fill_(-10.0)                               # 16 * 10 = 160 > 80
+    K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"])
+    rc = K.kda_last_device_error(torch.cuda.current_stream().cuda_stream)
+    assert rc == K.STATUS_CODE["KDA_ERR_GATE_RANGE"]
+
+
+def test_host_pointer_rejected():
+    d = KI.make_case([16], H=1, seed=18)
+    x = to_dev(d)
+    host_q = torch.zeros_like(d["q"])
+    rc = K.kda_chunk_prefill(host_q.data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                             x["g"].data_ptr(), x["beta"].data_ptr(), 0, 0, 1, 16, 1, 128, 128, 1,
+                             1.0, torch.empty_like(x["v"]).data_ptr(), 0, 0)
+    assert rc == K.STATUS_CODE["KDA_ERR_NOT_DEVICE_MEMORY"]
+
+
+def test_graph_capture_after_warm_call():
+    d = KI.make_case([128], H=2, seed=19, init_state=True)
+    x = to_dev(d)
+    out = torch.empty_like(x["v"])
+    fin = torch.empty((1, 2, 128, 128), device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                        initial_state=x["initial_state"], out=out, final_state=fin)
+        s.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        out.zero_()
+        with torch.cuda.graph(graph, stream=s):
+            K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                            initial_state=x["initial_state"], out=out, final_state=fin)
+        graph.replay()
+        s.synchronize()
+    K.check_device_error()
+    assert_parity(out, fin, *run_oracle(d), "graph")
