@@ -274,23 +274,23 @@ def main():
     torch.cuda.synchronize(dev)
     barrier(world)
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     barrier(world)
+    if K.kda_stage_timing_begin(args.steps) != 0:
+        raise RuntimeError("kda_stage_timing_begin failed")
     start.record(stream)
     for i in range(args.steps):
-        K.kda_set_stage_events([e.cuda_event for e in ev[i]])
         call()
     end.record(stream)
-    K.kda_set_stage_events(None)
     torch.cuda.synchronize(dev)
     barrier(world)
     K.check_device_error()
     ms = max_over_ranks(start.elapsed_time(end), world)
     clk = clocks.stop()
-    intra_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
-    recur_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    rc, intra_ms, recur_ms, ncalls = K.kda_stage_timing_end()
+    if rc != 0 or ncalls != args.steps:
+        raise RuntimeError(f"stage timing failed ({rc}, {ncalls} calls)")
 
     # end to end: pinned host inputs copied in, result copied out, every step
     e2e = None

@@ -130,13 +130,18 @@ KDA_API kda_status kda_workspace_release(void);
 KDA_API int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, int has_cu_seqlens);
 
 /*
- * Measurement hook. With n == 3, every later kda_chunk_prefill() call on this
- * host thread records events[0] on its stream just before the intra-chunk
- * kernel, events[1] between the intra-chunk and the recurrent kernel, and
- * events[2] after the recurrent kernel (the events are cudaEvent_t handles
- * owned by the caller). n == 0 turns it off. Any other n: KDA_ERR_BAD_SHAPE.
+ * Measurement hook (per host thread). kda_stage_timing_begin(max_calls)
+ * creates 3*max_calls timing events on the current device; each of the next
+ * max_calls kda_chunk_prefill() calls of this thread records one before the
+ * intra-chunk kernel, one between it and the recurrent kernel, and one after
+ * the recurrent kernel, on the call's stream. kda_stage_timing_end()
+ * waits for those events, writes the mean milliseconds per call of the
+ * intra-chunk stage (prologue excluded) and of the recurrent stage, and the
+ * number of calls timed, then frees the events. Host pointers; NULL outputs
+ * are skipped. Errors: KDA_ERR_BAD_SHAPE for max_calls < 1, KDA_ERR_CUDA.
  */
-KDA_API kda_status kda_set_stage_events(void *const *events, int n);
+KDA_API kda_status kda_stage_timing_begin(int max_calls);
+KDA_API kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *calls);
 
 /* Library build string: version and target architecture. Host only. */
 KDA_API const char *kda_build_info(void);

@@ -13,7 +13,8 @@ from ._binding import (  # noqa: F401
     kda_build_info,
     kda_chunk_prefill,
     kda_last_device_error,
-    kda_set_stage_events,
+    kda_stage_timing_begin,
+    kda_stage_timing_end,
     kda_status_string,
     kda_workspace_bytes,
     kda_workspace_release,

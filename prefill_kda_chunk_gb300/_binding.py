@@ -56,8 +56,12 @@ def lib() -> ctypes.CDLL:
             L.kda_workspace_release.argtypes = []
             L.kda_workspace_bytes.restype = i64
             L.kda_workspace_bytes.argtypes = [i64, i64, i64, i64, ctypes.c_int]
-            L.kda_set_stage_events.restype = ctypes.c_int
-            L.kda_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]
+            L.kda_stage_timing_begin.restype = ctypes.c_int
+            L.kda_stage_timing_begin.argtypes = [ctypes.c_int]
+            L.kda_stage_timing_end.restype = ctypes.c_int
+            L.kda_stage_timing_end.argtypes = [ctypes.POINTER(ctypes.c_double),
+                                               ctypes.POINTER(ctypes.c_double),
+                                               ctypes.POINTER(ctypes.c_int)]
             L.kda_build_info.restype = ctypes.c_char_p
             L.kda_build_info.argtypes = []
             _lib = L
@@ -89,12 +93,15 @@ def kda_workspace_bytes(B, T, H, N, has_cu_seqlens) -> int:
     return lib().kda_workspace_bytes(B, T, H, N, int(bool(has_cu_seqlens)))
 
 
-def kda_set_stage_events(events) -> int:
-    """events: three cudaEvent_t handles (ints), or None/[] to turn timing off."""
-    if not events:
-        return lib().kda_set_stage_events(None, 0)
-    arr = (ctypes.c_void_p * len(events))(*events)
-    return lib().kda_set_stage_events(arr, len(events))
+def kda_stage_timing_begin(max_calls: int) -> int:
+    return lib().kda_stage_timing_begin(int(max_calls))
+
+
+def kda_stage_timing_end():
+    """Returns (status, intra_ms_mean, recurrent_ms_mean, calls)."""
+    a, b, n = ctypes.c_double(), ctypes.c_double(), ctypes.c_int()
+    rc = lib().kda_stage_timing_end(ctypes.byref(a), ctypes.byref(b), ctypes.byref(n))
+    return rc, a.value, b.value, n.value
 
 
 def kda_build_info() -> str:

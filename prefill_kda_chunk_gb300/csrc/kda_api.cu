@@ -6,6 +6,7 @@
 
 #include <map>
 #include <mutex>
+#include <vector>
 
 #include "kda.h"
 #include "kda_device.cuh"
@@ -26,7 +27,11 @@ struct DeviceState {
 
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
-thread_local cudaEvent_t t_stage_events[3] = {nullptr, nullptr, nullptr};
+struct StageTiming {
+    std::vector<cudaEvent_t> ev;  // 3 per call
+    int used = 0;
+};
+thread_local StageTiming t_timing;
 
 constexpr int64_t kMaxElems = int64_t(1) << 40;
 
@@ -176,13 +181,14 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
         rc = init_device(dev, st);
         if (rc != KDA_OK) return rc;
     }
-    if (stream != nullptr) {
+    if (stream != nullptr && !capturing) {
         int sdev = -1;
         if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return KDA_ERR_CUDA;
         if (sdev != dev) return KDA_ERR_WRONG_DEVICE;
     }
     const void *ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, out, final_state};
     for (const void *p : ptrs) {
+        if (capturing) break;  // pointer queries are not stream work; checked on uncaptured calls
         rc = check_pointer_device(p, dev);
         if (rc != KDA_OK) return rc;
     }
@@ -217,26 +223,56 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
             return KDA_ERR_CUDA;
     }
     uint8_t *rec = wsb + 256 + pl.off_bytes;
-    const bool timed = t_stage_events[0] != nullptr;
-    if (timed && cudaEventRecord(t_stage_events[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
+    cudaEvent_t *tev = nullptr;
+    if (static_cast<size_t>(3 * (t_timing.used + 1)) <= t_timing.ev.size())
+        tev = &t_timing.ev[3 * t_timing.used++];
+    if (tev && cudaEventRecord(tev[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
     kda::IntraParams ip{q, k, v, g, beta, rec, st.err, geo};
     if (kda::launch_intra_chunk(ip, pl.max_chunks, stream) != cudaSuccess) return KDA_ERR_CUDA;
-    if (timed && cudaEventRecord(t_stage_events[1], stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (tev && cudaEventRecord(tev[1], stream) != cudaSuccess) return KDA_ERR_CUDA;
     kda::RecurParams rp{rec, initial_state, out, final_state, scale, st.err, geo};
     if (kda::launch_recurrent(rp, stream) != cudaSuccess) return KDA_ERR_CUDA;
-    if (timed && cudaEventRecord(t_stage_events[2], stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (tev && cudaEventRecord(tev[2], stream) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 
-kda_status kda_set_stage_events(void *const *events, int n) {
-    if (n == 0) {
-        t_stage_events[0] = t_stage_events[1] = t_stage_events[2] = nullptr;
-        return KDA_OK;
+static void free_timing() {
+    for (cudaEvent_t e : t_timing.ev) cudaEventDestroy(e);
+    t_timing.ev.clear();
+    t_timing.used = 0;
+}
+
+kda_status kda_stage_timing_begin(int max_calls) {
+    if (max_calls < 1) return KDA_ERR_BAD_SHAPE;
+    free_timing();
+    t_timing.ev.resize(3 * static_cast<size_t>(max_calls), nullptr);
+    for (auto &e : t_timing.ev)
+        if (cudaEventCreate(&e) != cudaSuccess) {
+            e = nullptr;
+            free_timing();
+            return KDA_ERR_CUDA;
+        }
+    return KDA_OK;
+}
+
+kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *calls) {
+    const int n = t_timing.used;
+    double a = 0.0, b = 0.0;
+    kda_status rc = KDA_OK;
+    if (n > 0 && cudaEventSynchronize(t_timing.ev[3 * n - 1]) != cudaSuccess) rc = KDA_ERR_CUDA;
+    for (int i = 0; i < n && rc == KDA_OK; ++i) {
+        float x = 0.f, y = 0.f;
+        if (cudaEventElapsedTime(&x, t_timing.ev[3 * i], t_timing.ev[3 * i + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&y, t_timing.ev[3 * i + 1], t_timing.ev[3 * i + 2]) != cudaSuccess)
+            rc = KDA_ERR_CUDA;
+        a += x;
+        b += y;
     }
-    if (n != 3 || events == nullptr) return KDA_ERR_BAD_SHAPE;
-    for (int i = 0; i < 3; ++i)
-        if (events[i] == nullptr) return KDA_ERR_NULL_ARG;
-    for (int i = 0; i < 3; ++i) t_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+    free_timing();
+    if (rc != KDA_OK) return rc;
+    if (intra_ms) *intra_ms = n ? a / n : 0.0;
+    if (recurrent_ms) *recurrent_ms = n ? b / n : 0.0;
+    if (calls) *calls = n;
     return KDA_OK;
 }
 
