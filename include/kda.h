@@ -58,7 +58,9 @@ typedef enum {
     KDA_ERR_GATE_RANGE = -10,       /* (device) a chunk's summed log decay left [-80, 80] */
     KDA_ERR_CAPTURE = -11,          /* workspace must grow while the stream is capturing */
     KDA_ERR_WRONG_DEVICE = -12,     /* a buffer or the stream belongs to another device */
-    KDA_ERR_NOT_DEVICE_MEMORY = -13 /* a pointer is not CUDA device (or managed) memory */
+    KDA_ERR_NOT_DEVICE_MEMORY = -13, /* a pointer is not CUDA device (or managed) memory */
+    KDA_ERR_SCRATCH_LIMIT = -14     /* kda_chunk_prefill_noalloc: the call needs more scratch
+                                       than its fixed 64 MiB array holds */
 } kda_status;
 
 /*
@@ -108,6 +110,31 @@ KDA_API kda_status kda_chunk_prefill(const void *q, const void *k, const void *v
                              const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
                              int64_t K, int64_t V, int64_t N, float scale, void *out,
                              float *final_state, void *stream);
+
+/*
+ * kda_chunk_prefill_noalloc -- the same computation, arguments and results
+ * as kda_chunk_prefill, for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for users of
+ * the library whose code may not call cudaMalloc/cudaMallocAsync (directly or
+ * through this library): a host framework that owns all device allocations,
+ * a serving loop that must not enter the driver's allocator on its hot path,
+ * or a sandboxed plug-in. It allocates nothing. Its scratch is one
+ * fixed-size device array inside the library (64 MiB, held on every GPU that
+ * loads the library until the process exits); a call that needs more
+ * (kda_workspace_bytes() > 64 MiB, about 3850 chunk-heads) returns
+ * KDA_ERR_SCRATCH_LIMIT before enqueuing anything. All calls share that
+ * array: calls whose GPU work overlaps (e.g. on two streams) race and give
+ * wrong results. The first call on a device does a one-time set-up with that
+ * device current (no allocation); make it before any stream capture. Device
+ * errors of this entry point are not reported by kda_last_device_error().
+ */
+KDA_API kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
+                                             const float *g, const float *beta,
+                                             const float *initial_state,
+                                             const int32_t *cu_seqlens, int64_t B, int64_t T,
+                                             int64_t H, int64_t K, int64_t V, int64_t N,
+                                             float scale, void *out, float *final_state,
+                                             void *stream);
 
 /* Static text for a status code (never NULL). */
 KDA_API const char *kda_status_string(kda_status status);

@@ -12,6 +12,7 @@ from ._binding import (  # noqa: F401
     chunk_prefill,
     kda_build_info,
     kda_chunk_prefill,
+    kda_chunk_prefill_noalloc,
     kda_last_device_error,
     kda_stage_timing_begin,
     kda_stage_timing_end,

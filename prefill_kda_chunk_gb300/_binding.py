@@ -20,7 +20,7 @@ STATUS = {
     -4: "KDA_ERR_MISALIGNED", -5: "KDA_ERR_BAD_CU_SEQLENS", -6: "KDA_ERR_CUDA",
     -7: "KDA_ERR_DEVICE_TIMEOUT", -8: "KDA_ERR_NO_DEVICE_SUPPORT", -9: "KDA_ERR_ALIAS",
     -10: "KDA_ERR_GATE_RANGE", -11: "KDA_ERR_CAPTURE", -12: "KDA_ERR_WRONG_DEVICE",
-    -13: "KDA_ERR_NOT_DEVICE_MEMORY",
+    -13: "KDA_ERR_NOT_DEVICE_MEMORY", -14: "KDA_ERR_SCRATCH_LIMIT",
 }
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
@@ -48,6 +48,8 @@ def lib() -> ctypes.CDLL:
             vp, i64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
             L.kda_chunk_prefill.restype = ctypes.c_int
             L.kda_chunk_prefill.argtypes = [vp] * 7 + [i64] * 6 + [f32, vp, vp, vp]
+            L.kda_chunk_prefill_noalloc.restype = ctypes.c_int
+            L.kda_chunk_prefill_noalloc.argtypes = [vp] * 7 + [i64] * 6 + [f32, vp, vp, vp]
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_status_string.argtypes = [ctypes.c_int]
             L.kda_last_device_error.restype = ctypes.c_int
@@ -75,6 +77,14 @@ def kda_chunk_prefill(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V
     """The C entry point, pointers as ints (0 = NULL). Returns the status."""
     return lib().kda_chunk_prefill(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V, N,
                                    scale, out, final_state, stream)
+
+
+def kda_chunk_prefill_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V, N,
+                              scale, out, final_state, stream) -> int:
+    """The allocation-free C entry point (fixed 64 MiB scratch inside the
+    library), pointers as ints. Returns the status."""
+    return lib().kda_chunk_prefill_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H,
+                                           K, V, N, scale, out, final_state, stream)
 
 
 def kda_status_string(code: int) -> str:

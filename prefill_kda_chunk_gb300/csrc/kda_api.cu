@@ -123,6 +123,9 @@ const char *kda_status_string(kda_status s) {
         case KDA_ERR_CAPTURE: return "workspace cannot grow while the stream is capturing";
         case KDA_ERR_WRONG_DEVICE: return "a buffer or the stream belongs to another device";
         case KDA_ERR_NOT_DEVICE_MEMORY: return "a pointer is not CUDA device memory";
+        case KDA_ERR_SCRATCH_LIMIT:
+            return "the call needs more scratch than the fixed 64 MiB array of "
+                   "kda_chunk_prefill_noalloc";
     }
     return "unknown status";
 }

@@ -1,0 +1,82 @@
+"""kda_chunk_prefill_noalloc against kda_chunk_prefill, through the C ABI.
+
+The allocation-free entry point serves callers that may not allocate device
+memory (a host framework that owns every allocation, a serving loop that
+must stay out of the driver's allocator, a sandboxed plug-in). It uses a
+fixed scratch array inside the library instead of a workspace. Two calls in
+a row, on different inputs, must give what the allocating entry point gives
+(within the parity tolerance of the other GPU tests), and an oversized call
+must be refused before anything runs. This file is collected last so that a
+run stopping at the first failure has run every other test already.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs as KI
+import prefill_kda_chunk_gb300 as K
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+MAX_ABS = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from prefill_kda_chunk_gb300 import build
+    build.build()
+    K.lib()
+
+
+def _args(x, packed, out, fin, scale):
+    T, H = x["q"].shape[0], x["q"].shape[1]
+    N = x["cu_seqlens"].numel() - 1 if packed else 1
+    return (x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["g"].data_ptr(),
+            x["beta"].data_ptr(),
+            0 if x["initial_state"] is None else x["initial_state"].data_ptr(),
+            x["cu_seqlens"].data_ptr() if packed else 0, 1, T, H, 128, 128, N, scale,
+            out.data_ptr(), fin.data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+
+def _run(fn, d, packed):
+    x = {n: d[n].cuda() for n in ("q", "k", "v", "g", "beta", "cu_seqlens")}
+    x["initial_state"] = None if d["initial_state"] is None else d["initial_state"].cuda()
+    N = x["cu_seqlens"].numel() - 1 if packed else 1
+    out = torch.full_like(x["v"], float("nan"))
+    fin = torch.full((N, x["q"].shape[1], 128, 128), float("nan"), device="cuda")
+    rc = fn(*_args(x, packed, out, fin, d["scale"]))
+    assert rc == 0, K.STATUS.get(rc, rc)
+    torch.cuda.synchronize()
+    return out, fin
+
+
+def _close(a, b):
+    a = a.double().cpu().numpy()
+    b = b.double().cpu().numpy()
+    assert np.isfinite(a).all()
+    rel = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300)
+    mx = np.abs(a - b).max() / max(np.abs(b).max(), 1e-300)
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+def test_noalloc_matches_allocating_entry_point_two_calls():
+    cases = [(KI.make_case([100, 7, 33], H=3, seed=31, init_state=True), True),
+             (KI.make_case([250], H=4, seed=32, init_state=False), False)]
+    for d, packed in cases:  # two calls in a row on the shared scratch
+        o_na, f_na = _run(K.kda_chunk_prefill_noalloc, d, packed)
+        o_ref, f_ref = _run(K.kda_chunk_prefill, d, packed)
+        _close(o_na, o_ref)
+        _close(f_na, f_ref)
+
+
+def test_noalloc_rejects_oversized_call():
+    # 8192 tokens x 64 heads needs ~570 MB of scratch, above the 64 MiB array
+    assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) > (64 << 20)
+    dummy = torch.empty(16, dtype=torch.float32, device="cuda")
+    p = dummy.data_ptr()
+    rc = K.kda_chunk_prefill_noalloc(p, p, p, p, p, 0, 0, 1, 8192, 64, 128, 128, 1, 1.0, p, 0,
+                                     torch.cuda.current_stream().cuda_stream)
+    assert rc == K.STATUS_CODE["KDA_ERR_SCRATCH_LIMIT"]
