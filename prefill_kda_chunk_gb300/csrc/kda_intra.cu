@@ -27,13 +27,18 @@ namespace {
 constexpr int kIntraWarps = 4;
 
 struct IntraWarpSmem {
-    uint8_t kg[4096];   // K*exp(G), swizzled
+    uint8_t kg[4096];   // K as loaded, then K*exp(G); swizzled
     uint8_t kn[4096];   // K*exp(-G), swizzled; later stages -W
-    uint8_t qg[4096];   // Q*exp(G), swizzled
+    uint8_t qg[4096];   // Q as loaded, then Q*exp(G); swizzled
     uint8_t v[4096];    // V, swizzled
     float a[16 * 17];   // masked, beta-scaled A
     float t[16 * 17];   // (I + A)^{-1}
 };
+
+// Per device: SM count and resident CTAs per SM of the intra-chunk kernel.
+constexpr int kMaxDev = 128;
+int g_sm_count[kMaxDev] = {};
+int g_blocks_per_sm[kMaxDev] = {};
 
 __device__ __forceinline__ bool locate_chunk(const ChunkGeometry &geo, int64_t c, int &n,
                                              int64_t &t0, int &L) {
@@ -61,57 +66,114 @@ __device__ __forceinline__ bool locate_chunk(const ChunkGeometry &geo, int64_t c
     return true;
 }
 
+// Queues the chunk's q, k, v rows as 16-byte async copies into their swizzled
+// tiles; rows at or past L are zero-filled without a read.
+__device__ __forceinline__ void load_chunk(const IntraParams &p, IntraWarpSmem &sm, int64_t t0,
+                                           int L, int h, int lane) {
+    const int H = p.geo.n_heads;
+    const int64_t rowe = static_cast<int64_t>(H) * kDim;
+    const int64_t base = (t0 * H + h) * kDim;
+    const __nv_bfloat16 *qp = static_cast<const __nv_bfloat16 *>(p.q) + base;
+    const __nv_bfloat16 *kp = static_cast<const __nv_bfloat16 *>(p.k) + base;
+    const __nv_bfloat16 *vp = static_cast<const __nv_bfloat16 *>(p.v) + base;
+    const uint32_t sq = smem_u32(sm.qg), sk = smem_u32(sm.kg), sv = smem_u32(sm.v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int idx = lane + 32 * j, r = idx >> 4, c = idx & 15;
+        const uint32_t dst = r * 256 + ((c ^ (r & 7)) << 4);
+        const int rr = r < L ? r : 0;
+        const uint32_t nb = r < L ? 16u : 0u;
+        cp_async16(sq + dst, qp + rr * rowe + c * 8, nb);
+        cp_async16(sk + dst, kp + rr * rowe + c * 8, nb);
+        cp_async16(sv + dst, vp + rr * rowe + c * 8, nb);
+    }
+    cp_async_commit();
+}
+
+// Asks L2 for the rows of a later chunk (lanes 0-15: q and k of row lane;
+// lanes 16-31: v and g of row lane-16).
+__device__ __forceinline__ void prefetch_chunk(const IntraParams &p, int64_t t0, int L, int h,
+                                               int lane) {
+    const int r = lane & 15;
+    if (r >= L) return;
+    const int H = p.geo.n_heads;
+    const int64_t off = ((t0 + r) * H + h) * kDim;
+    if (lane < 16) {
+        prefetch_l2(static_cast<const __nv_bfloat16 *>(p.q) + off, 256);
+        prefetch_l2(static_cast<const __nv_bfloat16 *>(p.k) + off, 256);
+    } else {
+        prefetch_l2(static_cast<const __nv_bfloat16 *>(p.v) + off, 256);
+        prefetch_l2(p.g + off, 512);
+    }
+}
+
+// Persistent: each warp walks (chunk, head) items with a grid-wide stride,
+// items ordered chunk-major so the warps of a CTA share a chunk's rows.
 __global__ void __launch_bounds__(kIntraWarps * 32)
-kda_intra_chunk_kernel(IntraParams p) {
+kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
     const ChunkGeometry &geo = p.geo;
     const int H = geo.n_heads;
-    const int h = blockIdx.y * kIntraWarps + warp;
-    if (h >= H) return;
     if (geo.cu != nullptr && (*geo.call_flags & kErrBadCu)) return;
+    IntraWarpSmem &sm = reinterpret_cast<IntraWarpSmem *>(smem_raw)[warp];
+    const int64_t items = max_chunks * H;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kIntraWarps;
+
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * kIntraWarps + warp; item < items;
+         item += stride) {
+    const int64_t chunk = item / H;
+    const int h = static_cast<int>(item - chunk * H);
     int n, L;
     int64_t t0;
-    if (!locate_chunk(geo, blockIdx.x, n, t0, L)) return;
+    if (!locate_chunk(geo, chunk, n, t0, L)) continue;
     (void)n;
-
-    IntraWarpSmem &sm = reinterpret_cast<IntraWarpSmem *>(smem_raw)[warp];
-    const int64_t row = static_cast<int64_t>(H) * kDim;
-    const int64_t base = (t0 * H + h) * kDim + 4 * lane;
-    uint8_t *rec = p.rec + (static_cast<int64_t>(blockIdx.x) * H + h) * kRecBytes;
-
-    // ---- chunk-local cumulative log decay; lane owns channels 4*lane..+3
-    float G[16][4];
-    float run[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        float4 gg = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (r < L) gg = __ldcs(reinterpret_cast<const float4 *>(p.g + base + r * row));
-        run[0] += gg.x; run[1] += gg.y; run[2] += gg.z; run[3] += gg.w;
-        G[r][0] = run[0]; G[r][1] = run[1]; G[r][2] = run[2]; G[r][3] = run[3];
+    load_chunk(p, sm, t0, L, h, lane);
+    {
+        const int64_t nx = item + stride;
+        int n2, L2;
+        int64_t t2;
+        if (nx < items && locate_chunk(geo, nx / H, n2, t2, L2))
+            prefetch_chunk(p, t2, L2, static_cast<int>(nx % H), lane);
     }
-    bool bad = false;
-#pragma unroll
-    for (int r = 0; r < 16; ++r)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) bad |= !(fabsf(G[r][e]) <= 80.f);
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.err, kErrGate);
-
+    uint8_t *rec = p.rec + (chunk * H + h) * kRecBytes;
     const float beta_l = (lane < L) ? __ldg(p.beta + (t0 + lane) * H + h) : 0.f;
 
-    // ---- gated operand tiles
-    const __nv_bfloat16 *qp = static_cast<const __nv_bfloat16 *>(p.q);
-    const __nv_bfloat16 *kp = static_cast<const __nv_bfloat16 *>(p.k);
-    const __nv_bfloat16 *vp = static_cast<const __nv_bfloat16 *>(p.v);
+    // ---- chunk-local cumulative log decay; lane owns channels 4*lane..+3
+    float4 graw[16];
+    {
+        const float *gp = p.g + (t0 * H + h) * kDim + 4 * lane;
+        const int64_t rowe = static_cast<int64_t>(H) * kDim;
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            graw[r] = (r < L) ? __ldcs(reinterpret_cast<const float4 *>(gp + r * rowe))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float G[16][4];
+    float run[4] = {0.f, 0.f, 0.f, 0.f};
+    float gmax = 0.f;
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-        uint2 qq = make_uint2(0u, 0u), kk = make_uint2(0u, 0u), vv = make_uint2(0u, 0u);
-        if (r < L) {
-            qq = __ldcs(reinterpret_cast<const uint2 *>(qp + base + r * row));
-            kk = __ldcs(reinterpret_cast<const uint2 *>(kp + base + r * row));
-            vv = __ldcs(reinterpret_cast<const uint2 *>(vp + base + r * row));
-        }
+        const float4 gg = graw[r];
+        run[0] += gg.x; run[1] += gg.y; run[2] += gg.z; run[3] += gg.w;
+        G[r][0] = run[0]; G[r][1] = run[1]; G[r][2] = run[2]; G[r][3] = run[3];
+        gmax = fmaxf(gmax, fmaxf(fmaxf(fabsf(run[0]), fabsf(run[1])),
+                                 fmaxf(fabsf(run[2]), fabsf(run[3]))));
+    }
+    if (__any_sync(0xffffffffu, !(gmax <= 80.f)) && lane == 0) atomicOr(p.err, kErrGate);
+    float eL[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) eL[e] = __expf(run[e]);
+    cp_async_wait_all();
+    __syncwarp();
+
+    // ---- gated operand tiles (in place for K e^G and Q e^G)
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        const int off = swz(r, 4 * lane);
+        const uint2 qq = *reinterpret_cast<const uint2 *>(sm.qg + off);
+        const uint2 kk = *reinterpret_cast<const uint2 *>(sm.kg + off);
         const float2 q01 = unpack_bf16(qq.x), q23 = unpack_bf16(qq.y);
         const float2 k01 = unpack_bf16(kk.x), k23 = unpack_bf16(kk.y);
         const float kv[4] = {k01.x, k01.y, k23.x, k23.y};
@@ -121,13 +183,11 @@ kda_intra_chunk_kernel(IntraParams p) {
         for (int e = 0; e < 4; ++e) {
             const float eg = __expf(G[r][e]);
             const float en = __expf(-G[r][e]);
-            const float ed = __expf(run[e] - G[r][e]);
             kg[e] = kv[e] * eg;
             kn[e] = kv[e] * en;
             qg[e] = qv[e] * eg;
-            kd[e] = kv[e] * ed;
+            kd[e] = kv[e] * (en * eL[e]);
         }
-        const int off = swz(r, 4 * lane);
         const uint2 ukg = make_uint2(pack_bf16(kg[0], kg[1]), pack_bf16(kg[2], kg[3]));
         const uint2 ukn = make_uint2(pack_bf16(kn[0], kn[1]), pack_bf16(kn[2], kn[3]));
         const uint2 uqg = make_uint2(pack_bf16(qg[0], qg[1]), pack_bf16(qg[2], qg[3]));
@@ -135,12 +195,10 @@ kda_intra_chunk_kernel(IntraParams p) {
         *reinterpret_cast<uint2 *>(sm.kg + off) = ukg;
         *reinterpret_cast<uint2 *>(sm.kn + off) = ukn;
         *reinterpret_cast<uint2 *>(sm.qg + off) = uqg;
-        *reinterpret_cast<uint2 *>(sm.v + off) = vv;
         *reinterpret_cast<uint2 *>(rec + kRecQg + off) = uqg;
         *reinterpret_cast<uint2 *>(rec + kRecKd + off) = ukd;
     }
-    *reinterpret_cast<float4 *>(rec + kRecGamma + 16 * lane) =
-        make_float4(__expf(run[0]), __expf(run[1]), __expf(run[2]), __expf(run[3]));
+    *reinterpret_cast<float4 *>(rec + kRecGamma + 16 * lane) = make_float4(eL[0], eL[1], eL[2], eL[3]);
     __syncwarp();
 
     // ---- A_raw = (K e^G)(K e^-G)^T and P_raw = (Q e^G)(K e^-G)^T, 16x16 each
@@ -254,6 +312,8 @@ kda_intra_chunk_kernel(IntraParams p) {
         const int idx = (it * 32 + lane) * 16;
         *reinterpret_cast<uint4 *>(rec + kRecW + idx) = *reinterpret_cast<const uint4 *>(sm.kn + idx);
     }
+    __syncwarp();
+    }  // items
 }
 
 // Validates cu_seqlens and writes each sequence's first chunk index
@@ -316,16 +376,36 @@ cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t to
 }
 
 cudaError_t configure_intra() {
-    return cudaFuncSetAttribute(kda_intra_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kIntraWarps * static_cast<int>(sizeof(IntraWarpSmem)));
+    const int smem = kIntraWarps * static_cast<int>(sizeof(IntraWarpSmem));
+    cudaError_t e = cudaFuncSetAttribute(kda_intra_chunk_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, nb = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kda_intra_chunk_kernel,
+                                                           kIntraWarps * 32, smem)) != cudaSuccess)
+        return e;
+    g_sm_count[dev] = sms;
+    g_blocks_per_sm[dev] = nb > 0 ? nb : 1;
+    return cudaSuccess;
 }
 
 cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStream_t stream) {
     if (max_chunks <= 0) return cudaSuccess;
     const int smem = kIntraWarps * static_cast<int>(sizeof(IntraWarpSmem));
-    dim3 grid(static_cast<unsigned>(max_chunks),
-              static_cast<unsigned>((p.geo.n_heads + kIntraWarps - 1) / kIntraWarps));
-    kda_intra_chunk_kernel<<<grid, kIntraWarps * 32, smem, stream>>>(p);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int64_t items = max_chunks * p.geo.n_heads;
+    int64_t blocks = (items + kIntraWarps - 1) / kIntraWarps;
+    if (dev >= 0 && dev < kMaxDev && g_sm_count[dev] > 0) {
+        const int64_t resident = static_cast<int64_t>(g_sm_count[dev]) * g_blocks_per_sm[dev];
+        if (blocks > resident) blocks = resident;
+    }
+    kda_intra_chunk_kernel<<<static_cast<unsigned>(blocks), kIntraWarps * 32, smem, stream>>>(
+        p, max_chunks);
     return cudaGetLastError();
 }
 
