@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--workload", default=KI.HEADLINE, choices=KI.WORKLOAD_ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ring-slot-mb", type=float, default=None,
+                    help="ring-slot size for segmented calls (library default if unset; <0 off)")
     return ap.parse_args()
 
 
@@ -248,6 +250,8 @@ def main():
         B.build()
     barrier(world)
     K.lib()
+    if args.ring_slot_mb is not None:
+        K.kda_set_ring_slot_bytes(int(args.ring_slot_mb * (1 << 20)) if args.ring_slot_mb >= 0 else -1)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
 

@@ -97,7 +97,10 @@ typedef enum {
  *
  * Workspace: the library keeps one scratch buffer per (device, stream),
  * grown stream-ordered (cudaMallocAsync / cudaFreeAsync) when a call needs
- * more (about 17 KB per chunk-head). Concurrent calls on different streams
+ * more (17,408 B per chunk-head, or two ring slots plus the carried states
+ * for a segmented call, see kda_set_ring_slot_bytes). A segmented call also
+ * forks onto two internal streams of that workspace and joins back to
+ * `stream` before returning. Concurrent calls on different streams
  * therefore never share scratch. Growing is refused with KDA_ERR_CAPTURE
  * while the stream is being captured into a graph: make one call of the
  * largest size before capturing. kda_workspace_release() frees them.
@@ -169,6 +172,19 @@ KDA_API int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, 
  */
 KDA_API kda_status kda_stage_timing_begin(int max_calls);
 KDA_API kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *calls);
+
+/*
+ * Tuning (process-wide, host only). Fixed-length calls whose chunk records
+ * (17,408 B per chunk-head) exceed `bytes` are split into segments of chunk
+ * positions: the intra-chunk kernel of segment j+1 runs on an internal
+ * low-priority stream while the recurrent kernel of segment j runs on an
+ * internal high-priority stream, and the records live in two ring slots of
+ * about `bytes` each, small enough to stay in L2 between the two kernels.
+ * 0 restores the default, which is no segmentation; a negative value also
+ * disables it.
+ * Takes effect for later calls (the workspace grows if needed).
+ */
+KDA_API kda_status kda_set_ring_slot_bytes(int64_t bytes);
 
 /* Library build string: version and target architecture. Host only. */
 KDA_API const char *kda_build_info(void);

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <vector>
@@ -14,9 +15,14 @@
 
 namespace {
 
+// Per caller stream: the scratch buffer and, for segmented calls, two
+// internal streams (intra-chunk work at the lowest priority, recurrent work
+// at the highest) with the events that order them.
 struct StreamWorkspace {
     void *ptr = nullptr;
     size_t bytes = 0;
+    cudaStream_t s_intra = nullptr, s_recur = nullptr;
+    std::vector<cudaEvent_t> ev;
 };
 
 struct DeviceState {
@@ -27,11 +33,22 @@ struct DeviceState {
 
 std::mutex g_mu;
 std::map<int, DeviceState> g_devices;
+// Measurement hook state (per host thread): event pairs around every launch
+// of the two kernels during the timed calls.
 struct StageTiming {
-    std::vector<cudaEvent_t> ev;  // 3 per call
-    int used = 0;
+    int max_calls = 0, calls = 0;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> intra, recur;
 };
 thread_local StageTiming t_timing;
+
+// Bytes of one ring slot of chunk records for segmented fixed-length calls
+// (0: default, < 0: never segment). Segmentation is off by default: on GB300
+// the recurrent kernel is latency-bound and loses more from sharing SMs with
+// the intra-chunk kernel than the L2-resident records gain (T=8192, H=64:
+// 590 us unsegmented against 685-1107 us with 96-12 MiB slots).
+std::atomic<int64_t> g_slot_bytes{0};
+constexpr int64_t kDefaultSlotBytes = -1;
+constexpr int64_t kMinSegChunks = 8;
 
 constexpr int64_t kMaxElems = int64_t(1) << 40;
 
@@ -39,9 +56,16 @@ int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
 struct Plan {
     int64_t tokens = 0;      // total tokens
-    int64_t max_chunks = 0;  // chunk records needed (upper bound when packed)
+    int64_t max_chunks = 0;  // chunk records of one launch (upper bound when packed)
     int64_t off_bytes = 0;   // chunk offset table
     int64_t ws_bytes = 0;
+    // Segmented fixed-length calls: nseg launches of each kernel over seg_len
+    // chunk positions each, records in two ring slots of slot_bytes, the state
+    // carried between segments in carry_bytes.
+    int nseg = 1;
+    int64_t seg_len = 0;
+    int64_t slot_bytes = 0;
+    int64_t carry_bytes = 0;
 };
 
 bool misaligned(const void *p, uintptr_t a) {
@@ -73,6 +97,26 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, P
     if (N * H * 2 >= (int64_t(1) << 31)) return KDA_ERR_BAD_SHAPE;
     pl->off_bytes = packed ? align256((N + 1) * 4) : 0;
     pl->ws_bytes = 256 + pl->off_bytes + pl->max_chunks * H * kda::kRecBytes;
+    pl->nseg = 1;
+    pl->seg_len = (T + 15) / 16;
+    if (!packed) {
+        const int64_t cps = (T + 15) / 16;
+        const int64_t per_pos = B * H * int64_t(kda::kRecBytes);
+        int64_t slot = g_slot_bytes.load();
+        if (slot == 0) slot = kDefaultSlotBytes;
+        if (slot > 0 && cps * per_pos > slot) {
+            int64_t seg = slot / per_pos;
+            if (seg < kMinSegChunks) seg = kMinSegChunks;
+            if (seg < cps) {
+                pl->nseg = static_cast<int>((cps + seg - 1) / seg);
+                pl->seg_len = seg;
+                pl->slot_bytes = align256(seg * per_pos);
+                pl->carry_bytes = align256(B * H * 128 * 128 * 4);
+                pl->max_chunks = B * seg;
+                pl->ws_bytes = 256 + 2 * pl->slot_bytes + pl->carry_bytes;
+            }
+        }
+    }
     return KDA_OK;
 }
 
@@ -218,6 +262,24 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
     geo.n_seqs = static_cast<int32_t>(N);
     geo.n_heads = static_cast<int32_t>(H);
     geo.chunks_per_seq = static_cast<int32_t>((T + 15) / 16);
+    geo.pos_begin = 0;
+    geo.seg_len = geo.chunks_per_seq;
+    geo.slot_stride = geo.chunks_per_seq;
+
+    const bool timed = t_timing.calls < t_timing.max_calls;
+    if (timed) ++t_timing.calls;
+    auto timed_launch = [&](bool intra, cudaStream_t s, auto &&launch) -> kda_status {
+        cudaEvent_t e0 = nullptr, e1 = nullptr;
+        if (timed) {
+            if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess)
+                return KDA_ERR_CUDA;
+            (intra ? t_timing.intra : t_timing.recur).emplace_back(e0, e1);
+            if (cudaEventRecord(e0, s) != cudaSuccess) return KDA_ERR_CUDA;
+        }
+        if (launch() != cudaSuccess) return KDA_ERR_CUDA;
+        if (timed && cudaEventRecord(e1, s) != cudaSuccess) return KDA_ERR_CUDA;
+        return KDA_OK;
+    };
 
     if (cu_seqlens != nullptr) {
         if (kda::launch_varlen_prologue(cu_seqlens, geo.n_seqs, pl.tokens,
@@ -226,56 +288,115 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
             return KDA_ERR_CUDA;
     }
     uint8_t *rec = wsb + 256 + pl.off_bytes;
-    cudaEvent_t *tev = nullptr;
-    if (static_cast<size_t>(3 * (t_timing.used + 1)) <= t_timing.ev.size())
-        tev = &t_timing.ev[3 * t_timing.used++];
-    if (tev && cudaEventRecord(tev[0], stream) != cudaSuccess) return KDA_ERR_CUDA;
-    kda::IntraParams ip{q, k, v, g, beta, rec, st.err, geo};
-    if (kda::launch_intra_chunk(ip, pl.max_chunks, stream) != cudaSuccess) return KDA_ERR_CUDA;
-    if (tev && cudaEventRecord(tev[1], stream) != cudaSuccess) return KDA_ERR_CUDA;
-    kda::RecurParams rp{rec, initial_state, out, final_state, scale, st.err, geo};
-    if (kda::launch_recurrent(rp, stream) != cudaSuccess) return KDA_ERR_CUDA;
-    if (tev && cudaEventRecord(tev[2], stream) != cudaSuccess) return KDA_ERR_CUDA;
+
+    if (pl.nseg == 1) {
+        kda::IntraParams ip{q, k, v, g, beta, rec, st.err, geo};
+        rc = timed_launch(true, stream, [&] { return kda::launch_intra_chunk(ip, pl.max_chunks, stream); });
+        if (rc != KDA_OK) return rc;
+        kda::RecurParams rp{rec, initial_state, out, final_state, scale, st.err, geo};
+        return timed_launch(false, stream, [&] { return kda::launch_recurrent(rp, stream); });
+    }
+
+    // ---- segmented: intra-chunk work of segment j+1 overlaps the recurrent
+    //      work of segment j; records alternate between two ring slots
+    if (ws.s_intra == nullptr) {
+        if (capturing) return KDA_ERR_CAPTURE;
+        int lo = 0, hi = 0;
+        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return KDA_ERR_CUDA;
+        if (cudaStreamCreateWithPriority(&ws.s_intra, cudaStreamNonBlocking, lo) != cudaSuccess ||
+            cudaStreamCreateWithPriority(&ws.s_recur, cudaStreamNonBlocking, hi) != cudaSuccess)
+            return KDA_ERR_CUDA;
+    }
+    const size_t nev = 1 + 2 * static_cast<size_t>(pl.nseg);
+    if (ws.ev.size() < nev) {
+        if (capturing) return KDA_ERR_CAPTURE;
+        while (ws.ev.size() < nev) {
+            cudaEvent_t e;
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return KDA_ERR_CUDA;
+            ws.ev.push_back(e);
+        }
+    }
+    cudaEvent_t ev_in = ws.ev[0];
+    cudaEvent_t *ev_intra = &ws.ev[1], *ev_recur = &ws.ev[1 + pl.nseg];
+    float *carry = reinterpret_cast<float *>(rec + 2 * pl.slot_bytes);
+    if (cudaEventRecord(ev_in, stream) != cudaSuccess ||
+        cudaStreamWaitEvent(ws.s_intra, ev_in, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(ws.s_recur, ev_in, 0) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    const int64_t cps = geo.chunks_per_seq;
+    for (int j = 0; j < pl.nseg; ++j) {
+        kda::ChunkGeometry gj = geo;
+        gj.pos_begin = static_cast<int32_t>(j * pl.seg_len);
+        const int64_t left = cps - j * pl.seg_len;
+        gj.seg_len = static_cast<int32_t>(left < pl.seg_len ? left : pl.seg_len);
+        gj.slot_stride = static_cast<int32_t>(pl.seg_len);
+        uint8_t *slot = rec + (j & 1) * pl.slot_bytes;
+        if (j >= 2 && cudaStreamWaitEvent(ws.s_intra, ev_recur[j - 2], 0) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        kda::IntraParams ip{q, k, v, g, beta, slot, st.err, gj};
+        const int64_t items = B * static_cast<int64_t>(gj.seg_len);
+        rc = timed_launch(true, ws.s_intra,
+                          [&] { return kda::launch_intra_chunk(ip, items, ws.s_intra); });
+        if (rc != KDA_OK) return rc;
+        if (cudaEventRecord(ev_intra[j], ws.s_intra) != cudaSuccess ||
+            cudaStreamWaitEvent(ws.s_recur, ev_intra[j], 0) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        const float *s_in = j == 0 ? initial_state : carry;
+        float *s_out = j == pl.nseg - 1 ? final_state : carry;
+        kda::RecurParams rp{slot, s_in, out, s_out, scale, st.err, gj};
+        rc = timed_launch(false, ws.s_recur, [&] { return kda::launch_recurrent(rp, ws.s_recur); });
+        if (rc != KDA_OK) return rc;
+        if (cudaEventRecord(ev_recur[j], ws.s_recur) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    if (cudaStreamWaitEvent(stream, ev_recur[pl.nseg - 1], 0) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 
 static void free_timing() {
-    for (cudaEvent_t e : t_timing.ev) cudaEventDestroy(e);
-    t_timing.ev.clear();
-    t_timing.used = 0;
+    for (auto *v : {&t_timing.intra, &t_timing.recur}) {
+        for (auto &pr : *v) {
+            if (pr.first) cudaEventDestroy(pr.first);
+            if (pr.second) cudaEventDestroy(pr.second);
+        }
+        v->clear();
+    }
+    t_timing.max_calls = t_timing.calls = 0;
 }
 
 kda_status kda_stage_timing_begin(int max_calls) {
     if (max_calls < 1) return KDA_ERR_BAD_SHAPE;
     free_timing();
-    t_timing.ev.resize(3 * static_cast<size_t>(max_calls), nullptr);
-    for (auto &e : t_timing.ev)
-        if (cudaEventCreate(&e) != cudaSuccess) {
-            e = nullptr;
-            free_timing();
-            return KDA_ERR_CUDA;
-        }
+    t_timing.max_calls = max_calls;
     return KDA_OK;
 }
 
 kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *calls) {
-    const int n = t_timing.used;
-    double a = 0.0, b = 0.0;
+    const int n = t_timing.calls;
+    double sum[2] = {0.0, 0.0};
     kda_status rc = KDA_OK;
-    if (n > 0 && cudaEventSynchronize(t_timing.ev[3 * n - 1]) != cudaSuccess) rc = KDA_ERR_CUDA;
-    for (int i = 0; i < n && rc == KDA_OK; ++i) {
-        float x = 0.f, y = 0.f;
-        if (cudaEventElapsedTime(&x, t_timing.ev[3 * i], t_timing.ev[3 * i + 1]) != cudaSuccess ||
-            cudaEventElapsedTime(&y, t_timing.ev[3 * i + 1], t_timing.ev[3 * i + 2]) != cudaSuccess)
-            rc = KDA_ERR_CUDA;
-        a += x;
-        b += y;
+    int which = 0;
+    for (auto *v : {&t_timing.intra, &t_timing.recur}) {
+        for (auto &pr : *v) {
+            float ms = 0.f;
+            if (cudaEventSynchronize(pr.second) != cudaSuccess ||
+                cudaEventElapsedTime(&ms, pr.first, pr.second) != cudaSuccess) {
+                rc = KDA_ERR_CUDA;
+                break;
+            }
+            sum[which] += ms;
+        }
+        ++which;
     }
     free_timing();
     if (rc != KDA_OK) return rc;
-    if (intra_ms) *intra_ms = n ? a / n : 0.0;
-    if (recurrent_ms) *recurrent_ms = n ? b / n : 0.0;
+    if (intra_ms) *intra_ms = n ? sum[0] / n : 0.0;
+    if (recurrent_ms) *recurrent_ms = n ? sum[1] / n : 0.0;
     if (calls) *calls = n;
+    return KDA_OK;
+}
+
+kda_status kda_set_ring_slot_bytes(int64_t bytes) {
+    g_slot_bytes.store(bytes);
     return KDA_OK;
 }
 
@@ -307,8 +428,13 @@ kda_status kda_workspace_release(void) {
     std::lock_guard<std::mutex> lock(g_mu);
     auto it = g_devices.find(dev);
     if (it == g_devices.end()) return KDA_OK;
-    for (auto &kv : it->second.ws)
-        if (kv.second.ptr != nullptr && cudaFree(kv.second.ptr) != cudaSuccess) return KDA_ERR_CUDA;
+    for (auto &kv : it->second.ws) {
+        StreamWorkspace &w = kv.second;
+        if (w.ptr != nullptr && cudaFree(w.ptr) != cudaSuccess) return KDA_ERR_CUDA;
+        for (cudaEvent_t e : w.ev) cudaEventDestroy(e);
+        if (w.s_intra) cudaStreamDestroy(w.s_intra);
+        if (w.s_recur) cudaStreamDestroy(w.s_recur);
+    }
     it->second.ws.clear();
     return KDA_OK;
 }

@@ -17,7 +17,17 @@ struct ChunkGeometry {
     int64_t seq_len;           // fixed: tokens per sequence; packed: total tokens
     int32_t n_seqs;
     int32_t n_heads;
-    int32_t chunks_per_seq;    // fixed only
+    int32_t chunks_per_seq;    // fixed only: chunks of one whole sequence
+    // Fixed-length only: one launch covers chunk positions
+    // [pos_begin, pos_begin + seg_len) of every sequence, and the record of
+    // (sequence n, position pos_begin + i, head h) sits at index
+    // (n * slot_stride + i) * H + h. The first position of a segment is
+    // treated as the start of a sequence by the intra-chunk kernel (no
+    // look-ahead terms), so each segment's recurrent launch starts afresh
+    // from the state the previous one left.
+    int32_t pos_begin;
+    int32_t seg_len;
+    int32_t slot_stride;
 };
 
 struct IntraParams {

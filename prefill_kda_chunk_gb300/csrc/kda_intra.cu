@@ -41,15 +41,18 @@ int g_sm_count[kMaxDev] = {};
 int g_blocks_per_sm[kMaxDev] = {};
 
 __device__ __forceinline__ bool locate_chunk(const ChunkGeometry &geo, int64_t c, int &n,
-                                             int64_t &t0, int &L) {
+                                             int64_t &t0, int &L, int64_t &rec_idx) {
     if (geo.cu == nullptr) {
-        const int64_t cps = geo.chunks_per_seq;
-        n = static_cast<int>(c / cps);
+        const int64_t per = geo.seg_len;
+        n = static_cast<int>(c / per);
         if (n >= geo.n_seqs) return false;
-        const int64_t i = c - static_cast<int64_t>(n) * cps;
+        const int64_t il = c - static_cast<int64_t>(n) * per;
+        const int64_t i = geo.pos_begin + il;
         t0 = static_cast<int64_t>(n) * geo.seq_len + 16 * i;
         const int64_t rem = geo.seq_len - 16 * i;
+        if (rem <= 0) return false;
         L = static_cast<int>(rem < 16 ? rem : 16);
+        rec_idx = static_cast<int64_t>(n) * geo.slot_stride + il;
         return true;
     }
     const int32_t *off = geo.chunk_off;
@@ -63,6 +66,7 @@ __device__ __forceinline__ bool locate_chunk(const ChunkGeometry &geo, int64_t c
     t0 = static_cast<int64_t>(geo.cu[n]) + 16 * (c - off[n]);
     const int64_t rem = static_cast<int64_t>(geo.cu[n + 1]) - t0;
     L = static_cast<int>(rem < 16 ? rem : 16);
+    rec_idx = c;
     return true;
 }
 
@@ -126,18 +130,18 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     const int64_t chunk = item / H;
     const int h = static_cast<int>(item - chunk * H);
     int n, L;
-    int64_t t0;
-    if (!locate_chunk(geo, chunk, n, t0, L)) continue;
+    int64_t t0, rec_idx;
+    if (!locate_chunk(geo, chunk, n, t0, L, rec_idx)) continue;
     (void)n;
     load_chunk(p, sm, t0, L, h, lane);
     {
         const int64_t nx = item + stride;
         int n2, L2;
-        int64_t t2;
-        if (nx < items && locate_chunk(geo, nx / H, n2, t2, L2))
+        int64_t t2, r2;
+        if (nx < items && locate_chunk(geo, nx / H, n2, t2, L2, r2))
             prefetch_chunk(p, t2, L2, static_cast<int>(nx % H), lane);
     }
-    uint8_t *rec = p.rec + (chunk * H + h) * kRecBytes;
+    uint8_t *rec = p.rec + (rec_idx * H + h) * kRecBytes;
     const float beta_l = (lane < L) ? __ldg(p.beta + (t0 + lane) * H + h) : 0.f;
 
     // ---- chunk-local cumulative log decay; lane owns channels 4*lane..+3

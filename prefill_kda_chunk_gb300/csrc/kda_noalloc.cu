@@ -84,8 +84,12 @@ extern "C" kda_status kda_chunk_prefill_noalloc(
     int64_t K, int64_t V, int64_t N, float scale, void *out, float *final_state, void *stream_) {
     if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_DIM;
     const bool packed = cu_seqlens != nullptr;
-    const int64_t need = kda_workspace_bytes(B, T, H, N, packed ? 1 : 0);
-    if (need <= 0) return KDA_ERR_BAD_SHAPE;
+    if (kda_workspace_bytes(B, T, H, N, packed ? 1 : 0) <= 0) return KDA_ERR_BAD_SHAPE;
+    // this entry point never splits a call into segments: every chunk record
+    // of the call is in the array at once
+    const int64_t need_off = packed ? (((N + 1) * 4 + 255) & ~int64_t(255)) : 0;
+    const int64_t need_chunks = packed ? (T + 15 * N) / 16 : B * ((T + 15) / 16);
+    const int64_t need = 256 + need_off + need_chunks * H * kda::kRecBytes;
     if (static_cast<size_t>(need) > kNoAllocScratchBytes) return KDA_ERR_SCRATCH_LIMIT;
     const int64_t tokens = packed ? T : B * T;
     if (tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL_ARG;
@@ -131,6 +135,9 @@ extern "C" kda_status kda_chunk_prefill_noalloc(
     geo.n_seqs = static_cast<int32_t>(N);
     geo.n_heads = static_cast<int32_t>(H);
     geo.chunks_per_seq = static_cast<int32_t>((T + 15) / 16);
+    geo.pos_begin = 0;
+    geo.seg_len = geo.chunks_per_seq;
+    geo.slot_stride = geo.chunks_per_seq;
     if (packed && kda::launch_varlen_prologue(cu_seqlens, geo.n_seqs, tokens,
                                               reinterpret_cast<int32_t *>(base + 256), call_flags,
                                               err, stream) != cudaSuccess)

@@ -62,16 +62,19 @@ kda_recurrent_kernel(RecurParams p) {
     if (geo.cu != nullptr && (*geo.call_flags & kErrBadCu)) return;
 
     int64_t tb, te, chunk0;
+    int nck;
     if (geo.cu == nullptr) {
-        tb = static_cast<int64_t>(n) * geo.seq_len;
-        te = tb + geo.seq_len;
-        chunk0 = static_cast<int64_t>(n) * geo.chunks_per_seq;
+        tb = static_cast<int64_t>(n) * geo.seq_len + 16 * static_cast<int64_t>(geo.pos_begin);
+        te = static_cast<int64_t>(n) * geo.seq_len + geo.seq_len;
+        chunk0 = static_cast<int64_t>(n) * geo.slot_stride;
+        const int64_t left = te > tb ? (te - tb + 15) / 16 : 0;
+        nck = static_cast<int>(left < geo.seg_len ? left : geo.seg_len);
     } else {
         tb = geo.cu[n];
         te = geo.cu[n + 1];
         chunk0 = geo.chunk_off[n];
+        nck = static_cast<int>((te - tb + 15) / 16);
     }
-    const int nck = static_cast<int>((te - tb + 15) / 16);
     const uint8_t *rec0 = p.rec + (chunk0 * H + h) * static_cast<int64_t>(kRecBytes);
     const uint32_t stage0 = smem_u32(smem);
 

@@ -41,9 +41,23 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
-    # 512 chunks x 64 heads x 17408 B + the flag block
-    assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 512 * 64 * 17408
-    assert K.kda_workspace_bytes(1, 8192, 64, 16, 1) == 256 + 256 + ((8192 + 15 * 16) // 16) * 64 * 17408
+    REC = 17408
+    try:
+        K.kda_set_ring_slot_bytes(-1)          # one launch of each kernel
+        # 512 chunks x 64 heads x 17408 B + the flag block
+        assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 512 * 64 * REC
+        K.kda_set_ring_slot_bytes(24 << 20)    # segmented when records exceed a slot
+        seg = (24 << 20) // (64 * REC)         # chunk positions per segment
+        slot = -(-(seg * 64 * REC) // 256) * 256
+        carry = 64 * 128 * 128 * 4
+        assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 2 * slot + carry
+        assert K.kda_workspace_bytes(1, 256, 2, 1, 0) == 256 + 16 * 2 * REC   # small: unsegmented
+        K.kda_set_ring_slot_bytes(0)           # default: one launch of each kernel
+        assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 512 * 64 * REC
+    finally:
+        K.kda_set_ring_slot_bytes(0)
+    # packed batches are never segmented
+    assert K.kda_workspace_bytes(1, 8192, 64, 16, 1) == 256 + 256 + ((8192 + 15 * 16) // 16) * 64 * REC
     assert K.kda_workspace_bytes(1, 8192, 64, 2, 0) == 0      # N != B without cu_seqlens
     assert K.kda_workspace_bytes(2, 100, 0, 2, 0) == 0        # H < 1
 

@@ -158,8 +158,11 @@ def test_split_call_equals_one_call():
                              initial_state=fa, scale=d["scale"])
     K.check_device_error()
     assert_parity(torch.cat([oa, ob]), fb, o_ref, f_ref, "split")
-    # chunk boundaries coincide (48 = 3 x 16), so the two paths are bitwise equal
-    assert torch.equal(torch.cat([oa, ob]), o) and torch.equal(fb, f)
+    # The one-call path forms U of chunk 3 with the one-chunk look-ahead while
+    # the second call starts that chunk afresh, so the two agree to rounding.
+    rel_o, _ = errs(torch.cat([oa, ob]), o.double().cpu().numpy())
+    rel_f, _ = errs(fb, f.double().cpu().numpy())
+    assert rel_o <= 2e-3 and rel_f <= 2e-3, (rel_o, rel_f)
 
 
 def test_in_place_state_and_no_final_state():
@@ -177,6 +180,33 @@ def test_in_place_state_and_no_final_state():
                              scale=d["scale"])
     K.check_device_error()
     assert f2 is None and torch.equal(o2, o)
+
+
+@pytest.mark.parametrize("T,Bn", [(300, 1), (129, 3), (256, 2)])
+def test_segmented_calls(T, Bn):
+    """Small ring slots force several segments (overlapped intra/recurrent
+    launches on internal streams, state carried between segments)."""
+    H = 2
+    d = KI.make_case([T] * Bn, H=H, seed=40 + T, init_state=True)
+    x = to_dev(d)
+    q, k, v, g = (x[n].view(Bn, T, H, 128) for n in ("q", "k", "v", "g"))
+    beta = x["beta"].view(Bn, T, H)
+    try:
+        K.kda_set_ring_slot_bytes(8 * Bn * H * 17408)       # 8 chunk positions per segment
+        o, f = K.chunk_prefill(q, k, v, g, beta, initial_state=x["initial_state"],
+                               scale=d["scale"])
+        st = x["initial_state"].clone()                     # in place, and no final state
+        o2, _ = K.chunk_prefill(q, k, v, g, beta, initial_state=st, final_state=st,
+                                scale=d["scale"])
+        o3, f3 = K.chunk_prefill(q, k, v, g, beta, initial_state=x["initial_state"],
+                                 output_final_state=False, scale=d["scale"])
+        K.check_device_error()
+    finally:
+        K.kda_set_ring_slot_bytes(0)
+    o_ref, f_ref = run_oracle(d)
+    assert_parity(o.view(Bn * T, H, 128), f, o_ref, f_ref, "segmented")
+    assert torch.equal(o2, o) and torch.equal(st, f)
+    assert f3 is None and torch.equal(o3, o)
 
 
 def test_deterministic():

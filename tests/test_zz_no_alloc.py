@@ -73,8 +73,9 @@ def test_noalloc_matches_allocating_entry_point_two_calls():
 
 
 def test_noalloc_rejects_oversized_call():
-    # 8192 tokens x 64 heads needs ~570 MB of scratch, above the 64 MiB array
-    assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) > (64 << 20)
+    # 8192 tokens x 64 heads: 512 chunks x 64 heads x 17408 B of chunk records
+    # (~570 MB, all held at once by this entry point), above the 64 MiB array
+    assert 512 * 64 * 17408 > (64 << 20)
     dummy = torch.empty(16, dtype=torch.float32, device="cuda")
     p = dummy.data_ptr()
     rc = K.kda_chunk_prefill_noalloc(p, p, p, p, p, 0, 0, 1, 8192, 64, 128, 128, 1, 1.0, p, 0,
