@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--workload", default=KI.HEADLINE, choices=KI.WORKLOAD_ORDER)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--recurrent-impl", type=int, default=None,
+                    help="0 = tcgen05 recurrent kernel, 1 = warp-MMA kernel (library default if unset)")
     ap.add_argument("--ring-slot-mb", type=float, default=None,
                     help="ring-slot size for segmented calls (library default if unset; <0 off)")
     return ap.parse_args()
@@ -250,6 +252,8 @@ def main():
         B.build()
     barrier(world)
     K.lib()
+    if args.recurrent_impl is not None:
+        K.kda_set_recurrent_impl(args.recurrent_impl)
     if args.ring_slot_mb is not None:
         K.kda_set_ring_slot_bytes(int(args.ring_slot_mb * (1 << 20)) if args.ring_slot_mb >= 0 else -1)
     dev = torch.device("cuda", local)

@@ -186,6 +186,15 @@ KDA_API kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, 
  */
 KDA_API kda_status kda_set_ring_slot_bytes(int64_t bytes);
 
+/*
+ * Selects the recurrent kernel for later calls (process-wide, host only):
+ * 0 = the 5th-generation tensor-core kernel (state in tensor memory,
+ * tcgen05 MMAs, one CTA per (sequence, head)), 1 = the warp-level MMA kernel
+ * (state in registers, one CTA per (sequence, head, 64 value channels)).
+ * Both compute the same result to rounding. Other values: KDA_ERR_BAD_SHAPE.
+ */
+KDA_API kda_status kda_set_recurrent_impl(int impl);
+
 /* Library build string: version and target architecture. Host only. */
 KDA_API const char *kda_build_info(void);
 

@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
             L.kda_stage_timing_end.argtypes = [ctypes.POINTER(ctypes.c_double),
                                                ctypes.POINTER(ctypes.c_double),
                                                ctypes.POINTER(ctypes.c_int)]
+            L.kda_set_recurrent_impl.restype = ctypes.c_int
+            L.kda_set_recurrent_impl.argtypes = [ctypes.c_int]
             L.kda_set_ring_slot_bytes.restype = ctypes.c_int
             L.kda_set_ring_slot_bytes.argtypes = [i64]
             L.kda_build_info.restype = ctypes.c_char_p
@@ -114,6 +116,11 @@ def kda_stage_timing_end():
     a, b, n = ctypes.c_double(), ctypes.c_double(), ctypes.c_int()
     rc = lib().kda_stage_timing_end(ctypes.byref(a), ctypes.byref(b), ctypes.byref(n))
     return rc, a.value, b.value, n.value
+
+
+def kda_set_recurrent_impl(impl: int) -> int:
+    """0 = tcgen05 / tensor-memory recurrent kernel, 1 = warp-MMA kernel."""
+    return lib().kda_set_recurrent_impl(int(impl))
 
 
 def kda_set_ring_slot_bytes(nbytes: int) -> int:

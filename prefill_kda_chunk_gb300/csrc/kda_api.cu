@@ -50,6 +50,13 @@ std::atomic<int64_t> g_slot_bytes{0};
 constexpr int64_t kDefaultSlotBytes = -1;
 constexpr int64_t kMinSegChunks = 8;
 
+// Recurrent kernel: 0 = tcgen05 / tensor memory, 1 = warp-level MMA.
+std::atomic<int> g_recur_impl{1};
+
+cudaError_t launch_recur(const kda::RecurParams &p, cudaStream_t s) {
+    return g_recur_impl.load() == 0 ? kda::launch_recurrent_tc(p, s) : kda::launch_recurrent(p, s);
+}
+
 constexpr int64_t kMaxElems = int64_t(1) << 40;
 
 int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
@@ -130,6 +137,7 @@ kda_status init_device(int dev, DeviceState &st) {
     if (cudaMemset(st.err, 0, 256) != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_intra() != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_recurrent() != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::configure_recurrent_tc() != cudaSuccess) return KDA_ERR_CUDA;
     st.ready = true;
     return KDA_OK;
 }
@@ -294,7 +302,7 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
         rc = timed_launch(true, stream, [&] { return kda::launch_intra_chunk(ip, pl.max_chunks, stream); });
         if (rc != KDA_OK) return rc;
         kda::RecurParams rp{rec, initial_state, out, final_state, scale, st.err, geo};
-        return timed_launch(false, stream, [&] { return kda::launch_recurrent(rp, stream); });
+        return timed_launch(false, stream, [&] { return launch_recur(rp, stream); });
     }
 
     // ---- segmented: intra-chunk work of segment j+1 overlaps the recurrent
@@ -344,7 +352,7 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
         const float *s_in = j == 0 ? initial_state : carry;
         float *s_out = j == pl.nseg - 1 ? final_state : carry;
         kda::RecurParams rp{slot, s_in, out, s_out, scale, st.err, gj};
-        rc = timed_launch(false, ws.s_recur, [&] { return kda::launch_recurrent(rp, ws.s_recur); });
+        rc = timed_launch(false, ws.s_recur, [&] { return launch_recur(rp, ws.s_recur); });
         if (rc != KDA_OK) return rc;
         if (cudaEventRecord(ev_recur[j], ws.s_recur) != cudaSuccess) return KDA_ERR_CUDA;
     }
@@ -392,6 +400,12 @@ kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *cal
     if (intra_ms) *intra_ms = n ? sum[0] / n : 0.0;
     if (recurrent_ms) *recurrent_ms = n ? sum[1] / n : 0.0;
     if (calls) *calls = n;
+    return KDA_OK;
+}
+
+kda_status kda_set_recurrent_impl(int impl) {
+    if (impl != 0 && impl != 1) return KDA_ERR_BAD_SHAPE;
+    g_recur_impl.store(impl);
     return KDA_OK;
 }
 

@@ -52,11 +52,13 @@ struct RecurParams {
 // Per-device, once: raise the dynamic shared-memory limits of the kernels.
 cudaError_t configure_intra();
 cudaError_t configure_recurrent();
+cudaError_t configure_recurrent_tc();
 
 cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t total_tokens,
                                    int32_t *chunk_off, int *call_flags, int *err,
                                    cudaStream_t stream);
 cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStream_t stream);
-cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream);
+cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream);     // warp MMA
+cudaError_t launch_recurrent_tc(const RecurParams &p, cudaStream_t stream);  // tcgen05 / TMEM
 
 }  // namespace kda

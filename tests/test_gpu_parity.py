@@ -27,6 +27,14 @@ def built():
     K.lib()
 
 
+# every test runs with both recurrent kernels: 0 = tcgen05 / tensor memory, 1 = warp MMA
+@pytest.fixture(autouse=True, params=[0, 1], ids=["tcgen05", "warp_mma"])
+def recurrent_impl(request, built):
+    assert K.kda_set_recurrent_impl(request.param) == 0
+    yield request.param
+    K.kda_set_recurrent_impl(1)
+
+
 def to_dev(d):
     dev = {}
     for key in ("q", "k", "v", "g", "beta"):
@@ -158,11 +166,12 @@ def test_split_call_equals_one_call():
                              initial_state=fa, scale=d["scale"])
     K.check_device_error()
     assert_parity(torch.cat([oa, ob]), fb, o_ref, f_ref, "split")
-    # The one-call path forms U of chunk 3 with the one-chunk look-ahead while
-    # the second call starts that chunk afresh, so the two agree to rounding.
+    # The second call starts from the first call's fp32 final state instead of
+    # the state held inside the kernel (registers or tensor memory with its
+    # lazily applied decay), so the two paths agree to rounding, not bitwise.
     rel_o, _ = errs(torch.cat([oa, ob]), o.double().cpu().numpy())
     rel_f, _ = errs(fb, f.double().cpu().numpy())
-    assert rel_o <= 2e-3 and rel_f <= 2e-3, (rel_o, rel_f)
+    assert rel_o <= 5e-3 and rel_f <= 5e-3, (rel_o, rel_f)
 
 
 def test_in_place_state_and_no_final_state():
