@@ -16,6 +16,13 @@
 // record into a ring of shared-memory stages with bulk async copies,
 // completion tracked by mbarriers; every wait is bounded and a timeout is
 // recorded in the device error word instead of hanging.
+//
+// Step order follows the chunk-to-chunk dependency chain (S -> U -> S): the
+// U product first, the decay of S while it drains, S^T Qg^T to keep the
+// tensor pipe busy, then the state update, and only after it the output
+// branch (P U, scaling, store), which nothing later depends on. The next
+// stage's barrier is tested right after the update MMAs are issued so that
+// its latency overlaps them.
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
@@ -25,6 +32,34 @@ namespace kda {
 namespace {
 
 constexpr int kStages = 4;
+
+// register-only MMA (not volatile: free to schedule around other work)
+__device__ __forceinline__ void mma_r(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                      uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// (a, b) *= (x, y) as one packed fp32x2 multiply
+__device__ __forceinline__ void mul2(float &a, float &b, float x, float y) {
+    asm("{\n .reg .b64 t, u;\n mov.b64 t, {%0, %1};\n mov.b64 u, {%2, %3};\n"
+        " mul.rn.f32x2 t, t, u;\n mov.b64 {%0, %1}, t;\n}\n"
+        : "+f"(a), "+f"(b) : "f"(x), "f"(y));
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                          uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
+}
 
 template <int BV>
 struct RecurLayout {
@@ -121,9 +156,10 @@ kda_recurrent_kernel(RecurParams p) {
     uint8_t *so = smem + Lay::kOStage + warp * 512;   // [16 tok][16 val] bf16
     __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(p.out);
 
+    bool ready = false;
     for (int i = 0; i < nck; ++i) {
         const int st = i % kStages;
-        if (!mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
+        if (!ready && !mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
             atomicOr(p.err, kErrTimeout);
             break;
         }
@@ -140,7 +176,7 @@ kda_recurrent_kernel(RecurParams p) {
             aS[kk][3] = pack_bf16(acc[2 * kk + 1][2], acc[2 * kk + 1][3]);
         }
 
-        // U^T = Ut^T - S^T W^T and (Q e^G S)^T = S^T Qg^T; two partial sums each
+        // U^T = Ut^T - S^T W^T first (it gates the state update), two partial sums
         float uT[2][2][4], oT[2][2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -155,51 +191,73 @@ kda_recurrent_kernel(RecurParams p) {
         }
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            uint32_t bw[4], bq[4];
+            uint32_t bw[4];
             const int rb = (quad >> 1) * 8 + (lane & 7), cb = 16 * kk + (quad & 1) * 8;
             ldsm_x4(sw + kRecW + swz(rb, cb), bw[0], bw[1], bw[2], bw[3]);
-            ldsm_x4(sw + kRecQg + swz(rb, cb), bq[0], bq[1], bq[2], bq[3]);
-            mma16816(uT[0][kk & 1], aS[kk], bw[0], bw[1]);
-            mma16816(uT[1][kk & 1], aS[kk], bw[2], bw[3]);
-            mma16816(oT[0][kk & 1], aS[kk], bq[0], bq[1]);
-            mma16816(oT[1][kk & 1], aS[kk], bq[2], bq[3]);
+            mma_r(uT[0][kk & 1], aS[kk], bw[0], bw[1]);
+            mma_r(uT[1][kk & 1], aS[kk], bw[2], bw[3]);
         }
-        float u[2][4], o[2][4];
+        // decay of the state, while the U products drain
+        const float *gam = reinterpret_cast<const float *>(stg + kRecGamma);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float2 gm = *reinterpret_cast<const float2 *>(gam + 8 * j + 2 * tig);
+            mul2(acc[j][0], acc[j][1], gm.x, gm.y);
+            mul2(acc[j][2], acc[j][3], gm.x, gm.y);
+        }
+        // (Q e^G S)^T = S^T Qg^T keeps the tensor pipe busy meanwhile
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t bq[4];
+            const int rb = (quad >> 1) * 8 + (lane & 7), cb = 16 * kk + (quad & 1) * 8;
+            ldsm_x4(sw + kRecQg + swz(rb, cb), bq[0], bq[1], bq[2], bq[3]);
+            mma_r(oT[0][kk & 1], aS[kk], bq[0], bq[1]);
+            mma_r(oT[1][kk & 1], aS[kk], bq[2], bq[3]);
+        }
+        uint32_t aU[4];
+        {
+            float u[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) u[nt][e] = uT[nt][0][e] + uT[nt][1][e];
+            aU[0] = pack_bf16(u[0][0], u[0][1]);
+            aU[1] = pack_bf16(u[0][2], u[0][3]);
+            aU[2] = pack_bf16(u[1][0], u[1][1]);
+            aU[3] = pack_bf16(u[1][2], u[1][3]);
+        }
+        // S^T <- S^T Diag(gamma) + U^T Kd
+#pragma unroll
+        for (int jp = 0; jp < 8; ++jp) {
+            uint32_t b[4];
+            const int rk = (quad & 1) * 8 + (lane & 7), ck = 16 * jp + (quad >> 1) * 8;
+            ldsm_x4_t(sw + kRecKd + swz(rk, ck), b[0], b[1], b[2], b[3]);
+            mma_r(acc[2 * jp], aU, b[0], b[1]);
+            mma_r(acc[2 * jp + 1], aU, b[2], b[3]);
+        }
+        // look at the next stage's barrier now; its latency hides behind the MMAs
+        if (i + 1 < nck) ready = mbar_test(bar_full + 8 * ((i + 1) % kStages), ((i + 1) / kStages) & 1);
+        // o^T = (Q e^G S)^T + U^T P^T, off the state's dependency chain
+        float o[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                u[nt][e] = uT[nt][0][e] + uT[nt][1][e];
-                o[nt][e] = oT[nt][0][e] + oT[nt][1][e];
-            }
-
-        // U^T as bf16 A fragments (M = value, K = token)
-        uint32_t aU[4];
-        aU[0] = pack_bf16(u[0][0], u[0][1]);
-        aU[1] = pack_bf16(u[0][2], u[0][3]);
-        aU[2] = pack_bf16(u[1][0], u[1][1]);
-        aU[3] = pack_bf16(u[1][2], u[1][3]);
-
-        // o^T += U^T P^T
+            for (int e = 0; e < 4; ++e) o[nt][e] = oT[nt][0][e] + oT[nt][1][e];
         {
             uint32_t bp[4];
             const int rp = (quad >> 1) * 8 + (lane & 7);
             ldsm_x4(sw + kRecP + rp * 32 + (quad & 1) * 16, bp[0], bp[1], bp[2], bp[3]);
-            mma16816(o[0], aU, bp[0], bp[1]);
-            mma16816(o[1], aU, bp[2], bp[3]);
+            mma_r(o[0], aU, bp[0], bp[1]);
+            mma_r(o[1], aU, bp[2], bp[3]);
         }
-
-        // o: stage [token][value] in shared memory, then 16-byte row stores
         const int64_t t0 = tb + 16 * i;
         const int L = static_cast<int>((te - t0) < 16 ? (te - t0) : 16);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            const int tk = 8 * nt + 2 * tig;
-            __nv_bfloat16 *so16 = reinterpret_cast<__nv_bfloat16 *>(so);
-            so16[tk * 16 + gid] = __float2bfloat16_rn(p.scale * o[nt][0]);
-            so16[(tk + 1) * 16 + gid] = __float2bfloat16_rn(p.scale * o[nt][1]);
-            so16[tk * 16 + gid + 8] = __float2bfloat16_rn(p.scale * o[nt][2]);
-            so16[(tk + 1) * 16 + gid + 8] = __float2bfloat16_rn(p.scale * o[nt][3]);
+        {
+            const float sc = p.scale;
+            const int j = lane >> 3, r = lane & 7;
+            stsm_x4_t(smem_u32(so) + ((j >> 1) * 8 + r) * 32 + (j & 1) * 16,
+                      pack_bf16(sc * o[0][0], sc * o[0][1]), pack_bf16(sc * o[0][2], sc * o[0][3]),
+                      pack_bf16(sc * o[1][0], sc * o[1][1]), pack_bf16(sc * o[1][2], sc * o[1][3]));
         }
         __syncwarp();
         {
@@ -208,22 +266,6 @@ kda_recurrent_kernel(RecurParams p) {
                 const uint4 val = *reinterpret_cast<const uint4 *>(so + tok * 32 + hf * 16);
                 *reinterpret_cast<uint4 *>(outp + ((t0 + tok) * H + h) * kDim + v0 + hf * 8) = val;
             }
-        }
-
-        // S^T <- S^T Diag(gamma) + U^T Kd
-        const float *gam = reinterpret_cast<const float *>(stg + kRecGamma);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float2 gm = *reinterpret_cast<const float2 *>(gam + 8 * j + 2 * tig);
-            acc[j][0] *= gm.x; acc[j][1] *= gm.y; acc[j][2] *= gm.x; acc[j][3] *= gm.y;
-        }
-#pragma unroll
-        for (int jp = 0; jp < 8; ++jp) {
-            uint32_t b[4];
-            const int rk = (quad & 1) * 8 + (lane & 7), ck = 16 * jp + (quad >> 1) * 8;
-            ldsm_x4_t(sw + kRecKd + swz(rk, ck), b[0], b[1], b[2], b[3]);
-            mma16816(acc[2 * jp], aU, b[0], b[1]);
-            mma16816(acc[2 * jp + 1], aU, b[2], b[3]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * st);
