@@ -16,6 +16,11 @@
 // and stores, per (chunk, head), the record the recurrent kernel consumes:
 // -W, Q*exp(G), K*exp(G_last - G), P, exp(G_last) and Ut^T. Rows past the
 // end of a sequence are zero (their k, v, q, beta and g are taken as 0).
+//
+// Record stores are evict-first (st.global.cs): the records are read back by
+// the recurrent kernel long after they leave L2, so keeping them there only
+// pushes out input rows. No L2 prefetch of later chunks either: on GB300 it
+// raised DRAM reads and cost time.
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
@@ -25,6 +30,25 @@ namespace kda {
 namespace {
 
 constexpr int kIntraWarps = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x on the special-function unit (inputs here stay within +-116, so the
+// flush of subnormal results never applies)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// two fp32 products in one packed instruction
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 x, y, z;\n mov.b64 x, {%2, %3};\n mov.b64 y, {%4, %5};\n"
+        " mul.rn.f32x2 z, x, y;\n mov.b64 {%0, %1}, z;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
 
 struct IntraWarpSmem {
     uint8_t kg[4096];   // K as loaded, then K*exp(G); swizzled
@@ -94,26 +118,9 @@ __device__ __forceinline__ void load_chunk(const IntraParams &p, IntraWarpSmem &
     cp_async_commit();
 }
 
-// Asks L2 for the rows of a later chunk (lanes 0-15: q and k of row lane;
-// lanes 16-31: v and g of row lane-16).
-__device__ __forceinline__ void prefetch_chunk(const IntraParams &p, int64_t t0, int L, int h,
-                                               int lane) {
-    const int r = lane & 15;
-    if (r >= L) return;
-    const int H = p.geo.n_heads;
-    const int64_t off = ((t0 + r) * H + h) * kDim;
-    if (lane < 16) {
-        prefetch_l2(static_cast<const __nv_bfloat16 *>(p.q) + off, 256);
-        prefetch_l2(static_cast<const __nv_bfloat16 *>(p.k) + off, 256);
-    } else {
-        prefetch_l2(static_cast<const __nv_bfloat16 *>(p.v) + off, 256);
-        prefetch_l2(p.g + off, 512);
-    }
-}
-
 // Persistent: each warp walks (chunk, head) items with a grid-wide stride,
 // items ordered chunk-major so the warps of a CTA share a chunk's rows.
-__global__ void __launch_bounds__(kIntraWarps * 32)
+__global__ void __launch_bounds__(kIntraWarps * 32, 3)
 kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -134,13 +141,6 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     if (!locate_chunk(geo, chunk, n, t0, L, rec_idx)) continue;
     (void)n;
     load_chunk(p, sm, t0, L, h, lane);
-    {
-        const int64_t nx = item + stride;
-        int n2, L2;
-        int64_t t2, r2;
-        if (nx < items && locate_chunk(geo, nx / H, n2, t2, L2, r2))
-            prefetch_chunk(p, t2, L2, static_cast<int>(nx % H), lane);
-    }
     uint8_t *rec = p.rec + (rec_idx * H + h) * kRecBytes;
     const float beta_l = (lane < L) ? __ldg(p.beta + (t0 + lane) * H + h) : 0.f;
 
@@ -154,21 +154,22 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
             graw[r] = (r < L) ? __ldcs(reinterpret_cast<const float4 *>(gp + r * rowe))
                               : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float G[16][4];
+    float G[16][4];   // cumulative log decay in base-2 units (G * log2 e)
     float run[4] = {0.f, 0.f, 0.f, 0.f};
     float gmax = 0.f;
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
         const float4 gg = graw[r];
         run[0] += gg.x; run[1] += gg.y; run[2] += gg.z; run[3] += gg.w;
-        G[r][0] = run[0]; G[r][1] = run[1]; G[r][2] = run[2]; G[r][3] = run[3];
+        G[r][0] = run[0] * kLog2e; G[r][1] = run[1] * kLog2e;
+        G[r][2] = run[2] * kLog2e; G[r][3] = run[3] * kLog2e;
         gmax = fmaxf(gmax, fmaxf(fmaxf(fabsf(run[0]), fabsf(run[1])),
                                  fmaxf(fabsf(run[2]), fabsf(run[3]))));
     }
     if (__any_sync(0xffffffffu, !(gmax <= 80.f)) && lane == 0) atomicOr(p.err, kErrGate);
     float eL[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) eL[e] = __expf(run[e]);
+    for (int e = 0; e < 4; ++e) eL[e] = ex2(G[15][e]);
     cp_async_wait_all();
     __syncwarp();
 
@@ -180,18 +181,21 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
         const uint2 kk = *reinterpret_cast<const uint2 *>(sm.kg + off);
         const float2 q01 = unpack_bf16(qq.x), q23 = unpack_bf16(qq.y);
         const float2 k01 = unpack_bf16(kk.x), k23 = unpack_bf16(kk.y);
-        const float kv[4] = {k01.x, k01.y, k23.x, k23.y};
-        const float qv[4] = {q01.x, q01.y, q23.x, q23.y};
-        float kg[4], kn[4], qg[4], kd[4];
+        float2 eg[2], en[2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float eg = __expf(G[r][e]);
-            const float en = __expf(-G[r][e]);
-            kg[e] = kv[e] * eg;
-            kn[e] = kv[e] * en;
-            qg[e] = qv[e] * eg;
-            kd[e] = kv[e] * (en * eL[e]);
+        for (int e = 0; e < 2; ++e) {
+            eg[e] = make_float2(ex2(G[r][2 * e]), ex2(G[r][2 * e + 1]));
+            en[e] = make_float2(ex2(-G[r][2 * e]), ex2(-G[r][2 * e + 1]));
         }
+        const float2 eL01 = make_float2(eL[0], eL[1]), eL23 = make_float2(eL[2], eL[3]);
+        const float2 kg01 = mul2(k01, eg[0]), kg23 = mul2(k23, eg[1]);
+        const float2 qg01 = mul2(q01, eg[0]), qg23 = mul2(q23, eg[1]);
+        const float2 kn01 = mul2(k01, en[0]), kn23 = mul2(k23, en[1]);
+        const float2 kd01 = mul2(kn01, eL01), kd23 = mul2(kn23, eL23);
+        const float kg[4] = {kg01.x, kg01.y, kg23.x, kg23.y};
+        const float kn[4] = {kn01.x, kn01.y, kn23.x, kn23.y};
+        const float qg[4] = {qg01.x, qg01.y, qg23.x, qg23.y};
+        const float kd[4] = {kd01.x, kd01.y, kd23.x, kd23.y};
         const uint2 ukg = make_uint2(pack_bf16(kg[0], kg[1]), pack_bf16(kg[2], kg[3]));
         const uint2 ukn = make_uint2(pack_bf16(kn[0], kn[1]), pack_bf16(kn[2], kn[3]));
         const uint2 uqg = make_uint2(pack_bf16(qg[0], qg[1]), pack_bf16(qg[2], qg[3]));
@@ -199,10 +203,11 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
         *reinterpret_cast<uint2 *>(sm.kg + off) = ukg;
         *reinterpret_cast<uint2 *>(sm.kn + off) = ukn;
         *reinterpret_cast<uint2 *>(sm.qg + off) = uqg;
-        *reinterpret_cast<uint2 *>(rec + kRecQg + off) = uqg;
-        *reinterpret_cast<uint2 *>(rec + kRecKd + off) = ukd;
+        __stcs(reinterpret_cast<uint2 *>(rec + kRecQg + off), uqg);
+        __stcs(reinterpret_cast<uint2 *>(rec + kRecKd + off), ukd);
     }
-    *reinterpret_cast<float4 *>(rec + kRecGamma + 16 * lane) = make_float4(eL[0], eL[1], eL[2], eL[3]);
+    __stcs(reinterpret_cast<float4 *>(rec + kRecGamma + 16 * lane),
+           make_float4(eL[0], eL[1], eL[2], eL[3]));
     __syncwarp();
 
     // ---- A_raw = (K e^G)(K e^-G)^T and P_raw = (Q e^G)(K e^-G)^T, 16x16 each
@@ -239,7 +244,8 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
             sm.a[r * 17 + i + 1] = a1;
             const float p0 = (i <= r) ? accP[nt][2 * hf] : 0.f;
             const float p1 = (i + 1 <= r) ? accP[nt][2 * hf + 1] : 0.f;
-            *reinterpret_cast<uint32_t *>(rec + kRecP + (r * 16 + i) * 2) = pack_bf16(p0, p1);
+            __stcs(reinterpret_cast<unsigned int *>(rec + kRecP + (r * 16 + i) * 2),
+                   pack_bf16(p0, p1));
         }
     }
     __syncwarp();
@@ -302,11 +308,11 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
         mma16816(u0, a, aT[0], aT[2]);  // tokens 0..7
         mma16816(u1, a, aT[1], aT[3]);  // tokens 8..15
         const int vr = 16 * mt + gid, tk = 2 * tig;
-        *reinterpret_cast<uint32_t *>(rec + kRecUt + (vr * 16 + tk) * 2) = pack_bf16(u0[0], u0[1]);
-        *reinterpret_cast<uint32_t *>(rec + kRecUt + ((vr + 8) * 16 + tk) * 2) = pack_bf16(u0[2], u0[3]);
-        *reinterpret_cast<uint32_t *>(rec + kRecUt + (vr * 16 + tk + 8) * 2) = pack_bf16(u1[0], u1[1]);
-        *reinterpret_cast<uint32_t *>(rec + kRecUt + ((vr + 8) * 16 + tk + 8) * 2) =
-            pack_bf16(u1[2], u1[3]);
+        unsigned int *ut = reinterpret_cast<unsigned int *>(rec + kRecUt);
+        __stcs(ut + (vr * 16 + tk) / 2, pack_bf16(u0[0], u0[1]));
+        __stcs(ut + ((vr + 8) * 16 + tk) / 2, pack_bf16(u0[2], u0[3]));
+        __stcs(ut + (vr * 16 + tk + 8) / 2, pack_bf16(u1[0], u1[1]));
+        __stcs(ut + ((vr + 8) * 16 + tk + 8) / 2, pack_bf16(u1[2], u1[3]));
     }
     __syncwarp();
 
@@ -314,7 +320,7 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const int idx = (it * 32 + lane) * 16;
-        *reinterpret_cast<uint4 *>(rec + kRecW + idx) = *reinterpret_cast<const uint4 *>(sm.kn + idx);
+        __stcs(reinterpret_cast<uint4 *>(rec + kRecW + idx), *reinterpret_cast<const uint4 *>(sm.kn + idx));
     }
     __syncwarp();
     }  // items
