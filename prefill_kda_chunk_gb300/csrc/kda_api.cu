@@ -298,10 +298,10 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
     uint8_t *rec = wsb + 256 + pl.off_bytes;
 
     if (pl.nseg == 1) {
-        kda::IntraParams ip{q, k, v, g, beta, rec, st.err, geo};
+        kda::IntraParams ip{q, k, v, g, beta, rec, scale, st.err, geo};
         rc = timed_launch(true, stream, [&] { return kda::launch_intra_chunk(ip, pl.max_chunks, stream); });
         if (rc != KDA_OK) return rc;
-        kda::RecurParams rp{rec, initial_state, out, final_state, scale, st.err, geo};
+        kda::RecurParams rp{rec, initial_state, out, final_state, st.err, geo};
         return timed_launch(false, stream, [&] { return launch_recur(rp, stream); });
     }
 
@@ -341,7 +341,7 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
         uint8_t *slot = rec + (j & 1) * pl.slot_bytes;
         if (j >= 2 && cudaStreamWaitEvent(ws.s_intra, ev_recur[j - 2], 0) != cudaSuccess)
             return KDA_ERR_CUDA;
-        kda::IntraParams ip{q, k, v, g, beta, slot, st.err, gj};
+        kda::IntraParams ip{q, k, v, g, beta, slot, scale, st.err, gj};
         const int64_t items = B * static_cast<int64_t>(gj.seg_len);
         rc = timed_launch(true, ws.s_intra,
                           [&] { return kda::launch_intra_chunk(ip, items, ws.s_intra); });
@@ -351,7 +351,7 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
             return KDA_ERR_CUDA;
         const float *s_in = j == 0 ? initial_state : carry;
         float *s_out = j == pl.nseg - 1 ? final_state : carry;
-        kda::RecurParams rp{slot, s_in, out, s_out, scale, st.err, gj};
+        kda::RecurParams rp{slot, s_in, out, s_out, st.err, gj};
         rc = timed_launch(false, ws.s_recur, [&] { return launch_recur(rp, ws.s_recur); });
         if (rc != KDA_OK) return rc;
         if (cudaEventRecord(ev_recur[j], ws.s_recur) != cudaSuccess) return KDA_ERR_CUDA;

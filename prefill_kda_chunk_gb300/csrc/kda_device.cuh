@@ -18,9 +18,9 @@ constexpr int kDim = 128;    // K = V
 // consecutive rows of one granule column fall in distinct shared-memory
 // banks (ldmatrix reads them without conflicts).
 constexpr int kRecW = 0;          // -W = -(T diag(beta)) (K * exp(G))   [16 tok][128 key], swizzled
-constexpr int kRecQg = 4096;      // Q * exp(G)                          [16 tok][128 key], swizzled
+constexpr int kRecQg = 4096;      // scale * Q * exp(G)                  [16 tok][128 key], swizzled
 constexpr int kRecKd = 8192;      // K * exp(G_last - G)                 [16 tok][128 key], swizzled
-constexpr int kRecP = 12288;      // P, lower triangle incl. diagonal    [16 r][16 i] bf16
+constexpr int kRecP = 12288;      // scale * P, lower triangle incl. diag [16 r][16 i] bf16
 constexpr int kRecGamma = 12800;  // exp(G_last)                         [128] fp32
 constexpr int kRecUt = 13312;     // (T diag(beta) V)^T                  [128 val][16 tok] bf16
 constexpr int kRecBytes = 17408;

@@ -35,6 +35,7 @@ struct IntraParams {
     const float *g;            // [tokens, H, 128]
     const float *beta;         // [tokens, H]
     uint8_t *rec;              // chunk records [chunks, H, kRecBytes]
+    float scale;               // output scale, folded into the record's Q e^G and P
     int *err;                  // sticky per-device error word
     ChunkGeometry geo;
 };
@@ -44,7 +45,6 @@ struct RecurParams {
     const float *s0;           // [N, H, 128, 128] or nullptr
     void *out;                 // bf16 [tokens, H, 128]
     float *s_final;            // [N, H, 128, 128] or nullptr
-    float scale;
     int *err;
     ChunkGeometry geo;
 };

@@ -14,7 +14,9 @@
 //   W      = Tm diag(beta) (K * exp(G)),   Ut = Tm diag(beta) V
 //
 // and stores, per (chunk, head), the record the recurrent kernel consumes:
-// -W, Q*exp(G), K*exp(G_last - G), P, exp(G_last) and Ut^T. Rows past the
+// -W, scale*Q*exp(G), K*exp(G_last - G), scale*P, exp(G_last) and Ut^T (the
+// output scale rides on the two output operands, so the recurrent kernel
+// never multiplies by it). Rows past the
 // end of a sequence are zero (their k, v, q, beta and g are taken as 0).
 //
 // Record stores are evict-first (st.global.cs): the records are read back by
@@ -53,7 +55,7 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
 struct IntraWarpSmem {
     uint8_t kg[4096];   // K as loaded, then K*exp(G); swizzled
     uint8_t kn[4096];   // K*exp(-G), swizzled; later stages -W
-    uint8_t qg[4096];   // Q as loaded, then Q*exp(G); swizzled
+    uint8_t qg[4096];   // Q as loaded, then scale*Q*exp(G); swizzled
     uint8_t v[4096];    // V, swizzled
     float a[16 * 17];   // masked, beta-scaled A
     float t[16 * 17];   // (I + A)^{-1}
@@ -173,7 +175,7 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     cp_async_wait_all();
     __syncwarp();
 
-    // ---- gated operand tiles (in place for K e^G and Q e^G)
+    // ---- gated operand tiles (in place for K e^G and scale Q e^G)
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
         const int off = swz(r, 4 * lane);
@@ -188,8 +190,9 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
             en[e] = make_float2(ex2(-G[r][2 * e]), ex2(-G[r][2 * e + 1]));
         }
         const float2 eL01 = make_float2(eL[0], eL[1]), eL23 = make_float2(eL[2], eL[3]);
+        const float2 sc2 = make_float2(p.scale, p.scale);
         const float2 kg01 = mul2(k01, eg[0]), kg23 = mul2(k23, eg[1]);
-        const float2 qg01 = mul2(q01, eg[0]), qg23 = mul2(q23, eg[1]);
+        const float2 qg01 = mul2(q01, mul2(eg[0], sc2)), qg23 = mul2(q23, mul2(eg[1], sc2));
         const float2 kn01 = mul2(k01, en[0]), kn23 = mul2(k23, en[1]);
         const float2 kd01 = mul2(kn01, eL01), kd23 = mul2(kn23, eL23);
         const float kg[4] = {kg01.x, kg01.y, kg23.x, kg23.y};
@@ -210,7 +213,7 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
            make_float4(eL[0], eL[1], eL[2], eL[3]));
     __syncwarp();
 
-    // ---- A_raw = (K e^G)(K e^-G)^T and P_raw = (Q e^G)(K e^-G)^T, 16x16 each
+    // ---- A_raw = (K e^G)(K e^-G)^T and P_raw = scale (Q e^G)(K e^-G)^T, 16x16 each
     const uint32_t s_kg = smem_u32(sm.kg), s_kn = smem_u32(sm.kn), s_qg = smem_u32(sm.qg);
     const uint32_t s_v = smem_u32(sm.v);
     float accA[2][4] = {}, accP[2][4] = {};

@@ -9,6 +9,8 @@
 //   o_r = scale ( (q_r * exp(G_r))^T S + sum_{i<=r} P[r,i] U_i )
 //   S  <- Diag(exp(G_last)) S + (K * exp(G_last - G))^T U
 //
+// (scale already multiplies the record's Q*exp(G) and P tiles.)
+//
 // The state lives in registers as S^T fragments of the warp MMA (each
 // consumer warp owns 16 value channels x all 128 key channels), which is at
 // the same time the A operand of S^T W^T (the transposed U product) and the
@@ -20,7 +22,7 @@
 // Step order follows the chunk-to-chunk dependency chain (S -> U -> S): the
 // U product first, the decay of S while it drains, S^T Qg^T to keep the
 // tensor pipe busy, then the state update, and only after it the output
-// branch (P U, scaling, store), which nothing later depends on. The next
+// branch (P U, store), which nothing later depends on. The next
 // stage's barrier is tested right after the update MMAs are issued so that
 // its latency overlaps them.
 
@@ -157,6 +159,8 @@ kda_recurrent_kernel(RecurParams p) {
     __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(p.out);
 
     bool ready = false;
+    __nv_bfloat16 *orow = outp + (tb * H + h) * kDim + v0;   // row 0 of the chunk's o tile
+    const int64_t ostep = 16 * static_cast<int64_t>(H) * kDim;
     for (int i = 0; i < nck; ++i) {
         const int st = i % kStages;
         if (!ready && !mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
@@ -236,8 +240,9 @@ kda_recurrent_kernel(RecurParams p) {
             mma_r(acc[2 * jp + 1], aU, b[2], b[3]);
         }
         // look at the next stage's barrier now; its latency hides behind the MMAs
-        if (i + 1 < nck) ready = mbar_test(bar_full + 8 * ((i + 1) % kStages), ((i + 1) / kStages) & 1);
-        // o^T = (Q e^G S)^T + U^T P^T, off the state's dependency chain
+        if (i + 1 < nck)
+            ready = mbar_test(bar_full + 8 * ((i + 1) % kStages), ((i + 1) / kStages) & 1);
+        // o^T = (Q e^G S)^T + U^T P^T (scale is in the record), off the chain
         float o[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -253,20 +258,21 @@ kda_recurrent_kernel(RecurParams p) {
         const int64_t t0 = tb + 16 * i;
         const int L = static_cast<int>((te - t0) < 16 ? (te - t0) : 16);
         {
-            const float sc = p.scale;
             const int j = lane >> 3, r = lane & 7;
             stsm_x4_t(smem_u32(so) + ((j >> 1) * 8 + r) * 32 + (j & 1) * 16,
-                      pack_bf16(sc * o[0][0], sc * o[0][1]), pack_bf16(sc * o[0][2], sc * o[0][3]),
-                      pack_bf16(sc * o[1][0], sc * o[1][1]), pack_bf16(sc * o[1][2], sc * o[1][3]));
+                      pack_bf16(o[0][0], o[0][1]), pack_bf16(o[0][2], o[0][3]),
+                      pack_bf16(o[1][0], o[1][1]), pack_bf16(o[1][2], o[1][3]));
         }
         __syncwarp();
         {
             const int tok = lane >> 1, hf = lane & 1;
             if (tok < L) {
                 const uint4 val = *reinterpret_cast<const uint4 *>(so + tok * 32 + hf * 16);
-                *reinterpret_cast<uint4 *>(outp + ((t0 + tok) * H + h) * kDim + v0 + hf * 8) = val;
+                *reinterpret_cast<uint4 *>(orow + tok * static_cast<int64_t>(H) * kDim + hf * 8) =
+                    val;
             }
         }
+        orow += ostep;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * st);
     }

@@ -6,7 +6,7 @@
 // entering chunk n:
 //
 //   U_n     = Ut_n - W_n S_n
-//   o_n     = Qg_n S_n + P_n U_n                    (times scale)
+//   o_n     = Qg_n S_n + P_n U_n                    (the record's Qg and P carry scale)
 //   S_{n+1} = Diag(gamma_n) S_n + Kd_n^T U_n
 //
 // State in tensor memory, decay carried lazily. TMEM holds Shat = Diag(c)^-1 S
@@ -242,7 +242,7 @@ kda_recurrent_tc_kernel(RecurParams p) {
                 for (int c = 0; c < 16; ++c)
                     if (c < L)
                         outp[((t0 + c) * H + h) * kDim + v] =
-                            __float2bfloat16_rn(p.scale * __uint_as_float(r[c]));
+                            __float2bfloat16_rn(__uint_as_float(r[c]));
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(kBarEmpty + s));
