@@ -46,7 +46,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--recurrent-impl", type=int, default=None,
-                    help="0 = tcgen05 recurrent kernel, 1 = warp-MMA kernel (library default if unset)")
+                    help="0 = tcgen05 recurrent kernel, 1 = warp-MMA kernel, 2 = hybrid "
+                         "(library default if unset)")
     ap.add_argument("--ring-slot-mb", type=float, default=None,
                     help="ring-slot size for segmented calls (library default if unset; <0 off)")
     return ap.parse_args()

@@ -190,8 +190,10 @@ KDA_API kda_status kda_set_ring_slot_bytes(int64_t bytes);
  * Selects the recurrent kernel for later calls (process-wide, host only):
  * 0 = the 5th-generation tensor-core kernel (state in tensor memory,
  * tcgen05 MMAs, one CTA per (sequence, head)), 1 = the warp-level MMA kernel
- * (state in registers, one CTA per (sequence, head, 64 value channels)).
- * Both compute the same result to rounding. Other values: KDA_ERR_BAD_SHAPE.
+ * (state in registers, one CTA per (sequence, head, 64 value channels)),
+ * 2 = hybrid: the warp-level MMA chain with the output product Qg S on
+ * tcgen05 (bf16 state handed over in tensor memory). All three compute the
+ * same result to rounding. Other values: KDA_ERR_BAD_SHAPE.
  */
 KDA_API kda_status kda_set_recurrent_impl(int impl);
 

@@ -50,11 +50,14 @@ std::atomic<int64_t> g_slot_bytes{0};
 constexpr int64_t kDefaultSlotBytes = -1;
 constexpr int64_t kMinSegChunks = 8;
 
-// Recurrent kernel: 0 = tcgen05 / tensor memory, 1 = warp-level MMA.
+// Recurrent kernel: 0 = tcgen05 / tensor memory, 1 = warp-level MMA,
+// 2 = hybrid (warp-MMA chain, output product on tcgen05).
 std::atomic<int> g_recur_impl{1};
 
-cudaError_t launch_recur(const kda::RecurParams &p, cudaStream_t s) {
-    return g_recur_impl.load() == 0 ? kda::launch_recurrent_tc(p, s) : kda::launch_recurrent(p, s);
+cudaError_t launch_recur(int impl, const kda::RecurParams &p, cudaStream_t s) {
+    if (impl == 0) return kda::launch_recurrent_tc(p, s);
+    if (impl == 2) return kda::launch_recurrent_hybrid(p, s);
+    return kda::launch_recurrent(p, s);
 }
 
 constexpr int64_t kMaxElems = int64_t(1) << 40;
@@ -138,6 +141,7 @@ kda_status init_device(int dev, DeviceState &st) {
     if (kda::configure_intra() != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_recurrent() != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_recurrent_tc() != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::configure_recurrent_hybrid() != cudaSuccess) return KDA_ERR_CUDA;
     st.ready = true;
     return KDA_OK;
 }
@@ -222,6 +226,9 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
     if (final_state != initial_state && overlap(final_state, ns, initial_state, ns))
         return KDA_ERR_ALIAS;
 
+    // one read of the kernel choice per call: the record layout depends on it
+    const int impl = g_recur_impl.load();
+
     // ---- device checks
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     int dev = -1;
@@ -298,11 +305,11 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
     uint8_t *rec = wsb + 256 + pl.off_bytes;
 
     if (pl.nseg == 1) {
-        kda::IntraParams ip{q, k, v, g, beta, rec, scale, st.err, geo};
+        kda::IntraParams ip{q, k, v, g, beta, rec, scale, impl == 2 ? 1 : 0, st.err, geo};
         rc = timed_launch(true, stream, [&] { return kda::launch_intra_chunk(ip, pl.max_chunks, stream); });
         if (rc != KDA_OK) return rc;
         kda::RecurParams rp{rec, initial_state, out, final_state, st.err, geo};
-        return timed_launch(false, stream, [&] { return launch_recur(rp, stream); });
+        return timed_launch(false, stream, [&] { return launch_recur(impl, rp, stream); });
     }
 
     // ---- segmented: intra-chunk work of segment j+1 overlaps the recurrent
@@ -341,7 +348,7 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
         uint8_t *slot = rec + (j & 1) * pl.slot_bytes;
         if (j >= 2 && cudaStreamWaitEvent(ws.s_intra, ev_recur[j - 2], 0) != cudaSuccess)
             return KDA_ERR_CUDA;
-        kda::IntraParams ip{q, k, v, g, beta, slot, scale, st.err, gj};
+        kda::IntraParams ip{q, k, v, g, beta, slot, scale, impl == 2 ? 1 : 0, st.err, gj};
         const int64_t items = B * static_cast<int64_t>(gj.seg_len);
         rc = timed_launch(true, ws.s_intra,
                           [&] { return kda::launch_intra_chunk(ip, items, ws.s_intra); });
@@ -352,7 +359,7 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
         const float *s_in = j == 0 ? initial_state : carry;
         float *s_out = j == pl.nseg - 1 ? final_state : carry;
         kda::RecurParams rp{slot, s_in, out, s_out, st.err, gj};
-        rc = timed_launch(false, ws.s_recur, [&] { return launch_recur(rp, ws.s_recur); });
+        rc = timed_launch(false, ws.s_recur, [&] { return launch_recur(impl, rp, ws.s_recur); });
         if (rc != KDA_OK) return rc;
         if (cudaEventRecord(ev_recur[j], ws.s_recur) != cudaSuccess) return KDA_ERR_CUDA;
     }
@@ -404,7 +411,7 @@ kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *cal
 }
 
 kda_status kda_set_recurrent_impl(int impl) {
-    if (impl != 0 && impl != 1) return KDA_ERR_BAD_SHAPE;
+    if (impl < 0 || impl > 2) return KDA_ERR_BAD_SHAPE;
     g_recur_impl.store(impl);
     return KDA_OK;
 }

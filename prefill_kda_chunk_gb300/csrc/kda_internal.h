@@ -36,6 +36,8 @@ struct IntraParams {
     const float *beta;         // [tokens, H]
     uint8_t *rec;              // chunk records [chunks, H, kRecBytes]
     float scale;               // output scale, folded into the record's Q e^G and P
+    int qg_tc;                 // 1: Q e^G in the tcgen05 operand layout of the hybrid
+                               //    recurrent kernel; 0: swizzled rows for ldmatrix
     int *err;                  // sticky per-device error word
     ChunkGeometry geo;
 };
@@ -53,6 +55,7 @@ struct RecurParams {
 cudaError_t configure_intra();
 cudaError_t configure_recurrent();
 cudaError_t configure_recurrent_tc();
+cudaError_t configure_recurrent_hybrid();
 
 cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t total_tokens,
                                    int32_t *chunk_off, int *call_flags, int *err,
@@ -60,5 +63,7 @@ cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t to
 cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStream_t stream);
 cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream);     // warp MMA
 cudaError_t launch_recurrent_tc(const RecurParams &p, cudaStream_t stream);  // tcgen05 / TMEM
+// warp-MMA chain with the output product on tcgen05; needs IntraParams::qg_tc = 1
+cudaError_t launch_recurrent_hybrid(const RecurParams &p, cudaStream_t stream);
 
 }  // namespace kda

@@ -175,6 +175,17 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     cp_async_wait_all();
     __syncwarp();
 
+    // byte offsets of this lane's two key pairs (2 lane, 2 lane + 1) in the
+    // tcgen05 layout of Q e^G (see kda_recurrent_hybrid.cu)
+    int qg_tc_off0, qg_tc_off1;
+    {
+        auto pair_off = [](int pr) {
+            const int j = pr & 7, kidx = 16 * (pr >> 3) + 2 * (2 * (j & 3) + (j >> 2));
+            return (kidx >> 3) * 128 + (kidx & 7) * 2;
+        };
+        qg_tc_off0 = pair_off(2 * lane);
+        qg_tc_off1 = pair_off(2 * lane + 1);
+    }
     // ---- gated operand tiles (in place for K e^G and scale Q e^G)
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -206,7 +217,15 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
         *reinterpret_cast<uint2 *>(sm.kg + off) = ukg;
         *reinterpret_cast<uint2 *>(sm.kn + off) = ukn;
         *reinterpret_cast<uint2 *>(sm.qg + off) = uqg;
-        __stcs(reinterpret_cast<uint2 *>(rec + kRecQg + off), uqg);
+        if (p.qg_tc) {
+            // K-major core matrices of 8 tokens x 8 keys; within a 16-key block
+            // key pair j goes to pair position 2 (j & 3) + (j >> 2)
+            const int rowoff = (r >> 3) * 2048 + (r & 7) * 16;
+            __stcs(reinterpret_cast<unsigned int *>(rec + kRecQg + qg_tc_off0 + rowoff), uqg.x);
+            __stcs(reinterpret_cast<unsigned int *>(rec + kRecQg + qg_tc_off1 + rowoff), uqg.y);
+        } else {
+            __stcs(reinterpret_cast<uint2 *>(rec + kRecQg + off), uqg);
+        }
         __stcs(reinterpret_cast<uint2 *>(rec + kRecKd + off), ukd);
     }
     __stcs(reinterpret_cast<float4 *>(rec + kRecGamma + 16 * lane),

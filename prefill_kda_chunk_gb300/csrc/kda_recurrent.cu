@@ -35,34 +35,6 @@ namespace {
 
 constexpr int kStages = 4;
 
-// register-only MMA (not volatile: free to schedule around other work)
-__device__ __forceinline__ void mma_r(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                      uint32_t b1) {
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};\n"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// (a, b) *= (x, y) as one packed fp32x2 multiply
-__device__ __forceinline__ void mul2(float &a, float &b, float x, float y) {
-    asm("{\n .reg .b64 t, u;\n mov.b64 t, {%0, %1};\n mov.b64 u, {%2, %3};\n"
-        " mul.rn.f32x2 t, t, u;\n mov.b64 {%0, %1}, t;\n}\n"
-        : "+f"(a), "+f"(b) : "f"(x), "f"(y));
-}
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
-                                          uint32_t r3) {
-    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
-                 "r"(r0), "r"(r1), "r"(r2), "r"(r3) : "memory");
-}
-
 template <int BV>
 struct RecurLayout {
     static constexpr int kWarps = BV / 16;          // consumer warps

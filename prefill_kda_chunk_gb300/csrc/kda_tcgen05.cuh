@@ -103,6 +103,22 @@ __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&r)[16]) {
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
+// ---- 16 lanes x 256 bits: the accumulator-fragment layout of mma.sync
+// m16n8. Thread t = 4 g + q holds (lane g, column 2q), (g, 2q + 1),
+// (g + 8, 2q), (g + 8, 2q + 1) of each 8-column block (lane offset in taddr).
+__device__ __forceinline__ void st_16x256b(uint32_t taddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                           uint32_t r3) {
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+__device__ __forceinline__ void ld_16x256b(uint32_t taddr, uint32_t &r0, uint32_t &r1,
+                                           uint32_t &r2, uint32_t &r3) {
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(taddr));
+}
+
 __device__ __forceinline__ void st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }

@@ -27,8 +27,9 @@ def built():
     K.lib()
 
 
-# every test runs with both recurrent kernels: 0 = tcgen05 / tensor memory, 1 = warp MMA
-@pytest.fixture(autouse=True, params=[0, 1], ids=["tcgen05", "warp_mma"])
+# every test runs with each recurrent kernel: 0 = tcgen05 / tensor memory, 1 = warp MMA,
+# 2 = hybrid (warp-MMA chain, output product on tcgen05)
+@pytest.fixture(autouse=True, params=[0, 1, 2], ids=["tcgen05", "warp_mma", "hybrid"])
 def recurrent_impl(request, built):
     assert K.kda_set_recurrent_impl(request.param) == 0
     yield request.param
