@@ -39,7 +39,7 @@ STATE_BYTES = 128 * 128 * 4
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=KI.HEADLINE, choices=KI.WORKLOAD_ORDER)
@@ -301,49 +301,93 @@ def main():
     if rc != 0 or ncalls != args.steps:
         raise RuntimeError(f"stage timing failed ({rc}, {ncalls} calls)")
 
-    # end to end: pinned host inputs copied in, result copied out, every step
+    # end to end: every step copies its inputs in from pinned host memory and its
+    # results (o and the final state) back out. Steps are pipelined the way a
+    # serving loop would run them: two device buffer sets, inputs of step i+1
+    # copied in on two copy streams while step i computes and is read back.
     e2e = None
     if not args.no_e2e:
-        hin = {n: d[n].pin_memory() for n in ("q", "k", "v", "g", "beta")}
+        names = ("q", "k", "v", "g", "beta")
+        hin = {n: d[n].pin_memory() for n in names}
         hs0 = None if s0 is None else d["initial_state"].pin_memory()
         hcu = d["cu_seqlens"].pin_memory() if w.varlen else None
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        hfin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
-        dbuf = {n: torch.empty_like(x[n]) for n in x}
-        ds0 = None if s0 is None else torch.empty_like(s0)
-        dcu = None if cu is None else torch.empty_like(cu)
+        nb = 2
+        dset = [{n: torch.empty_like(x[n]) for n in names} for _ in range(nb)]
+        ds0 = [None if s0 is None else torch.empty_like(s0) for _ in range(nb)]
+        dcu = [None if cu is None else torch.empty_like(cu) for _ in range(nb)]
+        dout = [torch.empty_like(out) for _ in range(nb)]
+        dfin = [torch.empty_like(fin) for _ in range(nb)]
+        hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(nb)]
+        hfin = [torch.empty(fin.shape, dtype=fin.dtype).pin_memory() for _ in range(nb)]
         h2d = sum(t.numel() * t.element_size() for t in hin.values())
         h2d += 0 if hs0 is None else hs0.numel() * 4
         h2d += 0 if hcu is None else hcu.numel() * 4
-        d2h = hout.numel() * 2 + hfin.numel() * 4
+        d2h = out.numel() * 2 + fin.numel() * 4
+        # the two copy-in streams take about half of the input bytes each
+        groups = (("g", "beta"), ("q", "k", "v"))
+        s_in = [torch.cuda.Stream(dev) for _ in groups]
+        s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev = lambda: torch.cuda.Event()
+        in_done = [[ev() for _ in range(nb)] for _ in groups]
+        cmp_done = [ev() for _ in range(nb)]
+        out_done = [ev() for _ in range(nb)]
+        used = [False] * nb
 
-        def e2e_step():
-            for n in dbuf:
-                dbuf[n].copy_(hin[n], non_blocking=True)
-            if ds0 is not None:
-                ds0.copy_(hs0, non_blocking=True)
-            if dcu is not None:
-                dcu.copy_(hcu, non_blocking=True)
-            call(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], ds0, dcu, out)
-            hout.copy_(out, non_blocking=True)
-            hfin.copy_(fin, non_blocking=True)
+        def e2e_step(i):
+            b = i % nb
+            for j, grp in enumerate(groups):
+                st = s_in[j]
+                if used[b]:
+                    st.wait_event(cmp_done[b])        # buffer set b is no longer read
+                with torch.cuda.stream(st):
+                    for n in grp:
+                        dset[b][n].copy_(hin[n], non_blocking=True)
+                    if j == 0 and ds0[b] is not None:
+                        ds0[b].copy_(hs0, non_blocking=True)
+                    if j == 0 and dcu[b] is not None:
+                        dcu[b].copy_(hcu, non_blocking=True)
+                in_done[j][b].record(st)
+            for j in range(len(groups)):
+                s_cmp.wait_event(in_done[j][b])
+            if used[b]:
+                s_cmp.wait_event(out_done[b])         # o / state of step i-2 are read back
+            with torch.cuda.stream(s_cmp):
+                K.chunk_prefill(dset[b]["q"], dset[b]["k"], dset[b]["v"], dset[b]["g"],
+                                dset[b]["beta"], initial_state=ds0[b], cu_seqlens=dcu[b],
+                                scale=d["scale"], out=dout[b], final_state=dfin[b])
+            cmp_done[b].record(s_cmp)
+            s_out.wait_event(cmp_done[b])
+            with torch.cuda.stream(s_out):
+                hout[b].copy_(dout[b], non_blocking=True)
+                hfin[b].copy_(dfin[b], non_blocking=True)
+            out_done[b].record(s_out)
+            used[b] = True
 
-        for _ in range(2):
-            e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize(dev)
         barrier(world)
         es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e2e_steps = max(3, min(args.steps, 20))
         es.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        for st in (*s_in, s_cmp, s_out):
+            st.wait_event(es)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        for st in (*s_in, s_cmp, s_out):
+            stream.wait_stream(st)
         ee.record(stream)
         torch.cuda.synchronize(dev)
         barrier(world)
         K.check_device_error()
+        # the last step's results must match the resident run's
+        if not (torch.equal(hout[(e2e_steps - 1) % nb], out.cpu())
+                and torch.equal(hfin[(e2e_steps - 1) % nb], fin.cpu())):
+            raise RuntimeError("end-to-end run differs from the resident run")
         ems = max_over_ranks(es.elapsed_time(ee), world)
         e2e = {"value": world * cnt["tokens"] * e2e_steps / (ems / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "pipelined": "2 buffer sets; copies of step i+1 overlap step i"}
 
     if rank != 0:
         return
