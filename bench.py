@@ -39,7 +39,9 @@ STATE_BYTES = 128 * 128 * 4
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 2000 for the CUDA path, about 1 s on the headline "
+                         "workload; 50 for the reference arm)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=KI.HEADLINE, choices=KI.WORKLOAD_ORDER)
@@ -50,7 +52,10 @@ def parse():
                          "(library default if unset)")
     ap.add_argument("--ring-slot-mb", type=float, default=None,
                     help="ring-slot size for segmented calls (library default if unset; <0 off)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 2000 if args.impl == "ours" else 50
+    return args
 
 
 def dist_setup():
