@@ -50,6 +50,10 @@ def parse():
     ap.add_argument("--recurrent-impl", type=int, default=None,
                     help="0 = tcgen05 recurrent kernel, 1 = warp-MMA kernel, 2 = hybrid "
                          "(library default if unset)")
+    ap.add_argument("--decode", default=None, metavar="NxH",
+                    help="time the one-token decode step instead (e.g. 256x64) and print its line")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="leave the decode measurement out of the default line")
     ap.add_argument("--ring-slot-mb", type=float, default=None,
                     help="ring-slot size for segmented calls (library default if unset; <0 off)")
     args = ap.parse_args()
@@ -244,6 +248,38 @@ def cpu_baseline(w, d):
             "sample": f"{Hs} of {w.H} heads x {w.T} tokens, {dt:.2f} s wall"}
 
 
+DECODE_BYTES = 4 * 256 + 512 + 4 + 2 * 128 * 128 * 4   # per (sequence, head): q k v o, g, beta, S in+out
+
+
+def bench_decode(K, dev, N, H, steps, warmup, hbm):
+    """Decode steps in place on a resident batch (state > L2), CUDA events."""
+    d = KI.make_case([1] * N, H=H, seed=9, init_state=True)
+    x = {n: d[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+    state = d["initial_state"].to(dev)
+    out = torch.empty_like(x["v"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        K.decode_step(x["q"], x["k"], x["v"], x["g"], x["beta"], state=state, scale=d["scale"],
+                      out=out, in_place=True)
+
+    for _ in range(max(warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / steps
+    gbs = N * H * DECODE_BYTES / (ms / 1e3) / 1e9
+    return {"workload": f"decode_N{N}_H{H}", "tokens_per_s": N / (ms / 1e3),
+            "token_heads_per_s": N * H / (ms / 1e3), "us_per_step": 1e3 * ms, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "bytes_per_step": N * H * DECODE_BYTES}}
+
+
 def main():
     args = parse()
     rank, world, local = dist_setup()
@@ -264,6 +300,17 @@ def main():
         K.kda_set_ring_slot_bytes(int(args.ring_slot_mb * (1 << 20)) if args.ring_slot_mb >= 0 else -1)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.decode:
+        Nd, Hd = (int(v) for v in args.decode.lower().split("x"))
+        hbm, _, _ = load_peaks()
+        r = bench_decode(K, dev, Nd, Hd, min(args.steps, 500), args.warmup, hbm)
+        if rank == 0:
+            print(json.dumps({"metric": f"KDA decode tokens/s (one token per sequence, N={Nd}, "
+                                        f"H={Hd}, D=128) on 1 GB300",
+                              "value": world * r["tokens_per_s"], "unit": "tokens/s",
+                              "n_gpus": world, "higher_is_better": True, "dtype": "bf16",
+                              "data": "synthetic", **r}), flush=True)
+        return
 
     w = KI.WORKLOADS[args.workload]
     d = KI.make_inputs(w)
@@ -438,6 +485,8 @@ def main():
             "config": config_of(w, d), "roofline": roof, "path_roofline": path_roof,
             "kernels": kernels, "gpu_launches": args.steps * (2 + int(w.varlen)),
             "clocks": clk, "e2e": e2e}
+    if not args.no_decode:
+        line["decode"] = bench_decode(K, dev, 256, 64, 200, args.warmup, hbm)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(w, d)
     print(json.dumps(line), flush=True)

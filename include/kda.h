@@ -139,6 +139,37 @@ KDA_API kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const
                                              float scale, void *out, float *final_state,
                                              void *stream);
 
+/*
+ * kda_decode_step -- one new token for each of N sequences: the KDA state
+ * update applied once per (sequence, head). The pages describe the state as
+ * fixed-size and updated for every new token ("Kimi K3 的三個系統設計",
+ * section 第一個設計); this is that step, batched:
+ *
+ *   S <- (I - beta k k^T) Diag(exp(g)) S + beta k v^T,   o = scale * S^T q
+ *
+ * with the post-update S, exactly the prefill recurrence at T = 1.
+ *
+ *   q, k, v      bf16 [N, H, 128], device, 16-byte aligned
+ *   g            fp32 [N, H, 128] per-token log decay (any value; the
+ *                exponentials are exact per channel, no range limit)
+ *   beta         fp32 [N, H]
+ *   state_in     fp32 [N, H, 128 (K), 128 (V)] or NULL (zero state)
+ *   state_out    fp32 [N, H, 128, 128], written; may be state_in itself
+ *                (in place) but may not overlap it otherwise
+ *   N, H         sequences and heads (N * H < 2^31); K = V = 128 only
+ *   out          bf16 [N, H, 128], written; may not overlap any input or state
+ *   stream       cudaStream_t (NULL = legacy default stream)
+ *
+ * Allocates nothing and reads no workspace: each (sequence, head) is one CTA
+ * that reads its state once and writes it once. Returns KDA_OK once the work
+ * is enqueued, or a synchronous error (the outputs are then untouched). It
+ * has no device-side error conditions.
+ */
+KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
+                                   const float *beta, const float *state_in, float *state_out,
+                                   int64_t N, int64_t H, int64_t K, int64_t V, float scale,
+                                   void *out, void *stream);
+
 /* Static text for a status code (never NULL). */
 KDA_API const char *kda_status_string(kda_status status);
 

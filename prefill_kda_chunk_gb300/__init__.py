@@ -10,6 +10,8 @@ from ._binding import (  # noqa: F401
     KdaError,
     check_device_error,
     chunk_prefill,
+    decode_step,
+    kda_decode_step,
     kda_build_info,
     kda_chunk_prefill,
     kda_chunk_prefill_noalloc,

@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
             L.kda_chunk_prefill.argtypes = [vp] * 7 + [i64] * 6 + [f32, vp, vp, vp]
             L.kda_chunk_prefill_noalloc.restype = ctypes.c_int
             L.kda_chunk_prefill_noalloc.argtypes = [vp] * 7 + [i64] * 6 + [f32, vp, vp, vp]
+            L.kda_decode_step.restype = ctypes.c_int
+            L.kda_decode_step.argtypes = [vp] * 7 + [i64] * 4 + [f32, vp, vp]
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_status_string.argtypes = [ctypes.c_int]
             L.kda_last_device_error.restype = ctypes.c_int
@@ -89,6 +91,13 @@ def kda_chunk_prefill_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, B, T,
     library), pointers as ints. Returns the status."""
     return lib().kda_chunk_prefill_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H,
                                            K, V, N, scale, out, final_state, stream)
+
+
+def kda_decode_step(q, k, v, g, beta, state_in, state_out, N, H, K, V, scale, out,
+                    stream) -> int:
+    """The one-token decode C entry point, pointers as ints (0 = NULL)."""
+    return lib().kda_decode_step(q, k, v, g, beta, state_in, state_out, N, H, K, V, scale, out,
+                                 stream)
 
 
 def kda_status_string(code: int) -> str:
@@ -195,6 +204,55 @@ def chunk_prefill(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=N
     if rc != 0:
         raise KdaError(rc, "kda_chunk_prefill")
     return out, final_state
+
+
+def decode_step(q, k, v, g, beta, state=None, scale=None, out=None, state_out=None,
+                in_place=False, stream=None):
+    """One decode token per sequence on the current CUDA device.
+
+    q, k, v: bf16 [N, H, 128]; g: fp32 [N, H, 128]; beta: fp32 [N, H];
+    state: fp32 [N, H, 128, 128] or None (zero state). Returns (o, new_state).
+    With in_place=True the new state is written over `state`.
+    """
+    import torch
+
+    if q.dim() != 3:
+        raise ValueError("q must be [N, H, K]")
+    N, H, K = q.shape
+    V = v.shape[-1]
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("g", g, torch.float32),
+                        ("beta", beta, torch.float32)):
+        if t.dtype != dt:
+            raise ValueError(f"{name} must be {dt}")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:-1] != q.shape[:-1]:
+        raise ValueError("q, k, g must share a shape and v must match it but for the last dim")
+    if tuple(beta.shape) != (N, H):
+        raise ValueError("beta must be [N, H]")
+    if state is not None:
+        if state.dtype != torch.float32 or not state.is_contiguous():
+            raise ValueError("state must be a contiguous fp32 tensor")
+        if tuple(state.shape) != (N, H, K, V):
+            raise ValueError(f"state must be [{N}, {H}, {K}, {V}]")
+    if in_place:
+        if state is None:
+            raise ValueError("in_place needs a state")
+        state_out = state
+    elif state_out is None:
+        state_out = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(K)
+    if out is None:
+        out = torch.empty_like(v)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                         _ptr(state_out), N, H, K, V, float(scale), _ptr(out), stream)
+    if rc != 0:
+        raise KdaError(rc, "kda_decode_step")
+    return out, state_out
 
 
 def check_device_error(stream=None):

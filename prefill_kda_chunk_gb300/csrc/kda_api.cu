@@ -186,6 +186,63 @@ const char *kda_status_string(kda_status s) {
     return "unknown status";
 }
 
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
+                           const float *beta, const float *state_in, float *state_out, int64_t N,
+                           int64_t H, int64_t K, int64_t V, float scale, void *out,
+                           void *stream_) {
+    // ---- checks that need no GPU
+    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_DIM;
+    if (N < 0 || H < 1 || H > (int64_t(1) << 24) || N > ((int64_t(1) << 31) - 1) / H)
+        return KDA_ERR_BAD_SHAPE;
+    const int64_t units = N * H;
+    if (units > 0 && (!q || !k || !v || !g || !beta || !out || !state_out))
+        return KDA_ERR_NULL_ARG;
+    if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(g, 16) ||
+        misaligned(out, 16) || misaligned(state_in, 16) || misaligned(state_out, 16) ||
+        misaligned(beta, 4))
+        return KDA_ERR_MISALIGNED;
+    const int64_t nqkv = units * 128 * 2, ng = units * 128 * 4, nb = units * 4;
+    const int64_t ns = units * 128 * 128 * 4;
+    const void *ins[] = {q, k, v, g, beta};
+    const int64_t nins[] = {nqkv, nqkv, nqkv, ng, nb};
+    for (int i = 0; i < 5; ++i) {
+        if (overlap(out, nqkv, ins[i], nins[i])) return KDA_ERR_ALIAS;
+        if (overlap(state_out, ns, ins[i], nins[i])) return KDA_ERR_ALIAS;
+    }
+    if (overlap(out, nqkv, state_in, ns) || overlap(out, nqkv, state_out, ns))
+        return KDA_ERR_ALIAS;
+    if (state_out != state_in && overlap(state_out, ns, state_in, ns)) return KDA_ERR_ALIAS;
+    if (units == 0) return KDA_OK;   // an empty batch enqueues nothing
+
+    // ---- device checks
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_devices[dev];
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return KDA_ERR_CUDA;
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
+    if (!st.ready) {
+        if (capturing) return KDA_ERR_CAPTURE;
+        const kda_status rc = init_device(dev, st);
+        if (rc != KDA_OK) return rc;
+    }
+    if (stream != nullptr && !capturing) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return KDA_ERR_CUDA;
+        if (sdev != dev) return KDA_ERR_WRONG_DEVICE;
+    }
+    const void *ptrs[] = {q, k, v, g, beta, state_in, state_out, out};
+    for (const void *ptr : ptrs) {
+        if (capturing) break;  // pointer queries are not stream work
+        const kda_status rc = check_pointer_device(ptr, dev);
+        if (rc != KDA_OK) return rc;
+    }
+    const kda::DecodeParams p{q, k, v, g, beta, state_in, state_out, out, scale};
+    return kda::launch_decode(p, units, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 const char *kda_build_info(void) {
     return "prefill_kda_chunk_gb300 0.1 (sm_103a; intra-chunk mma.sync + recurrent mma.sync, "
            "bulk-async staged)";

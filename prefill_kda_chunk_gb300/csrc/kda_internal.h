@@ -51,6 +51,17 @@ struct RecurParams {
     ChunkGeometry geo;
 };
 
+// One-token decode step for N*H independent (sequence, head) units.
+struct DecodeParams {
+    const void *q, *k, *v;     // bf16 [N, H, 128]
+    const float *g;            // [N, H, 128] per-token log decay
+    const float *beta;         // [N, H]
+    const float *s_in;         // [N, H, 128, 128] or nullptr (zero state)
+    float *s_out;              // [N, H, 128, 128]; may be s_in itself
+    void *out;                 // bf16 [N, H, 128]
+    float scale;
+};
+
 // Per-device, once: raise the dynamic shared-memory limits of the kernels.
 cudaError_t configure_intra();
 cudaError_t configure_recurrent();
@@ -65,5 +76,6 @@ cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream);     // 
 cudaError_t launch_recurrent_tc(const RecurParams &p, cudaStream_t stream);  // tcgen05 / TMEM
 // warp-MMA chain with the output product on tcgen05; needs IntraParams::qg_tc = 1
 cudaError_t launch_recurrent_hybrid(const RecurParams &p, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams &p, int64_t units, cudaStream_t stream);
 
 }  // namespace kda

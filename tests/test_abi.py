@@ -92,3 +92,37 @@ def call(**kw):
 ])
 def test_host_validation_rejects(lib, kw, code):
     assert call(**kw) == K.STATUS_CODE[code]
+
+
+def decode_call(**kw):
+    args = dict(q=A, k=A + 0x100000, v=A + 0x200000, g=A + 0x300000, beta=A + 0x400000,
+                state_in=A + 0x800000, state_out=A + 0x800000, N=2, H=3, K=128, V=128,
+                scale=1.0, out=A + 0x500000, stream=0)
+    args.update(kw)
+    return K.kda_decode_step(**args)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), "KDA_ERR_NULL_ARG"),
+    (dict(state_out=0), "KDA_ERR_NULL_ARG"),
+    (dict(out=0), "KDA_ERR_NULL_ARG"),
+    (dict(K=64), "KDA_ERR_UNSUPPORTED_DIM"),
+    (dict(V=64), "KDA_ERR_UNSUPPORTED_DIM"),
+    (dict(H=0), "KDA_ERR_BAD_SHAPE"),
+    (dict(N=-1), "KDA_ERR_BAD_SHAPE"),
+    (dict(N=1 << 30, H=4), "KDA_ERR_BAD_SHAPE"),
+    (dict(k=A + 0x100002), "KDA_ERR_MISALIGNED"),
+    (dict(state_in=A + 0x800004, state_out=A + 0x900000), "KDA_ERR_MISALIGNED"),
+    (dict(beta=A + 0x400001), "KDA_ERR_MISALIGNED"),
+    (dict(out=A + 0x100000), "KDA_ERR_ALIAS"),
+    (dict(out=A + 0x800000 + 256), "KDA_ERR_ALIAS"),
+    (dict(state_out=A + 0x300000), "KDA_ERR_ALIAS"),
+    (dict(state_out=A + 0x800000 + 4096), "KDA_ERR_ALIAS"),
+])
+def test_decode_host_validation_rejects(lib, kw, code):
+    assert decode_call(**kw) == K.STATUS_CODE[code]
+
+
+def test_decode_empty_batch_is_a_no_op(lib):
+    # N = 0: nothing to do, and no pointer is needed
+    assert K.kda_decode_step(0, 0, 0, 0, 0, 0, 0, 0, 4, 128, 128, 1.0, 0, 0) == 0
