@@ -52,6 +52,9 @@ def parse():
                          "(library default if unset)")
     ap.add_argument("--decode", default=None, metavar="NxH",
                     help="time the one-token decode step instead (e.g. 256x64) and print its line")
+    ap.add_argument("--preprocess", action="store_true",
+                    help="run the prefill with the in-kernel input preprocessing on (q/k "
+                         "normalisation, g read as gate logits): the same inputs, for timing")
     ap.add_argument("--no-decode", action="store_true",
                     help="leave the decode measurement out of the default line")
     ap.add_argument("--ring-slot-mb", type=float, default=None,
@@ -325,7 +328,8 @@ def main():
 
     def call(q=x["q"], k=x["k"], v=x["v"], g=x["g"], beta=x["beta"], s0=s0, cu=cu, out=out):
         K.chunk_prefill(q, k, v, g, beta, initial_state=s0, cu_seqlens=cu, scale=d["scale"],
-                        out=out, final_state=fin)
+                        out=out, final_state=fin, normalize_qk=args.preprocess,
+                        gate_logits=args.preprocess)
 
     clocks = ClockSampler(dev)
     clocks.start()
@@ -406,7 +410,8 @@ def main():
             with torch.cuda.stream(s_cmp):
                 K.chunk_prefill(dset[b]["q"], dset[b]["k"], dset[b]["v"], dset[b]["g"],
                                 dset[b]["beta"], initial_state=ds0[b], cu_seqlens=dcu[b],
-                                scale=d["scale"], out=dout[b], final_state=dfin[b])
+                                scale=d["scale"], out=dout[b], final_state=dfin[b],
+                                normalize_qk=args.preprocess, gate_logits=args.preprocess)
             cmp_done[b].record(s_cmp)
             s_out.wait_event(cmp_done[b])
             with torch.cuda.stream(s_out):
@@ -482,7 +487,9 @@ def main():
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": config_of(w, d), "roofline": roof, "path_roofline": path_roof,
+            "config": dict(config_of(w, d), **({"preprocess": "q/k norm + gate logits in-kernel"}
+                                                if args.preprocess else {})),
+            "roofline": roof, "path_roofline": path_roof,
             "kernels": kernels, "gpu_launches": args.steps * (2 + int(w.varlen)),
             "clocks": clk, "e2e": e2e}
     if not args.no_decode:

@@ -59,9 +59,22 @@ typedef enum {
     KDA_ERR_CAPTURE = -11,          /* workspace must grow while the stream is capturing */
     KDA_ERR_WRONG_DEVICE = -12,     /* a buffer or the stream belongs to another device */
     KDA_ERR_NOT_DEVICE_MEMORY = -13, /* a pointer is not CUDA device (or managed) memory */
-    KDA_ERR_SCRATCH_LIMIT = -14     /* kda_chunk_prefill_noalloc: the call needs more scratch
+    KDA_ERR_SCRATCH_LIMIT = -14,    /* kda_chunk_prefill_noalloc: the call needs more scratch
                                        than its fixed 64 MiB array holds */
+    KDA_ERR_BAD_FLAGS = -15         /* a preprocessing flag bit this library does not know */
 } kda_status;
+
+/*
+ * Input preprocessing done inside the kernels (the `flags` argument of
+ * kda_chunk_prefill_ex and kda_decode_step). The pages leave the production
+ * of q, k and g to the model; these let a caller hand over raw projections and
+ * skip a separate pass over them.
+ *   KDA_PRE_NORM_QK      q and k are raw: the kernels use x / sqrt(sum x^2 + 1e-6)
+ *                        over the 128 channels of each (token, head)
+ *   KDA_PRE_GATE_LOGITS  g holds gate logits x: the per-token log decay is
+ *                        logsigmoid(x) = -log(1 + exp(-x))
+ */
+enum { KDA_PRE_NORM_QK = 1, KDA_PRE_GATE_LOGITS = 2 };
 
 /*
  * kda_chunk_prefill -- chunked KDA prefill over a batch of sequences.
@@ -115,6 +128,20 @@ KDA_API kda_status kda_chunk_prefill(const void *q, const void *k, const void *v
                              float *final_state, void *stream);
 
 /*
+ * kda_chunk_prefill_ex -- kda_chunk_prefill with input preprocessing:
+ * `flags` is a bitwise OR of KDA_PRE_* (0 = kda_chunk_prefill exactly). An
+ * unknown bit returns KDA_ERR_BAD_FLAGS. Everything else, including the
+ * gate-range precondition on the resulting log decays, is as for
+ * kda_chunk_prefill.
+ */
+KDA_API kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v,
+                                        const float *g, const float *beta,
+                                        const float *initial_state, const int32_t *cu_seqlens,
+                                        int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                                        int64_t N, float scale, int flags, void *out,
+                                        float *final_state, void *stream);
+
+/*
  * kda_chunk_prefill_noalloc -- the same computation, arguments and results
  * as kda_chunk_prefill, for callers that cannot allocate device memory.
  * The pages have no counterpart to this entry point; it exists for users of
@@ -157,6 +184,8 @@ KDA_API kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const
  *   state_out    fp32 [N, H, 128, 128], written; may be state_in itself
  *                (in place) but may not overlap it otherwise
  *   N, H         sequences and heads (N * H < 2^31); K = V = 128 only
+ *   flags        KDA_PRE_* bits (0: q, k, g used as given), as for
+ *                kda_chunk_prefill_ex
  *   out          bf16 [N, H, 128], written; may not overlap any input or state
  *   stream       cudaStream_t (NULL = legacy default stream)
  *
@@ -168,7 +197,7 @@ KDA_API kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const
 KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
                                    const float *beta, const float *state_in, float *state_out,
                                    int64_t N, int64_t H, int64_t K, int64_t V, float scale,
-                                   void *out, void *stream);
+                                   int flags, void *out, void *stream);
 
 /* Static text for a status code (never NULL). */
 KDA_API const char *kda_status_string(kda_status status);

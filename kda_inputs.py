@@ -138,3 +138,30 @@ def make_case(seqlens: Sequence[int], H: int, seed: int, init_state: bool = Fals
     w = Workload(f"case_{seed}", seed=seed, T=sum(lens), H=H, n_seqs=len(lens),
                  varlen=len(lens) > 1, init_state=init_state, mu=mu, seqlens=tuple(lens))
     return make_inputs(w)
+
+
+def make_raw_case(seqlens: Sequence[int], H: int, seed: int, init_state: bool = False,
+                  mu: float = 3.0) -> dict:
+    """Like ``make_case`` but with raw projections, for the kernels' input
+    preprocessing: q and k are N(0, 1) rows times a per-(token, head) factor
+    drawn uniformly from [0.25, 4] (not normalised), rounded to bf16, and g
+    holds the gate logits x ~ N(mu, 1) themselves. v, beta, the initial state
+    and cu_seqlens are drawn as in ``make_inputs``."""
+    lens = [int(L) for L in seqlens]
+    T = sum(lens)
+    gen = torch.Generator().manual_seed(seed)
+    q = torch.randn(T, H, D, generator=gen, dtype=torch.float32)
+    k = torch.randn(T, H, D, generator=gen, dtype=torch.float32)
+    v = torch.randn(T, H, D, generator=gen, dtype=torch.float32)
+    xg = torch.randn(T, H, D, generator=gen, dtype=torch.float32) + mu
+    xb = torch.randn(T, H, generator=gen, dtype=torch.float32)
+    s0 = None
+    if init_state:
+        s0 = torch.randn(len(lens), H, D, D, generator=gen, dtype=torch.float32) * 0.02
+    fq = 0.25 + 3.75 * torch.rand(T, H, 1, generator=gen)
+    fk = 0.25 + 3.75 * torch.rand(T, H, 1, generator=gen)
+    cu = torch.zeros(len(lens) + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    return dict(q=(q * fq).to(torch.bfloat16), k=(k * fk).to(torch.bfloat16),
+                v=v.to(torch.bfloat16), g=xg, beta=torch.sigmoid(xb), initial_state=s0,
+                cu_seqlens=cu, seqlens=lens, scale=1.0 / math.sqrt(D))

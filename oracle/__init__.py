@@ -73,7 +73,7 @@ def _load():
             i64 = ctypes.c_int64
             lib.kda_oracle_recurrent.restype = ctypes.c_int
             lib.kda_oracle_recurrent.argtypes = [f32p] * 5 + [f64p, i64p] + [i64] * 4 + [
-                ctypes.c_double, f64p, i64, f64p, ctypes.c_int, ctypes.c_int]
+                ctypes.c_double, f64p, i64, f64p, ctypes.c_int, ctypes.c_int, ctypes.c_int]
             lib.kda_oracle_chunked.restype = ctypes.c_int
             lib.kda_oracle_chunked.argtypes = [f32p] * 5 + [f64p, i64p] + [i64] * 5 + [
                 ctypes.c_double, f64p, i64, f64p, ctypes.c_int]
@@ -127,9 +127,13 @@ def _prep(q, k, v, g, beta, initial_state, cu_seqlens):
 
 
 def recurrent(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
-              out_tokens=None, threads=0, mutation=0):
+              out_tokens=None, threads=0, mutation=0, normalize_qk=False, gate_logits=False):
     """Token-by-token fp64 recurrence. Returns (o [T, H, V], final [N, H, K, V])
     as float64 numpy arrays; o rows at or past ``out_tokens`` are left zero.
+
+    ``normalize_qk``: q and k are raw and are divided by sqrt(sum x^2 + 1e-6)
+    per (token, head) before use. ``gate_logits``: g holds gate logits x and
+    the log decay is logsigmoid(x). Both are done in fp64 inside the oracle.
 
     ``mutation`` plants a known mistake (see kda_recurrent.c); only the pin
     tests use it, to show that each pin catches what it should."""
@@ -143,7 +147,8 @@ def recurrent(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
         _ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float), _ptr(v, ctypes.c_float),
         _ptr(g, ctypes.c_float), _ptr(beta, ctypes.c_float), _ptr(s0, ctypes.c_double),
         _ptr(cu, ctypes.c_int64), N, H, K, V, float(scale), _ptr(o, ctypes.c_double), ot,
-        _ptr(fs, ctypes.c_double), int(threads), int(mutation))
+        _ptr(fs, ctypes.c_double), int(threads),
+        (1 if normalize_qk else 0) | (2 if gate_logits else 0), int(mutation))
     if rc:
         raise RuntimeError(f"kda_oracle_recurrent failed ({rc})")
     return o, fs

@@ -28,6 +28,12 @@
  * out [out_tokens, H, V] (only tokens t < out_tokens are written);
  * final_state [N, H, K, V].
  *
+ * `flags` asks for the input preprocessing that the library can do inside
+ * its kernels (the pages leave the production of q, k and g to the model, so
+ * these are readings, not page text): bit 1 = q and k are raw, use
+ * x / sqrt(sum_i x_i^2 + 1e-6) per (token, head); bit 2 = g holds gate
+ * logits x, use the log decay logsigmoid(x) = -log(1 + exp(-x)).
+ *
  * `mutation` plants a known mistake (0 = none). It exists so the pin tests
  * can show that each pin catches the mistakes it is meant to catch:
  *   1: o_t from the pre-update state S_{t-1}
@@ -51,11 +57,27 @@ typedef struct {
     int64_t N, H, K, V, out_tokens;
     double scale;
     double *out, *final_state;
+    int flags;
     int mutation;
     int64_t next;
     pthread_mutex_t mu;
     int err;
 } rec_ctx;
+
+/* logsigmoid(x) = -log(1 + e^-x), written so that neither branch overflows */
+static double log_sigmoid(double x)
+{
+    return x >= 0.0 ? -log1p(exp(-x)) : x - log1p(exp(x));
+}
+
+/* 1 / sqrt(sum x_i^2 + 1e-6), or 1 when the inputs are used as given */
+static double inv_norm(const float *x, int64_t n, int on)
+{
+    if (!on) return 1.0;
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; ++i) ss += (double)x[i] * (double)x[i];
+    return 1.0 / sqrt(ss + 1e-6);
+}
 
 static void rec_one(rec_ctx *c, int64_t n, int64_t h, double *S, double *kS, double *dec)
 {
@@ -72,15 +94,17 @@ static void rec_one(rec_ctx *c, int64_t n, int64_t h, double *S, double *kS, dou
         const float *gt = c->g + (t * H + h) * K;
         const float *vt = c->v + (t * H + h) * V;
         const double b = (double)c->beta[t * H + h];
+        const double rq = inv_norm(qt, K, c->flags & 1), rk = inv_norm(kt, K, c->flags & 1);
 
-        for (int64_t i = 0; i < K; ++i) dec[i] = exp((double)gt[i]);
+        for (int64_t i = 0; i < K; ++i)
+            dec[i] = exp((c->flags & 2) ? log_sigmoid((double)gt[i]) : (double)gt[i]);
 
         /* pre-update output, for mutation 1 only */
         if (m == 1 && t < c->out_tokens) {
             double *ot = c->out + (t * H + h) * V;
             for (int64_t j = 0; j < V; ++j) {
                 double acc = 0.0;
-                for (int64_t i = 0; i < K; ++i) acc += S[i * V + j] * (double)qt[i];
+                for (int64_t i = 0; i < K; ++i) acc += S[i * V + j] * (double)qt[i] * rq;
                 ot[j] = c->scale * acc;
             }
         }
@@ -95,13 +119,13 @@ static void rec_one(rec_ctx *c, int64_t n, int64_t h, double *S, double *kS, dou
         /* kS = k_t^T S */
         for (int64_t j = 0; j < V; ++j) {
             double acc = 0.0;
-            for (int64_t i = 0; i < K; ++i) acc += (double)kt[i] * S[i * V + j];
+            for (int64_t i = 0; i < K; ++i) acc += (double)kt[i] * rk * S[i * V + j];
             kS[j] = acc;
         }
 
         /* S <- S - beta k (k^T S) + beta k v^T */
         for (int64_t i = 0; i < K; ++i) {
-            const double ki = (double)kt[i];
+            const double ki = (double)kt[i] * rk;
             for (int64_t j = 0; j < V; ++j) {
                 double erase = (m == 4) ? ki * kS[j] : b * ki * kS[j];
                 double write = b * ki * (double)vt[j];
@@ -122,7 +146,7 @@ static void rec_one(rec_ctx *c, int64_t n, int64_t h, double *S, double *kS, dou
             double *ot = c->out + (t * H + h) * V;
             for (int64_t j = 0; j < V; ++j) {
                 double acc = 0.0;
-                for (int64_t i = 0; i < K; ++i) acc += S[i * V + j] * (double)qt[i];
+                for (int64_t i = 0; i < K; ++i) acc += S[i * V + j] * (double)qt[i] * rq;
                 ot[j] = (m == 6) ? c->scale * c->scale * acc : c->scale * acc;
             }
         }
@@ -160,7 +184,7 @@ int kda_oracle_recurrent(const float *q, const float *k, const float *v, const f
                          const float *beta, const double *s0, const int64_t *cu,
                          int64_t N, int64_t H, int64_t K, int64_t V, double scale,
                          double *out, int64_t out_tokens, double *final_state,
-                         int n_threads, int mutation)
+                         int n_threads, int flags, int mutation)
 {
     if (!q || !k || !v || !g || !beta || !cu || N < 0 || H <= 0 || K <= 0 || V <= 0) return 1;
     if (out_tokens > 0 && !out) return 1;
@@ -173,6 +197,7 @@ int kda_oracle_recurrent(const float *q, const float *k, const float *v, const f
     c.q = q; c.k = k; c.v = v; c.g = g; c.beta = beta; c.s0 = s0; c.cu = cu;
     c.N = N; c.H = H; c.K = K; c.V = V; c.out_tokens = out ? out_tokens : 0;
     c.scale = scale; c.out = out; c.final_state = final_state; c.mutation = mutation;
+    c.flags = flags;
     pthread_mutex_init(&c.mu, NULL);
 
     int64_t work = N * H;

@@ -5,6 +5,8 @@ include/kda.h (libkda_gb300.so, built in-tree by ``build.build()``); this
 package is its thin Python binding.
 """
 from ._binding import (  # noqa: F401
+    PRE_GATE_LOGITS,
+    PRE_NORM_QK,
     STATUS,
     STATUS_CODE,
     KdaError,
@@ -14,6 +16,7 @@ from ._binding import (  # noqa: F401
     kda_decode_step,
     kda_build_info,
     kda_chunk_prefill,
+    kda_chunk_prefill_ex,
     kda_chunk_prefill_noalloc,
     kda_last_device_error,
     kda_set_recurrent_impl,

@@ -20,8 +20,11 @@ STATUS = {
     -4: "KDA_ERR_MISALIGNED", -5: "KDA_ERR_BAD_CU_SEQLENS", -6: "KDA_ERR_CUDA",
     -7: "KDA_ERR_DEVICE_TIMEOUT", -8: "KDA_ERR_NO_DEVICE_SUPPORT", -9: "KDA_ERR_ALIAS",
     -10: "KDA_ERR_GATE_RANGE", -11: "KDA_ERR_CAPTURE", -12: "KDA_ERR_WRONG_DEVICE",
-    -13: "KDA_ERR_NOT_DEVICE_MEMORY", -14: "KDA_ERR_SCRATCH_LIMIT",
+    -13: "KDA_ERR_NOT_DEVICE_MEMORY", -14: "KDA_ERR_SCRATCH_LIMIT", -15: "KDA_ERR_BAD_FLAGS",
 }
+# input preprocessing flags (include/kda.h)
+PRE_NORM_QK = 1
+PRE_GATE_LOGITS = 2
 STATUS_CODE = {v: k for k, v in STATUS.items()}
 
 _lib = None
@@ -48,10 +51,12 @@ def lib() -> ctypes.CDLL:
             vp, i64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
             L.kda_chunk_prefill.restype = ctypes.c_int
             L.kda_chunk_prefill.argtypes = [vp] * 7 + [i64] * 6 + [f32, vp, vp, vp]
+            L.kda_chunk_prefill_ex.restype = ctypes.c_int
+            L.kda_chunk_prefill_ex.argtypes = [vp] * 7 + [i64] * 6 + [f32, ctypes.c_int, vp, vp, vp]
             L.kda_chunk_prefill_noalloc.restype = ctypes.c_int
             L.kda_chunk_prefill_noalloc.argtypes = [vp] * 7 + [i64] * 6 + [f32, vp, vp, vp]
             L.kda_decode_step.restype = ctypes.c_int
-            L.kda_decode_step.argtypes = [vp] * 7 + [i64] * 4 + [f32, vp, vp]
+            L.kda_decode_step.argtypes = [vp] * 7 + [i64] * 4 + [f32, ctypes.c_int, vp, vp]
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_status_string.argtypes = [ctypes.c_int]
             L.kda_last_device_error.restype = ctypes.c_int
@@ -85,6 +90,13 @@ def kda_chunk_prefill(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V
                                    scale, out, final_state, stream)
 
 
+def kda_chunk_prefill_ex(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V, N, scale,
+                         flags, out, final_state, stream) -> int:
+    """The C entry point with input preprocessing flags (PRE_*)."""
+    return lib().kda_chunk_prefill_ex(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V,
+                                      N, scale, flags, out, final_state, stream)
+
+
 def kda_chunk_prefill_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V, N,
                               scale, out, final_state, stream) -> int:
     """The allocation-free C entry point (fixed 64 MiB scratch inside the
@@ -93,11 +105,11 @@ def kda_chunk_prefill_noalloc(q, k, v, g, beta, initial_state, cu_seqlens, B, T,
                                            K, V, N, scale, out, final_state, stream)
 
 
-def kda_decode_step(q, k, v, g, beta, state_in, state_out, N, H, K, V, scale, out,
+def kda_decode_step(q, k, v, g, beta, state_in, state_out, N, H, K, V, scale, flags, out,
                     stream) -> int:
     """The one-token decode C entry point, pointers as ints (0 = NULL)."""
-    return lib().kda_decode_step(q, k, v, g, beta, state_in, state_out, N, H, K, V, scale, out,
-                                 stream)
+    return lib().kda_decode_step(q, k, v, g, beta, state_in, state_out, N, H, K, V, scale, flags,
+                                 out, stream)
 
 
 def kda_status_string(code: int) -> str:
@@ -147,8 +159,13 @@ def _ptr(t):
     return 0 if t is None else t.data_ptr()
 
 
+def _flags(normalize_qk, gate_logits):
+    return (PRE_NORM_QK if normalize_qk else 0) | (PRE_GATE_LOGITS if gate_logits else 0)
+
+
 def chunk_prefill(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None, out=None,
-                  final_state=None, output_final_state=True, stream=None):
+                  final_state=None, output_final_state=True, stream=None, normalize_qk=False,
+                  gate_logits=False):
     """Chunked KDA prefill on the current CUDA device.
 
     q, k, v: bf16 [T, H, 128] (packed or one sequence) or [B, T, H, 128];
@@ -156,6 +173,9 @@ def chunk_prefill(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=N
     or None; cu_seqlens: int32 [N+1] on the device or None. Returns
     (o, final_state) with o bf16 like v and final_state fp32 [N, H, 128, 128]
     (None if output_final_state is False and final_state is None).
+    normalize_qk / gate_logits: q, k are raw projections to be L2-normalised,
+    and g holds gate logits whose logsigmoid is the log decay (done in the
+    kernels).
     """
     import torch
 
@@ -198,21 +218,28 @@ def chunk_prefill(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=N
         final_state = torch.empty((N, H, K, V), dtype=torch.float32, device=q.device)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
-    rc = kda_chunk_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(initial_state),
-                           _ptr(cu_seqlens), B, T, H, K, V, N, float(scale), _ptr(out),
-                           _ptr(final_state), stream)
+    flags = _flags(normalize_qk, gate_logits)
+    if flags:
+        rc = kda_chunk_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                  _ptr(initial_state), _ptr(cu_seqlens), B, T, H, K, V, N,
+                                  float(scale), flags, _ptr(out), _ptr(final_state), stream)
+    else:
+        rc = kda_chunk_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                               _ptr(initial_state), _ptr(cu_seqlens), B, T, H, K, V, N,
+                               float(scale), _ptr(out), _ptr(final_state), stream)
     if rc != 0:
         raise KdaError(rc, "kda_chunk_prefill")
     return out, final_state
 
 
 def decode_step(q, k, v, g, beta, state=None, scale=None, out=None, state_out=None,
-                in_place=False, stream=None):
+                in_place=False, stream=None, normalize_qk=False, gate_logits=False):
     """One decode token per sequence on the current CUDA device.
 
     q, k, v: bf16 [N, H, 128]; g: fp32 [N, H, 128]; beta: fp32 [N, H];
     state: fp32 [N, H, 128, 128] or None (zero state). Returns (o, new_state).
-    With in_place=True the new state is written over `state`.
+    With in_place=True the new state is written over `state`. normalize_qk /
+    gate_logits as for chunk_prefill.
     """
     import torch
 
@@ -249,7 +276,8 @@ def decode_step(q, k, v, g, beta, state=None, scale=None, out=None, state_out=No
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     rc = kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
-                         _ptr(state_out), N, H, K, V, float(scale), _ptr(out), stream)
+                         _ptr(state_out), N, H, K, V, float(scale),
+                         _flags(normalize_qk, gate_logits), _ptr(out), stream)
     if rc != 0:
         raise KdaError(rc, "kda_decode_step")
     return out, state_out

@@ -182,15 +182,17 @@ const char *kda_status_string(kda_status s) {
         case KDA_ERR_SCRATCH_LIMIT:
             return "the call needs more scratch than the fixed 64 MiB array of "
                    "kda_chunk_prefill_noalloc";
+        case KDA_ERR_BAD_FLAGS: return "an unknown preprocessing flag bit is set";
     }
     return "unknown status";
 }
 
 kda_status kda_decode_step(const void *q, const void *k, const void *v, const float *g,
                            const float *beta, const float *state_in, float *state_out, int64_t N,
-                           int64_t H, int64_t K, int64_t V, float scale, void *out,
+                           int64_t H, int64_t K, int64_t V, float scale, int flags, void *out,
                            void *stream_) {
     // ---- checks that need no GPU
+    if ((flags & ~(KDA_PRE_NORM_QK | KDA_PRE_GATE_LOGITS)) != 0) return KDA_ERR_BAD_FLAGS;
     if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_DIM;
     if (N < 0 || H < 1 || H > (int64_t(1) << 24) || N > ((int64_t(1) << 31) - 1) / H)
         return KDA_ERR_BAD_SHAPE;
@@ -239,7 +241,7 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
         const kda_status rc = check_pointer_device(ptr, dev);
         if (rc != KDA_OK) return rc;
     }
-    const kda::DecodeParams p{q, k, v, g, beta, state_in, state_out, out, scale};
+    const kda::DecodeParams p{q, k, v, g, beta, state_in, state_out, out, scale, flags};
     return kda::launch_decode(p, units, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -258,8 +260,18 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
                              const float *beta, const float *initial_state,
                              const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
                              int64_t K, int64_t V, int64_t N, float scale, void *out,
-                             float *final_state, void *stream_) {
+                             float *final_state, void *stream) {
+    return kda_chunk_prefill_ex(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V, N,
+                                scale, 0, out, final_state, stream);
+}
+
+kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, const float *g,
+                                const float *beta, const float *initial_state,
+                                const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
+                                int64_t K, int64_t V, int64_t N, float scale, int flags,
+                                void *out, float *final_state, void *stream_) {
     // ---- checks that need no GPU
+    if ((flags & ~(KDA_PRE_NORM_QK | KDA_PRE_GATE_LOGITS)) != 0) return KDA_ERR_BAD_FLAGS;
     if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_DIM;
     Plan pl;
     kda_status rc = plan_sizes(B, T, H, N, cu_seqlens != nullptr, &pl);
@@ -362,7 +374,7 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
     uint8_t *rec = wsb + 256 + pl.off_bytes;
 
     if (pl.nseg == 1) {
-        kda::IntraParams ip{q, k, v, g, beta, rec, scale, impl == 2 ? 1 : 0, st.err, geo};
+        kda::IntraParams ip{q, k, v, g, beta, rec, scale, impl == 2 ? 1 : 0, flags, st.err, geo};
         rc = timed_launch(true, stream, [&] { return kda::launch_intra_chunk(ip, pl.max_chunks, stream); });
         if (rc != KDA_OK) return rc;
         kda::RecurParams rp{rec, initial_state, out, final_state, st.err, geo};
@@ -405,7 +417,7 @@ kda_status kda_chunk_prefill(const void *q, const void *k, const void *v, const 
         uint8_t *slot = rec + (j & 1) * pl.slot_bytes;
         if (j >= 2 && cudaStreamWaitEvent(ws.s_intra, ev_recur[j - 2], 0) != cudaSuccess)
             return KDA_ERR_CUDA;
-        kda::IntraParams ip{q, k, v, g, beta, slot, scale, impl == 2 ? 1 : 0, st.err, gj};
+        kda::IntraParams ip{q, k, v, g, beta, slot, scale, impl == 2 ? 1 : 0, flags, st.err, gj};
         const int64_t items = B * static_cast<int64_t>(gj.seg_len);
         rc = timed_launch(true, ws.s_intra,
                           [&] { return kda::launch_intra_chunk(ip, items, ws.s_intra); });

@@ -17,7 +17,8 @@
 // load and store is one contiguous 512-byte row. The state is read once and
 // written once: the kernel is bound by HBM bandwidth (131,072 + 1,540 B per
 // (sequence, head)). Exponentials are taken per channel exactly, so there is
-// no gate-range precondition here.
+// no gate-range precondition here. With the preprocessing flags, q and k are
+// divided by their L2 norms (a block reduction) and g is read as gate logits.
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
@@ -32,7 +33,7 @@ __global__ void __launch_bounds__(kDecThreads, 2)
 kda_decode_kernel(DecodeParams p) {
     __shared__ float s_k[kDim], s_ka[kDim], s_qa[kDim], s_a[kDim], s_v[kDim], s_d[kDim];
     __shared__ float s_red[2][8][kDim];
-    __shared__ float s_qk[4];
+    __shared__ float s_dot[3][4];   // per-warp partial q.q, k.k, q.k
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int64_t unit = blockIdx.x;   // sequence * H + head
     const int64_t row = unit * kDim;
@@ -48,23 +49,40 @@ kda_decode_kernel(DecodeParams p) {
         for (int m = 0; m < 16; ++m) s[m] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 
-    // this token's vectors
+    // this token's vectors (threads 0..127 own channel t)
+    float qv = 0.f, kv = 0.f, a = 0.f;
     if (t < kDim) {
         const __nv_bfloat16 *qp = static_cast<const __nv_bfloat16 *>(p.q);
         const __nv_bfloat16 *kp = static_cast<const __nv_bfloat16 *>(p.k);
         const __nv_bfloat16 *vp = static_cast<const __nv_bfloat16 *>(p.v);
-        const float qv = __bfloat162float(qp[row + t]);
-        const float kv = __bfloat162float(kp[row + t]);
-        const float a = __expf(p.g[row + t]);
+        qv = __bfloat162float(qp[row + t]);
+        kv = __bfloat162float(kp[row + t]);
+        const float gl = p.g[row + t];
+        a = __expf((p.pre & kPreGateLogits) ? log_sigmoid(gl) : gl);
+        s_v[t] = __bfloat162float(vp[row + t]);
+        float d3[3] = {qv * qv, kv * kv, qv * kv};
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) d3[c] += __shfl_xor_sync(0xffffffffu, d3[c], o);
+            if (lane == 0) s_dot[c][warp] = d3[c];
+        }
+    }
+    __syncthreads();
+    // q.k, with q and k divided by their L2 norms when asked to
+    float rq = 1.f, rk = 1.f;
+    if (p.pre & kPreNormQK) {
+        rq = rsqrtf(s_dot[0][0] + s_dot[0][1] + s_dot[0][2] + s_dot[0][3] + kNormEps);
+        rk = rsqrtf(s_dot[1][0] + s_dot[1][1] + s_dot[1][2] + s_dot[1][3] + kNormEps);
+    }
+    const float qk_all = (s_dot[2][0] + s_dot[2][1] + s_dot[2][2] + s_dot[2][3]) * rq * rk;
+    if (t < kDim) {
+        qv *= rq;
+        kv *= rk;
         s_k[t] = kv;
         s_ka[t] = kv * a;
         s_qa[t] = qv * a;
         s_a[t] = a;
-        s_v[t] = __bfloat162float(vp[row + t]);
-        float qk = qv * kv;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) qk += __shfl_xor_sync(0xffffffffu, qk, o);
-        if (lane == 0) s_qk[warp] = qk;
     }
     __syncthreads();
 
@@ -91,11 +109,11 @@ kda_decode_kernel(DecodeParams p) {
             u += s_red[0][r][t];
             w += s_red[1][r][t];
         }
-        const float qk = s_qk[0] + s_qk[1] + s_qk[2] + s_qk[3];
         const float beta = p.beta[unit];
         const float d = beta * (s_v[t] - u);
         s_d[t] = d;
-        static_cast<__nv_bfloat16 *>(p.out)[row + t] = __float2bfloat16_rn(p.scale * (w + qk * d));
+        static_cast<__nv_bfloat16 *>(p.out)[row + t] =
+            __float2bfloat16_rn(p.scale * (w + qk_all * d));
     }
     __syncthreads();
 
@@ -105,12 +123,12 @@ kda_decode_kernel(DecodeParams p) {
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
         const int i = warp + 8 * m;
-        const float a = s_a[i], kv = s_k[i];
+        const float ai = s_a[i], ki = s_k[i];
         float4 r;
-        r.x = fmaf(a, s[m].x, kv * d4.x);
-        r.y = fmaf(a, s[m].y, kv * d4.y);
-        r.z = fmaf(a, s[m].z, kv * d4.z);
-        r.w = fmaf(a, s[m].w, kv * d4.w);
+        r.x = fmaf(ai, s[m].x, ki * d4.x);
+        r.y = fmaf(ai, s[m].y, ki * d4.y);
+        r.z = fmaf(ai, s[m].z, ki * d4.z);
+        r.w = fmaf(ai, s[m].w, ki * d4.w);
         S1[(warp + 8 * m) * (kDim / 4) + lane] = r;
     }
 }

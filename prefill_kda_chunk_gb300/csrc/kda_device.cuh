@@ -25,6 +25,17 @@ constexpr int kRecGamma = 12800;  // exp(G_last)                         [128] f
 constexpr int kRecUt = 13312;     // (T diag(beta) V)^T                  [128 val][16 tok] bf16
 constexpr int kRecBytes = 17408;
 
+// Input preprocessing done inside the kernels (the flags of the C ABI):
+// q and k divided by their L2 norm per (token, head), and g given as gate
+// logits x with the log decay taken as logsigmoid(x).
+enum : int { kPreNormQK = 1, kPreGateLogits = 2 };
+constexpr float kNormEps = 1e-6f;
+
+__device__ __forceinline__ float log_sigmoid(float x) {
+    // log(1 / (1 + e^-x)) = min(x, 0) - log(1 + e^-|x|)
+    return fminf(x, 0.f) - __logf(1.f + __expf(-fabsf(x)));
+}
+
 // Error bits. kErrBadCu lives in the per-call flag word and the sticky
 // per-device word; the others only in the sticky word.
 enum : int { kErrBadCu = 1, kErrTimeout = 2, kErrGate = 4 };

@@ -38,6 +38,7 @@ struct IntraParams {
     float scale;               // output scale, folded into the record's Q e^G and P
     int qg_tc;                 // 1: Q e^G in the tcgen05 operand layout of the hybrid
                                //    recurrent kernel; 0: swizzled rows for ldmatrix
+    int pre;                   // kPreNormQK | kPreGateLogits (input preprocessing)
     int *err;                  // sticky per-device error word
     ChunkGeometry geo;
 };
@@ -60,6 +61,7 @@ struct DecodeParams {
     float *s_out;              // [N, H, 128, 128]; may be s_in itself
     void *out;                 // bf16 [N, H, 128]
     float scale;
+    int pre;                   // kPreNormQK | kPreGateLogits (input preprocessing)
 };
 
 // Per-device, once: raise the dynamic shared-memory limits of the kernels.

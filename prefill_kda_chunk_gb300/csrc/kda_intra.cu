@@ -122,6 +122,9 @@ __device__ __forceinline__ void load_chunk(const IntraParams &p, IntraWarpSmem &
 
 // Persistent: each warp walks (chunk, head) items with a grid-wide stride,
 // items ordered chunk-major so the warps of a CTA share a chunk's rows.
+// PRE = false compiles no preprocessing code at all (p.pre must be 0);
+// PRE = true reads the preprocessing flags from p.pre.
+template <bool PRE>
 __global__ void __launch_bounds__(kIntraWarps * 32, 3)
 kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -159,9 +162,14 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     float G[16][4];   // cumulative log decay in base-2 units (G * log2 e)
     float run[4] = {0.f, 0.f, 0.f, 0.f};
     float gmax = 0.f;
+    const bool gate_logits = PRE && (p.pre & kPreGateLogits) != 0;
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-        const float4 gg = graw[r];
+        float4 gg = graw[r];
+        if (gate_logits && r < L) {   // rows past the end keep g = 0
+            gg.x = log_sigmoid(gg.x); gg.y = log_sigmoid(gg.y);
+            gg.z = log_sigmoid(gg.z); gg.w = log_sigmoid(gg.w);
+        }
         run[0] += gg.x; run[1] += gg.y; run[2] += gg.z; run[3] += gg.w;
         G[r][0] = run[0] * kLog2e; G[r][1] = run[1] * kLog2e;
         G[r][2] = run[2] * kLog2e; G[r][3] = run[3] * kLog2e;
@@ -192,8 +200,21 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
         const int off = swz(r, 4 * lane);
         const uint2 qq = *reinterpret_cast<const uint2 *>(sm.qg + off);
         const uint2 kk = *reinterpret_cast<const uint2 *>(sm.kg + off);
-        const float2 q01 = unpack_bf16(qq.x), q23 = unpack_bf16(qq.y);
-        const float2 k01 = unpack_bf16(kk.x), k23 = unpack_bf16(kk.y);
+        float2 q01 = unpack_bf16(qq.x), q23 = unpack_bf16(qq.y);
+        float2 k01 = unpack_bf16(kk.x), k23 = unpack_bf16(kk.y);
+        if (PRE && (p.pre & kPreNormQK)) {
+            // L2 norms of this row's q and k over the 128 channels of the warp
+            float sq = q01.x * q01.x + q01.y * q01.y + q23.x * q23.x + q23.y * q23.y;
+            float sk = k01.x * k01.x + k01.y * k01.y + k23.x * k23.x + k23.y * k23.y;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            const float rq = rsqrtf(sq + kNormEps), rk = rsqrtf(sk + kNormEps);
+            q01.x *= rq; q01.y *= rq; q23.x *= rq; q23.y *= rq;
+            k01.x *= rk; k01.y *= rk; k23.x *= rk; k23.y *= rk;
+        }
         float2 eg[2], en[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
@@ -409,15 +430,18 @@ cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t to
 
 cudaError_t configure_intra() {
     const int smem = kIntraWarps * static_cast<int>(sizeof(IntraWarpSmem));
-    cudaError_t e = cudaFuncSetAttribute(kda_intra_chunk_kernel,
+    cudaError_t e = cudaFuncSetAttribute(kda_intra_chunk_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kda_intra_chunk_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0, nb = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
         return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kda_intra_chunk_kernel,
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kda_intra_chunk_kernel<false>,
                                                            kIntraWarps * 32, smem)) != cudaSuccess)
         return e;
     g_sm_count[dev] = sms;
@@ -436,8 +460,12 @@ cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStr
         const int64_t resident = static_cast<int64_t>(g_sm_count[dev]) * g_blocks_per_sm[dev];
         if (blocks > resident) blocks = resident;
     }
-    kda_intra_chunk_kernel<<<static_cast<unsigned>(blocks), kIntraWarps * 32, smem, stream>>>(
-        p, max_chunks);
+    if (p.pre != 0)
+        kda_intra_chunk_kernel<true><<<static_cast<unsigned>(blocks), kIntraWarps * 32, smem,
+                                       stream>>>(p, max_chunks);
+    else
+        kda_intra_chunk_kernel<false><<<static_cast<unsigned>(blocks), kIntraWarps * 32, smem,
+                                        stream>>>(p, max_chunks);
     return cudaGetLastError();
 }
 

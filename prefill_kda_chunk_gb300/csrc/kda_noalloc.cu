@@ -143,7 +143,7 @@ extern "C" kda_status kda_chunk_prefill_noalloc(
                                               err, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
     uint8_t *rec = base + 256 + off_bytes;
-    kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, err, geo};
+    kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, 0, err, geo};
     if (kda::launch_intra_chunk(ip, max_chunks, stream) != cudaSuccess) return KDA_ERR_CUDA;
     kda::RecurParams rp{rec, initial_state, out, final_state, err, geo};
     if (kda::launch_recurrent(rp, stream) != cudaSuccess) return KDA_ERR_CUDA;

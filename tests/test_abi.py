@@ -97,7 +97,7 @@ def test_host_validation_rejects(lib, kw, code):
 def decode_call(**kw):
     args = dict(q=A, k=A + 0x100000, v=A + 0x200000, g=A + 0x300000, beta=A + 0x400000,
                 state_in=A + 0x800000, state_out=A + 0x800000, N=2, H=3, K=128, V=128,
-                scale=1.0, out=A + 0x500000, stream=0)
+                scale=1.0, flags=0, out=A + 0x500000, stream=0)
     args.update(kw)
     return K.kda_decode_step(**args)
 
@@ -118,6 +118,8 @@ def decode_call(**kw):
     (dict(out=A + 0x800000 + 256), "KDA_ERR_ALIAS"),
     (dict(state_out=A + 0x300000), "KDA_ERR_ALIAS"),
     (dict(state_out=A + 0x800000 + 4096), "KDA_ERR_ALIAS"),
+    (dict(flags=4), "KDA_ERR_BAD_FLAGS"),
+    (dict(flags=-1), "KDA_ERR_BAD_FLAGS"),
 ])
 def test_decode_host_validation_rejects(lib, kw, code):
     assert decode_call(**kw) == K.STATUS_CODE[code]
@@ -125,4 +127,13 @@ def test_decode_host_validation_rejects(lib, kw, code):
 
 def test_decode_empty_batch_is_a_no_op(lib):
     # N = 0: nothing to do, and no pointer is needed
-    assert K.kda_decode_step(0, 0, 0, 0, 0, 0, 0, 0, 4, 128, 128, 1.0, 0, 0) == 0
+    assert K.kda_decode_step(0, 0, 0, 0, 0, 0, 0, 0, 4, 128, 128, 1.0, 0, 0, 0) == 0
+
+
+def test_prefill_ex_flags(lib):
+    args = dict(q=A, k=A + 0x100000, v=A + 0x200000, g=A + 0x300000, beta=A + 0x400000,
+                initial_state=0, cu_seqlens=0, B=1, T=16, H=1, K=128, V=128, N=1, scale=1.0,
+                out=A + 0x500000, final_state=0, stream=0)
+    assert K.kda_chunk_prefill_ex(**args, flags=8) == K.STATUS_CODE["KDA_ERR_BAD_FLAGS"]
+    # known flags pass the host checks and reach the argument checks after them
+    assert K.kda_chunk_prefill_ex(**dict(args, K=64), flags=3) == K.STATUS_CODE["KDA_ERR_UNSUPPORTED_DIM"]

@@ -143,6 +143,6 @@ def test_decode_rejects_host_memory():
     out = torch.empty_like(x["v"])
     rc = K.kda_decode_step(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
                            x["g"].data_ptr(), x["beta"].data_ptr(), 0, host_state.data_ptr(),
-                           2, 1, 128, 128, 1.0, out.data_ptr(),
+                           2, 1, 128, 128, 1.0, 0, out.data_ptr(),
                            torch.cuda.current_stream().cuda_stream)
     assert rc == K.STATUS_CODE["KDA_ERR_NOT_DEVICE_MEMORY"]

@@ -269,3 +269,75 @@ def test_each_planted_mistake_fails_a_pin(oracle_mod, m):
         if not err <= tol:
             failed.append(name)
     assert failed, f"mutation {m} ({MUTATIONS[m]}) passed every pin"
+
+
+# ---- input preprocessing (the kernels' flags): pinned against a library
+# routine, a closed form and invariants, not against a retyped formula
+
+def _raw_case(rng, T, H, K, V):
+    q = rng.standard_normal((T, H, K)) * rng.uniform(0.25, 4.0, (T, H, 1))
+    k = rng.standard_normal((T, H, K)) * rng.uniform(0.25, 4.0, (T, H, 1))
+    v = rng.standard_normal((T, H, V))
+    x = rng.standard_normal((T, H, K)) + 3.0
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))
+    s0 = rng.standard_normal((1, H, K, V)) * 0.02
+    f = lambda a: a.astype(np.float32)
+    return f(q), f(k), f(v), f(x), f(beta), s0
+
+
+def test_gate_logits_match_scipy_log_expit(oracle_mod):
+    """logsigmoid of the logits inside the oracle == scipy.special.log_expit
+    applied outside, including logits far out on both sides."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(5)
+    q, k, v, x, beta, s0 = _raw_case(rng, 40, 2, 16, 8)
+    x[3, 0, :4] = [30.0, -30.0, 0.0, 80.0]
+    a = oracle_mod.recurrent(q, k, v, x, beta, s0, gate_logits=True, normalize_qk=True)
+    g = special.log_expit(x.astype(np.float64)).astype(np.float32)
+    b = oracle_mod.recurrent(q, k, v, g, beta, s0, normalize_qk=True)
+    for u, w in zip(a, b):
+        assert _relerr(u, w) < 1e-6
+
+
+def test_gate_logit_zero_halves_the_state(oracle_mod):
+    """beta = 0 and logit 0: logsigmoid(0) = -log 2, so every token halves S."""
+    rng = np.random.default_rng(6)
+    q, k, v, x, beta, s0 = _raw_case(rng, 9, 1, 8, 4)
+    x[:] = 0.0
+    beta[:] = 0.0
+    _, fs = oracle_mod.recurrent(q, k, v, x, beta, s0, gate_logits=True)
+    assert _relerr(fs, s0 * 0.5 ** 9) < 1e-12
+
+
+def test_normalisation_is_scale_invariant(oracle_mod):
+    """With normalize_qk, scaling any q or k row by a positive factor changes
+    nothing (eps is negligible at these norms), and negating q flips o and
+    leaves the state alone."""
+    rng = np.random.default_rng(7)
+    q, k, v, x, beta, s0 = _raw_case(rng, 30, 2, 16, 8)
+    base = oracle_mod.recurrent(q, k, v, x, beta, s0, normalize_qk=True, gate_logits=True)
+    c = rng.uniform(0.1, 10.0, (30, 2, 1)).astype(np.float32)
+    scaled = oracle_mod.recurrent(q * c, k / c, v, x, beta, s0, normalize_qk=True,
+                                  gate_logits=True)
+    for u, w in zip(base, scaled):   # fp32 rounding of the scaled rows, carried over 30 tokens
+        assert _relerr(u, w) < 1e-4
+    o_neg, fs_neg = oracle_mod.recurrent(-q, k, v, x, beta, s0, normalize_qk=True,
+                                         gate_logits=True)
+    assert _relerr(o_neg, -base[0]) < 1e-12 and _relerr(fs_neg, base[1]) < 1e-12
+    # without normalisation the same scaling does change the result
+    plain = oracle_mod.recurrent(q, k, v, x, beta, s0, gate_logits=True)
+    plain_s = oracle_mod.recurrent(q * c, k / c, v, x, beta, s0, gate_logits=True)
+    assert _relerr(plain[1], plain_s[1]) > 1e-3
+
+
+def test_normalisation_keeps_unit_rows(oracle_mod):
+    """Rows that already have unit L2 norm pass through normalize_qk unchanged
+    (up to eps and fp32 rounding of the inputs)."""
+    rng = np.random.default_rng(8)
+    q, k, v, x, beta, s0 = _raw_case(rng, 30, 2, 16, 8)
+    qn = (q / np.linalg.norm(q.astype(np.float64), axis=-1, keepdims=True)).astype(np.float32)
+    kn = (k / np.linalg.norm(k.astype(np.float64), axis=-1, keepdims=True)).astype(np.float32)
+    a = oracle_mod.recurrent(qn, kn, v, x, beta, s0, normalize_qk=True, gate_logits=True)
+    b = oracle_mod.recurrent(qn, kn, v, x, beta, s0, gate_logits=True)
+    for u, w in zip(a, b):
+        assert _relerr(u, w) < 2e-6
