@@ -62,6 +62,15 @@ cudaError_t launch_recur(int impl, const kda::RecurParams &p, cudaStream_t s) {
 
 constexpr int64_t kMaxElems = int64_t(1) << 40;
 
+// Split replay (fixed-length calls, warp-MMA recurrent kernel). A recurrent
+// step is a serial chain, so with few (sequence, head) units most SMs idle
+// through T/16 steps. When twice the recurrent CTAs (2 per head) still fit one
+// per SM, a state-only pass over the first half of each sequence gives the
+// midpoint state, and one launch then replays both halves side by side: about
+// T/32 (light) + T/32 (full) steps on the chain instead of T/16 full ones.
+constexpr int64_t kSplitMinChunks = 64;    // per sequence
+constexpr int64_t kSplitMaxCtas = 148;     // doubled recurrent CTAs, below GB300's 152 SMs
+
 int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
 struct Plan {
@@ -76,6 +85,11 @@ struct Plan {
     int64_t seg_len = 0;
     int64_t slot_bytes = 0;
     int64_t carry_bytes = 0;
+    // Split replay of long fixed-length sequences (see kSplit*): the first
+    // split_chunks chunks of every sequence are run once to carry the state to
+    // the midpoint (mid_bytes of states), then both halves are replayed at once.
+    int64_t split_chunks = 0;
+    int64_t mid_bytes = 0;
 };
 
 bool misaligned(const void *p, uintptr_t a) {
@@ -109,6 +123,11 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, P
     pl->ws_bytes = 256 + pl->off_bytes + pl->max_chunks * H * kda::kRecBytes;
     pl->nseg = 1;
     pl->seg_len = (T + 15) / 16;
+    if (!packed && pl->seg_len >= kSplitMinChunks && 2 * (N * H * 2) <= kSplitMaxCtas) {
+        pl->split_chunks = pl->seg_len / 2;
+        pl->mid_bytes = align256(N * H * 128 * 128 * 4);
+        pl->ws_bytes += pl->mid_bytes;
+    }
     if (!packed) {
         const int64_t cps = (T + 15) / 16;
         const int64_t per_pos = B * H * int64_t(kda::kRecBytes);
@@ -124,6 +143,8 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, P
                 pl->carry_bytes = align256(B * H * 128 * 128 * 4);
                 pl->max_chunks = B * seg;
                 pl->ws_bytes = 256 + 2 * pl->slot_bytes + pl->carry_bytes;
+                pl->split_chunks = 0;
+                pl->mid_bytes = 0;
             }
         }
     }
@@ -378,6 +399,22 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
         rc = timed_launch(true, stream, [&] { return kda::launch_intra_chunk(ip, pl.max_chunks, stream); });
         if (rc != KDA_OK) return rc;
         kda::RecurParams rp{rec, initial_state, out, final_state, st.err, geo};
+        // (an in-place state would be read by one half while the other writes it)
+        if (pl.split_chunks > 0 && impl == 1 &&
+            (initial_state == nullptr || initial_state != final_state)) {
+            // state to the midpoint of every sequence, then both halves at once
+            float *mid = reinterpret_cast<float *>(rec + pl.max_chunks * H * kda::kRecBytes);
+            kda::RecurParams rl = rp;
+            rl.out = nullptr;
+            rl.s_final = mid;
+            rl.geo.seg_len = static_cast<int32_t>(pl.split_chunks);
+            rp.split_chunks = static_cast<int32_t>(pl.split_chunks);
+            rp.s_mid = mid;
+            return timed_launch(false, stream, [&] {
+                const cudaError_t e = kda::launch_recurrent_state_only(rl, stream);
+                return e != cudaSuccess ? e : kda::launch_recurrent(rp, stream);
+            });
+        }
         return timed_launch(false, stream, [&] { return launch_recur(impl, rp, stream); });
     }
 

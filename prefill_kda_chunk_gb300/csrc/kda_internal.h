@@ -50,6 +50,12 @@ struct RecurParams {
     float *s_final;            // [N, H, 128, 128] or nullptr
     int *err;
     ChunkGeometry geo;
+    // Split replay of fixed-length sequences (warp-MMA kernel only): with
+    // split_chunks = c > 0 the launch covers 2N (sequence, half) units; half 0
+    // is chunks [0, c) from s0, half 1 chunks [c, end) from s_mid, and only
+    // half 1 writes s_final.
+    int32_t split_chunks = 0;
+    const float *s_mid = nullptr;  // [N, H, 128, 128]
 };
 
 // One-token decode step for N*H independent (sequence, head) units.
@@ -75,6 +81,8 @@ cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t to
                                    cudaStream_t stream);
 cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStream_t stream);
 cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream);     // warp MMA
+// warp MMA without outputs: only carries the state (to s_final)
+cudaError_t launch_recurrent_state_only(const RecurParams &p, cudaStream_t stream);
 cudaError_t launch_recurrent_tc(const RecurParams &p, cudaStream_t stream);  // tcgen05 / TMEM
 // warp-MMA chain with the output product on tcgen05; needs IntraParams::qg_tc = 1
 cudaError_t launch_recurrent_hybrid(const RecurParams &p, cudaStream_t stream);

@@ -45,7 +45,8 @@ struct RecurLayout {
     static constexpr int kSmem = kBars + 2 * kStages * 8;
 };
 
-template <int BV>
+// OUT = false carries only the state (no output products, no o stores).
+template <int BV, bool OUT>
 __global__ void __launch_bounds__((BV / 16 + 1) * 32)
 kda_recurrent_kernel(RecurParams p) {
     using Lay = RecurLayout<BV>;
@@ -56,7 +57,7 @@ kda_recurrent_kernel(RecurParams p) {
     const int H = geo.n_heads;
     const int s = blockIdx.x % Lay::kSlices;
     const int h = (blockIdx.x / Lay::kSlices) % H;
-    const int n = blockIdx.x / (Lay::kSlices * H);
+    const int n = blockIdx.x / (Lay::kSlices * H);   // unit: sequence, or (half, sequence)
 
     const uint32_t bar_full = smem_u32(smem + Lay::kBars);
     const uint32_t bar_empty = bar_full + kStages * 8;
@@ -72,7 +73,22 @@ kda_recurrent_kernel(RecurParams p) {
 
     int64_t tb, te, chunk0;
     int nck;
-    if (geo.cu == nullptr) {
+    int seq = n;                       // the sequence whose states this CTA reads and writes
+    const float *s_in = p.s0;
+    float *s_out = p.s_final;
+    if (geo.cu == nullptr && p.split_chunks > 0) {
+        // split replay: half 0 = chunks [0, c) from s0, half 1 = [c, end) from s_mid
+        const int half = n / geo.n_seqs;
+        seq = n % geo.n_seqs;
+        const int64_t c = p.split_chunks;
+        const int64_t base = static_cast<int64_t>(seq) * geo.seq_len;
+        tb = base + (half ? 16 * c : 0);
+        te = half ? base + geo.seq_len : base + 16 * c;
+        chunk0 = static_cast<int64_t>(seq) * geo.slot_stride + (half ? c : 0);
+        nck = static_cast<int>(half ? (geo.seq_len + 15) / 16 - c : c);
+        s_in = half ? p.s_mid : p.s0;
+        s_out = half ? p.s_final : nullptr;
+    } else if (geo.cu == nullptr) {
         tb = static_cast<int64_t>(n) * geo.seq_len + 16 * static_cast<int64_t>(geo.pos_begin);
         te = static_cast<int64_t>(n) * geo.seq_len + geo.seq_len;
         chunk0 = static_cast<int64_t>(n) * geo.slot_stride;
@@ -111,9 +127,9 @@ kda_recurrent_kernel(RecurParams p) {
     const int vw = 16 * warp;          // first value channel of this warp within the slice
     const int v0 = s * BV + vw;        // ... within the head
     float acc[16][4];                  // S^T fragments: rows = value, cols = key
-    const int64_t sbase = (static_cast<int64_t>(n) * H + h) * kDim * kDim;
-    if (p.s0 != nullptr) {
-        const float *S0 = p.s0 + sbase;
+    const int64_t sbase = (static_cast<int64_t>(seq) * H + h) * kDim * kDim;
+    if (s_in != nullptr) {
+        const float *S0 = s_in + sbase;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int key = 8 * j + 2 * tig;
@@ -182,13 +198,15 @@ kda_recurrent_kernel(RecurParams p) {
             mul2(acc[j][2], acc[j][3], gm.x, gm.y);
         }
         // (Q e^G S)^T = S^T Qg^T keeps the tensor pipe busy meanwhile
+        if constexpr (OUT) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            uint32_t bq[4];
-            const int rb = (quad >> 1) * 8 + (lane & 7), cb = 16 * kk + (quad & 1) * 8;
-            ldsm_x4(sw + kRecQg + swz(rb, cb), bq[0], bq[1], bq[2], bq[3]);
-            mma_r(oT[0][kk & 1], aS[kk], bq[0], bq[1]);
-            mma_r(oT[1][kk & 1], aS[kk], bq[2], bq[3]);
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t bq[4];
+                const int rb = (quad >> 1) * 8 + (lane & 7), cb = 16 * kk + (quad & 1) * 8;
+                ldsm_x4(sw + kRecQg + swz(rb, cb), bq[0], bq[1], bq[2], bq[3]);
+                mma_r(oT[0][kk & 1], aS[kk], bq[0], bq[1]);
+                mma_r(oT[1][kk & 1], aS[kk], bq[2], bq[3]);
+            }
         }
         uint32_t aU[4];
         {
@@ -214,43 +232,45 @@ kda_recurrent_kernel(RecurParams p) {
         // look at the next stage's barrier now; its latency hides behind the MMAs
         if (i + 1 < nck)
             ready = mbar_test(bar_full + 8 * ((i + 1) % kStages), ((i + 1) / kStages) & 1);
-        // o^T = (Q e^G S)^T + U^T P^T (scale is in the record), off the chain
-        float o[2][4];
+        if constexpr (OUT) {
+            // o^T = (Q e^G S)^T + U^T P^T (scale is in the record), off the chain
+            float o[2][4];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[nt][e] = oT[nt][0][e] + oT[nt][1][e];
-        {
-            uint32_t bp[4];
-            const int rp = (quad >> 1) * 8 + (lane & 7);
-            ldsm_x4(sw + kRecP + rp * 32 + (quad & 1) * 16, bp[0], bp[1], bp[2], bp[3]);
-            mma_r(o[0], aU, bp[0], bp[1]);
-            mma_r(o[1], aU, bp[2], bp[3]);
-        }
-        const int64_t t0 = tb + 16 * i;
-        const int L = static_cast<int>((te - t0) < 16 ? (te - t0) : 16);
-        {
-            const int j = lane >> 3, r = lane & 7;
-            stsm_x4_t(smem_u32(so) + ((j >> 1) * 8 + r) * 32 + (j & 1) * 16,
-                      pack_bf16(o[0][0], o[0][1]), pack_bf16(o[0][2], o[0][3]),
-                      pack_bf16(o[1][0], o[1][1]), pack_bf16(o[1][2], o[1][3]));
-        }
-        __syncwarp();
-        {
-            const int tok = lane >> 1, hf = lane & 1;
-            if (tok < L) {
-                const uint4 val = *reinterpret_cast<const uint4 *>(so + tok * 32 + hf * 16);
-                *reinterpret_cast<uint4 *>(orow + tok * static_cast<int64_t>(H) * kDim + hf * 8) =
-                    val;
+                for (int e = 0; e < 4; ++e) o[nt][e] = oT[nt][0][e] + oT[nt][1][e];
+            {
+                uint32_t bp[4];
+                const int rp = (quad >> 1) * 8 + (lane & 7);
+                ldsm_x4(sw + kRecP + rp * 32 + (quad & 1) * 16, bp[0], bp[1], bp[2], bp[3]);
+                mma_r(o[0], aU, bp[0], bp[1]);
+                mma_r(o[1], aU, bp[2], bp[3]);
             }
+            const int64_t t0 = tb + 16 * i;
+            const int L = static_cast<int>((te - t0) < 16 ? (te - t0) : 16);
+            {
+                const int j = lane >> 3, r = lane & 7;
+                stsm_x4_t(smem_u32(so) + ((j >> 1) * 8 + r) * 32 + (j & 1) * 16,
+                          pack_bf16(o[0][0], o[0][1]), pack_bf16(o[0][2], o[0][3]),
+                          pack_bf16(o[1][0], o[1][1]), pack_bf16(o[1][2], o[1][3]));
+            }
+            __syncwarp();
+            {
+                const int tok = lane >> 1, hf = lane & 1;
+                if (tok < L) {
+                    const uint4 val = *reinterpret_cast<const uint4 *>(so + tok * 32 + hf * 16);
+                    *reinterpret_cast<uint4 *>(orow + tok * static_cast<int64_t>(H) * kDim + hf * 8) =
+                        val;
+                }
+            }
+            orow += ostep;
         }
-        orow += ostep;
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * st);
     }
 
-    if (p.s_final != nullptr) {
-        float *SF = p.s_final + sbase;
+    if (s_out != nullptr) {
+        float *SF = s_out + sbase;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int key = 8 * j + 2 * tig;
@@ -264,21 +284,35 @@ kda_recurrent_kernel(RecurParams p) {
 
 constexpr int kBV = 64;
 
+template <bool OUT>
+cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
+    using Lay = RecurLayout<kBV>;
+    const int64_t units = static_cast<int64_t>(p.geo.n_seqs) * (p.split_chunks > 0 ? 2 : 1);
+    const int64_t ctas = units * p.geo.n_heads * Lay::kSlices;
+    if (ctas <= 0) return cudaSuccess;
+    kda_recurrent_kernel<kBV, OUT><<<static_cast<unsigned>(ctas), (Lay::kWarps + 1) * 32,
+                                     Lay::kSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t configure_recurrent() {
-    return cudaFuncSetAttribute(kda_recurrent_kernel<kBV>,
+    cudaError_t e = cudaFuncSetAttribute(kda_recurrent_kernel<kBV, true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         RecurLayout<kBV>::kSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kda_recurrent_kernel<kBV, false>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 RecurLayout<kBV>::kSmem);
 }
 
 cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream) {
-    using Lay = RecurLayout<kBV>;
-    const int64_t ctas = static_cast<int64_t>(p.geo.n_seqs) * p.geo.n_heads * Lay::kSlices;
-    if (ctas <= 0) return cudaSuccess;
-    kda_recurrent_kernel<kBV><<<static_cast<unsigned>(ctas), (Lay::kWarps + 1) * 32, Lay::kSmem,
-                                stream>>>(p);
-    return cudaGetLastError();
+    return launch<true>(p, stream);
+}
+
+cudaError_t launch_recurrent_state_only(const RecurParams &p, cudaStream_t stream) {
+    return launch<false>(p, stream);
 }
 
 }  // namespace kda

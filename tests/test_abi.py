@@ -58,6 +58,11 @@ def test_workspace_bytes(lib):
         K.kda_set_ring_slot_bytes(0)
     # packed batches are never segmented
     assert K.kda_workspace_bytes(1, 8192, 64, 16, 1) == 256 + 256 + ((8192 + 15 * 16) // 16) * 64 * REC
+    # long sequences with few heads: records plus the midpoint states of the split replay
+    assert K.kda_workspace_bytes(1, 131072, 32, 1, 0) == 256 + 8192 * 32 * REC + 32 * 65536
+    assert K.kda_workspace_bytes(2, 2000, 3, 2, 0) == 256 + 2 * 125 * 3 * REC + 6 * 65536
+    assert K.kda_workspace_bytes(1, 1008, 3, 1, 0) == 256 + 63 * 3 * REC     # < 64 chunks
+    assert K.kda_workspace_bytes(1, 8192, 38, 1, 0) == 256 + 512 * 38 * REC  # 152 CTAs > 148
     assert K.kda_workspace_bytes(1, 8192, 64, 2, 0) == 0      # N != B without cu_seqlens
     assert K.kda_workspace_bytes(2, 100, 0, 2, 0) == 0        # H < 1
 

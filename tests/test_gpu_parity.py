@@ -219,6 +219,40 @@ def test_segmented_calls(T, Bn):
     assert f3 is None and torch.equal(o3, o)
 
 
+@pytest.mark.parametrize("T,B,init", [(1024, 1, False), (2003, 1, True), (1040, 3, True),
+                                      (4096, 2, False)])
+def test_split_replay_lengths(T, B, init):
+    """Long fixed-length sequences with few heads take the split replay on the
+    warp-MMA kernel (state to the midpoint, then both halves at once): odd
+    chunk counts, a partial last chunk, several sequences."""
+    H = 2
+    d = KI.make_case([T] * B, H=H, seed=T + B, init_state=init)
+    x = to_dev(d)
+    q4 = {n: x[n].view(B, T, *x[n].shape[1:]) for n in ("q", "k", "v", "g", "beta")}
+    o, f = K.chunk_prefill(q4["q"], q4["k"], q4["v"], q4["g"], q4["beta"],
+                           initial_state=x["initial_state"], scale=d["scale"])
+    K.check_device_error()
+    o_ref, f_ref = run_oracle(d)
+    assert_parity(o.view(B * T, H, 128), f, o_ref, f_ref)
+
+
+def test_split_replay_in_place_state():
+    """An in-place state never takes the split replay, and gives the same
+    result as an out-of-place call."""
+    T, H = 2048, 2
+    d = KI.make_case([T], H=H, seed=8, init_state=True)
+    x = to_dev(d)
+    o1, f1 = K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                             initial_state=x["initial_state"], scale=d["scale"])
+    st = x["initial_state"].clone()
+    o2, f2 = K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"], initial_state=st,
+                             scale=d["scale"], final_state=st)
+    K.check_device_error()
+    o_ref, f_ref = run_oracle(d)
+    assert_parity(o2, st, o_ref, f_ref)
+    assert_parity(o1, f1, o_ref, f_ref)
+
+
 def test_deterministic():
     d = KI.make_case([300], H=4, seed=13, init_state=True)
     o1, f1 = run_gpu(d, packed=False)
