@@ -64,7 +64,7 @@ kda_recurrent_kernel(RecurParams p) {
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(bar_full + 8 * i, 1);
-            mbar_init(bar_empty + 8 * i, Lay::kWarps);
+            mbar_init(bar_empty + 8 * i, Lay::kWarps * 32);
         }
         mbar_fence_init();
     }
@@ -265,8 +265,7 @@ kda_recurrent_kernel(RecurParams p) {
             }
             orow += ostep;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * st);
+        mbar_arrive(bar_empty + 8 * st);
     }
 
     if (s_out != nullptr) {
