@@ -29,4 +29,4 @@ from ._binding import (  # noqa: F401
     lib,
 )
 
-__version__ = "0.1.0"
+__version__ = "0.2.0"

@@ -267,8 +267,9 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
 }
 
 const char *kda_build_info(void) {
-    return "prefill_kda_chunk_gb300 0.1 (sm_103a; intra-chunk mma.sync + recurrent mma.sync, "
-           "bulk-async staged)";
+    return "prefill_kda_chunk_gb300 0.2 (sm_103a; intra-chunk mma.sync; recurrent warp-MMA chain "
+           "with bulk-async staged records and split replay, tcgen05 and hybrid kernels opt-in; "
+           "decode step; in-kernel q/k normalisation and gate logits)";
 }
 
 int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, int has_cu_seqlens) {
