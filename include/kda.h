@@ -111,7 +111,11 @@ enum { KDA_PRE_NORM_QK = 1, KDA_PRE_GATE_LOGITS = 2 };
  * Workspace: the library keeps one scratch buffer per (device, stream),
  * grown stream-ordered (cudaMallocAsync / cudaFreeAsync) when a call needs
  * more (17,408 B per chunk-head, or two ring slots plus the carried states
- * for a segmented call, see kda_set_ring_slot_bytes). A segmented call also
+ * for a segmented call, see kda_set_ring_slot_bytes). A fixed-length call
+ * with at least 64 chunks per sequence and 4*N*H <= 148 also reserves
+ * N*H*64 KiB of midpoint states: the warp-MMA recurrent kernel then carries
+ * the state to the middle of every sequence first and replays both halves
+ * side by side (same results to rounding; not with an in-place state). A segmented call also
  * forks onto two internal streams of that workspace and joins back to
  * `stream` before returning. Concurrent calls on different streams
  * therefore never share scratch. Growing is refused with KDA_ERR_CAPTURE
