@@ -118,3 +118,24 @@ def test_preprocessing_equals_preprocessed_inputs():
     rel_o = (o1.float() - o2.float()).norm() / o2.float().norm()
     rel_f = (f1 - f2).norm() / f2.norm()
     assert rel_o < 1e-2 and rel_f < 1e-2, (float(rel_o), float(rel_f))
+
+
+@pytest.mark.parametrize("impl", [0, 1, 2], ids=["tcgen05", "warp_mma", "hybrid"])
+def test_preprocessing_with_each_recurrent_kernel(impl):
+    """The preprocessing lives in the intra-chunk kernel, whose record layout
+    depends on the recurrent kernel (the hybrid one takes Q e^G in its
+    tcgen05 operand layout): check every combination."""
+    d = KI.make_raw_case([150, 33], H=2, seed=60 + impl, init_state=True)
+    x = {n: d[n].cuda().contiguous() for n in ("q", "k", "v", "g", "beta")}
+    assert K.kda_set_recurrent_impl(impl) == 0
+    try:
+        o, f = K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                               initial_state=d["initial_state"].cuda(),
+                               cu_seqlens=d["cu_seqlens"].cuda(), scale=d["scale"],
+                               normalize_qk=True, gate_logits=True)
+        K.check_device_error()
+    finally:
+        K.kda_set_recurrent_impl(1)
+    o_ref, f_ref = oracle(d, True, True)
+    check(o, o_ref, "o")
+    check(f, f_ref, "final_state")
