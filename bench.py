@@ -175,6 +175,19 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def launches_per_call(w, args):
+    """Kernels one unsegmented prefill call launches: the cu_seqlens prologue
+    (packed batches), the intra-chunk kernel, its exact-form companion, the
+    recurrent kernel, and the state-only pass of the split replay (warp-MMA
+    recurrent kernel, fixed-length sequences of >= 64 chunks, 4 N H <= 148)."""
+    n = 3 + int(w.varlen)
+    chunks = -(-(w.T // w.n_seqs) // 16)
+    impl = 1 if args.recurrent_impl is None else args.recurrent_impl
+    if not w.varlen and impl == 1 and chunks >= 64 and 4 * w.n_seqs * w.H <= 148:
+        n += 1
+    return n
+
+
 def traffic_for(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on this kernel source (else None)."""
@@ -490,7 +503,7 @@ def main():
             "config": dict(config_of(w, d), **({"preprocess": "q/k norm + gate logits in-kernel"}
                                                 if args.preprocess else {})),
             "roofline": roof, "path_roofline": path_roof,
-            "kernels": kernels, "gpu_launches": args.steps * (2 + int(w.varlen)),
+            "kernels": kernels, "gpu_launches": args.steps * launches_per_call(w, args),
             "clocks": clk, "e2e": e2e}
     if not args.no_decode:
         line["decode"] = bench_decode(K, dev, 256, 64, 200, args.warmup, hbm)

@@ -55,7 +55,7 @@ typedef enum {
     KDA_ERR_DEVICE_TIMEOUT = -7,    /* (device) a bounded wait inside a kernel ran out */
     KDA_ERR_NO_DEVICE_SUPPORT = -8, /* current device is not sm_103 */
     KDA_ERR_ALIAS = -9,             /* out or final_state overlaps an input */
-    KDA_ERR_GATE_RANGE = -10,       /* (device) a chunk's summed log decay left [-80, 80] */
+    KDA_ERR_GATE_RANGE = -10,       /* (device) log decay rose by more than 80 inside a chunk */
     KDA_ERR_CAPTURE = -11,          /* workspace must grow while the stream is capturing */
     KDA_ERR_WRONG_DEVICE = -12,     /* a buffer or the stream belongs to another device */
     KDA_ERR_NOT_DEVICE_MEMORY = -13, /* a pointer is not CUDA device (or managed) memory */
@@ -104,14 +104,19 @@ enum { KDA_PRE_NORM_QK = 1, KDA_PRE_GATE_LOGITS = 2 };
  * Alignment: q, k, v, g, out, initial_state, final_state 16-byte aligned;
  * beta and cu_seqlens 4-byte aligned.
  *
- * Precondition of the factored exponentials: within every 16-token chunk
- * the per-channel cumulative log decay stays in [-80, 80]; outside it the
- * device flags KDA_ERR_GATE_RANGE (results then unspecified).
+ * Gate range: g may be any finite log decay <= 0. Chunks whose per-channel
+ * cumulative log decay stays in [-80, 80] use factored exponentials
+ * exp(G_r) exp(-G_i); the others take an exact per-pair form (slower, same
+ * results to rounding). Positive g is allowed as long as the cumulative log
+ * decay does not rise by more than 80 between two points of a 16-token chunk
+ * (counting the chunk start as 0); beyond that exp() leaves fp32's range and
+ * the device flags KDA_ERR_GATE_RANGE (results then unspecified).
  *
  * Workspace: the library keeps one scratch buffer per (device, stream),
  * grown stream-ordered (cudaMallocAsync / cudaFreeAsync) when a call needs
- * more (17,408 B per chunk-head, or two ring slots plus the carried states
- * for a segmented call, see kda_set_ring_slot_bytes). A fixed-length call
+ * more (17,412 B per chunk-head: its record and one list entry; or two ring
+ * slots plus the carried states for a segmented call, see
+ * kda_set_ring_slot_bytes). A fixed-length call
  * with at least 64 chunks per sequence and 4*N*H <= 148 also reserves
  * N*H*64 KiB of midpoint states: the warp-MMA recurrent kernel then carries
  * the state to the middle of every sequence first and replays both halves
@@ -230,7 +235,8 @@ KDA_API int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, 
  * intra-chunk kernel, one between it and the recurrent kernel, and one after
  * the recurrent kernel, on the call's stream. kda_stage_timing_end()
  * waits for those events, writes the mean milliseconds per call of the
- * intra-chunk stage (prologue excluded) and of the recurrent stage, and the
+ * intra-chunk stage (prologue excluded; the intra-chunk kernel and the exact
+ * form of the chunks outside the factored range) and of the recurrent stage, and the
  * number of calls timed, then frees the events. Host pointers; NULL outputs
  * are skipped. Errors: KDA_ERR_BAD_SHAPE for max_calls < 1, KDA_ERR_CUDA.
  */

@@ -90,7 +90,14 @@ struct Plan {
     // the midpoint (mid_bytes of states), then both halves are replayed at once.
     int64_t split_chunks = 0;
     int64_t mid_bytes = 0;
+    // list of chunk-heads for the exact form (one int32 per item of a launch)
+    // at the end of the workspace; its two counters sit in the flag block
+    int64_t list_bytes = 0;
 };
+
+// flag block (the first 256 bytes of a workspace): per-call flag word at 0,
+// the exact-form list counters at kExactCtrOff
+constexpr int64_t kExactCtrOff = 64;
 
 bool misaligned(const void *p, uintptr_t a) {
     return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) != 0;
@@ -148,6 +155,8 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, P
             }
         }
     }
+    pl->list_bytes = align256(pl->max_chunks * H * 4);
+    pl->ws_bytes += pl->list_bytes;
     return KDA_OK;
 }
 
@@ -196,7 +205,7 @@ const char *kda_status_string(kda_status s) {
         case KDA_ERR_DEVICE_TIMEOUT: return "a bounded wait inside a kernel timed out";
         case KDA_ERR_NO_DEVICE_SUPPORT: return "the current device is not sm_103";
         case KDA_ERR_ALIAS: return "an output overlaps an input";
-        case KDA_ERR_GATE_RANGE: return "a chunk's cumulative log decay left [-80, 80]";
+        case KDA_ERR_GATE_RANGE: return "log decay rose by more than 80 within a chunk (exp leaves fp32)";
         case KDA_ERR_CAPTURE: return "workspace cannot grow while the stream is capturing";
         case KDA_ERR_WRONG_DEVICE: return "a buffer or the stream belongs to another device";
         case KDA_ERR_NOT_DEVICE_MEMORY: return "a pointer is not CUDA device memory";
@@ -357,6 +366,8 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
             return KDA_ERR_CUDA;
         }
         ws.bytes = pl.ws_bytes;
+        // the flag block starts zeroed (the exact-form list counters above all)
+        if (cudaMemsetAsync(ws.ptr, 0, 256, stream) != cudaSuccess) return KDA_ERR_CUDA;
     }
     uint8_t *wsb = static_cast<uint8_t *>(ws.ptr);
 
@@ -394,10 +405,18 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
             return KDA_ERR_CUDA;
     }
     uint8_t *rec = wsb + 256 + pl.off_bytes;
+    int32_t *exact_list = reinterpret_cast<int32_t *>(wsb + pl.ws_bytes - pl.list_bytes);
+    int *exact_ctr = reinterpret_cast<int *>(wsb + kExactCtrOff);
+    // the intra-chunk kernel, then the exact form of what it listed
+    auto intra = [&](const kda::IntraParams &ip, int64_t items, cudaStream_t s) {
+        const cudaError_t e = kda::launch_intra_chunk(ip, items, s);
+        return e != cudaSuccess ? e : kda::launch_intra_exact(ip, s);
+    };
 
     if (pl.nseg == 1) {
-        kda::IntraParams ip{q, k, v, g, beta, rec, scale, impl == 2 ? 1 : 0, flags, st.err, geo};
-        rc = timed_launch(true, stream, [&] { return kda::launch_intra_chunk(ip, pl.max_chunks, stream); });
+        kda::IntraParams ip{q, k, v, g, beta, rec, scale, impl == 2 ? 1 : 0, flags, st.err, geo,
+                            exact_list, exact_ctr};
+        rc = timed_launch(true, stream, [&] { return intra(ip, pl.max_chunks, stream); });
         if (rc != KDA_OK) return rc;
         kda::RecurParams rp{rec, initial_state, out, final_state, st.err, geo};
         // (an in-place state would be read by one half while the other writes it)
@@ -455,10 +474,10 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
         uint8_t *slot = rec + (j & 1) * pl.slot_bytes;
         if (j >= 2 && cudaStreamWaitEvent(ws.s_intra, ev_recur[j - 2], 0) != cudaSuccess)
             return KDA_ERR_CUDA;
-        kda::IntraParams ip{q, k, v, g, beta, slot, scale, impl == 2 ? 1 : 0, flags, st.err, gj};
+        kda::IntraParams ip{q, k, v, g, beta, slot, scale, impl == 2 ? 1 : 0, flags, st.err, gj,
+                            exact_list, exact_ctr};
         const int64_t items = B * static_cast<int64_t>(gj.seg_len);
-        rc = timed_launch(true, ws.s_intra,
-                          [&] { return kda::launch_intra_chunk(ip, items, ws.s_intra); });
+        rc = timed_launch(true, ws.s_intra, [&] { return intra(ip, items, ws.s_intra); });
         if (rc != KDA_OK) return rc;
         if (cudaEventRecord(ev_intra[j], ws.s_intra) != cudaSuccess ||
             cudaStreamWaitEvent(ws.s_recur, ev_intra[j], 0) != cudaSuccess)

@@ -41,6 +41,13 @@ struct IntraParams {
     int pre;                   // kPreNormQK | kPreGateLogits (input preprocessing)
     int *err;                  // sticky per-device error word
     ChunkGeometry geo;
+    // Chunk-heads outside the range of the factored exponentials: the
+    // intra-chunk kernel appends their item index (chunk * H + head) to
+    // exact_list, counting in exact_ctr[0]; the exact kernel consumes the list
+    // and zeroes both counters (exact_ctr[1] counts its finished CTAs). Both
+    // counters are 0 between calls; exact_list holds one entry per item.
+    int32_t *exact_list = nullptr;
+    int *exact_ctr = nullptr;
 };
 
 struct RecurParams {
@@ -80,6 +87,9 @@ cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t to
                                    int32_t *chunk_off, int *call_flags, int *err,
                                    cudaStream_t stream);
 cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStream_t stream);
+// the exact form over the chunk-heads the intra-chunk kernel listed; launch
+// after every launch_intra_chunk, on the same stream
+cudaError_t launch_intra_exact(const IntraParams &p, cudaStream_t stream);
 cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream);     // warp MMA
 // warp MMA without outputs: only carries the state (to s_final)
 cudaError_t launch_recurrent_state_only(const RecurParams &p, cudaStream_t stream);

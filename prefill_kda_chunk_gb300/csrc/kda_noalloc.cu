@@ -89,7 +89,8 @@ extern "C" kda_status kda_chunk_prefill_noalloc(
     // of the call is in the array at once
     const int64_t need_off = packed ? (((N + 1) * 4 + 255) & ~int64_t(255)) : 0;
     const int64_t need_chunks = packed ? (T + 15 * N) / 16 : B * ((T + 15) / 16);
-    const int64_t need = 256 + need_off + need_chunks * H * kda::kRecBytes;
+    const int64_t need_list = ((need_chunks * H * 4) + 255) & ~int64_t(255);
+    const int64_t need = 256 + need_off + need_chunks * H * kda::kRecBytes + need_list;
     if (static_cast<size_t>(need) > kNoAllocScratchBytes) return KDA_ERR_SCRATCH_LIMIT;
     const int64_t tokens = packed ? T : B * T;
     if (tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL_ARG;
@@ -143,8 +144,12 @@ extern "C" kda_status kda_chunk_prefill_noalloc(
                                               err, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
     uint8_t *rec = base + 256 + off_bytes;
-    kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, 0, err, geo};
+    // the exact-form list after the records, its counters in the flag block
+    int32_t *exact_list = reinterpret_cast<int32_t *>(rec + max_chunks * H * kda::kRecBytes);
+    int *exact_ctr = reinterpret_cast<int *>(base + 64);
+    kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, 0, err, geo, exact_list, exact_ctr};
     if (kda::launch_intra_chunk(ip, max_chunks, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::launch_intra_exact(ip, stream) != cudaSuccess) return KDA_ERR_CUDA;
     kda::RecurParams rp{rec, initial_state, out, final_state, err, geo};
     if (kda::launch_recurrent(rp, stream) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;

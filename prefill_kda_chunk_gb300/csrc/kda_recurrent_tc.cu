@@ -22,9 +22,9 @@
 // chunk record (W and Qg times c as tf32, Kd over c_{n+1} as bf16). Before a
 // step whose c_n gamma_n would fall below 1e-30 for some key, that key's
 // column of Shat is multiplied back by its c and c is reset to 1 (a
-// renormalisation pass over TMEM, rare unless decay is extreme); with the
-// gate-range precondition this keeps every operand inside the fp32 / bf16
-// range.
+// renormalisation pass over TMEM, rare unless decay is extreme). A chunk
+// decay gamma below 1e-30 is raised to 1e-30 (see the prep warps), so c stays
+// in [1e-30, 1] and every operand inside the fp32 / bf16 range.
 //
 // Warp roles (320 threads): warps 0-3 epilogue (thread v <-> TMEM lane v <->
 // value channel v), warps 4-7 prep, warp 8 producer (bulk async copies of the
@@ -279,7 +279,10 @@ kda_recurrent_tc_kernel(RecurParams p) {
             const uint8_t *stg = smem + s * kRecBytes;
             uint8_t *buf = smem + kOffPrep + b * kPrepBytes;
             // decay bookkeeping for key pt
-            const float g = reinterpret_cast<const float *>(stg + kRecGamma)[pt];
+            // a decay below 1e-30 (down to 0: a key that forgets at once) is
+            // taken as 1e-30, so 1 / c stays finite; the state row then keeps
+            // 1e-30 of its old value, far below fp32 resolution of the new one
+            const float g = fmaxf(reinterpret_cast<const float *>(stg + kRecGamma)[pt], 1e-30f);
             const bool ren = c * g < 1e-30f;
             fac[128 * b + pt] = ren ? c : 1.f;
             const float cu = ren ? 1.f : c;

@@ -295,13 +295,64 @@ def test_bad_cu_seqlens_reported_and_outputs_untouched():
     assert_parity(o, f, *run_oracle(d), "after-error")
 
 
-def test_gate_range_flagged():
+def test_gate_growth_flagged():
+    """Positive gates whose cumulative rise inside one chunk passes exp(80)
+    have no finite form in fp32 (neither factored nor exact): the device
+    flags them."""
     d = KI.make_case([32], H=1, seed=17)
     x = to_dev(d)
-    x["g"].fill_(-10.0)                               # 16 * 10 = 160 > 80
+    x["g"].fill_(6.0)                                 # 16 * 6 = 96 > 80
     K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"])
     rc = K.kda_last_device_error(torch.cuda.current_stream().cuda_stream)
     assert rc == K.STATUS_CODE["KDA_ERR_GATE_RANGE"]
+
+
+def out_of_range_chunk_heads(d):
+    """(chunk-heads whose cumulative log decay leaves [-80, 80], all chunk-heads)."""
+    cu = d["cu_seqlens"].tolist()
+    n_out = n_all = 0
+    for n in range(len(cu) - 1):
+        for t0 in range(cu[n], cu[n + 1], 16):
+            G = d["g"][t0:min(t0 + 16, cu[n + 1])].double().cumsum(0)
+            per_head = G.abs().amax(dim=(0, 2))
+            n_out += int((per_head > 80).sum())
+            n_all += per_head.numel()
+    return n_out, n_all
+
+
+@pytest.mark.parametrize("gval", [-5.0, -5.001, -6.0, -10.0, -60.0])
+def test_strong_uniform_decay(gval):
+    """A chunk whose cumulative log decay passes -80 in some channel takes the
+    exact (unfactored) form of A, P and the gated rows; -5 per token stays
+    just inside the factored form (16 * 5 = 80), -5.001 just outside. The
+    5-token tail chunk of the 37-token sequence stays factored. No flag."""
+    d = KI.make_case([37, 16, 100], H=2, seed=31, init_state=True)
+    d["g"] = torch.full_like(d["g"], gval)
+    o, f = run_gpu(d)
+    assert_parity(o, f, *run_oracle(d), f"g={gval}")
+
+
+def test_strong_mixed_decay_per_channel():
+    """Per-channel decays from about 0 to below -20 per token (logsigmoid of
+    N(-2, 4^2)), so chunks mix channels far outside the factored range with
+    ordinary ones, in a ragged packed batch."""
+    d = KI.make_case([200, 3, 77, 129], H=3, seed=32, init_state=True)
+    gen = torch.Generator().manual_seed(33)
+    x = torch.randn(d["g"].shape, generator=gen) * 4.0 - 2.0
+    d["g"] = torch.nn.functional.logsigmoid(x)
+    n_exact, n_all = out_of_range_chunk_heads(d)
+    assert 0 < n_exact < n_all, (n_exact, n_all)   # 30 of 84: both forms present
+    o, f = run_gpu(d)
+    assert_parity(o, f, *run_oracle(d), "mixed")
+
+
+def test_strong_decay_in_some_heads_only():
+    """One head decays strongly (exact form), the others not (factored):
+    the two forms side by side in one launch."""
+    d = KI.make_case([300], H=4, seed=34, init_state=True)
+    d["g"][:, 2, :] = -9.0
+    o, f = run_gpu(d)
+    assert_parity(o, f, *run_oracle(d), "head 2 strong")
 
 
 def test_host_pointer_rejected():

@@ -139,3 +139,26 @@ def test_preprocessing_with_each_recurrent_kernel(impl):
     o_ref, f_ref = oracle(d, True, True)
     check(o, o_ref, "o")
     check(f, f_ref, "final_state")
+
+
+@pytest.mark.parametrize("impl", [0, 1, 2], ids=["tcgen05", "warp_mma", "hybrid"])
+def test_preprocessing_strong_decay(impl):
+    """Gate logits far below 0 (log decays down to about -25 per token) make
+    the intra-chunk kernel take its exact form, which does the q/k
+    normalisation and the logsigmoid itself."""
+    d = KI.make_raw_case([150, 33], H=2, seed=70 + impl, init_state=True, mu=-6.0)
+    gen = torch.Generator().manual_seed(71)
+    d["g"] = d["g"] * 4.0 + 0.5 * torch.randn(d["g"].shape, generator=gen)
+    x = {n: d[n].cuda().contiguous() for n in ("q", "k", "v", "g", "beta")}
+    assert K.kda_set_recurrent_impl(impl) == 0
+    try:
+        o, f = K.chunk_prefill(x["q"], x["k"], x["v"], x["g"], x["beta"],
+                               initial_state=d["initial_state"].cuda(),
+                               cu_seqlens=d["cu_seqlens"].cuda(), scale=d["scale"],
+                               normalize_qk=True, gate_logits=True)
+        K.check_device_error()
+    finally:
+        K.kda_set_recurrent_impl(1)
+    o_ref, f_ref = oracle(d, True, True)
+    check(o, o_ref, "o")
+    check(f, f_ref, "final_state")
