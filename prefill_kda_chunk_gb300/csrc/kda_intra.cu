@@ -620,8 +620,10 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
 // item per warp at a time, warps strided over the list. With an empty list it
 // only reads the count. Otherwise the last CTA to finish zeroes the count (and
 // its own finish counter), so the next call starts from an empty list.
+// Two CTAs per SM: with the registers that frees it spills nothing, which
+// measured 2 % faster than three CTAs with spills.
 template <bool PRE>
-__global__ void __launch_bounds__(kIntraWarps * 32, 3)
+__global__ void __launch_bounds__(kIntraWarps * 32, 2)
 kda_intra_exact_kernel(IntraParams p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

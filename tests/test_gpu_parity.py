@@ -219,6 +219,36 @@ def test_segmented_calls(T, Bn):
     assert f3 is None and torch.equal(o3, o)
 
 
+def test_segmented_calls_strong_decay():
+    """The exact form in a segmented call: every segment's intra-chunk launch
+    lists its own out-of-range chunk-heads (one list, reused per segment on
+    the internal stream). Head 1 decays at -7 per token."""
+    T, Bn, H = 300, 2, 2
+    d = KI.make_case([T] * Bn, H=H, seed=45, init_state=True)
+    d["g"][:, 1, :] = -7.0
+    x = to_dev(d)
+    q, k, v, g = (x[n].view(Bn, T, H, 128) for n in ("q", "k", "v", "g"))
+    beta = x["beta"].view(Bn, T, H)
+    try:
+        K.kda_set_ring_slot_bytes(8 * Bn * H * 17408)       # 8 chunk positions per segment
+        o, f = K.chunk_prefill(q, k, v, g, beta, initial_state=x["initial_state"],
+                               scale=d["scale"])
+        K.check_device_error()
+    finally:
+        K.kda_set_ring_slot_bytes(0)
+    o_ref, f_ref = run_oracle(d)
+    assert_parity(o.view(Bn * T, H, 128), f, o_ref, f_ref, "segmented, strong decay")
+
+
+def test_split_replay_strong_decay():
+    """The exact form ahead of the split replay (state-only pass to the
+    midpoint, then both halves), every other channel at -6 per token."""
+    d = KI.make_case([1100], H=2, seed=46, init_state=True)
+    d["g"][:, :, ::2] = -6.0
+    o, f = run_gpu(d, packed=False)
+    assert_parity(o, f, *run_oracle(d), "split replay, strong decay")
+
+
 @pytest.mark.parametrize("T,B,init", [(1024, 1, False), (2003, 1, True), (1040, 3, True),
                                       (4096, 2, False)])
 def test_split_replay_lengths(T, B, init):

@@ -72,6 +72,18 @@ def test_noalloc_matches_allocating_entry_point_two_calls():
         _close(f_na, f_ref)
 
 
+def test_noalloc_strong_decay_matches():
+    """The exact form of strongly decaying chunks (its list lives in the
+    fixed scratch too): a packed batch with one head at -9 per token."""
+    d = KI.make_case([90, 40, 130], H=3, seed=33, init_state=True)
+    d["g"][:, 0, :] = -9.0
+    o_na, f_na = _run(K.kda_chunk_prefill_noalloc, d, True)
+    o_ref, f_ref = _run(K.kda_chunk_prefill, d, True)
+    K.check_device_error()
+    _close(o_na, o_ref)
+    _close(f_na, f_ref)
+
+
 def test_noalloc_rejects_oversized_call():
     # 8192 tokens x 64 heads: 512 chunks x 64 heads x 17408 B of chunk records
     # (~570 MB, all held at once by this entry point), above the 64 MiB array
