@@ -15,6 +15,10 @@ Three independently written forms of the same result:
 * ``unrolled`` (unrolled.py) -- the state written out as explicit products of
   per-token transition matrices, for a handful of tokens.
 
+And the gradients of the same map: ``recurrent_backward`` (kda_backward.c),
+the reverse pass of the token recurrence written line by line, pinned by
+central differences of its own forward pass.
+
 What is computed: Kimi Delta Attention keeps a fixed-size recurrent state per
 head that each new token updates ("Kimi K3 開源基礎設施", section "FlashKDA";
 "Kimi K3 的三個系統設計", section "第一個設計"). The update is the gated
@@ -39,7 +43,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "liboracle.so")
-_SOURCES = ["kda_recurrent.c", "kda_chunked.c"]
+_SOURCES = ["kda_recurrent.c", "kda_chunked.c", "kda_backward.c"]
 _lib = None
 _lock = threading.Lock()
 
@@ -77,6 +81,9 @@ def _load():
             lib.kda_oracle_chunked.restype = ctypes.c_int
             lib.kda_oracle_chunked.argtypes = [f32p] * 5 + [f64p, i64p] + [i64] * 5 + [
                 ctypes.c_double, f64p, i64, f64p, ctypes.c_int]
+            lib.kda_oracle_backward.restype = ctypes.c_int
+            lib.kda_oracle_backward.argtypes = [f64p] * 6 + [i64p] + [i64] * 4 + [
+                ctypes.c_double] + [f64p] * 10 + [ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -174,4 +181,57 @@ def chunked(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
     return o, fs
 
 
-__all__ = ["build", "recurrent", "chunked", "unrolled"]
+def recurrent_backward(q, k, v, g, beta, dout, initial_state=None, d_final_state=None,
+                       cu_seqlens=None, scale=None, mutation=0):
+    """Gradients of the token recurrence in fp64 (kda_backward.c), for the
+    loss L with dL/do = ``dout`` [T, H, V] and dL/d(final state) =
+    ``d_final_state`` [N, H, K, V] (None: 0). Inputs are taken as given, in
+    float64 (bf16 and fp32 values convert exactly).
+
+    Returns a dict of float64 numpy arrays: dq, dk, dg [T, H, K]; dv [T, H, V];
+    dbeta [T, H]; d_initial_state [N, H, K, V]; and the forward results o
+    [T, H, V] and final_state [N, H, K, V] of the same pass.
+
+    ``mutation`` plants a known mistake in the reverse pass (see
+    kda_backward.c); only the pin tests use it."""
+    q, k, v, g, beta, dout = (_f64(t) for t in (q, k, v, g, beta, dout))
+    if q.ndim != 3 or k.shape != q.shape or g.shape != q.shape:
+        raise ValueError("q, k, g must be [T, H, K]")
+    T, H, K = q.shape
+    if v.ndim != 3 or v.shape[:2] != (T, H) or dout.shape != v.shape:
+        raise ValueError("v and dout must be [T, H, V]")
+    V = v.shape[2]
+    if beta.shape != (T, H):
+        raise ValueError("beta must be [T, H]")
+    if cu_seqlens is None:
+        cu = np.array([0, T], dtype=np.int64)
+    else:
+        if hasattr(cu_seqlens, "detach"):
+            cu_seqlens = cu_seqlens.detach().cpu().numpy()
+        cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+        if cu[0] != 0 or cu[-1] != T or np.any(np.diff(cu) < 0):
+            raise ValueError("cu_seqlens must start at 0, end at T and not decrease")
+    N = len(cu) - 1
+    s0, dsf = _f64(initial_state), _f64(d_final_state)
+    for name, x in (("initial_state", s0), ("d_final_state", dsf)):
+        if x is not None and x.shape != (N, H, K, V):
+            raise ValueError(f"{name} must be [N, H, K, V]")
+    if scale is None:
+        scale = 1.0 / np.sqrt(K)
+    out = {"o": np.zeros((T, H, V)), "final_state": np.zeros((N, H, K, V)),
+           "dq": np.zeros((T, H, K)), "dk": np.zeros((T, H, K)), "dv": np.zeros((T, H, V)),
+           "dg": np.zeros((T, H, K)), "dbeta": np.zeros((T, H)),
+           "d_initial_state": np.zeros((N, H, K, V))}
+    d = ctypes.c_double
+    rc = _load().kda_oracle_backward(
+        _ptr(q, d), _ptr(k, d), _ptr(v, d), _ptr(g, d), _ptr(beta, d), _ptr(s0, d),
+        _ptr(cu, ctypes.c_int64), N, H, K, V, float(scale), _ptr(dout, d), _ptr(dsf, d),
+        _ptr(out["o"], d), _ptr(out["final_state"], d), _ptr(out["dq"], d), _ptr(out["dk"], d),
+        _ptr(out["dv"], d), _ptr(out["dg"], d), _ptr(out["dbeta"], d),
+        _ptr(out["d_initial_state"], d), int(mutation))
+    if rc:
+        raise RuntimeError(f"kda_oracle_backward failed ({rc})")
+    return out
+
+
+__all__ = ["build", "recurrent", "chunked", "unrolled", "recurrent_backward"]
