@@ -60,6 +60,9 @@ def parse():
                     help="leave the decode measurement out of the default line")
     ap.add_argument("--ring-slot-mb", type=float, default=None,
                     help="ring-slot size for segmented calls (library default if unset; <0 off)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the gradient call (kda_chunk_prefill_backward) on the workload "
+                         "instead of the prefill; prints its own line")
     ap.add_argument("--gate-mu", type=float, default=None,
                     help="mean of the gate pre-activation (g = logsigmoid(N(mu, 1))) instead of "
                          "the workload's; about -6 or below puts every chunk-head outside the "
@@ -303,6 +306,74 @@ def bench_decode(K, dev, N, H, steps, warmup, hbm):
                          "frac": gbs / hbm, "bytes_per_step": N * H * DECODE_BYTES}}
 
 
+# algorithmic bytes of the gradient call: per token-head q, k, v, dO (bf16)
+# and g, beta read, dq, dk, dv, dg, dbeta written (fp32); per (sequence, head)
+# the initial state and dL/d(final state) read and dL/d(initial state) written
+BWD_TOKEN_HEAD_BYTES = 4 * 128 * 2 + 128 * 4 + 4 + 4 * 128 * 4 + 4
+BWD_UNIT_BYTES = 3 * 128 * 128 * 4
+
+
+def bench_backward(K, dev, w, args, hbm):
+    """The gradient call on the workload's inputs (resident), CUDA events;
+    plus the fp64 gradient oracle on a bounded sample of host work."""
+    d = KI.make_inputs(w)
+    H, T = w.H, w.T
+    gen = torch.Generator().manual_seed(w.seed + 7)
+    n_seqs = len(d["seqlens"])
+    dout = torch.randn(T, H, 128, generator=gen).to(torch.bfloat16)
+    dsf = torch.randn(n_seqs, H, 128, 128, generator=gen) * 0.1
+    x = {n: d[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+    s0 = None if d["initial_state"] is None else d["initial_state"].to(dev)
+    cu = d["cu_seqlens"].to(dev) if w.varlen else None
+    if not w.varlen:
+        x = {n: t.view(1, T, *t.shape[1:]) for n, t in x.items()}
+    do_d, dsf_d = dout.to(dev).view(x["v"].shape), dsf.to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        return K.chunk_prefill_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], do_d,
+                                        initial_state=s0, cu_seqlens=cu, scale=d["scale"],
+                                        d_final_state=dsf_d)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    K.check_device_error()
+    torch.cuda.synchronize(dev)
+    steps = args.steps
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    K.check_device_error()
+    ms = a.elapsed_time(b) / steps
+    nbytes = T * H * BWD_TOKEN_HEAD_BYTES + n_seqs * H * BWD_UNIT_BYTES
+    gbs = nbytes / (ms / 1e3) / 1e9
+    line = {"metric": f"KDA prefill backward tokens/s (T={T}, H={H}, D=128) on 1 GB300",
+            "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "dtype": "fp32 (bf16 q, k, v, dO)", "data": "synthetic",
+            "config": dict(config_of(w, d), backward=True),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "traffic": None, "kernel": "kda_backward_kernel",
+                         "bytes_per_call": nbytes},
+            "gpu_launches": steps * (1 + int(w.varlen))}
+    if not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        Hs, Ts = min(H, 2), min(d["seqlens"][0], 1024)
+        sub = {n: d[n][:Ts, :Hs] for n in ("q", "k", "v", "g", "beta")}
+        t0 = time.perf_counter()
+        oracle.recurrent_backward(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"],
+                                  dout[:Ts, :Hs], scale=d["scale"])
+        sec = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": Ts * Hs / H / sec, "unit": "tokens/s", "cores": 1,
+                                "kind": "oracle",
+                                "sample": f"{Hs} of {H} heads x {Ts} tokens, {sec:.2f} s wall"}
+    return line
+
+
 def main():
     args = parse()
     rank, world, local = dist_setup()
@@ -338,6 +409,12 @@ def main():
     w = KI.WORKLOADS[args.workload]
     if args.gate_mu is not None:
         w = dataclasses.replace(w, mu=args.gate_mu)
+    if args.backward:
+        hbm, _, _ = load_peaks()
+        line = bench_backward(K, dev, w, args, hbm)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     d = KI.make_inputs(w)
     H = w.H
     cnt = workload_counts(d, H)

@@ -208,6 +208,45 @@ KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, 
                                    int64_t N, int64_t H, int64_t K, int64_t V, float scale,
                                    int flags, void *out, void *stream);
 
+/*
+ * kda_chunk_prefill_backward -- gradients of kda_chunk_prefill (training).
+ * The pages say that K3 trains with KDA ("Kimi K3 開源基礎設施"); this is the
+ * reverse mode of the same map, for a loss L with dL/do = d_out and
+ * dL/d(final_state) = d_final_state:
+ *
+ *   dq, dk, dg  fp32 [B*T, H, 128]  dL/dq, dL/dk, dL/dg (g = the log decay)
+ *   dv          fp32 [B*T, H, 128]  dL/dv
+ *   dbeta       fp32 [B*T, H]       dL/dbeta
+ *   d_initial_state  fp32 [N, H, 128, 128] or NULL (not written):
+ *               dL/d(initial_state) (the gradient of a zero state when
+ *               initial_state is NULL)
+ *
+ * Inputs exactly as for kda_chunk_prefill (q, k, v bf16; g, beta fp32;
+ * initial_state, cu_seqlens, B, T, H, K, V, N, scale), plus
+ *   d_out          bf16 [B*T, H, 128], device
+ *   d_final_state  fp32 [N, H, 128, 128] or NULL (= 0)
+ * Outputs are device memory the caller owns, every element written; none may
+ * overlap an input or another output. Alignment: 16 bytes for every array
+ * but beta, dbeta and cu_seqlens (4 bytes). No input preprocessing: q, k
+ * and g are used as given. Any finite g.
+ *
+ * Method: one CTA per (sequence, head) walks the sequence backwards token
+ * by token, the state recomputed from checkpoints taken every 16 tokens.
+ * Workspace (the call's stream's, as for the prefill): 64 KiB per 16-token
+ * chunk per head plus 1 MiB per (sequence, head). Errors as for the prefill
+ * (bad cu_seqlens contents are flagged on the device, see
+ * kda_last_device_error).
+ */
+KDA_API kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *v,
+                                              const float *g, const float *beta,
+                                              const float *initial_state,
+                                              const int32_t *cu_seqlens, int64_t B, int64_t T,
+                                              int64_t H, int64_t K, int64_t V, int64_t N,
+                                              float scale, const void *d_out,
+                                              const float *d_final_state, float *dq, float *dk,
+                                              float *dv, float *dg, float *dbeta,
+                                              float *d_initial_state, void *stream);
+
 /* Static text for a status code (never NULL). */
 KDA_API const char *kda_status_string(kda_status status);
 

@@ -12,10 +12,12 @@ from ._binding import (  # noqa: F401
     KdaError,
     check_device_error,
     chunk_prefill,
+    chunk_prefill_backward,
     decode_step,
     kda_decode_step,
     kda_build_info,
     kda_chunk_prefill,
+    kda_chunk_prefill_backward,
     kda_chunk_prefill_ex,
     kda_chunk_prefill_noalloc,
     kda_last_device_error,
@@ -29,4 +31,4 @@ from ._binding import (  # noqa: F401
     lib,
 )
 
-__version__ = "0.2.0"
+__version__ = "0.3.0"

@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             L.kda_chunk_prefill_noalloc.argtypes = [vp] * 7 + [i64] * 6 + [f32, vp, vp, vp]
             L.kda_decode_step.restype = ctypes.c_int
             L.kda_decode_step.argtypes = [vp] * 7 + [i64] * 4 + [f32, ctypes.c_int, vp, vp]
+            L.kda_chunk_prefill_backward.restype = ctypes.c_int
+            L.kda_chunk_prefill_backward.argtypes = [vp] * 7 + [i64] * 6 + [f32] + [vp] * 9
             L.kda_status_string.restype = ctypes.c_char_p
             L.kda_status_string.argtypes = [ctypes.c_int]
             L.kda_last_device_error.restype = ctypes.c_int
@@ -110,6 +112,15 @@ def kda_decode_step(q, k, v, g, beta, state_in, state_out, N, H, K, V, scale, fl
     """The one-token decode C entry point, pointers as ints (0 = NULL)."""
     return lib().kda_decode_step(q, k, v, g, beta, state_in, state_out, N, H, K, V, scale, flags,
                                  out, stream)
+
+
+def kda_chunk_prefill_backward(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V, N,
+                               scale, d_out, d_final_state, dq, dk, dv, dg, dbeta,
+                               d_initial_state, stream) -> int:
+    """The gradient C entry point, pointers as ints (0 = NULL)."""
+    return lib().kda_chunk_prefill_backward(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H,
+                                            K, V, N, scale, d_out, d_final_state, dq, dk, dv, dg,
+                                            dbeta, d_initial_state, stream)
 
 
 def kda_status_string(code: int) -> str:
@@ -281,6 +292,70 @@ def decode_step(q, k, v, g, beta, state=None, scale=None, out=None, state_out=No
     if rc != 0:
         raise KdaError(rc, "kda_decode_step")
     return out, state_out
+
+
+def chunk_prefill_backward(q, k, v, g, beta, d_out, initial_state=None, cu_seqlens=None,
+                           scale=None, d_final_state=None, d_initial_state=True, stream=None):
+    """Gradients of ``chunk_prefill`` on the current CUDA device.
+
+    Inputs as for chunk_prefill (no preprocessing flags), plus d_out (bf16,
+    like v: dL/do) and d_final_state (fp32 [N, H, 128, 128] or None = 0).
+    Returns (dq, dk, dv, dg, dbeta, d_initial_state), fp32, shaped like q, k,
+    v, g, beta and [N, H, 128, 128]; d_initial_state is None when asked for
+    with False.
+    """
+    import torch
+
+    if q.dim() == 4:
+        B, T, H, K = q.shape
+    elif q.dim() == 3:
+        B, (T, H, K) = 1, q.shape
+    else:
+        raise ValueError("q must be [T, H, K] or [B, T, H, K]")
+    V = v.shape[-1]
+    if cu_seqlens is not None:
+        if B != 1:
+            raise ValueError("cu_seqlens needs B == 1")
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("g", g, torch.float32),
+                        ("beta", beta, torch.float32), ("d_out", d_out, torch.bfloat16)):
+        if t.dtype != dt:
+            raise ValueError(f"{name} must be {dt}")
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if k.shape != q.shape or g.shape != q.shape or v.shape[:-1] != q.shape[:-1]:
+        raise ValueError("q, k, g must share a shape and v must match it but for the last dim")
+    if d_out.shape != v.shape:
+        raise ValueError("d_out must be shaped like v")
+    if tuple(beta.shape) != tuple(q.shape[:-1]):
+        raise ValueError("beta must be q.shape[:-1]")
+    for name, t in (("initial_state", initial_state), ("d_final_state", d_final_state)):
+        if t is not None:
+            if t.dtype != torch.float32 or not t.is_contiguous() or not t.is_cuda:
+                raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor")
+            if tuple(t.shape) != (N, H, K, V):
+                raise ValueError(f"{name} must be [{N}, {H}, {K}, {V}]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(K)
+    f32 = dict(dtype=torch.float32, device=q.device)
+    dq, dk, dg = (torch.empty(q.shape, **f32) for _ in range(3))
+    dv = torch.empty(v.shape, **f32)
+    dbeta = torch.empty(beta.shape, **f32)
+    ds0 = torch.empty((N, H, K, V), **f32) if d_initial_state else None
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = kda_chunk_prefill_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                    _ptr(initial_state), _ptr(cu_seqlens), B, T, H, K, V, N,
+                                    float(scale), _ptr(d_out), _ptr(d_final_state), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), _ptr(dg), _ptr(dbeta), _ptr(ds0), stream)
+    if rc != 0:
+        raise KdaError(rc, "kda_chunk_prefill_backward")
+    return dq, dk, dv, dg, dbeta, ds0
 
 
 def check_device_error(stream=None):

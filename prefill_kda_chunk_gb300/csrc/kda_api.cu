@@ -276,9 +276,10 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
 }
 
 const char *kda_build_info(void) {
-    return "prefill_kda_chunk_gb300 0.2 (sm_103a; intra-chunk mma.sync; recurrent warp-MMA chain "
-           "with bulk-async staged records and split replay, tcgen05 and hybrid kernels opt-in; "
-           "decode step; in-kernel q/k normalisation and gate logits)";
+    return "prefill_kda_chunk_gb300 0.3 (sm_103a; intra-chunk mma.sync with an exact form for "
+           "strong decay; recurrent warp-MMA chain with bulk-async staged records and split "
+           "replay, tcgen05 and hybrid kernels opt-in; decode step; in-kernel q/k normalisation "
+           "and gate logits; token-serial gradients)";
 }
 
 int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, int has_cu_seqlens) {
@@ -491,6 +492,114 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
     }
     if (cudaStreamWaitEvent(stream, ev_recur[pl.nseg - 1], 0) != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *v,
+                                      const float *g, const float *beta,
+                                      const float *initial_state, const int32_t *cu_seqlens,
+                                      int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                                      int64_t N, float scale, const void *d_out,
+                                      const float *d_final_state, float *dq, float *dk,
+                                      float *dv, float *dg, float *dbeta,
+                                      float *d_initial_state, void *stream_) {
+    // ---- checks that need no GPU
+    if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_DIM;
+    Plan pl;
+    kda_status rc = plan_sizes(B, T, H, N, cu_seqlens != nullptr, &pl);
+    if (rc != KDA_OK) return rc;
+    if (N * H > (int64_t(1) << 31) - 1) return KDA_ERR_BAD_SHAPE;
+    if (pl.tokens > 0 && (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv || !dg ||
+                          !dbeta))
+        return KDA_ERR_NULL_ARG;
+    if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(g, 16) ||
+        misaligned(d_out, 16) || misaligned(initial_state, 16) ||
+        misaligned(d_final_state, 16) || misaligned(dq, 16) || misaligned(dk, 16) ||
+        misaligned(dv, 16) || misaligned(dg, 16) || misaligned(d_initial_state, 16) ||
+        misaligned(beta, 4) || misaligned(dbeta, 4) || misaligned(cu_seqlens, 4))
+        return KDA_ERR_MISALIGNED;
+    const int64_t nqkv = pl.tokens * H * 128 * 2, nf = pl.tokens * H * 128 * 4;
+    const int64_t nb = pl.tokens * H * 4, ns = N * H * 128 * 128 * 4;
+    const int64_t ncu = cu_seqlens ? (N + 1) * 4 : 0;
+    const void *ins[] = {q, k, v, g, beta, initial_state, cu_seqlens, d_out, d_final_state};
+    const int64_t nins[] = {nqkv, nqkv, nqkv, nf, nb, ns, ncu, nqkv, ns};
+    void *outs[] = {dq, dk, dv, dg, dbeta, d_initial_state};
+    const int64_t nouts[] = {nf, nf, nf, nf, nb, ns};
+    for (int o = 0; o < 6; ++o) {
+        for (int i = 0; i < 9; ++i)
+            if (overlap(outs[o], nouts[o], ins[i], nins[i])) return KDA_ERR_ALIAS;
+        for (int o2 = o + 1; o2 < 6; ++o2)
+            if (overlap(outs[o], nouts[o], outs[o2], nouts[o2])) return KDA_ERR_ALIAS;
+    }
+
+    // ---- device checks
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState &st = g_devices[dev];
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return KDA_ERR_CUDA;
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
+    if (!st.ready) {
+        if (capturing) return KDA_ERR_CAPTURE;
+        rc = init_device(dev, st);
+        if (rc != KDA_OK) return rc;
+    }
+    if (stream != nullptr && !capturing) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return KDA_ERR_CUDA;
+        if (sdev != dev) return KDA_ERR_WRONG_DEVICE;
+    }
+    const void *ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, d_out, d_final_state,
+                          dq, dk, dv, dg, dbeta, d_initial_state};
+    for (const void *p : ptrs) {
+        if (capturing) break;  // pointer queries are not stream work
+        rc = check_pointer_device(p, dev);
+        if (rc != KDA_OK) return rc;
+    }
+
+    // workspace: flag block, chunk offsets (packed), one checkpoint state per
+    // 16 tokens per head, and a ring of 16 states per (sequence, head)
+    const int64_t chunks = cu_seqlens ? (pl.tokens + 15 * N) / 16 : B * ((T + 15) / 16);
+    const int64_t state_bytes = 128 * 128 * 4;
+    const int64_t ckpt_bytes = chunks * H * state_bytes, ring_bytes = N * H * 16 * state_bytes;
+    const int64_t need = 256 + pl.off_bytes + ckpt_bytes + ring_bytes;
+    StreamWorkspace &ws = st.ws[stream];
+    if (ws.bytes < static_cast<size_t>(need)) {
+        if (capturing) return KDA_ERR_CAPTURE;
+        if (ws.ptr != nullptr && cudaFreeAsync(ws.ptr, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        ws.ptr = nullptr;
+        ws.bytes = 0;
+        if (cudaMallocAsync(&ws.ptr, need, stream) != cudaSuccess) {
+            ws.ptr = nullptr;
+            return KDA_ERR_CUDA;
+        }
+        ws.bytes = need;
+        if (cudaMemsetAsync(ws.ptr, 0, 256, stream) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    uint8_t *wsb = static_cast<uint8_t *>(ws.ptr);
+
+    kda::ChunkGeometry geo{};
+    geo.cu = cu_seqlens;
+    geo.chunk_off = cu_seqlens ? reinterpret_cast<const int32_t *>(wsb + 256) : nullptr;
+    geo.call_flags = reinterpret_cast<const int *>(wsb);
+    geo.seq_len = cu_seqlens ? pl.tokens : T;
+    geo.n_seqs = static_cast<int32_t>(N);
+    geo.n_heads = static_cast<int32_t>(H);
+    geo.chunks_per_seq = static_cast<int32_t>((T + 15) / 16);
+    geo.pos_begin = 0;
+    geo.seg_len = geo.chunks_per_seq;
+    geo.slot_stride = geo.chunks_per_seq;
+    if (cu_seqlens != nullptr &&
+        kda::launch_varlen_prologue(cu_seqlens, geo.n_seqs, pl.tokens,
+                                    reinterpret_cast<int32_t *>(wsb + 256),
+                                    reinterpret_cast<int *>(wsb), st.err, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    float *ckpt = reinterpret_cast<float *>(wsb + 256 + pl.off_bytes);
+    float *ring = reinterpret_cast<float *>(wsb + 256 + pl.off_bytes + ckpt_bytes);
+    const kda::BackParams p{q, k, v, g, beta, initial_state, d_out, d_final_state, scale,
+                            dq, dk, dv, dg, dbeta, d_initial_state, ckpt, ring, geo};
+    return kda::launch_backward(p, N * H, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 static void free_timing() {

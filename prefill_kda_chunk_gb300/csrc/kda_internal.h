@@ -77,6 +77,25 @@ struct DecodeParams {
     int pre;                   // kPreNormQK | kPreGateLogits (input preprocessing)
 };
 
+// Gradients of the prefill for N*H independent (sequence, head) units; see
+// kda_backward.cu. The geometry's cu / chunk_off / call_flags / seq_len /
+// chunks_per_seq / n_heads are used as in the prefill.
+struct BackParams {
+    const void *q, *k, *v;     // bf16 [tokens, H, 128]
+    const float *g;            // [tokens, H, 128] per-token log decay
+    const float *beta;         // [tokens, H]
+    const float *s0;           // [N, H, 128, 128] or nullptr (zero state)
+    const void *dout;          // bf16 [tokens, H, 128]: dL/do
+    const float *dsf;          // [N, H, 128, 128] or nullptr: dL/d(final state)
+    float scale;
+    float *dq, *dk, *dv, *dg;  // fp32 [tokens, H, 128]
+    float *dbeta;              // fp32 [tokens, H]
+    float *ds0;                // fp32 [N, H, 128, 128] or nullptr: dL/d(initial state)
+    float *ckpt;               // workspace: one state per 16 tokens per head
+    float *ring;               // workspace: 16 states per unit
+    ChunkGeometry geo;
+};
+
 // Per-device, once: raise the dynamic shared-memory limits of the kernels.
 cudaError_t configure_intra();
 cudaError_t configure_recurrent();
@@ -97,5 +116,6 @@ cudaError_t launch_recurrent_tc(const RecurParams &p, cudaStream_t stream);  // 
 // warp-MMA chain with the output product on tcgen05; needs IntraParams::qg_tc = 1
 cudaError_t launch_recurrent_hybrid(const RecurParams &p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int64_t units, cudaStream_t stream);
+cudaError_t launch_backward(const BackParams &p, int64_t units, cudaStream_t stream);
 
 }  // namespace kda

@@ -149,3 +149,27 @@ def test_prefill_ex_flags(lib):
     assert K.kda_chunk_prefill_ex(**args, flags=8) == K.STATUS_CODE["KDA_ERR_BAD_FLAGS"]
     # known flags pass the host checks and reach the argument checks after them
     assert K.kda_chunk_prefill_ex(**dict(args, K=64), flags=3) == K.STATUS_CODE["KDA_ERR_UNSUPPORTED_DIM"]
+
+
+def bwd(**kw):
+    args = dict(q=A, k=A + 0x100000, v=A + 0x200000, g=A + 0x300000, beta=A + 0x400000,
+                initial_state=0, cu_seqlens=0, B=1, T=16, H=1, K=128, V=128, N=1, scale=1.0,
+                d_out=A + 0x500000, d_final_state=0, dq=A + 0x600000, dk=A + 0x700000,
+                dv=A + 0x800000, dg=A + 0x900000, dbeta=A + 0xA00000, d_initial_state=0,
+                stream=0)
+    args.update(kw)
+    return K.kda_chunk_prefill_backward(**args)
+
+
+def test_backward_argument_checks(lib):
+    S = K.STATUS_CODE
+    assert bwd(K=64) == S["KDA_ERR_UNSUPPORTED_DIM"]
+    assert bwd(H=0) == S["KDA_ERR_BAD_SHAPE"]
+    assert bwd(N=2) == S["KDA_ERR_BAD_SHAPE"]              # N != B without cu_seqlens
+    assert bwd(d_out=0) == S["KDA_ERR_NULL_ARG"]
+    assert bwd(dbeta=0) == S["KDA_ERR_NULL_ARG"]
+    assert bwd(dq=A + 0x600004) == S["KDA_ERR_MISALIGNED"]
+    assert bwd(dbeta=A + 0xA00002) == S["KDA_ERR_MISALIGNED"]
+    assert bwd(dk=A) == S["KDA_ERR_ALIAS"]                  # output over q
+    assert bwd(dv=A + 0x600000) == S["KDA_ERR_ALIAS"]       # two outputs overlap
+    assert bwd(d_initial_state=A + 0x500000) == S["KDA_ERR_ALIAS"]   # over d_out

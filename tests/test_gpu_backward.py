@@ -1,0 +1,151 @@
+"""Gradients of the prefill (kda_chunk_prefill_backward) against the fp64
+gradient oracle, through the C ABI.
+
+Same bar as the forward parity tests, for every output separately: relative
+L2 error <= 1e-2 and max abs error <= 2e-2 * max|ref|. dL/do is a seeded
+bf16 tensor and dL/d(final state) a seeded fp32 one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import kda_inputs as KI
+import prefill_kda_chunk_gb300 as K
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+MAX_ABS = 2e-2
+NAMES = ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from prefill_kda_chunk_gb300 import build
+    build.build()
+    K.lib()
+
+
+def make(seqlens, H, seed, init=True, dsf=True):
+    d = KI.make_case(seqlens, H=H, seed=seed, init_state=init)
+    gen = torch.Generator().manual_seed(seed + 1000)
+    T, N = sum(seqlens), len(seqlens)
+    d["dout"] = torch.randn(T, H, 128, generator=gen).to(torch.bfloat16)
+    d["dsf"] = (torch.randn(N, H, 128, 128, generator=gen) * 0.1) if dsf else None
+    return d
+
+
+def oracle_grads(d):
+    import oracle
+    r = oracle.recurrent_backward(d["q"], d["k"], d["v"], d["g"], d["beta"], d["dout"],
+                                  initial_state=d["initial_state"], d_final_state=d["dsf"],
+                                  cu_seqlens=d["cu_seqlens"], scale=d["scale"])
+    return [r[n] for n in NAMES]
+
+
+def gpu_grads(d, packed=True):
+    x = {n: d[n].cuda().contiguous() for n in ("q", "k", "v", "g", "beta", "dout")}
+    s0 = None if d["initial_state"] is None else d["initial_state"].cuda()
+    dsf = None if d["dsf"] is None else d["dsf"].cuda()
+    cu = d["cu_seqlens"].cuda() if packed else None
+    if not packed:   # fixed-length batch: [B, T, H, 128]
+        B = len(d["seqlens"])
+        x = {n: t.view(B, -1, *t.shape[1:]) for n, t in x.items()}
+    out = K.chunk_prefill_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["dout"],
+                                   initial_state=s0, cu_seqlens=cu, scale=d["scale"],
+                                   d_final_state=dsf)
+    K.check_device_error()
+    return out
+
+
+def check(x, ref, tag):
+    x = x.detach().double().cpu().numpy().reshape(ref.shape)
+    assert np.isfinite(x).all(), tag
+    rel = np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300)
+    mx = np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-300)
+    assert rel <= REL_L2 and mx <= MAX_ABS, f"{tag}: rel {rel:.2e} max {mx:.2e}"
+
+
+def check_all(d, got, tag):
+    for name, x, ref in zip(NAMES, got, oracle_grads(d)):
+        check(x, ref, f"{tag} {name}")
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 40])
+@pytest.mark.parametrize("init", [False, True])
+def test_backward_single_sequence(T, init):
+    d = make([T], H=2, seed=T + 10 * init, init=init)
+    check_all(d, gpu_grads(d), f"T={T}")
+
+
+def test_backward_ragged_packed_batch():
+    d = make([37, 0, 129, 16, 5], H=3, seed=21)
+    check_all(d, gpu_grads(d), "ragged")
+
+
+def test_backward_fixed_batch():
+    d = make([70, 70], H=2, seed=22)
+    check_all(d, gpu_grads(d, packed=False), "fixed B=2")
+
+
+def test_backward_without_final_state_gradient():
+    d = make([50], H=2, seed=23, dsf=False)
+    check_all(d, gpu_grads(d), "dsf=None")
+
+
+def test_backward_strong_decay():
+    d = make([64, 9], H=2, seed=24)
+    d["g"] = torch.full_like(d["g"], -9.0)
+    check_all(d, gpu_grads(d), "g=-9")
+
+
+def test_backward_zero_tokens_passes_state_gradient():
+    d = make([0, 0], H=2, seed=25)
+    got = gpu_grads(d)
+    torch.cuda.synchronize()
+    assert torch.equal(got[5].cpu(), d["dsf"])
+
+
+def test_backward_longer_sequence():
+    """Several hundred tokens in several heads: dS carried over many
+    checkpoint segments."""
+    d = make([700], H=4, seed=26)
+    check_all(d, gpu_grads(d), "T=700")
+
+
+def test_backward_bad_cu_seqlens_flagged():
+    d = make([20, 30], H=1, seed=27)
+    x = {n: d[n].cuda().contiguous() for n in ("q", "k", "v", "g", "beta", "dout")}
+    bad = torch.tensor([0, 35, 30], dtype=torch.int32, device="cuda")
+    K.chunk_prefill_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["dout"],
+                             cu_seqlens=bad)
+    rc = K.kda_last_device_error(torch.cuda.current_stream().cuda_stream)
+    assert rc == K.STATUS_CODE["KDA_ERR_BAD_CU_SEQLENS"]
+
+
+def test_backward_consistent_with_forward_by_directional_derivative():
+    """The loss is affine in v (the state is linear in v and the initial
+    state), so the GPU forward's L(v + D) - L(v - D) equals <dL/dv, 2 D>
+    exactly but for rounding: this ties the two GPU paths together. D is
+    the bf16-representable step actually taken."""
+    d = make([48], H=1, seed=28, init=True)
+    got = gpu_grads(d)
+    x = {n: d[n].cuda().contiguous() for n in ("q", "k", "g", "beta")}
+    s0 = d["initial_state"].cuda()
+    gen = torch.Generator().manual_seed(5)
+    step = 0.25 * torch.randn(d["v"].shape, generator=gen)
+    vp = (d["v"].float() + step).to(torch.bfloat16)
+    vm = (d["v"].float() - step).to(torch.bfloat16)
+
+    def loss(vv):
+        o, f = K.chunk_prefill(x["q"], x["k"], vv.cuda(), x["g"], x["beta"],
+                               initial_state=s0, scale=d["scale"])
+        torch.cuda.synchronize()
+        return float((o.double().cpu() * d["dout"].double()).sum()
+                     + (f.double().cpu() * d["dsf"].double()).sum())
+
+    diff = loss(vp) - loss(vm)
+    an = float((got[2].double().cpu() * (vp.double() - vm.double())).sum())
+    assert abs(diff - an) <= 0.03 * max(1.0, abs(an)), (diff, an)
