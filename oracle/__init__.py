@@ -17,7 +17,9 @@ Three independently written forms of the same result:
 
 And the gradients of the same map: ``recurrent_backward`` (kda_backward.c),
 the reverse pass of the token recurrence written line by line, pinned by
-central differences of its own forward pass.
+central differences of its own forward pass; and ``chunked_backward``
+(chunked_backward.py), the reverse pass of the chunk-wise WY form, checked
+against it.
 
 What is computed: Kimi Delta Attention keeps a fixed-size recurrent state per
 head that each new token updates ("Kimi K3 開源基礎設施", section "FlashKDA";
@@ -48,6 +50,7 @@ _lib = None
 _lock = threading.Lock()
 
 from .unrolled import unrolled  # noqa: E402  (pure numpy, no build needed)
+from .chunked_backward import chunked_backward  # noqa: E402  (pure numpy)
 
 
 def build(force: bool = False) -> str:
@@ -234,4 +237,4 @@ def recurrent_backward(q, k, v, g, beta, dout, initial_state=None, d_final_state
     return out
 
 
-__all__ = ["build", "recurrent", "chunked", "unrolled", "recurrent_backward"]
+__all__ = ["build", "recurrent", "chunked", "unrolled", "recurrent_backward", "chunked_backward"]

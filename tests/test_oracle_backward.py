@@ -8,7 +8,9 @@ other than itself:
   here by hand;
 * an empty sequence passes the final-state gradient straight through, and a
   packed batch equals its sequences run one by one;
-* each planted mistake in the reverse pass fails a finite-difference pin.
+* each planted mistake in the reverse pass fails a finite-difference pin;
+* the chunk-wise reverse pass (oracle/chunked_backward.py), written from the
+  chunk algebra, equals it at several chunk sizes.
 """
 import numpy as np
 import pytest
@@ -134,3 +136,33 @@ def test_each_planted_mistake_fails_a_pin(mutation):
     grads = run(x, mutation=mutation)
     worst = max(fd_error(x, name, grads) for name in GRAD)
     assert worst > 1e-3, (mutation, worst)
+
+
+def chunked(x, chunk):
+    return oracle.chunked_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["dout"],
+                                   initial_state=x["s0"], d_final_state=x["dsf"],
+                                   cu_seqlens=x["cu"], scale=x["scale"], chunk=chunk)
+
+
+KEYS = ("o", "final_state", "dq", "dk", "dv", "dg", "dbeta", "d_initial_state")
+
+
+@pytest.mark.parametrize("chunk", [1, 3, 16, 64])
+def test_chunked_reverse_pass_equals_token_reverse_pass(chunk):
+    x = case([37, 0, 20, 16], H=2, seed=12)
+    ref, got = run(x), chunked(x, chunk)
+    for key in KEYS:
+        np.testing.assert_allclose(got[key], ref[key], rtol=0,
+                                   atol=1e-12 * max(1.0, np.abs(ref[key]).max()), err_msg=key)
+
+
+def test_chunked_reverse_pass_strong_decay_no_states():
+    """Per-pair exponentials of the chunk form at decays far past the
+    factored range; no initial state and no final-state gradient."""
+    x = case([40], H=1, seed=13, init=False)
+    x["g"] = x["g"] * 0 - 8.0
+    x["dsf"] = None
+    ref, got = run(x), chunked(x, 16)
+    for key in KEYS:
+        np.testing.assert_allclose(got[key], ref[key], rtol=0,
+                                   atol=1e-12 * max(1.0, np.abs(ref[key]).max()), err_msg=key)
