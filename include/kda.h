@@ -140,8 +140,7 @@ KDA_API kda_status kda_chunk_prefill(const void *q, const void *k, const void *v
  * kda_chunk_prefill_ex -- kda_chunk_prefill with input preprocessing:
  * `flags` is a bitwise OR of KDA_PRE_* (0 = kda_chunk_prefill exactly). An
  * unknown bit returns KDA_ERR_BAD_FLAGS. Everything else, including the
- * gate-range precondition on the resulting log decays, is as for
- * kda_chunk_prefill.
+ * gate range of the resulting log decays, is as for kda_chunk_prefill.
  */
 KDA_API kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v,
                                         const float *g, const float *beta,

@@ -16,8 +16,8 @@
 // columns 4 (t % 32) .. +3 of rows t / 32 + 8 m, m = 0..15, so every warp
 // load and store is one contiguous 512-byte row. The state is read once and
 // written once: the kernel is bound by HBM bandwidth (131,072 + 1,540 B per
-// (sequence, head)). Exponentials are taken per channel exactly, so there is
-// no gate-range precondition here. With the preprocessing flags, q and k are
+// (sequence, head)). Exponentials are taken per channel exactly, so any
+// finite log decay is fine. With the preprocessing flags, q and k are
 // divided by their L2 norms (a block reduction) and g is read as gate logits.
 
 #include "kda_device.cuh"

@@ -24,8 +24,9 @@
 //     address, zeroing its flag block); make that first call before any
 //     stream capture.
 //   - Device-side errors of this entry point (bad cu_seqlens contents, a
-//     bounded wait that ran out, the gate-range precondition) are recorded
-//     in the array's flag block; kda_last_device_error() does not see them.
+//     bounded wait that ran out, a log decay rising by more than 80 within a
+//     chunk) are recorded in the array's flag block; kda_last_device_error()
+//     does not see them.
 
 #include <cuda_runtime.h>
 

@@ -291,7 +291,7 @@ def test_deterministic():
 
 
 def test_strong_decay_and_extreme_beta():
-    """Decay close to the precondition bound and beta at the ends of (0, 1)."""
+    """Decay just inside the factored range and beta at the ends of (0, 1)."""
     d = KI.make_case([64], H=2, seed=14, init_state=True)
     d["g"] = torch.full_like(d["g"], -4.5)          # 16 * 4.5 = 72 < 80 per chunk
     d["beta"][::2] = 1.0
