@@ -25,7 +25,8 @@
 // live in the layout of the decode kernel: 256 threads, thread t holding
 // columns 4 (t % 32) .. +3 of rows t / 32 + 8 m, m = 0..15, so every warp
 // access is one contiguous 512-byte row; column sums (S'^T k, dS^T k) go
-// through shared memory and row sums (four per row) through warp shuffles.
+// through shared memory and row sums (four per row) through warp
+// reduce-scatters (31 shuffles per 32 sums).
 // All arithmetic is fp32; q, k, v and dO are read as bf16.
 //
 // This is the first, token-serial form: its time is the serial chain of
@@ -225,29 +226,42 @@ kda_backward_kernel(BackParams p) {
                 if (lane == 0) sm.dbeta_part[warp] = db;
             }
             __syncthreads();
-            // row sums: S_t dO, dS w, S' x (before the erase), dS' o S_{t-1}
+            // row sums: S_t dO, dS w, S' x (before the erase), dS' o S_{t-1}.
+            // Per half of this thread's rows, the 32 partials (4 sums x 8 rows)
+            // reduce over the warp in one butterfly reduce-scatter of 31
+            // shuffles; lane l then holds sum l / 8 of row 8 hf + l % 8.
             const float4 w4 = reinterpret_cast<const float4 *>(sm.w)[lane];
             const float4 x4 = reinterpret_cast<const float4 *>(sm.x)[lane];
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int i = warp + 8 * m;
-                const float a = sm.a[i], kb = b * sm.k[i];
-                float4 st;
-                st.x = fmaf(a, S[m].x, kb * w4.x); st.y = fmaf(a, S[m].y, kb * w4.y);
-                st.z = fmaf(a, S[m].z, kb * w4.z); st.w = fmaf(a, S[m].w, kb * w4.w);
-                const float r_dq = warp_sum(dot4(st, do4));
-                const float r_dsw = warp_sum(dot4(dS[m], w4));
-                const float r_spx = warp_sum(a * dot4(S[m], x4));
-                dS[m].x = fmaf(-kb, x4.x, dS[m].x); dS[m].y = fmaf(-kb, x4.y, dS[m].y);
-                dS[m].z = fmaf(-kb, x4.z, dS[m].z); dS[m].w = fmaf(-kb, x4.w, dS[m].w);
-                const float r_da = warp_sum(dot4(dS[m], S[m]));
-                if (lane == 0) {
-                    sm.rowq[0][i] = scale * r_dq;
-                    sm.rowq[1][i] = r_dsw;
-                    sm.rowq[2][i] = r_spx;
-                    sm.rowq[3][i] = r_da;
+            for (int hf = 0; hf < 2; ++hf) {
+                float v[32];
+#pragma unroll
+                for (int mm = 0; mm < 8; ++mm) {
+                    const int m = 8 * hf + mm, i = warp + 8 * m;
+                    const float a = sm.a[i], kb = b * sm.k[i];
+                    float4 st;
+                    st.x = fmaf(a, S[m].x, kb * w4.x); st.y = fmaf(a, S[m].y, kb * w4.y);
+                    st.z = fmaf(a, S[m].z, kb * w4.z); st.w = fmaf(a, S[m].w, kb * w4.w);
+                    v[mm] = dot4(st, do4);
+                    v[8 + mm] = dot4(dS[m], w4);
+                    v[16 + mm] = a * dot4(S[m], x4);
+                    dS[m].x = fmaf(-kb, x4.x, dS[m].x); dS[m].y = fmaf(-kb, x4.y, dS[m].y);
+                    dS[m].z = fmaf(-kb, x4.z, dS[m].z); dS[m].w = fmaf(-kb, x4.w, dS[m].w);
+                    v[24 + mm] = dot4(dS[m], S[m]);
+                    dS[m].x *= a; dS[m].y *= a; dS[m].z *= a; dS[m].w *= a;
                 }
-                dS[m].x *= a; dS[m].y *= a; dS[m].z *= a; dS[m].w *= a;
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+                    const bool up = (lane & o) != 0;
+#pragma unroll
+                    for (int jj = 0; jj < o; ++jj) {
+                        const float send = up ? v[jj] : v[jj + o];
+                        const float keep = up ? v[jj + o] : v[jj];
+                        v[jj] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    }
+                }
+                const int qi = lane >> 3, i = warp + 8 * (8 * hf + (lane & 7));
+                sm.rowq[qi][i] = (qi == 0) ? scale * v[0] : v[0];
             }
             __syncthreads();
             if (t < kDim) {
