@@ -266,6 +266,12 @@ KDA_API kda_status kda_workspace_release(void);
 /* Workspace bytes a call with these sizes needs (0 on bad sizes). Host only. */
 KDA_API int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, int has_cu_seqlens);
 
+/* The same for kda_chunk_prefill_backward: 256 B of flags, the packed chunk
+ * offsets, 64 KiB per 16-token chunk per head and 1 MiB per (sequence,
+ * head). Both entry points share the stream's buffer, grown to the larger. */
+KDA_API int64_t kda_backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N,
+                                             int has_cu_seqlens);
+
 /*
  * Measurement hook (per host thread). kda_stage_timing_begin(max_calls)
  * creates 3*max_calls timing events on the current device; each of the next

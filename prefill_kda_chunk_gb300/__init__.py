@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     chunk_prefill_backward,
     decode_step,
     kda_decode_step,
+    kda_backward_workspace_bytes,
     kda_build_info,
     kda_chunk_prefill,
     kda_chunk_prefill_backward,

@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             L.kda_chunk_prefill_noalloc.argtypes = [vp] * 7 + [i64] * 6 + [f32, vp, vp, vp]
             L.kda_decode_step.restype = ctypes.c_int
             L.kda_decode_step.argtypes = [vp] * 7 + [i64] * 4 + [f32, ctypes.c_int, vp, vp]
+            L.kda_backward_workspace_bytes.restype = ctypes.c_int64
+            L.kda_backward_workspace_bytes.argtypes = [i64] * 4 + [ctypes.c_int]
             L.kda_chunk_prefill_backward.restype = ctypes.c_int
             L.kda_chunk_prefill_backward.argtypes = [vp] * 7 + [i64] * 6 + [f32] + [vp] * 9
             L.kda_status_string.restype = ctypes.c_char_p
@@ -112,6 +114,11 @@ def kda_decode_step(q, k, v, g, beta, state_in, state_out, N, H, K, V, scale, fl
     """The one-token decode C entry point, pointers as ints (0 = NULL)."""
     return lib().kda_decode_step(q, k, v, g, beta, state_in, state_out, N, H, K, V, scale, flags,
                                  out, stream)
+
+
+def kda_backward_workspace_bytes(B, T, H, N, has_cu_seqlens) -> int:
+    """Workspace bytes of a gradient call with these sizes (0 on bad sizes)."""
+    return lib().kda_backward_workspace_bytes(B, T, H, N, int(bool(has_cu_seqlens)))
 
 
 def kda_chunk_prefill_backward(q, k, v, g, beta, initial_state, cu_seqlens, B, T, H, K, V, N,

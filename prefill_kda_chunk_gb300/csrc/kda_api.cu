@@ -494,6 +494,28 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
     return KDA_OK;
 }
 
+// Gradient workspace: flag block, chunk offsets (packed), one checkpoint state
+// per 16 tokens per head, and a ring of 16 states per (sequence, head).
+static int64_t backward_ckpt_bytes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed,
+                                   const Plan &pl) {
+    const int64_t chunks = packed ? (pl.tokens + 15 * N) / 16 : B * ((T + 15) / 16);
+    return chunks * H * 128 * 128 * 4;
+}
+
+static int64_t backward_ws_bytes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed,
+                                 const Plan &pl) {
+    return 256 + pl.off_bytes + backward_ckpt_bytes(B, T, H, N, packed, pl) +
+           N * H * 16 * 128 * 128 * 4;
+}
+
+int64_t kda_backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N,
+                                     int has_cu_seqlens) {
+    Plan pl;
+    if (plan_sizes(B, T, H, N, has_cu_seqlens != 0, &pl) != KDA_OK) return 0;
+    if (N * H > (int64_t(1) << 31) - 1) return 0;
+    return backward_ws_bytes(B, T, H, N, has_cu_seqlens != 0, pl);
+}
+
 kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *v,
                                       const float *g, const float *beta,
                                       const float *initial_state, const int32_t *cu_seqlens,
@@ -558,12 +580,8 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
         if (rc != KDA_OK) return rc;
     }
 
-    // workspace: flag block, chunk offsets (packed), one checkpoint state per
-    // 16 tokens per head, and a ring of 16 states per (sequence, head)
-    const int64_t chunks = cu_seqlens ? (pl.tokens + 15 * N) / 16 : B * ((T + 15) / 16);
-    const int64_t state_bytes = 128 * 128 * 4;
-    const int64_t ckpt_bytes = chunks * H * state_bytes, ring_bytes = N * H * 16 * state_bytes;
-    const int64_t need = 256 + pl.off_bytes + ckpt_bytes + ring_bytes;
+    const int64_t ckpt_bytes = backward_ckpt_bytes(B, T, H, N, cu_seqlens != nullptr, pl);
+    const int64_t need = backward_ws_bytes(B, T, H, N, cu_seqlens != nullptr, pl);
     StreamWorkspace &ws = st.ws[stream];
     if (ws.bytes < static_cast<size_t>(need)) {
         if (capturing) return KDA_ERR_CAPTURE;

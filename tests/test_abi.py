@@ -173,3 +173,14 @@ def test_backward_argument_checks(lib):
     assert bwd(dk=A) == S["KDA_ERR_ALIAS"]                  # output over q
     assert bwd(dv=A + 0x600000) == S["KDA_ERR_ALIAS"]       # two outputs overlap
     assert bwd(d_initial_state=A + 0x500000) == S["KDA_ERR_ALIAS"]   # over d_out
+
+
+def test_backward_workspace_bytes(lib):
+    st, mib = 65536, 1 << 20
+    assert K.kda_backward_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 512 * 64 * st + 64 * mib
+    assert K.kda_backward_workspace_bytes(2, 17, 3, 2, 0) == 256 + 2 * 2 * 3 * st + 6 * mib
+    pc = (8192 + 15 * 16) // 16                       # packed: chunk bound, offsets table
+    assert K.kda_backward_workspace_bytes(1, 8192, 64, 16, 1) == (256 + 256 + pc * 64 * st
+                                                                 + 16 * 64 * mib)
+    assert K.kda_backward_workspace_bytes(1, 8192, 64, 2, 0) == 0   # N != B
+    assert K.kda_backward_workspace_bytes(1, 100, 0, 1, 0) == 0     # H < 1
