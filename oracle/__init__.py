@@ -86,7 +86,7 @@ def _load():
                 ctypes.c_double, f64p, i64, f64p, ctypes.c_int]
             lib.kda_oracle_backward.restype = ctypes.c_int
             lib.kda_oracle_backward.argtypes = [f64p] * 6 + [i64p] + [i64] * 4 + [
-                ctypes.c_double] + [f64p] * 10 + [ctypes.c_int]
+                ctypes.c_double] + [f64p] * 10 + [ctypes.c_int, ctypes.c_int]
             _lib = lib
     return _lib
 
@@ -185,7 +185,7 @@ def chunked(q, k, v, g, beta, initial_state=None, cu_seqlens=None, scale=None,
 
 
 def recurrent_backward(q, k, v, g, beta, dout, initial_state=None, d_final_state=None,
-                       cu_seqlens=None, scale=None, mutation=0):
+                       cu_seqlens=None, scale=None, threads=0, mutation=0):
     """Gradients of the token recurrence in fp64 (kda_backward.c), for the
     loss L with dL/do = ``dout`` [T, H, V] and dL/d(final state) =
     ``d_final_state`` [N, H, K, V] (None: 0). Inputs are taken as given, in
@@ -195,8 +195,10 @@ def recurrent_backward(q, k, v, g, beta, dout, initial_state=None, d_final_state
     dbeta [T, H]; d_initial_state [N, H, K, V]; and the forward results o
     [T, H, V] and final_state [N, H, K, V] of the same pass.
 
-    ``mutation`` plants a known mistake in the reverse pass (see
-    kda_backward.c); only the pin tests use it."""
+    ``threads``: host threads over the (sequence, head) pairs (0 = every
+    core; the results do not depend on it). ``mutation`` plants a known
+    mistake in the reverse pass (see kda_backward.c); only the pin tests use
+    it."""
     q, k, v, g, beta, dout = (_f64(t) for t in (q, k, v, g, beta, dout))
     if q.ndim != 3 or k.shape != q.shape or g.shape != q.shape:
         raise ValueError("q, k, g must be [T, H, K]")
@@ -231,7 +233,7 @@ def recurrent_backward(q, k, v, g, beta, dout, initial_state=None, d_final_state
         _ptr(cu, ctypes.c_int64), N, H, K, V, float(scale), _ptr(dout, d), _ptr(dsf, d),
         _ptr(out["o"], d), _ptr(out["final_state"], d), _ptr(out["dq"], d), _ptr(out["dk"], d),
         _ptr(out["dv"], d), _ptr(out["dg"], d), _ptr(out["dbeta"], d),
-        _ptr(out["d_initial_state"], d), int(mutation))
+        _ptr(out["d_initial_state"], d), int(threads), int(mutation))
     if rc:
         raise RuntimeError(f"kda_oracle_backward failed ({rc})")
     return out
