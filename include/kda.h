@@ -232,7 +232,8 @@ KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v, 
  * Method: one CTA per (sequence, head) walks the sequence backwards token
  * by token, the state recomputed from checkpoints taken every 16 tokens.
  * Workspace (the call's stream's, as for the prefill): 64 KiB per 16-token
- * chunk per head plus 1 MiB per (sequence, head). Errors as for the prefill
+ * chunk per head plus 1 MiB per CTA of the persistent kernel, min(N * H,
+ * 1024) of them. Errors as for the prefill
  * (bad cu_seqlens contents are flagged on the device, see
  * kda_last_device_error).
  */
@@ -267,8 +268,9 @@ KDA_API kda_status kda_workspace_release(void);
 KDA_API int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, int has_cu_seqlens);
 
 /* The same for kda_chunk_prefill_backward: 256 B of flags, the packed chunk
- * offsets, 64 KiB per 16-token chunk per head and 1 MiB per (sequence,
- * head). Both entry points share the stream's buffer, grown to the larger. */
+ * offsets, 64 KiB per 16-token chunk per head and 1 MiB for each of
+ * min(N * H, 1024) state rings. Both entry points share the stream's
+ * buffer, grown to the larger. */
 KDA_API int64_t kda_backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N,
                                              int has_cu_seqlens);
 

@@ -495,7 +495,8 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
 }
 
 // Gradient workspace: flag block, chunk offsets (packed), one checkpoint state
-// per 16 tokens per head, and a ring of 16 states per (sequence, head).
+// per 16 tokens per head, and a ring of 16 states per CTA of the persistent
+// gradient kernel (at most kBackwardMaxRings).
 static int64_t backward_ckpt_bytes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed,
                                    const Plan &pl) {
     const int64_t chunks = packed ? (pl.tokens + 15 * N) / 16 : B * ((T + 15) / 16);
@@ -504,8 +505,9 @@ static int64_t backward_ckpt_bytes(int64_t B, int64_t T, int64_t H, int64_t N, b
 
 static int64_t backward_ws_bytes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed,
                                  const Plan &pl) {
+    const int64_t rings = N * H < kda::kBackwardMaxRings ? N * H : kda::kBackwardMaxRings;
     return 256 + pl.off_bytes + backward_ckpt_bytes(B, T, H, N, packed, pl) +
-           N * H * 16 * 128 * 128 * 4;
+           rings * 16 * 128 * 128 * 4;
 }
 
 int64_t kda_backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N,

@@ -116,14 +116,18 @@ __device__ __forceinline__ void forward_step(const BackParams &p, BwdSmem &sm, f
 }
 
 __global__ void __launch_bounds__(kBwdThreads, 1)
-kda_backward_kernel(BackParams p) {
+kda_backward_kernel(BackParams p, int64_t units) {
     __shared__ BwdSmem sm;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const ChunkGeometry &geo = p.geo;
     const int H = geo.n_heads;
-    const int64_t unit = blockIdx.x;           // sequence * H + head
-    const int n = static_cast<int>(unit / H), h = static_cast<int>(unit % H);
     if (geo.cu != nullptr && (*geo.call_flags & kErrBadCu)) return;
+    // persistent: this CTA takes units blockIdx.x, + gridDim.x, ... and owns
+    // ring blockIdx.x for all of them
+    float4 *ring = reinterpret_cast<float4 *>(p.ring) +
+                   static_cast<int64_t>(blockIdx.x) * kRing * kStateF4;
+    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const int n = static_cast<int>(unit / H), h = static_cast<int>(unit % H);
     int64_t t0, L, coff;
     if (geo.cu == nullptr) {
         t0 = static_cast<int64_t>(n) * geo.seq_len;
@@ -138,7 +142,6 @@ kda_backward_kernel(BackParams p) {
     // checkpoint c of this unit: state index (coff + c) * H + h
     float4 *ckpt = reinterpret_cast<float4 *>(p.ckpt) + (coff * H + h) * kStateF4;
     const int64_t ck_stride = static_cast<int64_t>(H) * kStateF4;
-    float4 *ring = reinterpret_cast<float4 *>(p.ring) + unit * kRing * kStateF4;
     const int64_t me = static_cast<int64_t>(warp) * 32 + lane;   // + 256 m: this thread's float4
 
     // ---- forward pass, a checkpoint before every 16th token
@@ -279,13 +282,28 @@ kda_backward_kernel(BackParams p) {
 #pragma unroll
         for (int m = 0; m < 16; ++m) D[me + 256 * m] = dS[m];
     }
+    }  // units
 }
 
 }  // namespace
 
+static int64_t backward_grid(int64_t units) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kda_backward_kernel, kBwdThreads,
+                                                      0) != cudaSuccess)
+        return 0;
+    int64_t grid = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+    if (grid > kBackwardMaxRings) grid = kBackwardMaxRings;
+    return units < grid ? units : grid;
+}
+
 cudaError_t launch_backward(const BackParams &p, int64_t units, cudaStream_t stream) {
     if (units <= 0) return cudaSuccess;
-    kda_backward_kernel<<<static_cast<unsigned>(units), kBwdThreads, 0, stream>>>(p);
+    const int64_t grid = backward_grid(units);
+    if (grid <= 0) return cudaErrorInvalidConfiguration;
+    kda_backward_kernel<<<static_cast<unsigned>(grid), kBwdThreads, 0, stream>>>(p, units);
     return cudaGetLastError();
 }
 

@@ -92,7 +92,7 @@ struct BackParams {
     float *dbeta;              // fp32 [tokens, H]
     float *ds0;                // fp32 [N, H, 128, 128] or nullptr: dL/d(initial state)
     float *ckpt;               // workspace: one state per 16 tokens per head
-    float *ring;               // workspace: 16 states per unit
+    float *ring;               // workspace: 16 states per CTA of the launch
     ChunkGeometry geo;
 };
 
@@ -116,6 +116,10 @@ cudaError_t launch_recurrent_tc(const RecurParams &p, cudaStream_t stream);  // 
 // warp-MMA chain with the output product on tcgen05; needs IntraParams::qg_tc = 1
 cudaError_t launch_recurrent_hybrid(const RecurParams &p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int64_t units, cudaStream_t stream);
+// The gradient kernel is persistent: at most one CTA per resident slot and
+// never more than kBackwardMaxRings, each owning one 16-state ring of the
+// workspace (BackParams::ring holds min(units, kBackwardMaxRings) rings).
+constexpr int64_t kBackwardMaxRings = 1024;
 cudaError_t launch_backward(const BackParams &p, int64_t units, cudaStream_t stream);
 
 }  // namespace kda

@@ -182,5 +182,7 @@ def test_backward_workspace_bytes(lib):
     pc = (8192 + 15 * 16) // 16                       # packed: chunk bound, offsets table
     assert K.kda_backward_workspace_bytes(1, 8192, 64, 16, 1) == (256 + 256 + pc * 64 * st
                                                                  + 16 * 64 * mib)
+    # more (sequence, head) pairs than the persistent kernel has CTAs: 1024 rings
+    assert K.kda_backward_workspace_bytes(32, 16, 64, 32, 0) == 256 + 32 * 64 * st + 1024 * mib
     assert K.kda_backward_workspace_bytes(1, 8192, 64, 2, 0) == 0   # N != B
     assert K.kda_backward_workspace_bytes(1, 100, 0, 1, 0) == 0     # H < 1

@@ -115,6 +115,14 @@ def test_backward_longer_sequence():
     check_all(d, gpu_grads(d), "T=700")
 
 
+def test_backward_more_units_than_ctas():
+    """320 (sequence, head) units: the persistent kernel's CTAs take several
+    each, reusing their state ring (lengths 0..37, some past one segment)."""
+    lens = [(7 * i) % 38 for i in range(40)]
+    d = make(lens, H=8, seed=29)
+    check_all(d, gpu_grads(d), "320 units")
+
+
 def test_backward_bad_cu_seqlens_flagged():
     d = make([20, 30], H=1, seed=27)
     x = {n: d[n].cuda().contiguous() for n in ("q", "k", "v", "g", "beta", "dout")}
