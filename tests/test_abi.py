@@ -186,3 +186,22 @@ def test_backward_workspace_bytes(lib):
     assert K.kda_backward_workspace_bytes(32, 16, 64, 32, 0) == 256 + 32 * 64 * st + 1024 * mib
     assert K.kda_backward_workspace_bytes(1, 8192, 64, 2, 0) == 0   # N != B
     assert K.kda_backward_workspace_bytes(1, 100, 0, 1, 0) == 0     # H < 1
+
+
+def test_header_is_plain_c(tmp_path):
+    """include/kda.h compiles as strict C99 (no C++ or torch types leak into
+    the boundary), and a C caller can take every entry point's address."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not found")
+    names = declared_symbols()
+    src = tmp_path / "use_kda.c"
+    src.write_text('#include "kda.h"\n'
+                   "typedef void (*fp)(void);\n"
+                   "fp table[] = {\n" + "".join(f"    (fp){n},\n" for n in names) + "};\n")
+    inc = os.path.join(ROOT, "include")
+    r = subprocess.run(["gcc", "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror",
+                        "-I", inc, "-c", str(src), "-o", str(tmp_path / "use_kda.o")],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
