@@ -13,7 +13,10 @@ Three independently written forms of the same result:
   (kda_chunked.c), the algebra the GPU kernels use, written without blocking
   or factoring;
 * ``unrolled`` (unrolled.py) -- the state written out as explicit products of
-  per-token transition matrices, for a handful of tokens.
+  per-token transition matrices, for a handful of tokens;
+* ``segment_scan`` (segment_scan.py) -- the chunks of a sequence cut into
+  segments, each reduced to one affine state map on its own, combined
+  serially, then replayed (the segment-parallel form for long sequences).
 
 And the gradients of the same map: ``recurrent_backward`` (kda_backward.c),
 the reverse pass of the token recurrence written line by line, pinned by
@@ -51,6 +54,7 @@ _lock = threading.Lock()
 
 from .unrolled import unrolled  # noqa: E402  (pure numpy, no build needed)
 from .chunked_backward import chunked_backward  # noqa: E402  (pure numpy)
+from .segment_scan import segment_scan  # noqa: E402  (pure numpy)
 
 
 def build(force: bool = False) -> str:
@@ -239,4 +243,5 @@ def recurrent_backward(q, k, v, g, beta, dout, initial_state=None, d_final_state
     return out
 
 
-__all__ = ["build", "recurrent", "chunked", "unrolled", "recurrent_backward", "chunked_backward"]
+__all__ = ["build", "recurrent", "chunked", "unrolled", "recurrent_backward", "chunked_backward",
+           "segment_scan"]
