@@ -187,11 +187,13 @@ def launches_per_call(w, args):
     """Kernels one unsegmented prefill call launches: the cu_seqlens prologue
     (packed batches), the intra-chunk kernel, its exact-form companion, the
     recurrent kernel, and the state-only pass of the split replay (warp-MMA
-    recurrent kernel, fixed-length sequences of >= 64 chunks, 4 N H <= 148)."""
+    recurrent kernel, fixed-length sequences of >= 64 chunks, 4 N H <= SMs - 4)."""
     n = 3 + int(w.varlen)
     chunks = -(-(w.T // w.n_seqs) // 16)
     impl = 1 if args.recurrent_impl is None else args.recurrent_impl
-    if not w.varlen and impl == 1 and chunks >= 64 and 4 * w.n_seqs * w.H <= 148:
+    sms = (torch.cuda.get_device_properties(0).multi_processor_count
+           if torch.cuda.is_available() else 152)
+    if not w.varlen and impl == 1 and chunks >= 64 and 4 * w.n_seqs * w.H <= sms - 4:
         n += 1
     return n
 
@@ -223,14 +225,20 @@ def run_reference(args, rank, world):
         w = dataclasses.replace(w, mu=args.gate_mu)
     d = KI.make_inputs(w)
     cores = len(os.sched_getaffinity(0))
-    Hs = max(1, min(w.H, 4))
-    sub = {n: d[n][:, :Hs].contiguous() for n in ("q", "k", "v", "g", "beta")}
+    # one head per host core (the oracle runs one (sequence, head) per thread);
+    # a single long sequence is cut to a prefix so that a step stays near half
+    # a second (~63 us per token-head per core for the fp64 recurrence)
+    Hs = max(1, min(w.H, cores))
+    Ts = w.T
+    if len(d["seqlens"]) == 1:
+        Ts = max(16, min(w.T, int(0.5 * cores / 63e-6 / Hs)))
+    sub = {n: d[n][:Ts, :Hs].contiguous() for n in ("q", "k", "v", "g", "beta")}
     s0 = None if d["initial_state"] is None else d["initial_state"][:, :Hs].contiguous()
+    cu = d["cu_seqlens"] if Ts == w.T else torch.tensor([0, Ts], dtype=torch.int32)
 
     def step():
         oracle.recurrent(sub["q"], sub["k"], sub["v"], sub["g"], sub["beta"], initial_state=s0,
-                         cu_seqlens=d["cu_seqlens"], scale=d["scale"], out_tokens=w.T,
-                         threads=cores)
+                         cu_seqlens=cu, scale=d["scale"], out_tokens=Ts, threads=cores)
 
     for _ in range(args.warmup):
         step()
@@ -238,9 +246,11 @@ def run_reference(args, rank, world):
     for _ in range(args.steps):
         step()
     dt = time.perf_counter() - t0
-    tokens_equiv = w.T * Hs / w.H          # one step covers Hs of the H heads
+    tokens_equiv = Ts * Hs / w.H           # one step covers Hs of the H heads, Ts tokens
     value = args.steps * tokens_equiv / dt
-    sample = f"{Hs} of {w.H} heads, all {w.T} tokens, per step"
+    sample = (f"{Hs} of {w.H} heads, " +
+              (f"all {w.T} tokens" if Ts == w.T else f"the first {Ts} of {w.T} tokens") +
+              f", per step, {Hs} threads")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",

@@ -117,7 +117,7 @@ enum { KDA_PRE_NORM_QK = 1, KDA_PRE_GATE_LOGITS = 2 };
  * more (17,412 B per chunk-head: its record and one list entry; or two ring
  * slots plus the carried states for a segmented call, see
  * kda_set_ring_slot_bytes). A fixed-length call
- * with at least 64 chunks per sequence and 4*N*H <= 148 also reserves
+ * with at least 64 chunks per sequence and 4*N*H <= (SM count - 4) also reserves
  * N*H*64 KiB of midpoint states: the warp-MMA recurrent kernel then carries
  * the state to the middle of every sequence first and replays both halves
  * side by side (same results to rounding; not with an in-place state). A segmented call also
@@ -158,13 +158,19 @@ KDA_API kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void
  * a serving loop that must not enter the driver's allocator on its hot path,
  * or a sandboxed plug-in. It allocates nothing. Its scratch is one
  * fixed-size device array inside the library (64 MiB, held on every GPU that
- * loads the library until the process exits); a call that needs more
- * (kda_workspace_bytes() > 64 MiB, about 3850 chunk-heads) returns
- * KDA_ERR_SCRATCH_LIMIT before enqueuing anything. All calls share that
- * array: calls whose GPU work overlaps (e.g. on two streams) race and give
- * wrong results. The first call on a device does a one-time set-up with that
- * device current (no allocation); make it before any stream capture. Device
- * errors of this entry point are not reported by kda_last_device_error().
+ * loads the library until the process exits). The call holds at once a
+ * 256-byte flag block, the chunk-offset table of a packed batch ((N+1)*4 B),
+ * every chunk record (17,408 B per 16-token chunk per head) and a 4-byte
+ * list entry per chunk-head, each part rounded up to 256 B; a call that needs
+ * more than 64 MiB (about 3850 chunk-heads) returns KDA_ERR_SCRATCH_LIMIT
+ * before enqueuing anything. All calls share that array: calls whose GPU
+ * work overlaps (e.g. on two streams) race and give wrong results. The first
+ * call on a device does a one-time set-up with that device current (no
+ * allocation); make it before any stream capture (a first call on a
+ * capturing stream returns KDA_ERR_CAPTURE). Uncaptured calls check their
+ * pointers and stream like kda_chunk_prefill (KDA_ERR_NOT_DEVICE_MEMORY,
+ * KDA_ERR_WRONG_DEVICE). Device errors of this entry point are reported by
+ * kda_last_device_error() like those of the others.
  */
 KDA_API kda_status kda_chunk_prefill_noalloc(const void *q, const void *k, const void *v,
                                              const float *g, const float *beta,
@@ -253,7 +259,9 @@ KDA_API const char *kda_status_string(kda_status status);
 /*
  * Synchronises `stream`, then returns and clears the first error a kernel
  * of this library recorded on the current device since the last call
- * (KDA_OK if none). Device errors are sticky per device, not per stream.
+ * (KDA_OK if none). Device errors are sticky per device, not per stream;
+ * this reads both the library's error word and that of the fixed array of
+ * kda_chunk_prefill_noalloc (if that entry point has run on the device).
  */
 KDA_API kda_status kda_last_device_error(void *stream);
 

@@ -69,7 +69,20 @@ constexpr int64_t kMaxElems = int64_t(1) << 40;
 // midpoint state, and one launch then replays both halves side by side: about
 // T/32 (light) + T/32 (full) steps on the chain instead of T/16 full ones.
 constexpr int64_t kSplitMinChunks = 64;    // per sequence
-constexpr int64_t kSplitMaxCtas = 148;     // doubled recurrent CTAs, below GB300's 152 SMs
+constexpr int64_t kSplitSpareSms = 4;      // SMs left free beside the doubled recurrent grid
+
+// SM count of the current device; the sizing-only entry point kda_workspace_bytes
+// may run without a device, and then sizes for GB300's 152 SMs.
+int current_sm_count() {
+    int dev = -1, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0) {
+        cudaGetLastError();
+        return 152;
+    }
+    return sms;
+}
 
 int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
@@ -109,7 +122,8 @@ bool overlap(const void *a, int64_t na, const void *b, int64_t nb) {
     return x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
 }
 
-kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, Plan *pl) {
+kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, int sm_count,
+                      Plan *pl) {
     if (H < 1 || T < 0 || B < 1 || N < 1) return KDA_ERR_BAD_SHAPE;
     if (H > 65535 * 4) return KDA_ERR_BAD_SHAPE;
     if (packed) {
@@ -130,7 +144,7 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, P
     pl->ws_bytes = 256 + pl->off_bytes + pl->max_chunks * H * kda::kRecBytes;
     pl->nseg = 1;
     pl->seg_len = (T + 15) / 16;
-    if (!packed && pl->seg_len >= kSplitMinChunks && 2 * (N * H * 2) <= kSplitMaxCtas) {
+    if (!packed && pl->seg_len >= kSplitMinChunks && 2 * (N * H * 2) <= sm_count - kSplitSpareSms) {
         pl->split_chunks = pl->seg_len / 2;
         pl->mid_bytes = align256(N * H * 128 * 128 * 4);
         pl->ws_bytes += pl->mid_bytes;
@@ -177,6 +191,12 @@ kda_status init_device(int dev, DeviceState &st) {
 }
 
 kda_status check_pointer_device(const void *p, int dev) {
+    return static_cast<kda_status>(kda::pointer_device_status(p, dev));
+}
+
+}  // namespace
+
+int kda::pointer_device_status(const void *p, int dev) {
     if (p == nullptr) return KDA_OK;
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
@@ -188,8 +208,6 @@ kda_status check_pointer_device(const void *p, int dev) {
     if (at.device != dev) return KDA_ERR_WRONG_DEVICE;
     return KDA_OK;
 }
-
-}  // namespace
 
 extern "C" {
 
@@ -284,7 +302,7 @@ const char *kda_build_info(void) {
 
 int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, int has_cu_seqlens) {
     Plan pl;
-    if (plan_sizes(B, T, H, N, has_cu_seqlens != 0, &pl) != KDA_OK) return 0;
+    if (plan_sizes(B, T, H, N, has_cu_seqlens != 0, current_sm_count(), &pl) != KDA_OK) return 0;
     return pl.ws_bytes;
 }
 
@@ -306,7 +324,7 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
     if ((flags & ~(KDA_PRE_NORM_QK | KDA_PRE_GATE_LOGITS)) != 0) return KDA_ERR_BAD_FLAGS;
     if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_DIM;
     Plan pl;
-    kda_status rc = plan_sizes(B, T, H, N, cu_seqlens != nullptr, &pl);
+    kda_status rc = plan_sizes(B, T, H, N, cu_seqlens != nullptr, current_sm_count(), &pl);
     if (rc != KDA_OK) return rc;
     if (pl.tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL_ARG;
     if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(g, 16) ||
@@ -513,7 +531,7 @@ static int64_t backward_ws_bytes(int64_t B, int64_t T, int64_t H, int64_t N, boo
 int64_t kda_backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N,
                                      int has_cu_seqlens) {
     Plan pl;
-    if (plan_sizes(B, T, H, N, has_cu_seqlens != 0, &pl) != KDA_OK) return 0;
+    if (plan_sizes(B, T, H, N, has_cu_seqlens != 0, current_sm_count(), &pl) != KDA_OK) return 0;
     if (N * H > (int64_t(1) << 31) - 1) return 0;
     return backward_ws_bytes(B, T, H, N, has_cu_seqlens != 0, pl);
 }
@@ -529,7 +547,7 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
     // ---- checks that need no GPU
     if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_DIM;
     Plan pl;
-    kda_status rc = plan_sizes(B, T, H, N, cu_seqlens != nullptr, &pl);
+    kda_status rc = plan_sizes(B, T, H, N, cu_seqlens != nullptr, current_sm_count(), &pl);
     if (rc != KDA_OK) return rc;
     if (N * H > (int64_t(1) << 31) - 1) return KDA_ERR_BAD_SHAPE;
     if (pl.tokens > 0 && (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv || !dg ||
@@ -685,12 +703,18 @@ kda_status kda_last_device_error(void *stream_) {
     {
         std::lock_guard<std::mutex> lock(g_mu);
         auto it = g_devices.find(dev);
-        if (it == g_devices.end() || !it->second.ready) return KDA_OK;
-        err = it->second.err;
+        if (it != g_devices.end() && it->second.ready) err = it->second.err;
     }
     int word = 0;
-    if (cudaMemcpy(&word, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
-    if (word != 0 && cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    if (err != nullptr) {
+        if (cudaMemcpy(&word, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        if (word != 0 && cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return KDA_ERR_CUDA;
+    }
+    // the allocation-free entry point records its device errors in its own array
+    int na_word = 0;
+    if (!kda::noalloc_take_error(dev, &na_word)) return KDA_ERR_CUDA;
+    word |= na_word;
     if (word & kda::kErrBadCu) return KDA_ERR_BAD_CU_SEQLENS;
     if (word & kda::kErrTimeout) return KDA_ERR_DEVICE_TIMEOUT;
     if (word & kda::kErrGate) return KDA_ERR_GATE_RANGE;

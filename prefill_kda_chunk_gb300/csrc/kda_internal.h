@@ -122,4 +122,15 @@ cudaError_t launch_decode(const DecodeParams &p, int64_t units, cudaStream_t str
 constexpr int64_t kBackwardMaxRings = 1024;
 cudaError_t launch_backward(const BackParams &p, int64_t units, cudaStream_t stream);
 
+// Host-side checks shared by the entry points (kda_api.cu): 0 when `p` is
+// NULL, device memory of device `dev` or managed memory; otherwise the
+// kda_status the entry point returns (not device memory / wrong device).
+int pointer_device_status(const void *p, int dev);
+
+// The error word of the allocation-free entry point's fixed scratch array on
+// device `dev` (kda_noalloc.cu): read and cleared with a synchronous copy,
+// 0 when that array has not been set up on the device. Returns false if a
+// CUDA call failed.
+bool noalloc_take_error(int dev, int *word);
+
 }  // namespace kda

@@ -14,19 +14,24 @@
 // Costs and limits, stated for the user of this entry point:
 //   - Every GPU that loads this library holds kNoAllocScratchBytes (64 MiB)
 //     of device memory for that array until the process exits.
-//   - A call whose scratch need (kda_workspace_bytes) exceeds that size is
-//     rejected with KDA_ERR_SCRATCH_LIMIT before anything is enqueued.
+//   - A call whose scratch need exceeds that size is rejected with
+//     KDA_ERR_SCRATCH_LIMIT before anything is enqueued. The need is what
+//     this entry point holds at once: a 256-byte flag block, the chunk-offset
+//     table of a packed batch, every chunk record of the call (17,408 B per
+//     16-token chunk per head) and one 4-byte exact-form list entry per
+//     chunk-head, each part rounded up to 256 bytes (noalloc_scratch_need).
 //   - All calls share the one array, so calls whose GPU work overlaps (for
 //     example on two streams) race on it and give wrong results; serialise
 //     them.
 //   - The first call on a device does a one-time set-up with that device
 //     current (architecture check, kernel attributes, the array's device
 //     address, zeroing its flag block); make that first call before any
-//     stream capture.
+//     stream capture. A first call made while its stream is capturing is
+//     refused with KDA_ERR_CAPTURE.
 //   - Device-side errors of this entry point (bad cu_seqlens contents, a
 //     bounded wait that ran out, a log decay rising by more than 80 within a
-//     chunk) are recorded in the array's flag block; kda_last_device_error()
-//     does not see them.
+//     chunk) are recorded in the array's error word; kda_last_device_error()
+//     reads and clears it together with the library's own error word.
 
 #include <cuda_runtime.h>
 
@@ -67,6 +72,15 @@ kda_status noalloc_setup(int dev) {
     return KDA_OK;
 }
 
+// Bytes of the fixed array one call needs: flag block, chunk offsets (packed
+// batches), all chunk records at once and the exact-form list.
+int64_t noalloc_scratch_need(int64_t B, int64_t T, int64_t H, int64_t N, bool packed) {
+    const int64_t off = packed ? (((N + 1) * 4 + 255) & ~int64_t(255)) : 0;
+    const int64_t chunks = packed ? (T + 15 * N) / 16 : B * ((T + 15) / 16);
+    const int64_t list = ((chunks * H * 4) + 255) & ~int64_t(255);
+    return 256 + off + chunks * H * kda::kRecBytes + list;
+}
+
 bool na_misaligned(const void *p, uintptr_t a) {
     return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) != 0;
 }
@@ -79,6 +93,21 @@ bool na_overlap(const void *a, int64_t na, const void *b, int64_t nb) {
 
 }  // namespace
 
+bool kda::noalloc_take_error(int dev, int *word) {
+    *word = 0;
+    if (dev < 0 || dev >= kMaxDevices) return true;
+    uint8_t *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_na_mu);
+        if (!g_na_ready[dev]) return true;
+        base = g_na_base[dev];
+    }
+    int *err = reinterpret_cast<int *>(base + 4);
+    if (cudaMemcpy(word, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return false;
+    if (*word != 0 && cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return false;
+    return true;
+}
+
 extern "C" kda_status kda_chunk_prefill_noalloc(
     const void *q, const void *k, const void *v, const float *g, const float *beta,
     const float *initial_state, const int32_t *cu_seqlens, int64_t B, int64_t T, int64_t H,
@@ -88,10 +117,7 @@ extern "C" kda_status kda_chunk_prefill_noalloc(
     if (kda_workspace_bytes(B, T, H, N, packed ? 1 : 0) <= 0) return KDA_ERR_BAD_SHAPE;
     // this entry point never splits a call into segments: every chunk record
     // of the call is in the array at once
-    const int64_t need_off = packed ? (((N + 1) * 4 + 255) & ~int64_t(255)) : 0;
-    const int64_t need_chunks = packed ? (T + 15 * N) / 16 : B * ((T + 15) / 16);
-    const int64_t need_list = ((need_chunks * H * 4) + 255) & ~int64_t(255);
-    const int64_t need = 256 + need_off + need_chunks * H * kda::kRecBytes + need_list;
+    const int64_t need = noalloc_scratch_need(B, T, H, N, packed);
     if (static_cast<size_t>(need) > kNoAllocScratchBytes) return KDA_ERR_SCRATCH_LIMIT;
     const int64_t tokens = packed ? T : B * T;
     if (tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL_ARG;
@@ -114,16 +140,35 @@ extern "C" kda_status kda_chunk_prefill_noalloc(
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_CUDA;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return KDA_ERR_CUDA;
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
     uint8_t *base = nullptr;
     {
         std::lock_guard<std::mutex> lock(g_na_mu);
         if (!g_na_ready[dev]) {
+            // the set-up makes synchronous calls, which would end a capture
+            if (capturing) return KDA_ERR_CAPTURE;
             const kda_status rc = noalloc_setup(dev);
             if (rc != KDA_OK) return rc;
         }
         base = g_na_base[dev];
     }
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    // the same device checks as kda_chunk_prefill (they allocate nothing);
+    // pointer queries are not stream work, so a capturing call skips them
+    if (stream != nullptr && !capturing) {
+        int sdev = -1;
+        if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) return KDA_ERR_CUDA;
+        if (sdev != dev) return KDA_ERR_WRONG_DEVICE;
+    }
+    if (!capturing) {
+        const void *ptrs[] = {q, k, v, g, beta, initial_state, cu_seqlens, out, final_state};
+        for (const void *ptr : ptrs) {
+            const int rc = kda::pointer_device_status(ptr, dev);
+            if (rc != KDA_OK) return static_cast<kda_status>(rc);
+        }
+    }
     const int64_t off_bytes = packed ? (((N + 1) * 4 + 255) & ~int64_t(255)) : 0;
     const int64_t max_chunks = packed ? (T + 15 * N) / 16 : B * ((T + 15) / 16);
     int *call_flags = reinterpret_cast<int *>(base);

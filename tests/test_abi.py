@@ -69,7 +69,7 @@ def test_workspace_bytes(lib):
     assert K.kda_workspace_bytes(2, 2000, 3, 2, 0) == (256 + 2 * 125 * 3 * REC + 6 * 65536
                                                       + lst(2 * 125 * 3))
     assert K.kda_workspace_bytes(1, 1008, 3, 1, 0) == 256 + 63 * 3 * REC + lst(63 * 3)  # < 64 chunks
-    assert K.kda_workspace_bytes(1, 8192, 38, 1, 0) == 256 + 512 * 38 * REC + lst(512 * 38)  # > 148
+    assert K.kda_workspace_bytes(1, 8192, 38, 1, 0) == 256 + 512 * 38 * REC + lst(512 * 38)  # 4*38 > 152 - 4 (no device here: sized for 152 SMs)
     assert K.kda_workspace_bytes(1, 8192, 64, 2, 0) == 0      # N != B without cu_seqlens
     assert K.kda_workspace_bytes(2, 100, 0, 2, 0) == 0        # H < 1
 
@@ -205,3 +205,26 @@ def test_header_is_plain_c(tmp_path):
                         "-I", inc, "-c", str(src), "-o", str(tmp_path / "use_kda.o")],
                        capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_noalloc_scratch_limit_boundary(lib):
+    """The allocation-free entry point holds a 256 B flag block, every chunk
+    record (17,408 B per 16-token chunk per head) and a 4 B list entry per
+    chunk-head (rounded up to 256 B) in its fixed 64 MiB array. 3854 chunks
+    of one head fit (67,106,304 B), 3855 do not (67,123,712 B). The size
+    check comes before any CUDA call, so this needs no GPU: a call that fits
+    goes on to the device checks, which fail here (no device) or, on a GPU,
+    refuse the fake pointers, and nothing is launched either way."""
+    def need(c):
+        return 256 + c * 17408 + -(-(4 * c) // 256) * 256
+    assert need(3854) <= (64 << 20) < need(3855)
+
+    def na(T):
+        return K.kda_chunk_prefill_noalloc(A, A + (8 << 20), A + (16 << 20), A + (24 << 20),
+                                           A + (48 << 20), 0, 0, 1, T, 1, 128, 128, 1, 1.0,
+                                           A + (64 << 20), 0, 0)
+    assert na(3855 * 16) == K.STATUS_CODE["KDA_ERR_SCRATCH_LIMIT"]
+    assert na(3854 * 16 + 1) == K.STATUS_CODE["KDA_ERR_SCRATCH_LIMIT"]
+    assert na(3854 * 16) in (K.STATUS_CODE["KDA_ERR_CUDA"],
+                             K.STATUS_CODE["KDA_ERR_NOT_DEVICE_MEMORY"],
+                             K.STATUS_CODE["KDA_ERR_NO_DEVICE_SUPPORT"])

@@ -157,3 +157,28 @@ def test_backward_consistent_with_forward_by_directional_derivative():
     diff = loss(vp) - loss(vm)
     an = float((got[2].double().cpu() * (vp.double() - vm.double())).sum())
     assert abs(diff - an) <= 0.03 * max(1.0, abs(an)), (diff, an)
+
+
+def test_backward_benchmarked_workload_sampled():
+    """The gradient call at the size it is timed at (fixed_T8192_H64: one
+    sequence of 8192 tokens, 64 heads), every output checked against the
+    oracle on a sample of heads: the heads are independent units, so the
+    oracle runs on each sampled head's slice of the inputs alone."""
+    d = KI.make_inputs(KI.WORKLOADS["fixed_T8192_H64"])
+    T, H = d["q"].shape[0], d["q"].shape[1]
+    gen = torch.Generator().manual_seed(4242)
+    d["dout"] = torch.randn(T, H, 128, generator=gen).to(torch.bfloat16)
+    d["dsf"] = torch.randn(1, H, 128, 128, generator=gen) * 0.1
+    got = gpu_grads(d)
+    torch.cuda.synchronize()
+    got = [t.cpu() for t in got]
+    rng = np.random.default_rng(7)
+    heads = sorted(int(h) for h in rng.choice(H, size=4, replace=False))
+    for h in heads:
+        sub = {n: d[n][:, h:h + 1].contiguous() for n in ("q", "k", "v", "g", "beta", "dout")}
+        sub["initial_state"] = (None if d["initial_state"] is None
+                                else d["initial_state"][:, h:h + 1].contiguous())
+        sub["dsf"] = d["dsf"][:, h:h + 1].contiguous()
+        sub["cu_seqlens"], sub["scale"] = d["cu_seqlens"], d["scale"]
+        for name, x, ref in zip(NAMES, got, oracle_grads(sub)):
+            check(x[:, h:h + 1], ref, f"head {h} {name}")
