@@ -21,6 +21,9 @@ namespace {
 struct StreamWorkspace {
     void *ptr = nullptr;
     size_t bytes = 0;
+    // the 64-token ring counters (fused launches) hold zeros; any other use of
+    // the buffer may overwrite them
+    bool ring_clean = false;
     cudaStream_t s_intra = nullptr, s_recur = nullptr;
     std::vector<cudaEvent_t> ev;
 };
@@ -51,8 +54,14 @@ constexpr int64_t kDefaultSlotBytes = -1;
 constexpr int64_t kMinSegChunks = 8;
 
 // Recurrent kernel: 0 = tcgen05 / tensor memory, 1 = warp-level MMA,
-// 2 = hybrid (warp-MMA chain, output product on tcgen05).
+// 2 = hybrid (warp-MMA chain, output product on tcgen05); 3 = 64-token chunks
+// on tcgen05, intra-chunk kernel then recurrent kernel; 4 = 64-token chunks,
+// both in one cooperative launch with the records in an L2-resident ring
+// (3 when the heads leave too few SMs for the record builders).
 std::atomic<int> g_recur_impl{1};
+constexpr int kImplC64Split = 3, kImplC64Fused = 4;
+constexpr int64_t kC64Ring = 4;          // ring slots per head (fused launch)
+constexpr int kC64MinBuilders = 16;      // SMs left for record builders in a fused launch
 
 cudaError_t launch_recur(int impl, const kda::RecurParams &p, cudaStream_t s) {
     if (impl == 0) return kda::launch_recurrent_tc(p, s);
@@ -87,6 +96,9 @@ int current_sm_count() {
 int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
 struct Plan {
+    int impl = 1;            // recurrent kernel / path actually used (see g_recur_impl)
+    int64_t c64_chunks = 0;  // 64-token paths: chunks of the call (upper bound when packed)
+    int64_t c64_sync = 0;    // fused 64-token path: byte offset of the ring counters
     int64_t tokens = 0;      // total tokens
     int64_t max_chunks = 0;  // chunk records of one launch (upper bound when packed)
     int64_t off_bytes = 0;   // chunk offset table
@@ -123,7 +135,7 @@ bool overlap(const void *a, int64_t na, const void *b, int64_t nb) {
 }
 
 kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, int sm_count,
-                      Plan *pl) {
+                      int impl, Plan *pl) {
     if (H < 1 || T < 0 || B < 1 || N < 1) return KDA_ERR_BAD_SHAPE;
     if (H > 65535 * 4) return KDA_ERR_BAD_SHAPE;
     if (packed) {
@@ -171,6 +183,25 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, i
     }
     pl->list_bytes = align256(pl->max_chunks * H * 4);
     pl->ws_bytes += pl->list_bytes;
+    pl->impl = impl;
+    if (impl >= kImplC64Split) {
+        // 64-token chunks: flag block, 64-token chunk offsets (packed), then the
+        // records of every chunk-head (split) or a ring of kC64Ring per head and
+        // its counters (fused). TMA coordinates are 32-bit.
+        if (pl->tokens >= (int64_t(1) << 31)) return KDA_ERR_BAD_SHAPE;
+        pl->c64_chunks = packed ? (T + 63 * N) / 64 : B * ((T + 63) / 64);
+        if (impl == kImplC64Fused && H + kC64MinBuilders > sm_count) pl->impl = kImplC64Split;
+        pl->nseg = 1;
+        pl->split_chunks = 0;
+        pl->mid_bytes = 0;
+        pl->list_bytes = 0;
+        if (pl->impl == kImplC64Split) {
+            pl->ws_bytes = 256 + pl->off_bytes + pl->c64_chunks * H * kda::kC64RecBytes;
+        } else {
+            pl->c64_sync = 256 + pl->off_bytes + kC64Ring * H * kda::kC64RecBytes;
+            pl->ws_bytes = pl->c64_sync + align256((kC64Ring * H + H) * 8 + 64);
+        }
+    }
     return KDA_OK;
 }
 
@@ -186,6 +217,7 @@ kda_status init_device(int dev, DeviceState &st) {
     if (kda::configure_recurrent() != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_recurrent_tc() != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_recurrent_hybrid() != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::configure_c64() != cudaSuccess) return KDA_ERR_CUDA;
     st.ready = true;
     return KDA_OK;
 }
@@ -302,7 +334,9 @@ const char *kda_build_info(void) {
 
 int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, int has_cu_seqlens) {
     Plan pl;
-    if (plan_sizes(B, T, H, N, has_cu_seqlens != 0, current_sm_count(), &pl) != KDA_OK) return 0;
+    if (plan_sizes(B, T, H, N, has_cu_seqlens != 0, current_sm_count(), g_recur_impl.load(), &pl) !=
+        KDA_OK)
+        return 0;
     return pl.ws_bytes;
 }
 
@@ -323,8 +357,11 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
     // ---- checks that need no GPU
     if ((flags & ~(KDA_PRE_NORM_QK | KDA_PRE_GATE_LOGITS)) != 0) return KDA_ERR_BAD_FLAGS;
     if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_DIM;
+    // one read of the kernel choice per call: the record layout depends on it
+    const int impl = g_recur_impl.load();
     Plan pl;
-    kda_status rc = plan_sizes(B, T, H, N, cu_seqlens != nullptr, current_sm_count(), &pl);
+    const int sm_count = current_sm_count();
+    kda_status rc = plan_sizes(B, T, H, N, cu_seqlens != nullptr, sm_count, impl, &pl);
     if (rc != KDA_OK) return rc;
     if (pl.tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL_ARG;
     if (misaligned(q, 16) || misaligned(k, 16) || misaligned(v, 16) || misaligned(g, 16) ||
@@ -344,9 +381,6 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
         return KDA_ERR_ALIAS;
     if (final_state != initial_state && overlap(final_state, ns, initial_state, ns))
         return KDA_ERR_ALIAS;
-
-    // one read of the kernel choice per call: the record layout depends on it
-    const int impl = g_recur_impl.load();
 
     // ---- device checks
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
@@ -385,22 +419,11 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
             return KDA_ERR_CUDA;
         }
         ws.bytes = pl.ws_bytes;
+        ws.ring_clean = false;
         // the flag block starts zeroed (the exact-form list counters above all)
         if (cudaMemsetAsync(ws.ptr, 0, 256, stream) != cudaSuccess) return KDA_ERR_CUDA;
     }
     uint8_t *wsb = static_cast<uint8_t *>(ws.ptr);
-
-    kda::ChunkGeometry geo{};
-    geo.cu = cu_seqlens;
-    geo.chunk_off = cu_seqlens ? reinterpret_cast<const int32_t *>(wsb + 256) : nullptr;
-    geo.call_flags = reinterpret_cast<const int *>(wsb);
-    geo.seq_len = cu_seqlens ? pl.tokens : T;
-    geo.n_seqs = static_cast<int32_t>(N);
-    geo.n_heads = static_cast<int32_t>(H);
-    geo.chunks_per_seq = static_cast<int32_t>((T + 15) / 16);
-    geo.pos_begin = 0;
-    geo.seg_len = geo.chunks_per_seq;
-    geo.slot_stride = geo.chunks_per_seq;
 
     const bool timed = t_timing.calls < t_timing.max_calls;
     if (timed) ++t_timing.calls;
@@ -416,6 +439,66 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
         if (timed && cudaEventRecord(e1, s) != cudaSuccess) return KDA_ERR_CUDA;
         return KDA_OK;
     };
+
+    if (pl.impl >= kImplC64Split) {
+        // ---- 64-token chunks on tcgen05
+        const bool fused = pl.impl == kImplC64Fused;
+        if (!fused) ws.ring_clean = false;
+        if (cu_seqlens != nullptr &&
+            kda::launch_varlen_prologue(cu_seqlens, static_cast<int32_t>(N), pl.tokens,
+                                        reinterpret_cast<int32_t *>(wsb + 256),
+                                        reinterpret_cast<int *>(wsb), st.err, stream,
+                                        6) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        kda::C64Args a{};
+        a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.s0 = initial_state;
+        a.out = out; a.s_final = final_state;
+        a.cu = cu_seqlens;
+        a.chunk_off = cu_seqlens ? reinterpret_cast<const int32_t *>(wsb + 256) : nullptr;
+        a.call_flags = reinterpret_cast<const int *>(wsb);
+        a.err = st.err;
+        a.tokens = pl.tokens;
+        a.seq_len = cu_seqlens ? pl.tokens : T;
+        a.max_chunks = pl.c64_chunks;
+        a.n_seqs = static_cast<int32_t>(N);
+        a.n_heads = static_cast<int32_t>(H);
+        a.cps = static_cast<int32_t>((T + 63) / 64);
+        a.scale = scale;
+        a.pre = flags;
+        a.rec = wsb + 256 + pl.off_bytes;
+        if (!fused) {
+            rc = timed_launch(true, stream, [&] { return kda::launch_c64_intra(a, sm_count, stream); });
+            if (rc != KDA_OK) return rc;
+            return timed_launch(false, stream, [&] { return kda::launch_c64_chain(a, stream); });
+        }
+        if (pl.tokens == 0)   // nothing for the builders: the chains alone carry the states
+            return timed_launch(false, stream, [&] { return kda::launch_c64_chain(a, stream); });
+        long long *sync = reinterpret_cast<long long *>(wsb + pl.c64_sync);
+        if (!ws.ring_clean) {
+            if (cudaMemsetAsync(sync, 0, (kC64Ring * H + H) * 8 + 64, stream) != cudaSuccess)
+                return KDA_ERR_CUDA;
+            ws.ring_clean = true;   // each fused launch leaves them zero again
+        }
+        a.ring_depth = static_cast<int>(kC64Ring);
+        a.n_chain = static_cast<int>(H);
+        a.ready = sync;
+        a.consumed = sync + kC64Ring * H;
+        a.exit_ctr = reinterpret_cast<int *>(sync + kC64Ring * H + H);
+        return timed_launch(false, stream, [&] { return kda::launch_c64_fused(a, sm_count, stream); });
+    }
+    ws.ring_clean = false;
+
+    kda::ChunkGeometry geo{};
+    geo.cu = cu_seqlens;
+    geo.chunk_off = cu_seqlens ? reinterpret_cast<const int32_t *>(wsb + 256) : nullptr;
+    geo.call_flags = reinterpret_cast<const int *>(wsb);
+    geo.seq_len = cu_seqlens ? pl.tokens : T;
+    geo.n_seqs = static_cast<int32_t>(N);
+    geo.n_heads = static_cast<int32_t>(H);
+    geo.chunks_per_seq = static_cast<int32_t>((T + 15) / 16);
+    geo.pos_begin = 0;
+    geo.seg_len = geo.chunks_per_seq;
+    geo.slot_stride = geo.chunks_per_seq;
 
     if (cu_seqlens != nullptr) {
         if (kda::launch_varlen_prologue(cu_seqlens, geo.n_seqs, pl.tokens,
@@ -531,7 +614,7 @@ static int64_t backward_ws_bytes(int64_t B, int64_t T, int64_t H, int64_t N, boo
 int64_t kda_backward_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N,
                                      int has_cu_seqlens) {
     Plan pl;
-    if (plan_sizes(B, T, H, N, has_cu_seqlens != 0, current_sm_count(), &pl) != KDA_OK) return 0;
+    if (plan_sizes(B, T, H, N, has_cu_seqlens != 0, current_sm_count(), 1, &pl) != KDA_OK) return 0;
     if (N * H > (int64_t(1) << 31) - 1) return 0;
     return backward_ws_bytes(B, T, H, N, has_cu_seqlens != 0, pl);
 }
@@ -547,7 +630,7 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
     // ---- checks that need no GPU
     if (K != 128 || V != 128) return KDA_ERR_UNSUPPORTED_DIM;
     Plan pl;
-    kda_status rc = plan_sizes(B, T, H, N, cu_seqlens != nullptr, current_sm_count(), &pl);
+    kda_status rc = plan_sizes(B, T, H, N, cu_seqlens != nullptr, current_sm_count(), 1, &pl);
     if (rc != KDA_OK) return rc;
     if (N * H > (int64_t(1) << 31) - 1) return KDA_ERR_BAD_SHAPE;
     if (pl.tokens > 0 && (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv || !dg ||
@@ -684,7 +767,7 @@ kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *cal
 }
 
 kda_status kda_set_recurrent_impl(int impl) {
-    if (impl < 0 || impl > 2) return KDA_ERR_BAD_SHAPE;
+    if (impl < 0 || impl > kImplC64Fused) return KDA_ERR_BAD_SHAPE;
     g_recur_impl.store(impl);
     return KDA_OK;
 }

@@ -1,0 +1,1468 @@
+// Chunked KDA prefill with 64-token chunks on the 5th-generation tensor core.
+//
+// The two kernels of different parallelism that the pages describe ("Kimi K3
+// 的三個系統設計", section "為什麼 FlashKDA 選擇 16-token chunks": a
+// token-parallel intra-chunk kernel and a recurrent inter-chunk kernel), with
+// the chunk widened from 16 to 64 tokens so that every product of the
+// recurrent step is a tcgen05 MMA with M = 128:
+//
+//   intra-chunk, per (64-token chunk, head), G_r = sum_{u<=r} g_u per channel:
+//     A  = strict_lower( (beta K e^G) (K e^-G)^T )      Gram, one tcgen05 MMA group
+//     P  = scale lower( (Q e^G) (K e^-G)^T )             (same MMA, rows 64..127)
+//     T  = (I + A)^-1                                    blocked forward substitution:
+//          16 x 16 diagonal blocks in fp32, off-diagonal blocks by tf32 warp MMAs
+//     W  = T (beta K e^G),  Ut = T (beta V)              tcgen05 MMAs
+//   recurrent, per (sequence, head), state S^T (V x K, fp32) in tensor memory:
+//     U^T = Ut^T - S^T W^T,  o^T = S^T (scale Qg)^T + U^T (scale P)^T
+//     S^T <- S^T Diag(gamma) + U^T Kd
+//
+// The inputs are staged by TMA tensor-map loads (cp.async.bulk.tensor), the
+// records by bulk copies. Chunks whose cumulative log decay leaves [-80, 80]
+// in some channel (strong decay) get A and P from exact per-pair
+// exponentials instead of the factored form; everything else is shared.
+//
+// Launch forms: the intra-chunk kernel over all chunk-heads followed by the
+// recurrent kernel (records in the workspace), or one cooperative kernel in
+// which some CTAs run the recurrent chains while the others build the records
+// into a small ring that stays in L2 (ring_depth slots per head, ready and
+// consumed counters in global memory, every wait bounded).
+
+#include <cuda.h>
+
+#include "kda_c64.cuh"
+#include "kda_device.cuh"
+#include "kda_internal.h"
+#include "kda_tcgen05.cuh"
+
+namespace kda {
+namespace c64 {
+
+namespace {
+
+constexpr int kThreads = 320;    // 10 warps
+constexpr float kLog2e = 1.4426950408889634f;
+// |G| bound of the factored exponentials (natural-log units)
+constexpr float kFactorRange = 80.f;
+
+// ------------------------------------------------------------------ shared memory
+// recurrent role
+constexpr int kCStages = 2;
+constexpr int kCOffAS = kCStages * kRecBytes;     // S^T bf16 operand, 128 x 128 keys
+constexpr int kCOffAU = kCOffAS + 32768;          // U^T bf16 operand, 128 x 64 tokens
+constexpr int kCOffO = kCOffAU + 16384;           // o staging [64 tok][128 v] bf16
+constexpr int kCOffMisc = kCOffO + 16384;         // tmem base, abort flag
+constexpr int kCOffBar = kCOffMisc + 64;
+enum {
+    kCBFull = 0, kCBEmpty = 2, kCBSop = 4, kCBUdone = 5, kCBUop = 6, kCBSdone = 7,
+    kCBOdone = 8, kCBOfree = 10, kCBTear = 12, kCBDrain = 13, kCNumBars = 14
+};
+constexpr int kCSmem = kCOffBar + kCNumBars * 8;
+// intra-chunk role
+constexpr int kIOffQ = 0, kIOffK = 16384, kIOffV = 32768, kIOffG = 49152;  // TMA tiles
+constexpr int kIOffBeta = 81920;                  // fp32 [64]
+constexpr int kIOffGA = 82944;                    // [beta K e^G ; scale Q e^G] 128 x 128 keys
+constexpr int kIOffGB = kIOffGA + 32768;          // K e^-G: 64 x 128 keys (exact form: P fp32)
+constexpr int kIOffWB = kIOffGB + 16384;          // (beta K e^G)^T: 128 keys x 64 tokens
+constexpr int kIOffUA = kIOffWB + 16384;          // (beta V)^T: 128 v x 64 tokens
+constexpr int kIOffTA = kIOffUA + 16384;          // T: 64 x 64 tokens, bf16
+constexpr int kIOffAT = kIOffTA + 8192;           // A and T, fp32 [64][68]
+constexpr int kATStride = 68;
+constexpr int kIOffTot = kIOffAT + 64 * kATStride * 4;   // per token block sums [8][128]
+constexpr int kIOffRed = kIOffTot + 4096;         // [8] per-warp range maxima, [8] flags
+constexpr int kIOffMisc = kIOffRed + 64;          // tmem base, abort, item flags
+constexpr int kIOffBar = kIOffMisc + 64;
+enum { kIBIn = 0, kIBA = 1, kIBGram = 2, kIBInv = 3, kIBWU = 4, kIBTear = 5, kIBDrain = 6,
+       kINumBars = 7 };
+constexpr int kISmem = kIOffBar + kINumBars * 8;
+constexpr int kSmem = kCSmem > kISmem ? kCSmem : kISmem;
+static_assert(kSmem <= 227 * 1024, "shared memory");
+
+// tensor memory columns
+constexpr uint32_t kCTmemCols = 512;   // S^T [0,128), D1 x2 [128,384)
+constexpr uint32_t kITmemCols = 256;   // Gram [0,64), W [64,192), Ut^T [192,256)
+
+constexpr uint32_t kIdFull = tc::idesc(128, 64, 1);    // M=128, N=64
+constexpr uint32_t kIdSq = tc::idesc(128, 128, 1);     // M=128, N=128
+constexpr uint32_t kIdW = tc::idesc(64, 128, 1);       // M=64, N=128
+
+// ------------------------------------------------------------------ small helpers
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads:
+// every thread gets the same answer (used to leave a loop together).
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %3, 0;\n"
+        " bar.red.or.pred q, %1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(id), "r"(n), "r"(pred ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
+    asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// D += A * B, m16n8k8, tf32 operands, fp32 accumulate
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                       uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+
+// 32 lanes x 32 bits, 32 or 64 consecutive columns (thread i <-> lane i)
+__device__ __forceinline__ void tld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tst32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// Bounded mbarrier wait that also gives up once another warp raised the abort flag.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         int *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ long long ld_acquire(const long long *p) {
+    long long v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];\n" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(long long *p, long long v) {
+    asm volatile("st.release.gpu.global.b64 [%0], %1;\n" ::"l"(p), "l"(v) : "memory");
+}
+
+// Bounded wait for a global counter written by another CTA of the same
+// (cooperative) launch to reach `target`.
+__device__ __forceinline__ bool wait_counter(const long long *p, long long target,
+                                             volatile int *abort_flag, int *err) {
+    if (ld_acquire(p) >= target) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        for (int i = 0; i < 16; ++i) {
+            __nanosleep(64);
+            if (ld_acquire(p) >= target) return true;
+        }
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ parameters
+struct Params {
+    CUtensorMap tm_q, tm_k, tm_v, tm_g;   // (128 channels, H, tokens), box (128, 1, 64)
+    const float *beta;                    // [tokens, H]
+    const float *s0;                      // [N, H, 128, 128] or nullptr
+    void *out;                            // bf16 [tokens, H, 128]
+    float *s_final;                       // [N, H, 128, 128] or nullptr
+    uint8_t *rec;                         // records
+    int *err;                             // sticky device error word
+    const int32_t *cu;                    // packed: cu_seqlens [N+1]
+    const int32_t *chunk_off;             // packed: first 64-token chunk of each sequence [N+1]
+    const int *call_flags;                // packed: per-call flags (bad cu_seqlens)
+    int64_t seq_len;                      // fixed: tokens per sequence; packed: total tokens
+    int64_t max_chunks;                   // chunks of the call (upper bound when packed)
+    int32_t n_seqs, n_heads, cps;         // cps: chunks per sequence (fixed)
+    float scale;
+    int pre;                              // kPreNormQK | kPreGateLogits
+    // ring form (one cooperative launch)
+    int ring_depth;                       // 0: record of (chunk c, head h) at c * H + h
+    int n_chain;                          // CTAs [0, n_chain) run chains (head = blockIdx.x)
+    long long *ready;                     // [ring_depth * H]: chunk index + 1 of the slot's record
+    long long *consumed;                  // [H]: chunks of head h copied out by its chain
+    int *exit_ctr;                        // CTAs finished (the last one clears the counters)
+};
+
+// Where chunk c is: sequence n, first token t0, length L. False past the end.
+__device__ __forceinline__ bool locate(const Params &p, int64_t c, int &n, int64_t &t0, int &L) {
+    if (p.cu == nullptr) {
+        if (c >= static_cast<int64_t>(p.n_seqs) * p.cps) return false;
+        n = static_cast<int>(c / p.cps);
+        const int64_t i = c - static_cast<int64_t>(n) * p.cps;
+        t0 = static_cast<int64_t>(n) * p.seq_len + kC * i;
+        const int64_t rem = p.seq_len - kC * i;
+        L = static_cast<int>(rem < kC ? rem : kC);
+        return true;
+    }
+    const int32_t *off = p.chunk_off;
+    if (c >= off[p.n_seqs]) return false;
+    int lo = 0, hi = p.n_seqs;   // off[lo] <= c < off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (off[mid] <= c) lo = mid; else hi = mid;
+    }
+    n = lo;
+    t0 = static_cast<int64_t>(p.cu[n]) + kC * (c - off[n]);
+    const int64_t rem = static_cast<int64_t>(p.cu[n + 1]) - t0;
+    L = static_cast<int>(rem < kC ? rem : kC);
+    return true;
+}
+
+__device__ __forceinline__ uint8_t *record_of(const Params &p, int64_t c, int h) {
+    const int64_t H = p.n_heads;
+    const int64_t slot = p.ring_depth > 0 ? (c % p.ring_depth) : c;
+    return p.rec + (slot * H + h) * static_cast<int64_t>(kRecBytes);
+}
+
+// ============================================================================
+// Intra-chunk role: warps 0-7 compute, warp 8 issues the TMA loads and MMAs.
+// Items (chunk c, head h) = c * H + h, taken with a stride of `nworkers`.
+// ============================================================================
+namespace {
+
+// Forward substitution of one 16 x 16 diagonal block (warp w, lanes 0-15
+// each solve one column), in place in the fp32 A/T buffer.
+__device__ __forceinline__ void invert_diag(float *at, int w, int lane) {
+    const int j = lane & 15, b = 16 * w;
+    float t[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        float s = (r == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int i = 0; i < r; ++i) s = fmaf(-at[(b + r) * kATStride + b + i], t[i], s);
+        t[r] = s;
+    }
+    __syncwarp();
+    if (lane < 16) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) at[(b + r) * kATStride + b + j] = t[r];
+    }
+    __syncwarp();
+}
+
+// Element (r, c) of block (I, J) of A or T in the shared fp32 buffer: A's
+// strictly lower blocks in place, T's diagonal blocks in place of A's, T's
+// blocks below the diagonal stored transposed in the upper triangle.
+__device__ __forceinline__ float a_blk(const float *at, int I, int J, int r, int c) {
+    return at[(16 * I + r) * kATStride + 16 * J + c];
+}
+__device__ __forceinline__ float t_blk(const float *at, int I, int J, int r, int c) {
+    return I == J ? at[(16 * I + r) * kATStride + 16 * J + c]
+                  : at[(16 * J + c) * kATStride + 16 * I + r];
+}
+
+// acc (16 x 16, two m16n8 fragments) += X(I,K) * T(K,J), X = A (use_a) or T
+__device__ __forceinline__ void blk_mma(float (&acc)[2][4], const float *at, bool xa, int I, int K,
+                                        int J, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int kk = 0; kk < 16; kk += 8) {
+        const uint32_t a0 = tf32(xa ? a_blk(at, I, K, g, kk + t) : t_blk(at, I, K, g, kk + t));
+        const uint32_t a1 =
+            tf32(xa ? a_blk(at, I, K, g + 8, kk + t) : t_blk(at, I, K, g + 8, kk + t));
+        const uint32_t a2 =
+            tf32(xa ? a_blk(at, I, K, g, kk + t + 4) : t_blk(at, I, K, g, kk + t + 4));
+        const uint32_t a3 =
+            tf32(xa ? a_blk(at, I, K, g + 8, kk + t + 4) : t_blk(at, I, K, g + 8, kk + t + 4));
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t b0 = tf32(t_blk(at, K, J, kk + t, 8 * nt + g));
+            const uint32_t b1 = tf32(t_blk(at, K, J, kk + t + 4, 8 * nt + g));
+            mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+        }
+    }
+}
+
+// T(I,J) = -T(I,I) * X where X (16 x 16, fragments) is staged in scratch.
+__device__ __forceinline__ void finish_blk(float *at, float *scratch, const float (&x)[2][4],
+                                           int I, int J, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        scratch[g * 17 + 8 * nt + 2 * t] = x[nt][0];
+        scratch[g * 17 + 8 * nt + 2 * t + 1] = x[nt][1];
+        scratch[(g + 8) * 17 + 8 * nt + 2 * t] = x[nt][2];
+        scratch[(g + 8) * 17 + 8 * nt + 2 * t + 1] = x[nt][3];
+    }
+    __syncwarp();
+    float acc[2][4] = {};
+#pragma unroll
+    for (int kk = 0; kk < 16; kk += 8) {
+        const uint32_t a0 = tf32(t_blk(at, I, I, g, kk + t));
+        const uint32_t a1 = tf32(t_blk(at, I, I, g + 8, kk + t));
+        const uint32_t a2 = tf32(t_blk(at, I, I, g, kk + t + 4));
+        const uint32_t a3 = tf32(t_blk(at, I, I, g + 8, kk + t + 4));
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t b0 = tf32(scratch[(kk + t) * 17 + 8 * nt + g]);
+            const uint32_t b1 = tf32(scratch[(kk + t + 4) * 17 + 8 * nt + g]);
+            mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
+        }
+    }
+    // store transposed: T(I,J)[r][c] at at[16J + c][16I + r]
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int c0 = 8 * nt + 2 * t;
+        at[(16 * J + c0) * kATStride + 16 * I + g] = -acc[nt][0];
+        at[(16 * J + c0 + 1) * kATStride + 16 * I + g] = -acc[nt][1];
+        at[(16 * J + c0) * kATStride + 16 * I + g + 8] = -acc[nt][2];
+        at[(16 * J + c0 + 1) * kATStride + 16 * I + g + 8] = -acc[nt][3];
+    }
+    __syncwarp();
+}
+
+// T = (I + A)^{-1} for the 64 x 64 strictly lower A in `at` (warps 0-3 of
+// the compute group; the caller synchronises the group before and after).
+__device__ __forceinline__ void invert64(float *at, float *scratch, int warp, int lane) {
+    invert_diag(at, warp, lane);
+    named_sync(2, 128);
+    // level 1: T(I, I-1) for I = 1..3 on warps 0..2
+    if (warp < 3) {
+        const int I = warp + 1;
+        float x[2][4] = {};
+        blk_mma(x, at, true, I, I - 1, I - 1, lane);
+        finish_blk(at, scratch + warp * 16 * 17, x, I, I - 1, lane);
+    }
+    named_sync(2, 128);
+    // level 2: T(I, I-2) for I = 2, 3 on warps 0, 1
+    if (warp < 2) {
+        const int I = warp + 2;
+        float x[2][4] = {};
+        blk_mma(x, at, true, I, I - 2, I - 2, lane);
+        blk_mma(x, at, true, I, I - 1, I - 2, lane);
+        finish_blk(at, scratch + warp * 16 * 17, x, I, I - 2, lane);
+    }
+    named_sync(2, 128);
+    // level 3: T(3, 0) on warp 0
+    if (warp == 0) {
+        float x[2][4] = {};
+        blk_mma(x, at, true, 3, 0, 0, lane);
+        blk_mma(x, at, true, 3, 1, 0, lane);
+        blk_mma(x, at, true, 3, 2, 0, lane);
+        finish_blk(at, scratch, x, 3, 0, lane);
+    }
+}
+
+template <bool PRE>
+__device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nworkers) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.n_heads;
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bar0 = sb + kIOffBar;
+    auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kIOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kIOffMisc + 4);
+    volatile int *item_exact = reinterpret_cast<volatile int *>(smem + kIOffMisc + 8);
+    if (tid == 0) {
+        mbar_init(bar(kIBIn), 1);
+        mbar_init(bar(kIBA), 8);
+        mbar_init(bar(kIBGram), 1);
+        mbar_init(bar(kIBInv), 8);
+        mbar_init(bar(kIBWU), 1);
+        mbar_init(bar(kIBTear), kThreads / 32);
+        mbar_init(bar(kIBDrain), 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 8) {
+        tc::alloc(smem_u32(tmem_slot), kITmemCols);
+        tc::relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = p.cu != nullptr && (*p.call_flags & kErrBadCu);
+    const int64_t items = skip ? 0 : p.max_chunks * H;
+
+    // next item of this worker at or after `item` that holds a real chunk
+    auto next_real = [&](int64_t item) {
+        while (item < items) {
+            int n, L;
+            int64_t t0;
+            if (locate(p, item / H, n, t0, L)) break;
+            item += nworkers;
+        }
+        return item;
+    };
+
+    if (warp == 8) {
+        // ================================================ TMA loads and MMA issue
+        if (lane == 0) {
+            int it = 0, loads = 0;
+            auto issue_loads = [&](int64_t itm) {
+                const int64_t c = itm / H;
+                const int h = static_cast<int>(itm - c * H);
+                int n, L;
+                int64_t t0;
+                locate(p, c, n, t0, L);
+                mbar_arrive_expect_tx(bar(kIBIn), 3 * 16384 + 32768);
+                const int z = static_cast<int>(t0);
+                tma_load_3d(sb + kIOffQ, &p.tm_q, 0, h, z, bar(kIBIn));
+                tma_load_3d(sb + kIOffK, &p.tm_k, 0, h, z, bar(kIBIn));
+                tma_load_3d(sb + kIOffV, &p.tm_v, 0, h, z, bar(kIBIn));
+                tma_load_3d(sb + kIOffG, &p.tm_g, 0, h, z, bar(kIBIn));
+                ++loads;
+            };
+            int64_t item = next_real(worker);
+            if (item < items) issue_loads(item);
+            for (; item < items; ++it) {
+                // phase A done: operand tiles written, input tiles free
+                if (!wait_bar(bar(kIBA), it & 1, abort_flag, p.err)) break;
+                const bool exact = *item_exact != 0;
+                const int64_t next = next_real(item + nworkers);
+                if (!exact) {
+                    if (next < items) issue_loads(next);
+                    tc::fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tmem + 0, tc::sdesc(sb + kIOffGA + kk * 256, 128, 2048),
+                               tc::sdesc(sb + kIOffGB + kk * 256, 128, 2048), kIdFull, kk > 0);
+                    tc::commit(bar(kIBGram));
+                }
+                // T ready (the exact form also read the input tiles until now)
+                if (!wait_bar(bar(kIBInv), it & 1, abort_flag, p.err)) break;
+                if (exact && next < items) issue_loads(next);
+                tc::fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    // W = T (beta K e^G): M = 64 rows r, N = 128 keys, K = 64 tokens
+                    mma_ss(tmem + 64, tc::sdesc(sb + kIOffTA + kk * 256, 128, 1024),
+                           tc::sdesc(sb + kIOffWB + kk * 256, 128, 1024), kIdW, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    // Ut^T = (beta V)^T T^T: M = 128 v, N = 64 rows r, K = 64 tokens
+                    mma_ss(tmem + 192, tc::sdesc(sb + kIOffUA + kk * 256, 128, 1024),
+                           tc::sdesc(sb + kIOffTA + kk * 256, 128, 1024), kIdFull, kk > 0);
+                }
+                tc::commit(bar(kIBWU));
+                item = next;
+            }
+            // drain: the last input load and every MMA issued have completed
+            if (loads > 0) wait_bar(bar(kIBIn), (loads - 1) & 1, abort_flag, p.err);
+            tc::commit(bar(kIBDrain));
+            wait_bar(bar(kIBDrain), 0, abort_flag, p.err);
+        }
+    } else if (warp < 8) {
+        // ================================================ compute warps (256 threads)
+        const int ct = tid;                 // 0..255
+        const int bt = ct & 127;            // 8 x 8 block of the 64 x 128 tile
+        const int role = ct >> 7;           // 0: exp(G) products, 1: exp(-G) products
+        const int tb = bt >> 4, cb = bt & 15;
+        const int row0 = 8 * tb, ch0 = 8 * cb;
+        float *tot = reinterpret_cast<float *>(smem + kIOffTot);
+        int *red = reinterpret_cast<int *>(smem + kIOffRed);
+        float *at = reinterpret_cast<float *>(smem + kIOffAT);
+        float *betas = reinterpret_cast<float *>(smem + kIOffBeta);
+        int it = 0;
+        for (int64_t item = next_real(worker); item < items; item = next_real(item + nworkers)) {
+            const int64_t c = item / H;
+            const int h = static_cast<int>(item - c * H);
+            int n, L;
+            int64_t t0;
+            locate(p, c, n, t0, L);
+            (void)n;
+            uint8_t *rec = record_of(p, c, h);
+            // ring form: the slot's previous record must have been copied out
+            if (p.ring_depth > 0 && ct == 0 && c >= p.ring_depth)
+                wait_counter(p.consumed + h, c - p.ring_depth + 1, abort_flag, p.err);
+            if (ct < kC) betas[ct] = ct < L ? __ldg(p.beta + (t0 + ct) * H + h) : 0.f;
+            wait_bar(bar(kIBIn), it & 1, abort_flag, p.err);
+
+            // ---- cumulative log decay of this thread's 8 x 8 block (base 2)
+            float G[8][8];
+            bool anypos = false;
+            {
+                const float *gs = reinterpret_cast<const float *>(smem + kIOffG);
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    const float4 x0 = *reinterpret_cast<const float4 *>(gs + (row0 + r) * 128 + ch0);
+                    const float4 x1 =
+                        *reinterpret_cast<const float4 *>(gs + (row0 + r) * 128 + ch0 + 4);
+                    const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                    const bool real = row0 + r < L;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        float gv = real ? x[j] : 0.f;
+                        if (PRE && (p.pre & kPreGateLogits) && real) gv = log_sigmoid(gv);
+                        anypos |= gv > 0.f;
+                        G[r][j] = (r > 0 ? G[r - 1][j] : 0.f) + gv * kLog2e;
+                    }
+                }
+            }
+            if (role == 0) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) tot[tb * 128 + ch0 + j] = G[7][j];
+            }
+            if (named_sync_or(1, 256, *abort_flag != 0)) break;
+            float gl[8];   // G_last of each channel (base 2)
+            {
+                float pre8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) { gl[j] = 0.f; pre8[j] = 0.f; }
+                for (int b2 = 0; b2 < 8; ++b2) {
+                    const float4 y0 = *reinterpret_cast<const float4 *>(tot + b2 * 128 + ch0);
+                    const float4 y1 = *reinterpret_cast<const float4 *>(tot + b2 * 128 + ch0 + 4);
+                    const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (b2 < tb) pre8[j] += y[j];
+                        gl[j] += y[j];
+                    }
+                }
+                float gmax = 0.f;
+#pragma unroll
+                for (int r = 0; r < 8; ++r)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        G[r][j] += pre8[j];
+                        gmax = fmaxf(gmax, fabsf(G[r][j]));
+                    }
+                // the factored form holds while |G| <= 80 (natural log); with
+                // positive gates in the chunk while |G| <= 40, so that no
+                // lower-triangle product exp(G_r - G_i) exceeds exp(80) either
+                const float lim = anypos ? 0.5f * kFactorRange * kLog2e : kFactorRange * kLog2e;
+                const unsigned any_bad = __ballot_sync(0xffffffffu, !(gmax <= lim));
+                if (lane == 0) red[warp] = any_bad != 0;
+            }
+            named_sync(1, 256);
+            bool exact = false;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) exact |= red[w] != 0;
+
+            // ---- gated operand tiles and the record's Qg, Kd, gamma, row by row
+            const bool norm = PRE && (p.pre & kPreNormQK);
+            const uint8_t *qs = smem + kIOffQ, *ks = smem + kIOffK, *vs = smem + kIOffV;
+            // row r's 8 channels of a bf16 tile (zero past the sequence end), and
+            // the row's L2 norm over the 16 threads that share it when asked
+            auto load8 = [&](const uint8_t *tile, int r, float (&x)[8]) {
+                const uint4 u = *reinterpret_cast<const uint4 *>(tile + (row0 + r) * 256 + ch0 * 2);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                const bool real = row0 + r < L;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = unpack_bf16(w4[e]);
+                    x[2 * e] = real ? f.x : 0.f;
+                    x[2 * e + 1] = real ? f.y : 0.f;
+                }
+            };
+            auto normalise = [&](float (&x)[8]) {
+                float ss = 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float rn = rsqrtf(ss + kNormEps);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) x[j] *= rn;
+            };
+            auto pack8 = [](const float (&x)[8]) {
+                return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
+                                  pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+            };
+            if (role == 0) {
+                // scale Q e^G -> GA rows 64+ and record B1 rows 64+;
+                // beta K e^G -> GA rows 0-63 and, transposed, WB
+                float kb[8][8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    float q[8], k[8];
+                    load8(qs, r, q);
+                    load8(ks, r, k);
+                    if (norm) { normalise(q); normalise(k); }
+                    const float br = betas[row0 + r];
+                    float qg[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float e = ex2f(G[r][j]);
+                        qg[j] = q[j] * e * p.scale;
+                        kb[r][j] = k[j] * e * br;
+                    }
+                    const uint4 uq = pack8(qg);
+                    *reinterpret_cast<uint4 *>(smem + kIOffGA + kmaj(64 + row0 + r, ch0, 128)) = uq;
+                    st_global_v4(rec + kRecB1 + kmaj(64 + row0 + r, ch0, 128), uq);
+                    *reinterpret_cast<uint4 *>(smem + kIOffGA + kmaj(row0 + r, ch0, 128)) = pack8(kb[r]);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 u = make_uint4(pack_bf16(kb[0][j], kb[1][j]), pack_bf16(kb[2][j], kb[3][j]),
+                                               pack_bf16(kb[4][j], kb[5][j]), pack_bf16(kb[6][j], kb[7][j]));
+                    *reinterpret_cast<uint4 *>(smem + kIOffWB + kmaj(ch0 + j, row0, 64)) = u;
+                }
+                if (tb == 0) {
+                    float gm[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) gm[j] = ex2f(gl[j]);
+                    st_global_v4(rec + kRecGam + ch0 * 4,
+                                 make_uint4(__float_as_uint(gm[0]), __float_as_uint(gm[1]),
+                                            __float_as_uint(gm[2]), __float_as_uint(gm[3])));
+                    st_global_v4(rec + kRecGam + ch0 * 4 + 16,
+                                 make_uint4(__float_as_uint(gm[4]), __float_as_uint(gm[5]),
+                                            __float_as_uint(gm[6]), __float_as_uint(gm[7])));
+                }
+                if (exact) {
+                    // the exact form reads G (base 2) from the g tile
+                    float *gs = reinterpret_cast<float *>(smem + kIOffG);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        *reinterpret_cast<float4 *>(gs + (row0 + r) * 128 + ch0) =
+                            make_float4(G[r][0], G[r][1], G[r][2], G[r][3]);
+                        *reinterpret_cast<float4 *>(gs + (row0 + r) * 128 + ch0 + 4) =
+                            make_float4(G[r][4], G[r][5], G[r][6], G[r][7]);
+                    }
+                }
+            } else {
+                // K e^-G -> GB; Kd = K e^(G_last - G) -> record B2 (transposed)
+                float egl[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) egl[j] = ex2f(gl[j]);
+                float kd[8][8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    float k[8];
+                    load8(ks, r, k);
+                    if (norm) normalise(k);
+                    float kn[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (exact) {
+                            kn[j] = 0.f;   // unused by the exact form
+                            kd[r][j] = k[j] * ex2f(gl[j] - G[r][j]);
+                        } else {
+                            kn[j] = k[j] * ex2f(-G[r][j]);
+                            kd[r][j] = kn[j] * egl[j];
+                        }
+                    }
+                    *reinterpret_cast<uint4 *>(smem + kIOffGB + kmaj(row0 + r, ch0, 128)) = pack8(kn);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 u = make_uint4(pack_bf16(kd[0][j], kd[1][j]), pack_bf16(kd[2][j], kd[3][j]),
+                                               pack_bf16(kd[4][j], kd[5][j]), pack_bf16(kd[6][j], kd[7][j]));
+                    st_global_v4(rec + kRecB2 + kmaj(ch0 + j, row0, 64), u);
+                }
+                // beta V -> UA (transposed); reuses kd's registers
+#pragma unroll
+                for (int r = 0; r < 8; ++r) {
+                    float vv[8];
+                    load8(vs, r, vv);
+                    const float br = betas[row0 + r];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) kd[r][j] = vv[j] * br;
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint4 u = make_uint4(pack_bf16(kd[0][j], kd[1][j]), pack_bf16(kd[2][j], kd[3][j]),
+                                               pack_bf16(kd[4][j], kd[5][j]), pack_bf16(kd[6][j], kd[7][j]));
+                    *reinterpret_cast<uint4 *>(smem + kIOffUA + kmaj(ch0 + j, row0, 64)) = u;
+                }
+            }
+            if (ct == 0) *item_exact = exact ? 1 : 0;
+            fence_async_smem();
+            tc::fence_before();
+            named_sync(1, 256);
+            if (lane == 0) mbar_arrive(bar(kIBA));
+
+            // ---- A (fp32, for the inversion) and P (to the record)
+            if (!exact) {
+                wait_bar(bar(kIBGram), it & 1, abort_flag, p.err);
+                tc::fence_after();
+                const int q4 = warp & 3, half = warp >> 2;
+                const int row = 32 * q4 + lane;    // Gram row: 0-63 A rows, 64-127 P rows
+                uint32_t d[32];
+                tld32(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 32 * half, d);
+                tc::ld_wait();
+                if (row < 64) {
+                    const int r = row;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int i = 32 * half + j;
+                        at[r * kATStride + i] = (i < r) ? __uint_as_float(d[j]) : 0.f;
+                    }
+                } else {
+                    const int r = row - 64;
+#pragma unroll
+                    for (int g8 = 0; g8 < 4; ++g8) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i0 = 32 * half + 8 * g8 + 2 * e;
+                            const float v0 = (i0 <= r) ? __uint_as_float(d[8 * g8 + 2 * e]) : 0.f;
+                            const float v1 =
+                                (i0 + 1 <= r) ? __uint_as_float(d[8 * g8 + 2 * e + 1]) : 0.f;
+                            w4[e] = pack_bf16(v0, v1);
+                        }
+                        st_global_v4(rec + kRecB3 + kmaj(r, 32 * half + 8 * g8, 64),
+                                     make_uint4(w4[0], w4[1], w4[2], w4[3]));
+                    }
+                }
+                tc::fence_before();
+            } else {
+                // exact per-pair exponentials: 8 threads per row pair (rp, 63 - rp),
+                // pairs (r, i <= r) with i = sub (mod 8)
+                const float *gs = reinterpret_cast<const float *>(smem + kIOffG);
+                float *pf = reinterpret_cast<float *>(smem + kIOffGB);   // P fp32 [64][64]
+                // inverse row norms of q (0..63) and k (64..127) when normalising
+                float *rn = reinterpret_cast<float *>(smem + kIOffTot);
+                if (ct < 128) {
+                    float x = 1.f;
+                    if (norm) {
+                        const uint8_t *row = (ct < 64 ? qs : ks) + (ct & 63) * 256;
+                        float ss = 0.f;
+                        for (int c8 = 0; c8 < 16; ++c8) {
+                            const uint4 u = *reinterpret_cast<const uint4 *>(row + c8 * 16);
+                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = unpack_bf16(w4[e]);
+                                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+                            }
+                        }
+                        x = rsqrtf(ss + kNormEps);
+                    }
+                    rn[ct] = x;
+                }
+                named_sync(1, 256);
+                const int rp = ct >> 3, sub = ct & 7;
+                bool overflow = false;
+                for (int side = 0; side < 2; ++side) {
+                    const int r = side == 0 ? rp : 63 - rp;
+                    for (int i = sub; i <= r; i += 8) {
+                        float sa = 0.f, sp = 0.f;
+                        for (int c8 = 0; c8 < 16; ++c8) {
+                            const uint4 kr = *reinterpret_cast<const uint4 *>(ks + r * 256 + c8 * 16);
+                            const uint4 qr = *reinterpret_cast<const uint4 *>(qs + r * 256 + c8 * 16);
+                            const uint4 ki = *reinterpret_cast<const uint4 *>(ks + i * 256 + c8 * 16);
+                            const uint32_t krw[4] = {kr.x, kr.y, kr.z, kr.w};
+                            const uint32_t qrw[4] = {qr.x, qr.y, qr.z, qr.w};
+                            const uint32_t kiw[4] = {ki.x, ki.y, ki.z, ki.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 a = unpack_bf16(krw[e]), bq = unpack_bf16(qrw[e]),
+                                             cc = unpack_bf16(kiw[e]);
+                                const int ch = 8 * c8 + 2 * e;
+                                const float x0 = gs[r * 128 + ch] - gs[i * 128 + ch];
+                                const float x1 = gs[r * 128 + ch + 1] - gs[i * 128 + ch + 1];
+                                overflow |= x0 > kFactorRange * kLog2e || x1 > kFactorRange * kLog2e;
+                                const float e0 = ex2f(x0), e1 = ex2f(x1);
+                                sa = fmaf(a.x * cc.x, e0, sa);
+                                sa = fmaf(a.y * cc.y, e1, sa);
+                                sp = fmaf(bq.x * cc.x, e0, sp);
+                                sp = fmaf(bq.y * cc.y, e1, sp);
+                            }
+                        }
+                        const bool real = r < L && i < L;
+                        const float rki = rn[64 + i];
+                        at[r * kATStride + i] = (i < r && real) ? betas[r] * rn[64 + r] * rki * sa : 0.f;
+                        pf[r * 64 + i] = real ? p.scale * rn[r] * rki * sp : 0.f;
+                    }
+                }
+                if (overflow) atomicOr(p.err, kErrGate);
+                named_sync(1, 256);
+                // zeros above the diagonal of A; P to the record
+                for (int x = ct; x < 64 * 64; x += 256) {
+                    const int r = x >> 6, i = x & 63;
+                    if (i >= r) at[r * kATStride + i] = 0.f;
+                }
+                for (int gidx = ct; gidx < 64 * 8; gidx += 256) {
+                    const int r = gidx >> 3, g8 = gidx & 7;
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i0 = 8 * g8 + 2 * e;
+                        w4[e] = pack_bf16(i0 <= r ? pf[r * 64 + i0] : 0.f,
+                                          i0 + 1 <= r ? pf[r * 64 + i0 + 1] : 0.f);
+                    }
+                    st_global_v4(rec + kRecB3 + kmaj(r, 8 * g8, 64),
+                                 make_uint4(w4[0], w4[1], w4[2], w4[3]));
+                }
+            }
+            if (named_sync_or(1, 256, *abort_flag != 0)) break;
+
+            // ---- T = (I + A)^{-1} (warps 0-3), then T in bf16 for the MMAs
+            if (warp < 4) {
+                // scratch for the off-diagonal blocks: the Gram operand tile is free now
+                float *scratch = reinterpret_cast<float *>(smem + kIOffGA);
+                invert64(at, scratch, warp, lane);
+            }
+            named_sync(1, 256);
+            for (int gidx = ct; gidx < 64 * 8; gidx += 256) {
+                const int r = gidx >> 3, g8 = gidx & 7;
+                const int I = r >> 4;
+                uint32_t w4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float v2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int i = 8 * g8 + 2 * e + u, J = i >> 4;
+                        v2[u] = J > I ? 0.f : (J == I ? at[r * kATStride + i] : at[i * kATStride + r]);
+                    }
+                    w4[e] = pack_bf16(v2[0], v2[1]);
+                }
+                *reinterpret_cast<uint4 *>(smem + kIOffTA + kmaj(r, 8 * g8, 64)) =
+                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            fence_async_smem();
+            tc::fence_before();
+            named_sync(1, 256);
+            if (lane == 0) mbar_arrive(bar(kIBInv));
+
+            // ---- Ut^T and -W to the record
+            wait_bar(bar(kIBWU), it & 1, abort_flag, p.err);
+            tc::fence_after();
+            {
+                const int q4 = warp & 3, half = warp >> 2;
+                const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+                // Ut^T row v = 32 q4 + lane, tokens [32 half, 32 half + 32)
+                uint32_t d[32];
+                tld32(tmem + lane_base + 192 + 32 * half, d);
+                tc::ld_wait();
+                const int v = 32 * q4 + lane;
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    const int j = 4 * half + j4;
+                    st_global_v4(rec + kRecUt + ut_off(v, j),
+                                 make_uint4(pack_bf16(__uint_as_float(d[8 * j4]), __uint_as_float(d[8 * j4 + 1])),
+                                            pack_bf16(__uint_as_float(d[8 * j4 + 2]), __uint_as_float(d[8 * j4 + 3])),
+                                            pack_bf16(__uint_as_float(d[8 * j4 + 4]), __uint_as_float(d[8 * j4 + 5])),
+                                            pack_bf16(__uint_as_float(d[8 * j4 + 6]), __uint_as_float(d[8 * j4 + 7]))));
+                }
+                // W (M = 64): row r = 16 q4 + lane in lanes 32 q4 + (0..15)
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t w[32];
+                    tld32(tmem + lane_base + 64 + 64 * half + 32 * c2, w);
+                    tc::ld_wait();
+                    if (lane < 16) {
+                        const int r = 16 * q4 + lane;
+#pragma unroll
+                        for (int k8 = 0; k8 < 4; ++k8) {
+                            const int key = 64 * half + 32 * c2 + 8 * k8;
+                            st_global_v4(rec + kRecB1 + kmaj(r, key, 128),
+                                         make_uint4(pack_bf16(-__uint_as_float(w[8 * k8]), -__uint_as_float(w[8 * k8 + 1])),
+                                                    pack_bf16(-__uint_as_float(w[8 * k8 + 2]), -__uint_as_float(w[8 * k8 + 3])),
+                                                    pack_bf16(-__uint_as_float(w[8 * k8 + 4]), -__uint_as_float(w[8 * k8 + 5])),
+                                                    pack_bf16(-__uint_as_float(w[8 * k8 + 6]), -__uint_as_float(w[8 * k8 + 7]))));
+                        }
+                    }
+                }
+            }
+            tc::fence_before();
+            const bool stop = named_sync_or(1, 256, *abort_flag != 0);
+            if (p.ring_depth > 0 && ct == 0 && !stop) {
+                __threadfence();
+                st_release(p.ready + (c % p.ring_depth) * H + h, c + 1);
+            }
+            ++it;
+            if (stop) break;
+        }
+    }
+
+    // ---- teardown: every warp, then TMEM is freed by warp 8
+    tc::fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kIBTear));
+    if (warp == 8) {
+        wait_bar(bar(kIBTear), 0, abort_flag, p.err);
+        tc::fence_after();
+        tc::dealloc(tmem, kITmemCols);
+    }
+}
+
+// ============================================================================
+// Recurrent role: one (sequence, head) chain at a time.
+// warps 0-7 epilogues (lane quadrant warp % 4, column half warp / 4),
+// warp 8 record copies, warp 9 MMA issue and TMEM.
+// ============================================================================
+__device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, int n_step) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.n_heads;
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t bar0 = sb + kCOffBar;
+    auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kCOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kCOffMisc + 4);
+    if (tid == 0) {
+        for (int s = 0; s < kCStages; ++s) {
+            mbar_init(bar(kCBFull + s), 1);
+            mbar_init(bar(kCBEmpty + s), 9);
+        }
+        mbar_init(bar(kCBSop), 8);
+        mbar_init(bar(kCBUdone), 1);
+        mbar_init(bar(kCBUop), 8);
+        mbar_init(bar(kCBSdone), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(kCBOdone + b), 1);
+            mbar_init(bar(kCBOfree + b), 8);
+        }
+        mbar_init(bar(kCBTear), kThreads / 32);
+        mbar_init(bar(kCBDrain), 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 9) {
+        tc::alloc(smem_u32(tmem_slot), kCTmemCols);
+        tc::relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const bool skip = p.cu != nullptr && (*p.call_flags & kErrBadCu);
+
+    // chunks of sequence n: first global chunk index and count
+    auto seq_chunks = [&](int n, int64_t &c0, int &nck, int64_t &tb, int64_t &te) {
+        if (p.cu == nullptr) {
+            c0 = static_cast<int64_t>(n) * p.cps;
+            nck = p.cps;
+            tb = static_cast<int64_t>(n) * p.seq_len;
+            te = tb + p.seq_len;
+        } else {
+            c0 = p.chunk_off[n];
+            nck = p.chunk_off[n + 1] - p.chunk_off[n];
+            tb = p.cu[n];
+            te = p.cu[n + 1];
+        }
+    };
+
+    if (skip) {
+        // nothing
+    } else if (warp < 8) {
+        // ===================================================== epilogues
+        // A failed (bounded) wait raises the abort flag and the warp goes on;
+        // the eight warps leave together at the next OR-reducing barrier.
+        const int q4 = warp & 3, half = warp >> 2;
+        const int v = 32 * q4 + lane;                      // value channel, TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+        const uint32_t tS = tmem + lane_base;              // S^T, columns = keys
+        __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(p.out);
+        uint8_t *ost = smem + kCOffO;
+        int64_t gi = 0;                                    // global step counter
+        bool stop = false;
+        // o of a finished step: D1 columns 64.. of buffer b -> staging -> global
+        auto out_epi = [&](int64_t gstep, int64_t t0, int L) {
+            const int b = static_cast<int>(gstep & 1);
+            wait_bar(bar(kCBOdone + b), (gstep >> 1) & 1, abort_flag, p.err);
+            tc::fence_after();
+            uint32_t d[32];
+            tld32(tS + 128 + 128 * b + 64 + 32 * half, d);
+            tc::ld_wait();
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kCBOfree + b));
+            named_sync(3, 256);   // the staging tile is free again
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                *reinterpret_cast<__nv_bfloat16 *>(ost + (32 * half + j) * 256 + v * 2) =
+                    __float2bfloat16_rn(__uint_as_float(d[j]));
+            named_sync(3, 256);
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const int gidx = tid + 256 * x, r = gidx >> 4, c16 = gidx & 15;
+                if (r < L)
+                    st_global_v4(outp + ((t0 + r) * H + h) * 128 + c16 * 8,
+                                 *reinterpret_cast<const uint4 *>(ost + r * 256 + c16 * 16));
+            }
+        };
+        for (int n = n_first; n < p.n_seqs && !stop; n += n_step) {
+            int64_t c0, tb, te;
+            int nck;
+            seq_chunks(n, c0, nck, tb, te);
+            const int64_t sbase = (static_cast<int64_t>(n) * H + h) * 128 * 128;
+            // initial state into S^T: column keys [64 half, 64 half + 64), lane v
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t r[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int key = 64 * half + 32 * c2 + j;
+                    r[j] = __float_as_uint(p.s0 ? p.s0[sbase + key * 128 + v] : 0.f);
+                }
+                tst32(tS + 64 * half + 32 * c2, r);
+            }
+            tc::st_wait();
+            int64_t prev_t0 = 0;
+            int prev_L = 0;
+            for (int i = 0; i < nck; ++i, ++gi) {
+                const int s = static_cast<int>(gi % kCStages);
+                const int b = static_cast<int>(gi & 1);
+                const uint8_t *stg = smem + s * kRecBytes;
+                wait_bar(bar(kCBFull + s), (gi / kCStages) & 1, abort_flag, p.err);
+                if (i > 0) wait_bar(bar(kCBSdone), (gi - 1) & 1, abort_flag, p.err);
+                tc::fence_after();
+                // ---- state: S^T (keys of this half) -> bf16 operand; decay in place
+                const float *gam = reinterpret_cast<const float *>(stg + kRecGam);
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t r[32];
+                    tld32(tS + 64 * half + 32 * c2, r);
+                    tc::ld_wait();
+#pragma unroll
+                    for (int k8 = 0; k8 < 4; ++k8) {
+                        const int key = 64 * half + 32 * c2 + 8 * k8;
+                        *reinterpret_cast<uint4 *>(smem + kCOffAS + kmaj(v, key, 128)) =
+                            make_uint4(pack_bf16(__uint_as_float(r[8 * k8]), __uint_as_float(r[8 * k8 + 1])),
+                                       pack_bf16(__uint_as_float(r[8 * k8 + 2]), __uint_as_float(r[8 * k8 + 3])),
+                                       pack_bf16(__uint_as_float(r[8 * k8 + 4]), __uint_as_float(r[8 * k8 + 5])),
+                                       pack_bf16(__uint_as_float(r[8 * k8 + 6]), __uint_as_float(r[8 * k8 + 7])));
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 gg = *reinterpret_cast<const float4 *>(gam + 64 * half + 32 * c2 + j);
+                        r[j] = __float_as_uint(__uint_as_float(r[j]) * gg.x);
+                        r[j + 1] = __float_as_uint(__uint_as_float(r[j + 1]) * gg.y);
+                        r[j + 2] = __float_as_uint(__uint_as_float(r[j + 2]) * gg.z);
+                        r[j + 3] = __float_as_uint(__uint_as_float(r[j + 3]) * gg.w);
+                    }
+                    tst32(tS + 64 * half + 32 * c2, r);
+                }
+                tc::st_wait();
+                fence_async_smem();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kCBSop));
+                // ---- U^T = Ut^T + D1[:, 0:64] (tokens of this half) -> bf16 operand
+                wait_bar(bar(kCBUdone), gi & 1, abort_flag, p.err);
+                tc::fence_after();
+                {
+                    uint32_t d[32];
+                    tld32(tS + 128 + 128 * b + 32 * half, d);
+                    tc::ld_wait();
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const int j = 4 * half + j4;
+                        const uint4 u = *reinterpret_cast<const uint4 *>(stg + kRecUt + ut_off(v, j));
+                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+                        uint32_t o4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 f = unpack_bf16(uw[e]);
+                            o4[e] = pack_bf16(f.x + __uint_as_float(d[8 * j4 + 2 * e]),
+                                              f.y + __uint_as_float(d[8 * j4 + 2 * e + 1]));
+                        }
+                        *reinterpret_cast<uint4 *>(smem + kCOffAU + kmaj(v, 8 * j, 64)) =
+                            make_uint4(o4[0], o4[1], o4[2], o4[3]);
+                    }
+                }
+                fence_async_smem();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(kCBUop));
+                    mbar_arrive(bar(kCBEmpty + s));
+                }
+                // ---- o of the previous step while this step's update runs
+                if (i > 0) out_epi(gi - 1, prev_t0, prev_L);
+                prev_t0 = tb + static_cast<int64_t>(kC) * i;
+                prev_L = static_cast<int>(te - prev_t0 < kC ? te - prev_t0 : kC);
+                if (named_sync_or(3, 256, *abort_flag != 0)) { stop = true; break; }
+            }
+            if (stop) break;
+            if (nck > 0) {
+                out_epi(gi - 1, prev_t0, prev_L);
+                wait_bar(bar(kCBSdone), (gi - 1) & 1, abort_flag, p.err);
+                tc::fence_after();
+            }
+            if (named_sync_or(3, 256, *abort_flag != 0)) break;
+            if (p.s_final != nullptr) {
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t r[32];
+                    tld32(tS + 64 * half + 32 * c2, r);
+                    tc::ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int key = 64 * half + 32 * c2 + j;
+                        p.s_final[sbase + key * 128 + v] = __uint_as_float(r[j]);
+                    }
+                }
+            }
+            tc::fence_before();
+        }
+    } else if (warp == 8) {
+        // ===================================================== record copies
+        if (lane == 0) {
+            int64_t gi = 0, issued = 0;
+            int64_t pend_c = -1, pend_gi = 0;   // ring form: copy whose completion is unpublished
+            bool ok = true;
+            for (int n = n_first; n < p.n_seqs && ok; n += n_step) {
+                int64_t c0, tb, te;
+                int nck;
+                seq_chunks(n, c0, nck, tb, te);
+                for (int i = 0; i < nck; ++i, ++gi) {
+                    const int s = static_cast<int>(gi % kCStages);
+                    const int64_t c = c0 + i;
+                    if (gi >= kCStages &&
+                        !wait_bar(bar(kCBEmpty + s), ((gi / kCStages) - 1) & 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    if (p.ring_depth > 0) {
+                        if (!wait_counter(p.ready + (c % p.ring_depth) * H + h, c + 1, abort_flag,
+                                          p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        asm volatile("fence.proxy.async.global;\n" ::: "memory");
+                    }
+                    const uint8_t *src = record_of(p, c, h);
+                    mbar_arrive_expect_tx(bar(kCBFull + s), kRecBytes);
+#pragma unroll
+                    for (int part = 0; part < 4; ++part)
+                        bulk_g2s(sb + s * kRecBytes + part * (kRecBytes / 4), src + part * (kRecBytes / 4),
+                                 kRecBytes / 4, bar(kCBFull + s));
+                    issued = gi + 1;
+                    if (p.ring_depth > 0) {
+                        if (pend_c >= 0) {
+                            const int ps = static_cast<int>(pend_gi % kCStages);
+                            if (!wait_bar(bar(kCBFull + ps), (pend_gi / kCStages) & 1, abort_flag, p.err)) {
+                                ok = false;
+                                break;
+                            }
+                            st_release(p.consumed + h, pend_c + 1);
+                        }
+                        pend_c = c;
+                        pend_gi = gi;
+                    }
+                }
+            }
+            if (ok && p.ring_depth > 0 && pend_c >= 0) {
+                const int ps = static_cast<int>(pend_gi % kCStages);
+                if (wait_bar(bar(kCBFull + ps), (pend_gi / kCStages) & 1, abort_flag, p.err))
+                    st_release(p.consumed + h, pend_c + 1);
+            }
+            // drain: no copy of this CTA is still in flight when it exits
+            for (int64_t g2 = issued - kCStages; g2 < issued; ++g2) {
+                if (g2 < 0) continue;
+                const int ps = static_cast<int>(g2 % kCStages);
+                mbar_wait(bar(kCBFull + ps), (g2 / kCStages) & 1);
+            }
+        }
+    } else {
+        // ===================================================== MMA issue
+        if (lane == 0) {
+            int64_t gi = 0;
+            bool ok = true;
+            const uint32_t aS = sb + kCOffAS, aU = sb + kCOffAU;
+            for (int n = n_first; n < p.n_seqs && ok; n += n_step) {
+                int64_t c0, tb, te;
+                int nck;
+                seq_chunks(n, c0, nck, tb, te);
+                for (int i = 0; i < nck; ++i, ++gi) {
+                    const int s = static_cast<int>(gi % kCStages);
+                    const int b = static_cast<int>(gi & 1);
+                    const uint32_t stg = sb + s * kRecBytes;
+                    const uint32_t d1 = tmem + 128 + 128 * b;
+                    if (!wait_bar(bar(kCBFull + s), (gi / kCStages) & 1, abort_flag, p.err) ||
+                        !wait_bar(bar(kCBSop), gi & 1, abort_flag, p.err) ||
+                        (gi >= 2 &&
+                         !wait_bar(bar(kCBOfree + b), ((gi >> 1) - 1) & 1, abort_flag, p.err))) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    // D1[:, 0:64] = S^T (-W)^T ;  D1[:, 64:128] = S^T (scale Qg)^T
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(d1, tc::sdesc(aS + kk * 256, 128, 2048),
+                               tc::sdesc(stg + kRecB1 + kk * 256, 128, 2048), kIdFull, kk > 0);
+                    tc::commit(bar(kCBUdone));
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(d1 + 64, tc::sdesc(aS + kk * 256, 128, 2048),
+                               tc::sdesc(stg + kRecB1 + 16384 + kk * 256, 128, 2048), kIdFull,
+                               kk > 0);
+                    if (!wait_bar(bar(kCBUop), gi & 1, abort_flag, p.err)) { ok = false; break; }
+                    tc::fence_after();
+                    // S^T += U^T Kd
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tmem, tc::sdesc(aU + kk * 256, 128, 1024),
+                               tc::sdesc(stg + kRecB2 + kk * 256, 128, 1024), kIdSq, 1);
+                    tc::commit(bar(kCBSdone));
+                    // D1[:, 64:128] += U^T (scale P)^T
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(d1 + 64, tc::sdesc(aU + kk * 256, 128, 1024),
+                               tc::sdesc(stg + kRecB3 + kk * 256, 128, 1024), kIdFull, 1);
+                    tc::commit(bar(kCBOdone + b));
+                    tc::commit(bar(kCBEmpty + s));
+                }
+            }
+            // every MMA this thread issued has completed before the teardown
+            tc::commit(bar(kCBDrain));
+            wait_bar(bar(kCBDrain), 0, abort_flag, p.err);
+        }
+    }
+
+    // ---- teardown
+    tc::fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(kCBTear));
+    if (warp == 9) {
+        wait_bar(bar(kCBTear), 0, abort_flag, p.err);
+        tc::fence_after();
+        tc::dealloc(tmem, kCTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ kernels
+template <bool PRE>
+__global__ void __launch_bounds__(kThreads, 1) kda_c64_intra_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    intra_role<PRE>(p, smem, blockIdx.x, gridDim.x);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) kda_c64_chain_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int H = p.n_heads;
+    chain_role(p, smem, blockIdx.x % H, blockIdx.x / H, p.n_seqs);
+}
+
+// One cooperative launch: CTAs [0, n_chain) run head blockIdx.x's chains over
+// all sequences, the others build the records into the ring. The last CTA to
+// finish clears the ring counters for the next call.
+template <bool PRE>
+__global__ void __launch_bounds__(kThreads, 1) kda_c64_fused_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (static_cast<int>(blockIdx.x) < p.n_chain)
+        chain_role(p, smem, blockIdx.x, 0, 1);
+    else
+        intra_role<PRE>(p, smem, blockIdx.x - p.n_chain, gridDim.x - p.n_chain);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(p.exit_ctr, 1) == static_cast<int>(gridDim.x) - 1) {
+            const int nr = p.ring_depth * p.n_heads;
+            for (int i = 0; i < nr; ++i) p.ready[i] = 0;
+            for (int i = 0; i < p.n_heads; ++i) p.consumed[i] = 0;
+            *p.exit_ctr = 0;
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+}  // namespace c64
+}  // namespace kda
+
+// ============================================================================
+// Host side
+// ============================================================================
+namespace kda {
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<EncodeTiledFn>(nullptr);
+        }
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// [tokens, H, 128] row-major as a 3D tiled map (channel, head, token); a box
+// is 64 tokens x 1 head x 128 channels, rows past the end read as zero.
+bool encode_rows(CUtensorMap *m, const void *base, bool f32, int64_t H, int64_t tokens) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t es = f32 ? 4 : 2;
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(tokens)};
+    const cuuint64_t strides[2] = {128 * es, static_cast<cuuint64_t>(H) * 128 * es};
+    const cuuint32_t box[3] = {128, 1, static_cast<cuuint32_t>(c64::kC)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_params(const C64Args &a, c64::Params *p) {
+    *p = c64::Params{};
+    if (!encode_rows(&p->tm_q, a.q, false, a.n_heads, a.tokens) ||
+        !encode_rows(&p->tm_k, a.k, false, a.n_heads, a.tokens) ||
+        !encode_rows(&p->tm_v, a.v, false, a.n_heads, a.tokens) ||
+        !encode_rows(&p->tm_g, a.g, true, a.n_heads, a.tokens))
+        return false;
+    p->beta = a.beta;
+    p->s0 = a.s0;
+    p->out = a.out;
+    p->s_final = a.s_final;
+    p->rec = a.rec;
+    p->err = a.err;
+    p->cu = a.cu;
+    p->chunk_off = a.chunk_off;
+    p->call_flags = a.call_flags;
+    p->seq_len = a.seq_len;
+    p->max_chunks = a.max_chunks;
+    p->n_seqs = a.n_seqs;
+    p->n_heads = a.n_heads;
+    p->cps = a.cps;
+    p->scale = a.scale;
+    p->pre = a.pre;
+    p->ring_depth = a.ring_depth;
+    p->n_chain = a.n_chain;
+    p->ready = a.ready;
+    p->consumed = a.consumed;
+    p->exit_ctr = a.exit_ctr;
+    return true;
+}
+
+}  // namespace
+
+cudaError_t configure_c64() {
+    const void *fns[] = {reinterpret_cast<const void *>(c64::kda_c64_intra_kernel<false>),
+                         reinterpret_cast<const void *>(c64::kda_c64_intra_kernel<true>),
+                         reinterpret_cast<const void *>(c64::kda_c64_chain_kernel),
+                         reinterpret_cast<const void *>(c64::kda_c64_fused_kernel<false>),
+                         reinterpret_cast<const void *>(c64::kda_c64_fused_kernel<true>)};
+    for (const void *f : fns) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, c64::kSmem);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+cudaError_t launch_c64_intra(const C64Args &a, int intra_ctas, cudaStream_t stream) {
+    if (a.tokens <= 0) return cudaSuccess;
+    c64::Params p;
+    if (!make_params(a, &p)) return cudaErrorInvalidValue;
+    p.ring_depth = 0;
+    p.n_chain = 0;
+    const int64_t items = a.max_chunks * a.n_heads;
+    int64_t grid = intra_ctas < items ? intra_ctas : items;
+    if (grid < 1) grid = 1;
+    if (a.pre != 0)
+        c64::kda_c64_intra_kernel<true><<<static_cast<unsigned>(grid), c64::kThreads, c64::kSmem,
+                                          stream>>>(p);
+    else
+        c64::kda_c64_intra_kernel<false><<<static_cast<unsigned>(grid), c64::kThreads, c64::kSmem,
+                                           stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_c64_chain(const C64Args &a, cudaStream_t stream) {
+    const int64_t units = static_cast<int64_t>(a.n_seqs) * a.n_heads;
+    if (units <= 0) return cudaSuccess;
+    c64::Params p;
+    if (a.tokens > 0) {
+        if (!make_params(a, &p)) return cudaErrorInvalidValue;
+    } else {
+        // no tokens: the chains only carry the initial states to the final ones
+        p = c64::Params{};
+        p.s0 = a.s0;
+        p.s_final = a.s_final;
+        p.err = a.err;
+        p.cu = a.cu;
+        p.chunk_off = a.chunk_off;
+        p.call_flags = a.call_flags;
+        p.n_seqs = a.n_seqs;
+        p.n_heads = a.n_heads;
+    }
+    p.ring_depth = 0;
+    p.n_chain = 0;
+    c64::kda_c64_chain_kernel<<<static_cast<unsigned>(units), c64::kThreads, c64::kSmem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_c64_fused(const C64Args &a, int grid, cudaStream_t stream) {
+    if (a.tokens <= 0) return cudaSuccess;
+    c64::Params p;
+    if (!make_params(a, &p)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(c64::kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(c64::kSmem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return a.pre != 0 ? cudaLaunchKernelEx(&cfg, c64::kda_c64_fused_kernel<true>, p)
+                      : cudaLaunchKernelEx(&cfg, c64::kda_c64_fused_kernel<false>, p);
+}
+
+}  // namespace kda

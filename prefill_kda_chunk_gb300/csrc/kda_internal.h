@@ -102,9 +102,10 @@ cudaError_t configure_recurrent();
 cudaError_t configure_recurrent_tc();
 cudaError_t configure_recurrent_hybrid();
 
+// chunk_off[n] = first chunk of sequence n for chunks of 2^chunk_shift tokens
 cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t total_tokens,
                                    int32_t *chunk_off, int *call_flags, int *err,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream, int chunk_shift = 4);
 cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStream_t stream);
 // the exact form over the chunk-heads the intra-chunk kernel listed; launch
 // after every launch_intra_chunk, on the same stream
@@ -121,6 +122,40 @@ cudaError_t launch_decode(const DecodeParams &p, int64_t units, cudaStream_t str
 // workspace (BackParams::ring holds min(units, kBackwardMaxRings) rings).
 constexpr int64_t kBackwardMaxRings = 1024;
 cudaError_t launch_backward(const BackParams &p, int64_t units, cudaStream_t stream);
+
+// The 64-token chunk path on the 5th-generation tensor core (kda_c64.cu).
+struct C64Args {
+    const void *q, *k, *v;      // bf16 [tokens, H, 128]
+    const float *g, *beta;      // [tokens, H, 128], [tokens, H]
+    const float *s0;            // [N, H, 128, 128] or nullptr
+    void *out;                  // bf16 [tokens, H, 128]
+    float *s_final;             // [N, H, 128, 128] or nullptr
+    const int32_t *cu;          // packed: cu_seqlens [N+1]; fixed: nullptr
+    const int32_t *chunk_off;   // packed: first 64-token chunk of each sequence [N+1]
+    const int *call_flags;      // packed: per-call flags of the prologue
+    int *err;                   // sticky per-device error word
+    int64_t tokens;             // rows of q
+    int64_t seq_len;            // fixed: tokens per sequence; packed: total tokens
+    int64_t max_chunks;         // 64-token chunks (upper bound when packed)
+    int32_t n_seqs, n_heads, cps;   // cps: chunks per sequence (fixed)
+    float scale;
+    int pre;                    // kPreNormQK | kPreGateLogits
+    uint8_t *rec;               // records: max_chunks * H (split) or ring_depth * H (fused)
+    int ring_depth;             // fused: ring slots per head
+    int n_chain;                // fused: chain CTAs (one per head)
+    long long *ready;           // fused: [ring_depth * H], zero between calls
+    long long *consumed;        // fused: [H], zero between calls
+    int *exit_ctr;              // fused: zero between calls
+};
+constexpr int64_t kC64RecBytes = 74240;   // bytes of one (64-token chunk, head) record
+cudaError_t configure_c64();
+// the intra-chunk kernel over every chunk-head (persistent, intra_ctas CTAs)
+cudaError_t launch_c64_intra(const C64Args &a, int intra_ctas, cudaStream_t stream);
+// one recurrent CTA per (sequence, head), records from the intra-chunk kernel
+cudaError_t launch_c64_chain(const C64Args &a, cudaStream_t stream);
+// one cooperative kernel of `grid` CTAs: a.n_chain = H chain CTAs (each over
+// all sequences of its head) and grid - H record builders feeding the ring
+cudaError_t launch_c64_fused(const C64Args &a, int grid, cudaStream_t stream);
 
 // Host-side checks shared by the entry points (kda_api.cu): 0 when `p` is
 // NULL, device memory of device `dev` or managed memory; otherwise the

@@ -667,10 +667,11 @@ kda_intra_exact_kernel(IntraParams p) {
 }
 
 // Validates cu_seqlens and writes each sequence's first chunk index
-// (exclusive prefix sum of ceil(len/16)). One CTA of 1024 threads.
+// (exclusive prefix sum of ceil(len / 2^shift): 16- or 64-token chunks). One
+// CTA of 1024 threads.
 __global__ void __launch_bounds__(1024)
 kda_varlen_prologue_kernel(const int32_t *cu, int32_t n_seqs, int64_t total, int32_t *chunk_off,
-                           int *call_flags, int *err) {
+                           int *call_flags, int *err, int shift) {
     __shared__ int warp_sums[32];
     __shared__ int s_bad;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -684,7 +685,7 @@ kda_varlen_prologue_kernel(const int32_t *cu, int32_t n_seqs, int64_t total, int
             const int64_t a = cu[i], b = cu[i + 1];
             bool bad = (b < a) || (i == 0 && a != 0) || (i == n_seqs - 1 && b != total);
             if (bad) s_bad = 1;
-            else cnt = static_cast<int>((b - a + 15) / 16);
+            else cnt = static_cast<int>((b - a + (int64_t(1) << shift) - 1) >> shift);
         }
         int x = cnt;
 #pragma unroll
@@ -719,9 +720,9 @@ kda_varlen_prologue_kernel(const int32_t *cu, int32_t n_seqs, int64_t total, int
 
 cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t total_tokens,
                                    int32_t *chunk_off, int *call_flags, int *err,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, int chunk_shift) {
     kda_varlen_prologue_kernel<<<1, 1024, 0, stream>>>(cu, n_seqs, total_tokens, chunk_off,
-                                                       call_flags, err);
+                                                       call_flags, err, chunk_shift);
     return cudaGetLastError();
 }
 
