@@ -21,9 +21,10 @@ namespace {
 struct StreamWorkspace {
     void *ptr = nullptr;
     size_t bytes = 0;
-    // the 64-token ring counters (fused launches) hold zeros; any other use of
-    // the buffer may overwrite them
-    bool ring_clean = false;
+    // bytes at offset 256 known to hold zeros for the 64-token ring counters
+    // (a fused launch leaves its counters zero; any other use of the buffer
+    // may overwrite them)
+    int64_t ring_clean = 0;
     cudaStream_t s_intra = nullptr, s_recur = nullptr;
     std::vector<cudaEvent_t> ev;
 };
@@ -198,8 +199,9 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, i
         if (pl->impl == kImplC64Split) {
             pl->ws_bytes = 256 + pl->off_bytes + pl->c64_chunks * H * kda::kC64RecBytes;
         } else {
-            pl->c64_sync = 256 + pl->off_bytes + kC64Ring * H * kda::kC64RecBytes;
-            pl->ws_bytes = pl->c64_sync + align256((kC64Ring * H + H) * 8 + 64);
+            // the ring counters sit right after the flag block, whatever H is
+            pl->c64_sync = align256((kC64Ring * H + H) * 8 + 64);
+            pl->ws_bytes = 256 + pl->c64_sync + pl->off_bytes + kC64Ring * H * kda::kC64RecBytes;
         }
     }
     return KDA_OK;
@@ -419,7 +421,7 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
             return KDA_ERR_CUDA;
         }
         ws.bytes = pl.ws_bytes;
-        ws.ring_clean = false;
+        ws.ring_clean = 0;
         // the flag block starts zeroed (the exact-form list counters above all)
         if (cudaMemsetAsync(ws.ptr, 0, 256, stream) != cudaSuccess) return KDA_ERR_CUDA;
     }
@@ -443,10 +445,12 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
     if (pl.impl >= kImplC64Split) {
         // ---- 64-token chunks on tcgen05
         const bool fused = pl.impl == kImplC64Fused;
-        if (!fused) ws.ring_clean = false;
+        if (!fused) ws.ring_clean = 0;
+        // fused: [flags | ring counters | chunk offsets | ring]; split: [flags | offsets | records]
+        const int64_t off_at = 256 + (fused ? pl.c64_sync : 0);
         if (cu_seqlens != nullptr &&
             kda::launch_varlen_prologue(cu_seqlens, static_cast<int32_t>(N), pl.tokens,
-                                        reinterpret_cast<int32_t *>(wsb + 256),
+                                        reinterpret_cast<int32_t *>(wsb + off_at),
                                         reinterpret_cast<int *>(wsb), st.err, stream,
                                         6) != cudaSuccess)
             return KDA_ERR_CUDA;
@@ -454,7 +458,7 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
         a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.s0 = initial_state;
         a.out = out; a.s_final = final_state;
         a.cu = cu_seqlens;
-        a.chunk_off = cu_seqlens ? reinterpret_cast<const int32_t *>(wsb + 256) : nullptr;
+        a.chunk_off = cu_seqlens ? reinterpret_cast<const int32_t *>(wsb + off_at) : nullptr;
         a.call_flags = reinterpret_cast<const int *>(wsb);
         a.err = st.err;
         a.tokens = pl.tokens;
@@ -465,7 +469,7 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
         a.cps = static_cast<int32_t>((T + 63) / 64);
         a.scale = scale;
         a.pre = flags;
-        a.rec = wsb + 256 + pl.off_bytes;
+        a.rec = wsb + off_at + pl.off_bytes;
         if (!fused) {
             rc = timed_launch(true, stream, [&] { return kda::launch_c64_intra(a, sm_count, stream); });
             if (rc != KDA_OK) return rc;
@@ -473,11 +477,10 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
         }
         if (pl.tokens == 0)   // nothing for the builders: the chains alone carry the states
             return timed_launch(false, stream, [&] { return kda::launch_c64_chain(a, stream); });
-        long long *sync = reinterpret_cast<long long *>(wsb + pl.c64_sync);
-        if (!ws.ring_clean) {
-            if (cudaMemsetAsync(sync, 0, (kC64Ring * H + H) * 8 + 64, stream) != cudaSuccess)
-                return KDA_ERR_CUDA;
-            ws.ring_clean = true;   // each fused launch leaves them zero again
+        long long *sync = reinterpret_cast<long long *>(wsb + 256);
+        if (ws.ring_clean < pl.c64_sync) {
+            if (cudaMemsetAsync(sync, 0, pl.c64_sync, stream) != cudaSuccess) return KDA_ERR_CUDA;
+            ws.ring_clean = pl.c64_sync;   // each fused launch leaves its counters zero again
         }
         a.ring_depth = static_cast<int>(kC64Ring);
         a.n_chain = static_cast<int>(H);
@@ -486,7 +489,7 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
         a.exit_ctr = reinterpret_cast<int *>(sync + kC64Ring * H + H);
         return timed_launch(false, stream, [&] { return kda::launch_c64_fused(a, sm_count, stream); });
     }
-    ws.ring_clean = false;
+    ws.ring_clean = 0;
 
     kda::ChunkGeometry geo{};
     geo.cu = cu_seqlens;
@@ -699,6 +702,7 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
         if (cudaMemsetAsync(ws.ptr, 0, 256, stream) != cudaSuccess) return KDA_ERR_CUDA;
     }
     uint8_t *wsb = static_cast<uint8_t *>(ws.ptr);
+    ws.ring_clean = 0;   // this call overwrites the area of the 64-token ring counters
 
     kda::ChunkGeometry geo{};
     geo.cu = cu_seqlens;

@@ -46,15 +46,12 @@ constexpr float kFactorRange = 80.f;
 
 // ------------------------------------------------------------------ shared memory
 // recurrent role
-constexpr int kCStages = 2;
-constexpr int kCOffAS = kCStages * kRecBytes;     // S^T bf16 operand, 128 x 128 keys
-constexpr int kCOffAU = kCOffAS + 32768;          // U^T bf16 operand, 128 x 64 tokens
-constexpr int kCOffO = kCOffAU + 16384;           // o staging [64 tok][128 v] bf16
-constexpr int kCOffMisc = kCOffO + 16384;         // tmem base, abort flag
+constexpr int kCStages = 3;
+constexpr int kCOffMisc = kCStages * kRecBytes;   // tmem base, abort flag
 constexpr int kCOffBar = kCOffMisc + 64;
 enum {
-    kCBFull = 0, kCBEmpty = 2, kCBSop = 4, kCBUdone = 5, kCBUop = 6, kCBSdone = 7,
-    kCBOdone = 8, kCBOfree = 10, kCBTear = 12, kCBDrain = 13, kCNumBars = 14
+    kCBFull = 0, kCBEmpty = 3, kCBSop = 6, kCBUdone = 8, kCBUop = 9, kCBSdone = 10,
+    kCBOdone = 11, kCBOfree = 12, kCBTear = 13, kCBDrain = 14, kCNumBars = 15
 };
 constexpr int kCSmem = kCOffBar + kCNumBars * 8;
 // intra-chunk role
@@ -78,7 +75,8 @@ constexpr int kSmem = kCSmem > kISmem ? kCSmem : kISmem;
 static_assert(kSmem <= 227 * 1024, "shared memory");
 
 // tensor memory columns
-constexpr uint32_t kCTmemCols = 512;   // S^T [0,128), D1 x2 [128,384)
+constexpr uint32_t kCTmemCols = 512;   // S^T [0,128), O^T [128,192), U^T [192,256),
+                                       // bf16 S^T x2 [256,384), bf16 U^T [384,416)
 constexpr uint32_t kITmemCols = 256;   // Gram [0,64), W [64,192), Ut^T [192,256)
 
 constexpr uint32_t kIdFull = tc::idesc(128, 64, 1);    // M=128, N=64
@@ -428,7 +426,7 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
         mbar_init(bar(kIBGram), 1);
         mbar_init(bar(kIBInv), 8);
         mbar_init(bar(kIBWU), 1);
-        mbar_init(bar(kIBTear), kThreads / 32);
+        mbar_init(bar(kIBTear), blockDim.x / 32);
         mbar_init(bar(kIBDrain), 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -650,7 +648,7 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
                     }
                     const uint4 uq = pack8(qg);
                     *reinterpret_cast<uint4 *>(smem + kIOffGA + kmaj(64 + row0 + r, ch0, 128)) = uq;
-                    st_global_v4(rec + kRecB1 + kmaj(64 + row0 + r, ch0, 128), uq);
+                    st_global_v4(rec + kRecB1 + kmaj(row0 + r, ch0, 128), uq);
                     *reinterpret_cast<uint4 *>(smem + kIOffGA + kmaj(row0 + r, ch0, 128)) = pack8(kb[r]);
                 }
 #pragma unroll
@@ -909,7 +907,7 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
 #pragma unroll
                         for (int k8 = 0; k8 < 4; ++k8) {
                             const int key = 64 * half + 32 * c2 + 8 * k8;
-                            st_global_v4(rec + kRecB1 + kmaj(r, key, 128),
+                            st_global_v4(rec + kRecB1 + kmaj(64 + r, key, 128),
                                          make_uint4(pack_bf16(-__uint_as_float(w[8 * k8]), -__uint_as_float(w[8 * k8 + 1])),
                                                     pack_bf16(-__uint_as_float(w[8 * k8 + 2]), -__uint_as_float(w[8 * k8 + 3])),
                                                     pack_bf16(-__uint_as_float(w[8 * k8 + 4]), -__uint_as_float(w[8 * k8 + 5])),
@@ -941,10 +939,51 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
 }
 
 // ============================================================================
-// Recurrent role: one (sequence, head) chain at a time.
-// warps 0-7 epilogues (lane quadrant warp % 4, column half warp / 4),
-// warp 8 record copies, warp 9 MMA issue and TMEM.
+// Recurrent role: one (sequence, head) chain at a time, 448 threads.
+// warps 0-7 state and U epilogues (lane quadrant warp % 4, key / token half
+// warp / 4), warp 8 record copies, warp 9 MMA issue (one elected lane) and
+// TMEM, warps 10-13 the o epilogue.
+// Tensor memory: S^T [0,128), O^T [128,192), U^T [192,256) in fp32, and the
+// bf16 operands S^T (two buffers, [256,320) and [320,384)) and U^T
+// [384,416), two values per column. Per step, in issue order:
+//   MMA-U: U = S^T (-W)^T          (N = 64, K = 128 keys; the first half of
+//                                   the keys as soon as the state epilogue has them)
+//   MMA-B: [S | O] += U^T [Kd^T ; scale P]^T   (N = 192, K = 64 tokens: one
+//                                   group, since O sits between S and U)
+//   MMA-O: O += S^T (scale Qg)^T   (N = 64, after the state is ready again)
+// The o warps read O and set it back to zero before MMA-B of the next step.
 // ============================================================================
+constexpr int kChainThreads = 448;
+
+__device__ __forceinline__ void mma_ss_e(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                         uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void commit_e(uint32_t bar) {
+    asm volatile(
+        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+            bar)
+        : "memory");
+}
+
+constexpr uint32_t kIdA = tc::idesc(128, 64, 1);       // MMA-A halves: M=128, N=64
+constexpr uint32_t kIdB = tc::idesc(128, 192, 1);      // MMA-B: M=128, N=192
+constexpr uint32_t kTAs = 256, kTAu = 384;             // bf16 operand columns
+
+__device__ __forceinline__ void mma_ts_e(uint32_t d, uint32_t a, uint64_t b, uint32_t id,
+                                         uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+
 __device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, int n_step) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = p.n_heads;
@@ -959,14 +998,13 @@ __device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, i
             mbar_init(bar(kCBEmpty + s), 9);
         }
         mbar_init(bar(kCBSop), 8);
+        mbar_init(bar(kCBSop + 1), 8);
         mbar_init(bar(kCBUdone), 1);
         mbar_init(bar(kCBUop), 8);
         mbar_init(bar(kCBSdone), 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(kCBOdone + b), 1);
-            mbar_init(bar(kCBOfree + b), 8);
-        }
-        mbar_init(bar(kCBTear), kThreads / 32);
+        mbar_init(bar(kCBOdone), 1);
+        mbar_init(bar(kCBOfree), 4);
+        mbar_init(bar(kCBTear), kChainThreads / 32);
         mbar_init(bar(kCBDrain), 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -981,7 +1019,7 @@ __device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, i
     const uint32_t tmem = *tmem_slot;
     const bool skip = p.cu != nullptr && (*p.call_flags & kErrBadCu);
 
-    // chunks of sequence n: first global chunk index and count
+    // chunks of sequence n: first global chunk index and count, token range
     auto seq_chunks = [&](int n, int64_t &c0, int &nck, int64_t &tb, int64_t &te) {
         if (p.cu == nullptr) {
             c0 = static_cast<int64_t>(n) * p.cps;
@@ -999,48 +1037,20 @@ __device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, i
     if (skip) {
         // nothing
     } else if (warp < 8) {
-        // ===================================================== epilogues
+        // ===================================================== state and U epilogues
         // A failed (bounded) wait raises the abort flag and the warp goes on;
         // the eight warps leave together at the next OR-reducing barrier.
         const int q4 = warp & 3, half = warp >> 2;
         const int v = 32 * q4 + lane;                      // value channel, TMEM lane
-        const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-        const uint32_t tS = tmem + lane_base;              // S^T, columns = keys
-        __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(p.out);
-        uint8_t *ost = smem + kCOffO;
+        const uint32_t tS = tmem + (static_cast<uint32_t>(32 * q4) << 16);
         int64_t gi = 0;                                    // global step counter
         bool stop = false;
-        // o of a finished step: D1 columns 64.. of buffer b -> staging -> global
-        auto out_epi = [&](int64_t gstep, int64_t t0, int L) {
-            const int b = static_cast<int>(gstep & 1);
-            wait_bar(bar(kCBOdone + b), (gstep >> 1) & 1, abort_flag, p.err);
-            tc::fence_after();
-            uint32_t d[32];
-            tld32(tS + 128 + 128 * b + 64 + 32 * half, d);
-            tc::ld_wait();
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kCBOfree + b));
-            named_sync(3, 256);   // the staging tile is free again
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                *reinterpret_cast<__nv_bfloat16 *>(ost + (32 * half + j) * 256 + v * 2) =
-                    __float2bfloat16_rn(__uint_as_float(d[j]));
-            named_sync(3, 256);
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                const int gidx = tid + 256 * x, r = gidx >> 4, c16 = gidx & 15;
-                if (r < L)
-                    st_global_v4(outp + ((t0 + r) * H + h) * 128 + c16 * 8,
-                                 *reinterpret_cast<const uint4 *>(ost + r * 256 + c16 * 16));
-            }
-        };
         for (int n = n_first; n < p.n_seqs && !stop; n += n_step) {
             int64_t c0, tb, te;
             int nck;
             seq_chunks(n, c0, nck, tb, te);
             const int64_t sbase = (static_cast<int64_t>(n) * H + h) * 128 * 128;
-            // initial state into S^T: column keys [64 half, 64 half + 64), lane v
+            // initial state into S^T: keys [64 half, 64 half + 64), lane v
             for (int c2 = 0; c2 < 2; ++c2) {
                 uint32_t r[32];
 #pragma unroll
@@ -1051,102 +1061,150 @@ __device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, i
                 tst32(tS + 64 * half + 32 * c2, r);
             }
             tc::st_wait();
-            int64_t prev_t0 = 0;
-            int prev_L = 0;
             for (int i = 0; i < nck; ++i, ++gi) {
                 const int s = static_cast<int>(gi % kCStages);
-                const int b = static_cast<int>(gi & 1);
                 const uint8_t *stg = smem + s * kRecBytes;
                 wait_bar(bar(kCBFull + s), (gi / kCStages) & 1, abort_flag, p.err);
                 if (i > 0) wait_bar(bar(kCBSdone), (gi - 1) & 1, abort_flag, p.err);
                 tc::fence_after();
-                // ---- state: S^T (keys of this half) -> bf16 operand; decay in place
-                const float *gam = reinterpret_cast<const float *>(stg + kRecGam);
+                // ---- state: S^T (keys of this half) -> bf16 operand in TMEM (buffer
+                //      gi % 2); keys [64 half + 32 c2, +32) signal barrier sop + c2; the
+                //      decayed state goes back to TMEM after both signals
+                const float *gam = reinterpret_cast<const float *>(stg + kRecGam) + 64 * half;
+                const uint32_t tAs = tS + kTAs + 64 * static_cast<uint32_t>(gi & 1) + 32 * half;
+                uint32_t r0[32], r1[32];
+                tld32(tS + 64 * half, r0);
+                tld32(tS + 64 * half + 32, r1);
+                tc::ld_wait();
 #pragma unroll
                 for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t r[32];
-                    tld32(tS + 64 * half + 32 * c2, r);
-                    tc::ld_wait();
+                    const uint32_t (&r)[32] = c2 ? r1 : r0;
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int k8 = 0; k8 < 4; ++k8) {
-                        const int key = 64 * half + 32 * c2 + 8 * k8;
-                        *reinterpret_cast<uint4 *>(smem + kCOffAS + kmaj(v, key, 128)) =
-                            make_uint4(pack_bf16(__uint_as_float(r[8 * k8]), __uint_as_float(r[8 * k8 + 1])),
-                                       pack_bf16(__uint_as_float(r[8 * k8 + 2]), __uint_as_float(r[8 * k8 + 3])),
-                                       pack_bf16(__uint_as_float(r[8 * k8 + 4]), __uint_as_float(r[8 * k8 + 5])),
-                                       pack_bf16(__uint_as_float(r[8 * k8 + 6]), __uint_as_float(r[8 * k8 + 7])));
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        pk[j] = pack_bf16(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                    tc::st16(tAs + 16 * c2, pk);
+                    tc::st_wait();
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kCBSop + c2));
+                }
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t (&r)[32] = c2 ? r1 : r0;
 #pragma unroll
                     for (int j = 0; j < 32; j += 4) {
-                        const float4 gg = *reinterpret_cast<const float4 *>(gam + 64 * half + 32 * c2 + j);
-                        r[j] = __float_as_uint(__uint_as_float(r[j]) * gg.x);
-                        r[j + 1] = __float_as_uint(__uint_as_float(r[j + 1]) * gg.y);
-                        r[j + 2] = __float_as_uint(__uint_as_float(r[j + 2]) * gg.z);
-                        r[j + 3] = __float_as_uint(__uint_as_float(r[j + 3]) * gg.w);
+                        const float4 gg = *reinterpret_cast<const float4 *>(gam + 32 * c2 + j);
+                        float a0 = __uint_as_float(r[j]), a1 = __uint_as_float(r[j + 1]);
+                        float a2 = __uint_as_float(r[j + 2]), a3 = __uint_as_float(r[j + 3]);
+                        mul2(a0, a1, gg.x, gg.y);
+                        mul2(a2, a3, gg.z, gg.w);
+                        r[j] = __float_as_uint(a0);
+                        r[j + 1] = __float_as_uint(a1);
+                        r[j + 2] = __float_as_uint(a2);
+                        r[j + 3] = __float_as_uint(a3);
                     }
                     tst32(tS + 64 * half + 32 * c2, r);
                 }
-                tc::st_wait();
-                fence_async_smem();
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(kCBSop));
-                // ---- U^T = Ut^T + D1[:, 0:64] (tokens of this half) -> bf16 operand
+                // ---- U^T = Ut^T + (-W S)^T (tokens of this half) -> bf16 operand in TMEM
                 wait_bar(bar(kCBUdone), gi & 1, abort_flag, p.err);
                 tc::fence_after();
                 {
                     uint32_t d[32];
-                    tld32(tS + 128 + 128 * b + 32 * half, d);
+                    tld32(tS + 192 + 32 * half, d);
+                    uint4 u4[4];
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4)
+                        u4[j4] = *reinterpret_cast<const uint4 *>(stg + kRecUt + ut_off(v, 4 * half + j4));
                     tc::ld_wait();
+                    uint32_t pk[16];
 #pragma unroll
                     for (int j4 = 0; j4 < 4; ++j4) {
-                        const int j = 4 * half + j4;
-                        const uint4 u = *reinterpret_cast<const uint4 *>(stg + kRecUt + ut_off(v, j));
-                        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-                        uint32_t o4[4];
+                        const uint32_t uw[4] = {u4[j4].x, u4[j4].y, u4[j4].z, u4[j4].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             const float2 f = unpack_bf16(uw[e]);
-                            o4[e] = pack_bf16(f.x + __uint_as_float(d[8 * j4 + 2 * e]),
-                                              f.y + __uint_as_float(d[8 * j4 + 2 * e + 1]));
+                            pk[4 * j4 + e] = pack_bf16(f.x + __uint_as_float(d[8 * j4 + 2 * e]),
+                                                       f.y + __uint_as_float(d[8 * j4 + 2 * e + 1]));
                         }
-                        *reinterpret_cast<uint4 *>(smem + kCOffAU + kmaj(v, 8 * j, 64)) =
-                            make_uint4(o4[0], o4[1], o4[2], o4[3]);
                     }
+                    tc::st16(tS + kTAu + 16 * half, pk);
+                    tc::st_wait();
                 }
-                fence_async_smem();
                 tc::fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(bar(kCBUop));
                     mbar_arrive(bar(kCBEmpty + s));
                 }
-                // ---- o of the previous step while this step's update runs
-                if (i > 0) out_epi(gi - 1, prev_t0, prev_L);
-                prev_t0 = tb + static_cast<int64_t>(kC) * i;
-                prev_L = static_cast<int>(te - prev_t0 < kC ? te - prev_t0 : kC);
                 if (named_sync_or(3, 256, *abort_flag != 0)) { stop = true; break; }
             }
             if (stop) break;
             if (nck > 0) {
-                out_epi(gi - 1, prev_t0, prev_L);
                 wait_bar(bar(kCBSdone), (gi - 1) & 1, abort_flag, p.err);
                 tc::fence_after();
             }
             if (named_sync_or(3, 256, *abort_flag != 0)) break;
             if (p.s_final != nullptr) {
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t r[32];
-                    tld32(tS + 64 * half + 32 * c2, r);
-                    tc::ld_wait();
+                uint32_t r0[32], r1[32];
+                tld32(tS + 64 * half, r0);
+                tld32(tS + 64 * half + 32, r1);
+                tc::ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int key = 64 * half + 32 * c2 + j;
-                        p.s_final[sbase + key * 128 + v] = __uint_as_float(r[j]);
-                    }
+                for (int j = 0; j < 32; ++j) {
+                    p.s_final[sbase + (64 * half + j) * 128 + v] = __uint_as_float(r0[j]);
+                    p.s_final[sbase + (64 * half + 32 + j) * 128 + v] = __uint_as_float(r1[j]);
                 }
             }
             tc::fence_before();
+        }
+    } else if (warp >= 10) {
+        // ===================================================== o epilogue
+        // O accumulates U^T P^T (MMA-B) and S^T Qg^T (MMA-O) from zero: these
+        // warps clear it once at the start and again after each read
+        const int q4 = warp & 3;
+        const int v = 32 * q4 + lane;
+        const uint32_t tO = tmem + (static_cast<uint32_t>(32 * q4) << 16) + 128;
+        __nv_bfloat16 *outp = static_cast<__nv_bfloat16 *>(p.out);
+        uint32_t zero[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) zero[j] = 0u;
+        tst32(tO, zero);
+        tst32(tO + 32, zero);
+        tc::st_wait();
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kCBOfree));
+        int64_t gi = 0;
+        bool ok = true;
+        for (int n = n_first; n < p.n_seqs && ok; n += n_step) {
+            int64_t c0, tb, te;
+            int nck;
+            seq_chunks(n, c0, nck, tb, te);
+            for (int i = 0; i < nck; ++i, ++gi) {
+                if (!wait_bar(bar(kCBOdone), gi & 1, abort_flag, p.err)) { ok = false; break; }
+                tc::fence_after();
+                uint32_t d0[32], d1[32];
+                tld32(tO, d0);
+                tld32(tO + 32, d1);
+                tc::ld_wait();
+                tst32(tO, zero);
+                tst32(tO + 32, zero);
+                tc::st_wait();
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kCBOfree));
+                const int64_t t0 = tb + static_cast<int64_t>(kC) * i;
+                const int L = static_cast<int>(te - t0 < kC ? te - t0 : kC);
+                __nv_bfloat16 *op = outp + (t0 * H + h) * 128 + v;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < L) op[static_cast<int64_t>(j) * H * 128] = __float2bfloat16_rn(__uint_as_float(d0[j]));
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (32 + j < L)
+                        op[static_cast<int64_t>(32 + j) * H * 128] = __float2bfloat16_rn(__uint_as_float(d1[j]));
+            }
         }
     } else if (warp == 8) {
         // ===================================================== record copies
@@ -1208,60 +1266,60 @@ __device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, i
             }
         }
     } else {
-        // ===================================================== MMA issue
-        if (lane == 0) {
-            int64_t gi = 0;
-            bool ok = true;
-            const uint32_t aS = sb + kCOffAS, aU = sb + kCOffAU;
-            for (int n = n_first; n < p.n_seqs && ok; n += n_step) {
-                int64_t c0, tb, te;
-                int nck;
-                seq_chunks(n, c0, nck, tb, te);
-                for (int i = 0; i < nck; ++i, ++gi) {
-                    const int s = static_cast<int>(gi % kCStages);
-                    const int b = static_cast<int>(gi & 1);
-                    const uint32_t stg = sb + s * kRecBytes;
-                    const uint32_t d1 = tmem + 128 + 128 * b;
-                    if (!wait_bar(bar(kCBFull + s), (gi / kCStages) & 1, abort_flag, p.err) ||
-                        !wait_bar(bar(kCBSop), gi & 1, abort_flag, p.err) ||
-                        (gi >= 2 &&
-                         !wait_bar(bar(kCBOfree + b), ((gi >> 1) - 1) & 1, abort_flag, p.err))) {
-                        ok = false;
-                        break;
+        // ===================================================== MMA issue (warp 9, one elected lane)
+        int64_t gi = 0;
+        bool ok = true;
+        for (int n = n_first; n < p.n_seqs && ok; n += n_step) {
+            int64_t c0, tb, te;
+            int nck;
+            seq_chunks(n, c0, nck, tb, te);
+            for (int i = 0; i < nck; ++i, ++gi) {
+                const int s = static_cast<int>(gi % kCStages);
+                const uint32_t stg = sb + s * kRecBytes;
+                const uint32_t tAs = tmem + kTAs + 64 * static_cast<uint32_t>(gi & 1);
+                const uint64_t dQ = tc::sdesc(stg + kRecB1, 128, 2048);           // rows 0-63: Qg
+                const uint64_t dW = tc::sdesc(stg + kRecB1 + 16384, 128, 2048);   // rows 64-127: -W
+                const uint64_t dB2 = tc::sdesc(stg + kRecB2, 128, 1024);
+                if (!wait_bar(bar(kCBFull + s), (gi / kCStages) & 1, abort_flag, p.err)) { ok = false; break; }
+                // U = S^T (-W)^T, the key blocks (16 keys) of each state chunk once it is in
+                // (chunk c2 of the two key halves h: blocks 4 h + 2 c2 and 4 h + 2 c2 + 1)
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    if (!wait_bar(bar(kCBSop + c2), gi & 1, abort_flag, p.err)) { ok = false; break; }
+                    __syncwarp();
+                    tc::fence_after();
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int k16 = 4 * (x >> 1) + 2 * c2 + (x & 1);
+                        mma_ts_e(tmem + 192, tAs + 8 * k16, dW + 16 * k16, kIdA,
+                                 (c2 > 0 || x > 0) ? 1u : 0u);
                     }
-                    tc::fence_after();
-                    // D1[:, 0:64] = S^T (-W)^T ;  D1[:, 64:128] = S^T (scale Qg)^T
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(d1, tc::sdesc(aS + kk * 256, 128, 2048),
-                               tc::sdesc(stg + kRecB1 + kk * 256, 128, 2048), kIdFull, kk > 0);
-                    tc::commit(bar(kCBUdone));
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(d1 + 64, tc::sdesc(aS + kk * 256, 128, 2048),
-                               tc::sdesc(stg + kRecB1 + 16384 + kk * 256, 128, 2048), kIdFull,
-                               kk > 0);
-                    if (!wait_bar(bar(kCBUop), gi & 1, abort_flag, p.err)) { ok = false; break; }
-                    tc::fence_after();
-                    // S^T += U^T Kd
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(tmem, tc::sdesc(aU + kk * 256, 128, 1024),
-                               tc::sdesc(stg + kRecB2 + kk * 256, 128, 1024), kIdSq, 1);
-                    tc::commit(bar(kCBSdone));
-                    // D1[:, 64:128] += U^T (scale P)^T
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_ss(d1 + 64, tc::sdesc(aU + kk * 256, 128, 1024),
-                               tc::sdesc(stg + kRecB3 + kk * 256, 128, 1024), kIdFull, 1);
-                    tc::commit(bar(kCBOdone + b));
-                    tc::commit(bar(kCBEmpty + s));
                 }
+                if (!ok) break;
+                commit_e(bar(kCBUdone));
+                // [S | O] += U^T [Kd^T ; scale P]^T, once U^T is in and O was read and cleared
+                if (!wait_bar(bar(kCBUop), gi & 1, abort_flag, p.err) ||
+                    !wait_bar(bar(kCBOfree), gi & 1, abort_flag, p.err)) {
+                    ok = false;
+                    break;
+                }
+                __syncwarp();
+                tc::fence_after();
+#pragma unroll
+                for (int k16 = 0; k16 < 4; ++k16)
+                    mma_ts_e(tmem, tmem + kTAu + 8 * k16, dB2 + 16 * k16, kIdB, 1);
+                commit_e(bar(kCBSdone));
+                // O += S^T (scale Qg)^T
+#pragma unroll
+                for (int k16 = 0; k16 < 8; ++k16)
+                    mma_ts_e(tmem + 128, tAs + 8 * k16, dQ + 16 * k16, kIdA, 1);
+                commit_e(bar(kCBOdone));
+                commit_e(bar(kCBEmpty + s));
             }
-            // every MMA this thread issued has completed before the teardown
-            tc::commit(bar(kCBDrain));
-            wait_bar(bar(kCBDrain), 0, abort_flag, p.err);
         }
+        // every MMA this warp issued has completed before the teardown
+        commit_e(bar(kCBDrain));
+        wait_bar(bar(kCBDrain), 0, abort_flag, p.err);
     }
 
     // ---- teardown
@@ -1282,7 +1340,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_c64_intra_kernel(const __grid
     intra_role<PRE>(p, smem, blockIdx.x, gridDim.x);
 }
 
-__global__ void __launch_bounds__(kThreads, 1) kda_c64_chain_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kChainThreads, 1) kda_c64_chain_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int H = p.n_heads;
     chain_role(p, smem, blockIdx.x % H, blockIdx.x / H, p.n_seqs);
@@ -1292,7 +1350,7 @@ __global__ void __launch_bounds__(kThreads, 1) kda_c64_chain_kernel(const __grid
 // all sequences, the others build the records into the ring. The last CTA to
 // finish clears the ring counters for the next call.
 template <bool PRE>
-__global__ void __launch_bounds__(kThreads, 1) kda_c64_fused_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kChainThreads, 1) kda_c64_fused_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     if (static_cast<int>(blockIdx.x) < p.n_chain)
         chain_role(p, smem, blockIdx.x, 0, 1);
@@ -1443,7 +1501,7 @@ cudaError_t launch_c64_chain(const C64Args &a, cudaStream_t stream) {
     }
     p.ring_depth = 0;
     p.n_chain = 0;
-    c64::kda_c64_chain_kernel<<<static_cast<unsigned>(units), c64::kThreads, c64::kSmem, stream>>>(p);
+    c64::kda_c64_chain_kernel<<<static_cast<unsigned>(units), c64::kChainThreads, c64::kSmem, stream>>>(p);
     return cudaGetLastError();
 }
 
@@ -1453,7 +1511,7 @@ cudaError_t launch_c64_fused(const C64Args &a, int grid, cudaStream_t stream) {
     if (!make_params(a, &p)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(c64::kThreads);
+    cfg.blockDim = dim3(c64::kChainThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(c64::kSmem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -26,10 +26,11 @@ constexpr int kC = 64;   // tokens per chunk
 
 // Record of one (chunk, head). With S the K x V state entering the chunk:
 //   U = Ut - W S,  o = scale Qg S + scale P U,  S' = Diag(gamma) S + Kd^T U
-constexpr int kRecB1 = 0;        // [-W ; scale Q e^G]: 128 rows (64 of -W, then 64 of Qg)
+constexpr int kRecB1 = 0;        // [scale Q e^G ; -W]: 128 rows (64 of Qg, then 64 of -W)
                                  //   x 128 keys, bf16 K-major tiles (32 KiB)
 constexpr int kRecB2 = 32768;    // Kd^T = (K e^(G_last - G))^T: 128 key rows x 64 tokens (16 KiB)
-constexpr int kRecB3 = 49152;    // scale P: 64 rows r x 64 tokens i, lower incl. diagonal (8 KiB)
+constexpr int kRecB3 = 49152;    // scale P: 64 rows r x 64 tokens i, lower incl. diagonal (8 KiB);
+                                 //   B2 and B3 together are one 192-row tile [Kd^T ; P]
 constexpr int kRecUt = 57344;    // Ut^T = (T diag(beta) V)^T: [128 v][64 tok] bf16, the 16-byte
                                  //   granule j of row v stored at granule j ^ (v % 8) (16 KiB)
 constexpr int kRecGam = 73728;   // exp(G_last): fp32 [128]
