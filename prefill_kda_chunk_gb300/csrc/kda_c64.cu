@@ -64,8 +64,8 @@ constexpr int kIOffUA = kIOffWB + 16384;          // (beta V)^T: 128 v x 64 toke
 constexpr int kIOffTA = kIOffUA + 16384;          // T: 64 x 64 tokens, bf16
 constexpr int kIOffAT = kIOffTA + 8192;           // A and T, fp32 [64][68]
 constexpr int kATStride = 68;
-constexpr int kIOffTot = kIOffAT + 64 * kATStride * 4;   // per token block sums [8][128]
-constexpr int kIOffRed = kIOffTot + 4096;         // [8] per-warp range maxima, [8] flags
+constexpr int kIOffTot = kIOffAT + 64 * kATStride * 4;   // half sums [2][128], norm partials
+constexpr int kIOffRed = kIOffTot + 8192;         // [8] per-warp range flags
 constexpr int kIOffMisc = kIOffRed + 64;          // tmem base, abort, item flags
 constexpr int kIOffBar = kIOffMisc + 64;
 enum { kIBIn = 0, kIBA = 1, kIBGram = 2, kIBInv = 3, kIBWU = 4, kIBTear = 5, kIBDrain = 6,
@@ -80,7 +80,6 @@ constexpr uint32_t kCTmemCols = 512;   // S^T [0,128), O^T [128,192), U^T [192,2
 constexpr uint32_t kITmemCols = 256;   // Gram [0,64), W [64,192), Ut^T [192,256)
 
 constexpr uint32_t kIdFull = tc::idesc(128, 64, 1);    // M=128, N=64
-constexpr uint32_t kIdSq = tc::idesc(128, 128, 1);     // M=128, N=128
 constexpr uint32_t kIdW = tc::idesc(64, 128, 1);       // M=64, N=128
 
 // ------------------------------------------------------------------ small helpers
@@ -131,24 +130,6 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1
         "{%8,%9}, {%0,%1,%2,%3};\n"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y,
-                                            int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
-                                       uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(id), "r"(acc)
-        : "memory");
 }
 
 // 32 lanes x 32 bits, 32 or 64 consecutive columns (thread i <-> lane i)
@@ -287,22 +268,94 @@ __device__ __forceinline__ uint8_t *record_of(const Params &p, int64_t c, int h)
 // ============================================================================
 namespace {
 
+// Input tiles as the TMA writes them with 128-byte swizzling: panels of 64
+// token rows x 128 bytes (64 bf16 or 32 fp32 channels), the 16-byte chunk c
+// of row r stored at chunk c ^ (r % 8). Byte offset of (row r, channel ch):
+__device__ __forceinline__ uint32_t sw_bf16(int r, int ch) {
+    return static_cast<uint32_t>((ch >> 6) * 8192 + r * 128 + ((((ch & 63) >> 3) ^ (r & 7)) << 4) +
+                                 (ch & 7) * 2);
+}
+__device__ __forceinline__ uint32_t sw_f32(int r, int ch) {
+    return static_cast<uint32_t>((ch >> 5) * 8192 + r * 128 + ((((ch & 31) >> 2) ^ (r & 7)) << 4) +
+                                 (ch & 3) * 4);
+}
+
+// Fragment of an 8 x 8 bf16 tile (thread i: row i / 4, columns 2 (i % 4) and
+// +1) transposed across the warp.
+__device__ __forceinline__ uint32_t movt(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ void ldsm_x4_addr(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void st_global_u32(void *ptr, uint32_t v) {
+    asm volatile("st.global.b32 [%0], %1;\n" ::"l"(ptr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_e(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                              int z, uint32_t bar) {
+    asm volatile(
+        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+        " @e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];\n}\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ss_e(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
+                                         uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(a), "l"(b), "r"(id), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void commit_e(uint32_t bar) {
+    asm volatile(
+        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+            bar)
+        : "memory");
+}
+__device__ __forceinline__ void arrive_tx_e(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+        " @e mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n}\n" ::"r"(bar),
+        "r"(bytes)
+        : "memory");
+}
+
+// bf16 T (64 x 64, K-major core matrices) for the MMAs: element (r, i)
+__device__ __forceinline__ void ta_put(uint8_t *ta, int r, int i, float x) {
+    *reinterpret_cast<__nv_bfloat16 *>(ta + kmaj(r, i, 64)) = __float2bfloat16_rn(x);
+}
+
 // Forward substitution of one 16 x 16 diagonal block (warp w, lanes 0-15
-// each solve one column), in place in the fp32 A/T buffer.
-__device__ __forceinline__ void invert_diag(float *at, int w, int lane) {
+// each solve one column), in place in the fp32 A/T buffer, and in bf16 to TA.
+__device__ __forceinline__ void invert_diag(float *at, uint8_t *ta, int w, int lane) {
     const int j = lane & 15, b = 16 * w;
     float t[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-        float s = (r == j) ? 1.f : 0.f;
+        // four independent partial sums keep the dependent chain short
+        float s4[4] = {(r == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < r; ++i) s = fmaf(-at[(b + r) * kATStride + b + i], t[i], s);
-        t[r] = s;
+        for (int i = 0; i < r; ++i) s4[i & 3] = fmaf(-at[(b + r) * kATStride + b + i], t[i], s4[i & 3]);
+        t[r] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     }
     __syncwarp();
     if (lane < 16) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) at[(b + r) * kATStride + b + j] = t[r];
+        for (int r = 0; r < 16; ++r) {
+            at[(b + r) * kATStride + b + j] = t[r];
+            ta_put(ta, b + r, b + j, t[r]);
+        }
     }
     __syncwarp();
 }
@@ -318,19 +371,16 @@ __device__ __forceinline__ float t_blk(const float *at, int I, int J, int r, int
                   : at[(16 * J + c) * kATStride + 16 * I + r];
 }
 
-// acc (16 x 16, two m16n8 fragments) += X(I,K) * T(K,J), X = A (use_a) or T
-__device__ __forceinline__ void blk_mma(float (&acc)[2][4], const float *at, bool xa, int I, int K,
-                                        int J, int lane) {
+// acc (16 x 16, two m16n8 fragments) += A(I,K) * T(K,J)
+__device__ __forceinline__ void blk_mma(float (&acc)[2][4], const float *at, int I, int K, int J,
+                                        int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int kk = 0; kk < 16; kk += 8) {
-        const uint32_t a0 = tf32(xa ? a_blk(at, I, K, g, kk + t) : t_blk(at, I, K, g, kk + t));
-        const uint32_t a1 =
-            tf32(xa ? a_blk(at, I, K, g + 8, kk + t) : t_blk(at, I, K, g + 8, kk + t));
-        const uint32_t a2 =
-            tf32(xa ? a_blk(at, I, K, g, kk + t + 4) : t_blk(at, I, K, g, kk + t + 4));
-        const uint32_t a3 =
-            tf32(xa ? a_blk(at, I, K, g + 8, kk + t + 4) : t_blk(at, I, K, g + 8, kk + t + 4));
+        const uint32_t a0 = tf32(a_blk(at, I, K, g, kk + t));
+        const uint32_t a1 = tf32(a_blk(at, I, K, g + 8, kk + t));
+        const uint32_t a2 = tf32(a_blk(at, I, K, g, kk + t + 4));
+        const uint32_t a3 = tf32(a_blk(at, I, K, g + 8, kk + t + 4));
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const uint32_t b0 = tf32(t_blk(at, K, J, kk + t, 8 * nt + g));
@@ -340,9 +390,10 @@ __device__ __forceinline__ void blk_mma(float (&acc)[2][4], const float *at, boo
     }
 }
 
-// T(I,J) = -T(I,I) * X where X (16 x 16, fragments) is staged in scratch.
-__device__ __forceinline__ void finish_blk(float *at, float *scratch, const float (&x)[2][4],
-                                           int I, int J, int lane) {
+// T(I,J) = -T(I,I) * X where X (16 x 16, fragments) is staged in scratch;
+// to the fp32 buffer (transposed) and in bf16 to TA.
+__device__ __forceinline__ void finish_blk(float *at, uint8_t *ta, float *scratch,
+                                           const float (&x)[2][4], int I, int J, int lane) {
     const int g = lane >> 2, t = lane & 3;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -366,7 +417,6 @@ __device__ __forceinline__ void finish_blk(float *at, float *scratch, const floa
             mma_tf32(acc[nt], a0, a1, a2, a3, b0, b1);
         }
     }
-    // store transposed: T(I,J)[r][c] at at[16J + c][16I + r]
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
         const int c0 = 8 * nt + 2 * t;
@@ -374,39 +424,54 @@ __device__ __forceinline__ void finish_blk(float *at, float *scratch, const floa
         at[(16 * J + c0 + 1) * kATStride + 16 * I + g] = -acc[nt][1];
         at[(16 * J + c0) * kATStride + 16 * I + g + 8] = -acc[nt][2];
         at[(16 * J + c0 + 1) * kATStride + 16 * I + g + 8] = -acc[nt][3];
+        *reinterpret_cast<uint32_t *>(ta + kmaj(16 * I + g, 16 * J + c0, 64)) =
+            pack_bf16(-acc[nt][0], -acc[nt][1]);
+        *reinterpret_cast<uint32_t *>(ta + kmaj(16 * I + g + 8, 16 * J + c0, 64)) =
+            pack_bf16(-acc[nt][2], -acc[nt][3]);
     }
     __syncwarp();
 }
 
 // T = (I + A)^{-1} for the 64 x 64 strictly lower A in `at` (warps 0-3 of
 // the compute group; the caller synchronises the group before and after).
-__device__ __forceinline__ void invert64(float *at, float *scratch, int warp, int lane) {
-    invert_diag(at, warp, lane);
+// T goes to `at` (fp32, blocks below the diagonal transposed) and to TA (bf16,
+// blocks above the diagonal are zero).
+__device__ __forceinline__ void invert64(float *at, uint8_t *ta, float *scratch, int warp,
+                                         int lane) {
+    // zero TA's blocks above the diagonal: (I, J) with J > I, 6 blocks of 16 x 16
+    for (int x = threadIdx.x; x < 6 * 32; x += 128) {
+        const int blk = x >> 5, piece = x & 31;           // 32 pieces of 16 bytes per block
+        const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        const int r = 16 * I + (piece >> 1), c8 = 16 * J + 8 * (piece & 1);
+        *reinterpret_cast<uint4 *>(ta + kmaj(r, c8, 64)) = make_uint4(0, 0, 0, 0);
+    }
+    invert_diag(at, ta, warp, lane);
     named_sync(2, 128);
     // level 1: T(I, I-1) for I = 1..3 on warps 0..2
     if (warp < 3) {
         const int I = warp + 1;
         float x[2][4] = {};
-        blk_mma(x, at, true, I, I - 1, I - 1, lane);
-        finish_blk(at, scratch + warp * 16 * 17, x, I, I - 1, lane);
+        blk_mma(x, at, I, I - 1, I - 1, lane);
+        finish_blk(at, ta, scratch + warp * 16 * 17, x, I, I - 1, lane);
     }
     named_sync(2, 128);
     // level 2: T(I, I-2) for I = 2, 3 on warps 0, 1
     if (warp < 2) {
         const int I = warp + 2;
         float x[2][4] = {};
-        blk_mma(x, at, true, I, I - 2, I - 2, lane);
-        blk_mma(x, at, true, I, I - 1, I - 2, lane);
-        finish_blk(at, scratch + warp * 16 * 17, x, I, I - 2, lane);
+        blk_mma(x, at, I, I - 2, I - 2, lane);
+        blk_mma(x, at, I, I - 1, I - 2, lane);
+        finish_blk(at, ta, scratch + warp * 16 * 17, x, I, I - 2, lane);
     }
     named_sync(2, 128);
     // level 3: T(3, 0) on warp 0
     if (warp == 0) {
         float x[2][4] = {};
-        blk_mma(x, at, true, 3, 0, 0, lane);
-        blk_mma(x, at, true, 3, 1, 0, lane);
-        blk_mma(x, at, true, 3, 2, 0, lane);
-        finish_blk(at, scratch, x, 3, 0, lane);
+        blk_mma(x, at, 3, 0, 0, lane);
+        blk_mma(x, at, 3, 1, 0, lane);
+        blk_mma(x, at, 3, 2, 0, lane);
+        finish_blk(at, ta, scratch, x, 3, 0, lane);
     }
 }
 
@@ -454,74 +519,75 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
     };
 
     if (warp == 8) {
-        // ================================================ TMA loads and MMA issue
-        if (lane == 0) {
-            int it = 0, loads = 0;
-            auto issue_loads = [&](int64_t itm) {
-                const int64_t c = itm / H;
-                const int h = static_cast<int>(itm - c * H);
-                int n, L;
-                int64_t t0;
-                locate(p, c, n, t0, L);
-                mbar_arrive_expect_tx(bar(kIBIn), 3 * 16384 + 32768);
-                const int z = static_cast<int>(t0);
-                tma_load_3d(sb + kIOffQ, &p.tm_q, 0, h, z, bar(kIBIn));
-                tma_load_3d(sb + kIOffK, &p.tm_k, 0, h, z, bar(kIBIn));
-                tma_load_3d(sb + kIOffV, &p.tm_v, 0, h, z, bar(kIBIn));
-                tma_load_3d(sb + kIOffG, &p.tm_g, 0, h, z, bar(kIBIn));
-                ++loads;
-            };
-            int64_t item = next_real(worker);
-            if (item < items) issue_loads(item);
-            for (; item < items; ++it) {
-                // phase A done: operand tiles written, input tiles free
-                if (!wait_bar(bar(kIBA), it & 1, abort_flag, p.err)) break;
-                const bool exact = *item_exact != 0;
-                const int64_t next = next_real(item + nworkers);
-                if (!exact) {
-                    if (next < items) issue_loads(next);
-                    tc::fence_after();
+        // ================================================ TMA loads and MMA issue (whole warp,
+        // one elected lane issues)
+        int it = 0, loads = 0;
+        auto issue_loads = [&](int64_t itm) {
+            const int64_t c = itm / H;
+            const int h = static_cast<int>(itm - c * H);
+            int n, L;
+            int64_t t0;
+            locate(p, c, n, t0, L);
+            arrive_tx_e(bar(kIBIn), 3 * 16384 + 32768);
+            const int z = static_cast<int>(t0);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tmem + 0, tc::sdesc(sb + kIOffGA + kk * 256, 128, 2048),
-                               tc::sdesc(sb + kIOffGB + kk * 256, 128, 2048), kIdFull, kk > 0);
-                    tc::commit(bar(kIBGram));
-                }
-                // T ready (the exact form also read the input tiles until now)
-                if (!wait_bar(bar(kIBInv), it & 1, abort_flag, p.err)) break;
-                if (exact && next < items) issue_loads(next);
+            for (int x = 0; x < 2; ++x) {
+                tma_load_3d_e(sb + kIOffQ + 8192 * x, &p.tm_q, 64 * x, h, z, bar(kIBIn));
+                tma_load_3d_e(sb + kIOffK + 8192 * x, &p.tm_k, 64 * x, h, z, bar(kIBIn));
+                tma_load_3d_e(sb + kIOffV + 8192 * x, &p.tm_v, 64 * x, h, z, bar(kIBIn));
+            }
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+                tma_load_3d_e(sb + kIOffG + 8192 * x, &p.tm_g, 32 * x, h, z, bar(kIBIn));
+            ++loads;
+        };
+        const uint64_t dGA = tc::sdesc(sb + kIOffGA, 128, 2048), dGB = tc::sdesc(sb + kIOffGB, 128, 2048);
+        const uint64_t dTA = tc::sdesc(sb + kIOffTA, 128, 1024), dWB = tc::sdesc(sb + kIOffWB, 128, 1024);
+        const uint64_t dUA = tc::sdesc(sb + kIOffUA, 128, 1024);
+        int64_t item = next_real(worker);
+        if (item < items) issue_loads(item);
+        for (; item < items; ++it) {
+            // phase A done: operand tiles written, input tiles free
+            if (!wait_bar(bar(kIBA), it & 1, abort_flag, p.err)) break;
+            __syncwarp();
+            const bool exact = *item_exact != 0;
+            const int64_t next = next_real(item + nworkers);
+            if (!exact) {
                 tc::fence_after();
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    // W = T (beta K e^G): M = 64 rows r, N = 128 keys, K = 64 tokens
-                    mma_ss(tmem + 64, tc::sdesc(sb + kIOffTA + kk * 256, 128, 1024),
-                           tc::sdesc(sb + kIOffWB + kk * 256, 128, 1024), kIdW, kk > 0);
-                }
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    // Ut^T = (beta V)^T T^T: M = 128 v, N = 64 rows r, K = 64 tokens
-                    mma_ss(tmem + 192, tc::sdesc(sb + kIOffUA + kk * 256, 128, 1024),
-                           tc::sdesc(sb + kIOffTA + kk * 256, 128, 1024), kIdFull, kk > 0);
-                }
-                tc::commit(bar(kIBWU));
-                item = next;
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss_e(tmem + 0, dGA + 16 * kk, dGB + 16 * kk, kIdFull, kk > 0);
+                commit_e(bar(kIBGram));
+                if (next < items) issue_loads(next);
             }
-            // drain: the last input load and every MMA issued have completed
-            if (loads > 0) wait_bar(bar(kIBIn), (loads - 1) & 1, abort_flag, p.err);
-            tc::commit(bar(kIBDrain));
-            wait_bar(bar(kIBDrain), 0, abort_flag, p.err);
+            // T ready (the exact form also read the input tiles until now)
+            if (!wait_bar(bar(kIBInv), it & 1, abort_flag, p.err)) break;
+            __syncwarp();
+            if (exact && next < items) issue_loads(next);
+            tc::fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)   // W = T (beta K e^G): M = 64, N = 128 keys, K = 64 tokens
+                mma_ss_e(tmem + 64, dTA + 16 * kk, dWB + 16 * kk, kIdW, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)   // Ut^T = (beta V)^T T^T: M = 128 v, N = 64, K = 64
+                mma_ss_e(tmem + 192, dUA + 16 * kk, dTA + 16 * kk, kIdFull, kk > 0);
+            commit_e(bar(kIBWU));
+            item = next;
         }
+        // drain: the last input load and every MMA issued have completed
+        if (loads > 0) wait_bar(bar(kIBIn), (loads - 1) & 1, abort_flag, p.err);
+        commit_e(bar(kIBDrain));
+        wait_bar(bar(kIBDrain), 0, abort_flag, p.err);
     } else if (warp < 8) {
         // ================================================ compute warps (256 threads)
         const int ct = tid;                 // 0..255
-        const int bt = ct & 127;            // 8 x 8 block of the 64 x 128 tile
-        const int role = ct >> 7;           // 0: exp(G) products, 1: exp(-G) products
-        const int tb = bt >> 4, cb = bt & 15;
-        const int row0 = 8 * tb, ch0 = 8 * cb;
-        float *tot = reinterpret_cast<float *>(smem + kIOffTot);
+        const int gq = lane >> 2, tq = lane & 3;   // fragment row / column pair
+        float *tot = reinterpret_cast<float *>(smem + kIOffTot);   // [2][128] half sums
         int *red = reinterpret_cast<int *>(smem + kIOffRed);
         float *at = reinterpret_cast<float *>(smem + kIOffAT);
+        uint8_t *ta = smem + kIOffTA;
         float *betas = reinterpret_cast<float *>(smem + kIOffBeta);
+        float *gs = reinterpret_cast<float *>(smem + kIOffG);
         int it = 0;
         for (int64_t item = next_real(worker); item < items; item = next_real(item + nworkers)) {
             const int64_t c = item / H;
@@ -537,192 +603,179 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
             if (ct < kC) betas[ct] = ct < L ? __ldg(p.beta + (t0 + ct) * H + h) : 0.f;
             wait_bar(bar(kIBIn), it & 1, abort_flag, p.err);
 
-            // ---- cumulative log decay of this thread's 8 x 8 block (base 2)
-            float G[8][8];
+            // ---- cumulative log decay (base 2), in place in the g tile: thread =
+            //      channel ct % 128, tokens [32 half, 32 half + 32); the second half
+            //      adds the first half's sum
+            float gmax = 0.f;
             bool anypos = false;
             {
-                const float *gs = reinterpret_cast<const float *>(smem + kIOffG);
+                const int ch = ct & 127, th = ct >> 7;
+                // rows 8 k + j of this half: the swizzle term depends on j only
+                const uint32_t o0 = sw_f32(32 * th, ch);
+                float x[32];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const float4 x0 = *reinterpret_cast<const float4 *>(gs + (row0 + r) * 128 + ch0);
-                    const float4 x1 =
-                        *reinterpret_cast<const float4 *>(gs + (row0 + r) * 128 + ch0 + 4);
-                    const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-                    const bool real = row0 + r < L;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        float gv = real ? x[j] : 0.f;
-                        if (PRE && (p.pre & kPreGateLogits) && real) gv = log_sigmoid(gv);
-                        anypos |= gv > 0.f;
-                        G[r][j] = (r > 0 ? G[r - 1][j] : 0.f) + gv * kLog2e;
-                    }
+                for (int r = 0; r < 32; ++r) {
+                    const uint32_t o = o0 + (r >> 3) * 1024 + (r & 7) * 128 +
+                                       ((((ch & 31) >> 2) ^ (r & 7)) - ((ch & 31) >> 2)) * 16;
+                    x[r] = *reinterpret_cast<const float *>(reinterpret_cast<const uint8_t *>(gs) + o);
                 }
-            }
-            if (role == 0) {
+                float run = 0.f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) tot[tb * 128 + ch0 + j] = G[7][j];
-            }
-            if (named_sync_or(1, 256, *abort_flag != 0)) break;
-            float gl[8];   // G_last of each channel (base 2)
-            {
-                float pre8[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) { gl[j] = 0.f; pre8[j] = 0.f; }
-                for (int b2 = 0; b2 < 8; ++b2) {
-                    const float4 y0 = *reinterpret_cast<const float4 *>(tot + b2 * 128 + ch0);
-                    const float4 y1 = *reinterpret_cast<const float4 *>(tot + b2 * 128 + ch0 + 4);
-                    const float y[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (b2 < tb) pre8[j] += y[j];
-                        gl[j] += y[j];
-                    }
+                for (int r = 0; r < 32; ++r) {
+                    const int t = 32 * th + r;
+                    float xv = t < L ? x[r] : 0.f;
+                    if (PRE && (p.pre & kPreGateLogits) && t < L) xv = log_sigmoid(xv);
+                    anypos |= xv > 0.f;
+                    run = fmaf(xv, kLog2e, run);
+                    x[r] = run;
                 }
-                float gmax = 0.f;
+                tot[th * 128 + ch] = run;
+                if (named_sync_or(1, 256, *abort_flag != 0)) break;
+                const float carry = th ? tot[ch] : 0.f;
 #pragma unroll
-                for (int r = 0; r < 8; ++r)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        G[r][j] += pre8[j];
-                        gmax = fmaxf(gmax, fabsf(G[r][j]));
-                    }
+                for (int r = 0; r < 32; ++r) {
+                    const uint32_t o = o0 + (r >> 3) * 1024 + (r & 7) * 128 +
+                                       ((((ch & 31) >> 2) ^ (r & 7)) - ((ch & 31) >> 2)) * 16;
+                    const float v = x[r] + carry;
+                    *reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(gs) + o) = v;
+                    gmax = fmaxf(gmax, fabsf(v));
+                }
                 // the factored form holds while |G| <= 80 (natural log); with
                 // positive gates in the chunk while |G| <= 40, so that no
                 // lower-triangle product exp(G_r - G_i) exceeds exp(80) either
-                const float lim = anypos ? 0.5f * kFactorRange * kLog2e : kFactorRange * kLog2e;
+                const bool pos = __any_sync(0xffffffffu, anypos);
+                const float lim = pos ? 0.5f * kFactorRange * kLog2e : kFactorRange * kLog2e;
                 const unsigned any_bad = __ballot_sync(0xffffffffu, !(gmax <= lim));
-                if (lane == 0) red[warp] = any_bad != 0;
+                if (lane == 0) red[warp] = (any_bad != 0) | (pos ? 2 : 0);
             }
             named_sync(1, 256);
             bool exact = false;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) exact |= red[w] != 0;
+            for (int w = 0; w < 8; ++w) exact |= (red[w] & 1) != 0;
 
-            // ---- gated operand tiles and the record's Qg, Kd, gamma, row by row
+            // ---- gated operand tiles and the record's Qg, Kd, gamma (fragment layout:
+            //      warp w owns channels [16 w, 16 w + 16), thread (gq, tq) the rows
+            //      8 tb + gq and channel pairs 2 tq of each 8 x 8 core matrix)
             const bool norm = PRE && (p.pre & kPreNormQK);
-            const uint8_t *qs = smem + kIOffQ, *ks = smem + kIOffK, *vs = smem + kIOffV;
-            // row r's 8 channels of a bf16 tile (zero past the sequence end), and
-            // the row's L2 norm over the 16 threads that share it when asked
-            auto load8 = [&](const uint8_t *tile, int r, float (&x)[8]) {
-                const uint4 u = *reinterpret_cast<const uint4 *>(tile + (row0 + r) * 256 + ch0 * 2);
-                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-                const bool real = row0 + r < L;
+            float glast[2][2], egl[2][2];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = unpack_bf16(w4[e]);
-                    x[2 * e] = real ? f.x : 0.f;
-                    x[2 * e + 1] = real ? f.y : 0.f;
+            for (int cw = 0; cw < 2; ++cw)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int ch = 16 * warp + 8 * cw + 2 * tq + e;
+                    glast[cw][e] = tot[ch] + tot[128 + ch];
+                    egl[cw][e] = ex2f(glast[cw][e]);
                 }
-            };
-            auto normalise = [&](float (&x)[8]) {
-                float ss = 0.f;
+            if (gq == 0) {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) ss = fmaf(x[j], x[j], ss);
-#pragma unroll
-                for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-                const float rn = rsqrtf(ss + kNormEps);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) x[j] *= rn;
-            };
-            auto pack8 = [](const float (&x)[8]) {
-                return make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]),
-                                  pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-            };
-            if (role == 0) {
-                // scale Q e^G -> GA rows 64+ and record B1 rows 64+;
-                // beta K e^G -> GA rows 0-63 and, transposed, WB
-                float kb[8][8];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    float q[8], k[8];
-                    load8(qs, r, q);
-                    load8(ks, r, k);
-                    if (norm) { normalise(q); normalise(k); }
-                    const float br = betas[row0 + r];
-                    float qg[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float e = ex2f(G[r][j]);
-                        qg[j] = q[j] * e * p.scale;
-                        kb[r][j] = k[j] * e * br;
-                    }
-                    const uint4 uq = pack8(qg);
-                    *reinterpret_cast<uint4 *>(smem + kIOffGA + kmaj(64 + row0 + r, ch0, 128)) = uq;
-                    st_global_v4(rec + kRecB1 + kmaj(row0 + r, ch0, 128), uq);
-                    *reinterpret_cast<uint4 *>(smem + kIOffGA + kmaj(row0 + r, ch0, 128)) = pack8(kb[r]);
+                for (int cw = 0; cw < 2; ++cw) {
+                    const int ch = 16 * warp + 8 * cw + 2 * tq;
+                    *reinterpret_cast<float2 *>(rec + kRecGam + ch * 4) = make_float2(egl[cw][0], egl[cw][1]);
                 }
+            }
+            // row norms (over the 128 channels) for in-kernel q / k normalisation
+            // need the whole row: done per row by the 32 threads... only when asked
+            float rq[8], rk[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 u = make_uint4(pack_bf16(kb[0][j], kb[1][j]), pack_bf16(kb[2][j], kb[3][j]),
-                                               pack_bf16(kb[4][j], kb[5][j]), pack_bf16(kb[6][j], kb[7][j]));
-                    *reinterpret_cast<uint4 *>(smem + kIOffWB + kmaj(ch0 + j, row0, 64)) = u;
-                }
-                if (tb == 0) {
-                    float gm[8];
+            for (int tb = 0; tb < 8; ++tb) { rq[tb] = 1.f; rk[tb] = 1.f; }
+            if (norm) {
+                // each warp sums its 16 channels of every row; the 8 partials of a row
+                // meet in shared memory (the half-sum area is free again)
+                float *part = tot + 256;   // [2][64][8]
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) gm[j] = ex2f(gl[j]);
-                    st_global_v4(rec + kRecGam + ch0 * 4,
-                                 make_uint4(__float_as_uint(gm[0]), __float_as_uint(gm[1]),
-                                            __float_as_uint(gm[2]), __float_as_uint(gm[3])));
-                    st_global_v4(rec + kRecGam + ch0 * 4 + 16,
-                                 make_uint4(__float_as_uint(gm[4]), __float_as_uint(gm[5]),
-                                            __float_as_uint(gm[6]), __float_as_uint(gm[7])));
-                }
-                if (exact) {
-                    // the exact form reads G (base 2) from the g tile
-                    float *gs = reinterpret_cast<float *>(smem + kIOffG);
+                for (int tb = 0; tb < 8; ++tb) {
+                    if (lane < 16) {
+                        const int r = 8 * tb + (lane & 7), which = lane >> 3;   // 0: q, 1: k
+                        const uint8_t *tile = smem + (which ? kIOffK : kIOffQ);
+                        float ss = 0.f;
 #pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        *reinterpret_cast<float4 *>(gs + (row0 + r) * 128 + ch0) =
-                            make_float4(G[r][0], G[r][1], G[r][2], G[r][3]);
-                        *reinterpret_cast<float4 *>(gs + (row0 + r) * 128 + ch0 + 4) =
-                            make_float4(G[r][4], G[r][5], G[r][6], G[r][7]);
-                    }
-                }
-            } else {
-                // K e^-G -> GB; Kd = K e^(G_last - G) -> record B2 (transposed)
-                float egl[8];
+                        for (int c8 = 0; c8 < 2; ++c8) {
+                            const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw_bf16(r, 16 * warp + 8 * c8));
+                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                for (int j = 0; j < 8; ++j) egl[j] = ex2f(gl[j]);
-                float kd[8][8];
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    float k[8];
-                    load8(ks, r, k);
-                    if (norm) normalise(k);
-                    float kn[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (exact) {
-                            kn[j] = 0.f;   // unused by the exact form
-                            kd[r][j] = k[j] * ex2f(gl[j] - G[r][j]);
-                        } else {
-                            kn[j] = k[j] * ex2f(-G[r][j]);
-                            kd[r][j] = kn[j] * egl[j];
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = unpack_bf16(w4[e]);
+                                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+                            }
                         }
+                        part[(which * 64 + r) * 8 + warp] = ss;
                     }
-                    *reinterpret_cast<uint4 *>(smem + kIOffGB + kmaj(row0 + r, ch0, 128)) = pack8(kn);
                 }
+                named_sync(1, 256);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 u = make_uint4(pack_bf16(kd[0][j], kd[1][j]), pack_bf16(kd[2][j], kd[3][j]),
-                                               pack_bf16(kd[4][j], kd[5][j]), pack_bf16(kd[6][j], kd[7][j]));
-                    st_global_v4(rec + kRecB2 + kmaj(ch0 + j, row0, 64), u);
+                for (int tb = 0; tb < 8; ++tb) {
+                    const int r = 8 * tb + gq;
+                    float sq = 0.f, sk = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        sq += part[r * 8 + w];
+                        sk += part[(64 + r) * 8 + w];
+                    }
+                    rq[tb] = rsqrtf(sq + kNormEps);
+                    rk[tb] = rsqrtf(sk + kNormEps);
                 }
-                // beta V -> UA (transposed); reuses kd's registers
+            }
+            // loop-invariant parts of the addresses: row 8 tb + gq of a tile sits
+            // tb * 1024 bytes after row gq (the swizzle depends on the row mod 8)
+            const uint32_t g_off0 = sw_f32(gq, 16 * warp + 2 * tq);
+            const uint32_t g_off1 = sw_f32(gq, 16 * warp + 8 + 2 * tq);
+            const uint32_t lm_off = sw_bf16(lane & 7, 16 * warp + 8 * ((lane >> 3) & 1)) +
+                                    1024 * (lane >> 4);
+            const uint32_t o_tk0 = kmaj(0, 16 * warp, 128) + gq * 16 + tq * 4;   // + tb 2048 + cw 128
+            const uint32_t o_kt0 = kmaj(16 * warp, 0, 64) + gq * 16 + tq * 4;    // + cw 1024 + tb 128
+            uint8_t *const sGA = smem + kIOffGA + o_tk0, *const sGB = smem + kIOffGB + o_tk0;
+            uint8_t *const sWB = smem + kIOffWB + o_kt0, *const sUA = smem + kIOffUA + o_kt0;
+            uint8_t *const gB1 = rec + kRecB1 + o_tk0, *const gB2 = rec + kRecB2 + o_kt0;
+            const float *const beta_r = betas + gq;
+            const float sc = p.scale;
 #pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    float vv[8];
-                    load8(vs, r, vv);
-                    const float br = betas[row0 + r];
+            for (int tbp = 0; tbp < 4; ++tbp) {
+                // ldmatrix x4: matrices (tb, cw) for tb = 2 tbp, 2 tbp + 1 and cw = 0, 1
+                uint32_t qf[4], kf[4], vf[4];
+                ldsm_x4_addr(sb + kIOffQ + lm_off + 2048 * tbp, qf);
+                ldsm_x4_addr(sb + kIOffK + lm_off + 2048 * tbp, kf);
+                ldsm_x4_addr(sb + kIOffV + lm_off + 2048 * tbp, vf);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) kd[r][j] = vv[j] * br;
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint4 u = make_uint4(pack_bf16(kd[0][j], kd[1][j]), pack_bf16(kd[2][j], kd[3][j]),
-                                               pack_bf16(kd[4][j], kd[5][j]), pack_bf16(kd[6][j], kd[7][j]));
-                    *reinterpret_cast<uint4 *>(smem + kIOffUA + kmaj(ch0 + j, row0, 64)) = u;
+                for (int m = 0; m < 4; ++m) {
+                    const int tb = 2 * tbp + (m >> 1), cw = m & 1;
+                    const bool real = 8 * tb + gq < L;
+                    const float2 g2 = *reinterpret_cast<const float2 *>(
+                        reinterpret_cast<const uint8_t *>(gs) + (cw ? g_off1 : g_off0) + 1024 * tb);
+                    const float br = beta_r[8 * tb];
+                    float2 q2 = unpack_bf16(qf[m]), k2 = unpack_bf16(kf[m]), v2 = unpack_bf16(vf[m]);
+                    if (!real) { q2 = make_float2(0.f, 0.f); k2 = q2; }
+                    if (norm) {
+                        q2.x *= rq[tb]; q2.y *= rq[tb];
+                        k2.x *= rk[tb]; k2.y *= rk[tb];
+                    }
+                    const float e0 = ex2f(g2.x), e1 = ex2f(g2.y);
+                    float2 qg = q2, kb = k2, kn = k2, kd, bv = v2;
+                    mul2(qg.x, qg.y, e0 * sc, e1 * sc);
+                    mul2(kb.x, kb.y, e0 * br, e1 * br);
+                    if (!exact) {
+                        mul2(kn.x, kn.y, ex2f(-g2.x), ex2f(-g2.y));
+                        kd = kn;
+                        mul2(kd.x, kd.y, egl[cw][0], egl[cw][1]);
+                    } else {
+                        kn = make_float2(0.f, 0.f);
+                        kd = make_float2(k2.x * ex2f(glast[cw][0] - g2.x), k2.y * ex2f(glast[cw][1] - g2.y));
+                    }
+                    mul2(bv.x, bv.y, br, br);
+                    const uint32_t uqg = pack_bf16(qg.x, qg.y), ukb = pack_bf16(kb.x, kb.y);
+                    const uint32_t ukn = pack_bf16(kn.x, kn.y), ukd = pack_bf16(kd.x, kd.y);
+                    const uint32_t ubv = pack_bf16(bv.x, bv.y);
+                    // [tok][key] core matrices: GA rows 0-63 (beta K e^G) and 64-127
+                    // (scale Q e^G), GB (K e^-G); record B1 rows 0-63 (scale Q e^G)
+                    const int otk = 2048 * tb + 128 * cw;
+                    *reinterpret_cast<uint32_t *>(sGA + otk) = ukb;
+                    *reinterpret_cast<uint32_t *>(sGA + 16384 + otk) = uqg;
+                    *reinterpret_cast<uint32_t *>(sGB + otk) = ukn;
+                    st_global_u32(gB1 + otk, uqg);
+                    // [key][tok] core matrices (transposed): WB, UA; record B2 (Kd^T)
+                    const int okt = 1024 * cw + 128 * tb;
+                    *reinterpret_cast<uint32_t *>(sWB + okt) = movt(ukb);
+                    *reinterpret_cast<uint32_t *>(sUA + okt) = movt(ubv);
+                    st_global_u32(gB2 + okt, movt(ukd));
                 }
             }
             if (ct == 0) *item_exact = exact ? 1 : 0;
@@ -768,17 +821,18 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
             } else {
                 // exact per-pair exponentials: 8 threads per row pair (rp, 63 - rp),
                 // pairs (r, i <= r) with i = sub (mod 8)
-                const float *gs = reinterpret_cast<const float *>(smem + kIOffG);
+                const uint8_t *qs = smem + kIOffQ, *ks = smem + kIOffK;
                 float *pf = reinterpret_cast<float *>(smem + kIOffGB);   // P fp32 [64][64]
                 // inverse row norms of q (0..63) and k (64..127) when normalising
-                float *rn = reinterpret_cast<float *>(smem + kIOffTot);
+                float *rn = tot;
                 if (ct < 128) {
                     float x = 1.f;
                     if (norm) {
-                        const uint8_t *row = (ct < 64 ? qs : ks) + (ct & 63) * 256;
+                        const uint8_t *tile = ct < 64 ? qs : ks;
+                        const int r = ct & 63;
                         float ss = 0.f;
                         for (int c8 = 0; c8 < 16; ++c8) {
-                            const uint4 u = *reinterpret_cast<const uint4 *>(row + c8 * 16);
+                            const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw_bf16(r, 8 * c8));
                             const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
@@ -798,9 +852,9 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
                     for (int i = sub; i <= r; i += 8) {
                         float sa = 0.f, sp = 0.f;
                         for (int c8 = 0; c8 < 16; ++c8) {
-                            const uint4 kr = *reinterpret_cast<const uint4 *>(ks + r * 256 + c8 * 16);
-                            const uint4 qr = *reinterpret_cast<const uint4 *>(qs + r * 256 + c8 * 16);
-                            const uint4 ki = *reinterpret_cast<const uint4 *>(ks + i * 256 + c8 * 16);
+                            const uint4 kr = *reinterpret_cast<const uint4 *>(ks + sw_bf16(r, 8 * c8));
+                            const uint4 qr = *reinterpret_cast<const uint4 *>(qs + sw_bf16(r, 8 * c8));
+                            const uint4 ki = *reinterpret_cast<const uint4 *>(ks + sw_bf16(i, 8 * c8));
                             const uint32_t krw[4] = {kr.x, kr.y, kr.z, kr.w};
                             const uint32_t qrw[4] = {qr.x, qr.y, qr.z, qr.w};
                             const uint32_t kiw[4] = {ki.x, ki.y, ki.z, ki.w};
@@ -809,8 +863,11 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
                                 const float2 a = unpack_bf16(krw[e]), bq = unpack_bf16(qrw[e]),
                                              cc = unpack_bf16(kiw[e]);
                                 const int ch = 8 * c8 + 2 * e;
-                                const float x0 = gs[r * 128 + ch] - gs[i * 128 + ch];
-                                const float x1 = gs[r * 128 + ch + 1] - gs[i * 128 + ch + 1];
+                                const float2 gr = *reinterpret_cast<const float2 *>(
+                                    reinterpret_cast<const uint8_t *>(gs) + sw_f32(r, ch));
+                                const float2 gi = *reinterpret_cast<const float2 *>(
+                                    reinterpret_cast<const uint8_t *>(gs) + sw_f32(i, ch));
+                                const float x0 = gr.x - gi.x, x1 = gr.y - gi.y;
                                 overflow |= x0 > kFactorRange * kLog2e || x1 > kFactorRange * kLog2e;
                                 const float e0 = ex2f(x0), e1 = ex2f(x1);
                                 sa = fmaf(a.x * cc.x, e0, sa);
@@ -847,29 +904,11 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
             }
             if (named_sync_or(1, 256, *abort_flag != 0)) break;
 
-            // ---- T = (I + A)^{-1} (warps 0-3), then T in bf16 for the MMAs
+            // ---- T = (I + A)^{-1} (warps 0-3), straight to bf16 TA for the MMAs
             if (warp < 4) {
                 // scratch for the off-diagonal blocks: the Gram operand tile is free now
                 float *scratch = reinterpret_cast<float *>(smem + kIOffGA);
-                invert64(at, scratch, warp, lane);
-            }
-            named_sync(1, 256);
-            for (int gidx = ct; gidx < 64 * 8; gidx += 256) {
-                const int r = gidx >> 3, g8 = gidx & 7;
-                const int I = r >> 4;
-                uint32_t w4[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    float v2[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int i = 8 * g8 + 2 * e + u, J = i >> 4;
-                        v2[u] = J > I ? 0.f : (J == I ? at[r * kATStride + i] : at[i * kATStride + r]);
-                    }
-                    w4[e] = pack_bf16(v2[0], v2[1]);
-                }
-                *reinterpret_cast<uint4 *>(smem + kIOffTA + kmaj(r, 8 * g8, 64)) =
-                    make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                invert64(at, ta, scratch, warp, lane);
             }
             fence_async_smem();
             tc::fence_before();
@@ -885,6 +924,14 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
                 // Ut^T row v = 32 q4 + lane, tokens [32 half, 32 half + 32)
                 uint32_t d[32];
                 tld32(tmem + lane_base + 192 + 32 * half, d);
+                // W (M = 64): rows 16 q4 + (0..15) in lanes 32 q4 + (0..15); the
+                // 16-lane shape gives thread (gq, tq) rows gq, gq + 8 and the column
+                // pair 2 tq of each 8-column block
+                uint32_t w[8][4];
+#pragma unroll
+                for (int b8 = 0; b8 < 8; ++b8)
+                    tc::ld_16x256b(tmem + lane_base + 64 + 64 * half + 8 * b8, w[b8][0], w[b8][1],
+                                   w[b8][2], w[b8][3]);
                 tc::ld_wait();
                 const int v = 32 * q4 + lane;
 #pragma unroll
@@ -896,24 +943,14 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
                                             pack_bf16(__uint_as_float(d[8 * j4 + 4]), __uint_as_float(d[8 * j4 + 5])),
                                             pack_bf16(__uint_as_float(d[8 * j4 + 6]), __uint_as_float(d[8 * j4 + 7]))));
                 }
-                // W (M = 64): row r = 16 q4 + lane in lanes 32 q4 + (0..15)
 #pragma unroll
-                for (int c2 = 0; c2 < 2; ++c2) {
-                    uint32_t w[32];
-                    tld32(tmem + lane_base + 64 + 64 * half + 32 * c2, w);
-                    tc::ld_wait();
-                    if (lane < 16) {
-                        const int r = 16 * q4 + lane;
-#pragma unroll
-                        for (int k8 = 0; k8 < 4; ++k8) {
-                            const int key = 64 * half + 32 * c2 + 8 * k8;
-                            st_global_v4(rec + kRecB1 + kmaj(64 + r, key, 128),
-                                         make_uint4(pack_bf16(-__uint_as_float(w[8 * k8]), -__uint_as_float(w[8 * k8 + 1])),
-                                                    pack_bf16(-__uint_as_float(w[8 * k8 + 2]), -__uint_as_float(w[8 * k8 + 3])),
-                                                    pack_bf16(-__uint_as_float(w[8 * k8 + 4]), -__uint_as_float(w[8 * k8 + 5])),
-                                                    pack_bf16(-__uint_as_float(w[8 * k8 + 6]), -__uint_as_float(w[8 * k8 + 7]))));
-                        }
-                    }
+                for (int b8 = 0; b8 < 8; ++b8) {
+                    const int key = 64 * half + 8 * b8 + 2 * tq;
+                    const int r0 = 16 * q4 + gq;
+                    st_global_u32(rec + kRecB1 + kmaj(64 + r0, key, 128),
+                                  pack_bf16(-__uint_as_float(w[b8][0]), -__uint_as_float(w[b8][1])));
+                    st_global_u32(rec + kRecB1 + kmaj(64 + r0 + 8, key, 128),
+                                  pack_bf16(-__uint_as_float(w[b8][2]), -__uint_as_float(w[b8][3])));
                 }
             }
             tc::fence_before();
@@ -954,22 +991,6 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
 // The o warps read O and set it back to zero before MMA-B of the next step.
 // ============================================================================
 constexpr int kChainThreads = 448;
-
-__device__ __forceinline__ void mma_ss_e(uint32_t d, uint64_t a, uint64_t b, uint32_t id,
-                                         uint32_t acc) {
-    asm volatile(
-        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
-        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(a), "l"(b), "r"(id), "r"(acc)
-        : "memory");
-}
-__device__ __forceinline__ void commit_e(uint32_t bar) {
-    asm volatile(
-        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
-        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
-            bar)
-        : "memory");
-}
 
 constexpr uint32_t kIdA = tc::idesc(128, 64, 1);       // MMA-A halves: M=128, N=64
 constexpr uint32_t kIdB = tc::idesc(128, 192, 1);      // MMA-B: M=128, N=192
@@ -1401,18 +1422,19 @@ EncodeTiledFn encode_fn() {
 }
 
 // [tokens, H, 128] row-major as a 3D tiled map (channel, head, token); a box
-// is 64 tokens x 1 head x 128 channels, rows past the end read as zero.
+// is 64 tokens x 1 head x 128 bytes of channels (64 bf16 or 32 fp32), stored
+// with 128-byte swizzling; rows past the end read as zero.
 bool encode_rows(CUtensorMap *m, const void *base, bool f32, int64_t H, int64_t tokens) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t es = f32 ? 4 : 2;
     const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(tokens)};
     const cuuint64_t strides[2] = {128 * es, static_cast<cuuint64_t>(H) * 128 * es};
-    const cuuint32_t box[3] = {128, 1, static_cast<cuuint32_t>(c64::kC)};
+    const cuuint32_t box[3] = {f32 ? 32u : 64u, 1, static_cast<cuuint32_t>(c64::kC)};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
