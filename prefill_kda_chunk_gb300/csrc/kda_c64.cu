@@ -39,7 +39,6 @@ namespace c64 {
 
 namespace {
 
-constexpr int kThreads = 320;    // 10 warps
 constexpr float kLog2e = 1.4426950408889634f;
 // |G| bound of the factored exponentials (natural-log units)
 constexpr float kFactorRange = 80.f;
@@ -54,30 +53,40 @@ enum {
     kCBOdone = 11, kCBOfree = 12, kCBTear = 13, kCBDrain = 14, kCNumBars = 15
 };
 constexpr int kCSmem = kCOffBar + kCNumBars * 8;
-// intra-chunk role
-constexpr int kIOffQ = 0, kIOffK = 16384, kIOffV = 32768, kIOffG = 49152;  // TMA tiles
-constexpr int kIOffBeta = 81920;                  // fp32 [64]
-constexpr int kIOffGA = 82944;                    // [beta K e^G ; scale Q e^G] 128 x 128 keys
-constexpr int kIOffGB = kIOffGA + 32768;          // K e^-G: 64 x 128 keys (exact form: P fp32)
-constexpr int kIOffWB = kIOffGB + 16384;          // (beta K e^G)^T: 128 keys x 64 tokens
-constexpr int kIOffUA = kIOffWB + 16384;          // (beta V)^T: 128 v x 64 tokens
-constexpr int kIOffTA = kIOffUA + 16384;          // T: 64 x 64 tokens, bf16
-constexpr int kIOffAT = kIOffTA + 8192;           // A and T, fp32 [64][68]
+// intra-chunk role (a three-stage pipeline over items, see intra_role)
+constexpr int kIOffG = 0;                         // G (base-2 cumulative log decay), fp32,
+                                                  //   4 swizzled panels of 64 rows x 32 channels
+constexpr int kIOffBeta = 32768;                  // fp32 [64]
+constexpr int kIOffGA = 33792;                    // [beta K e^G ; scale Q e^G] 128 x 128 keys
+                                                  //   (exact form: A and P staging, fp32 [128][64])
+constexpr int kIOffGB = kIOffGA + 32768;          // K e^-G: 64 x 128 keys (norm partials first)
+constexpr int kIOffWB = kIOffGB + 16384;          // (beta K e^G)^T x2: 128 keys x 64 tokens
+constexpr int kIOffUA = kIOffWB + 2 * 16384;      // (beta V)^T x2: 128 v x 64 tokens
+constexpr int kIOffTA = kIOffUA + 2 * 16384;      // T: 64 x 64 tokens, bf16
+constexpr int kIOffAT = kIOffTA + 8192;           // A^T (strict upper) and T (lower), fp32 [64][68]
 constexpr int kATStride = 68;
-constexpr int kIOffTot = kIOffAT + 64 * kATStride * 4;   // half sums [2][128], norm partials
-constexpr int kIOffRed = kIOffTot + 8192;         // [8] per-warp range flags
-constexpr int kIOffMisc = kIOffRed + 64;          // tmem base, abort, item flags
-constexpr int kIOffBar = kIOffMisc + 64;
-enum { kIBIn = 0, kIBA = 1, kIBGram = 2, kIBInv = 3, kIBWU = 4, kIBTear = 5, kIBDrain = 6,
-       kINumBars = 7 };
+constexpr int kIOffScr = kIOffAT + 64 * kATStride * 4;   // inversion scratch, 4 x 16 x 17 fp32
+constexpr int kIOffTot = kIOffScr + 4352;         // half sums [2][128] fp32
+constexpr int kIOffRed = kIOffTot + 1024;         // [8] per-warp range flags
+constexpr int kIOffMisc = kIOffRed + 64;          // tmem base, abort flag
+constexpr int kIOffQKV = 180224;                  // q, k, v tiles (TMA, 128-byte swizzled),
+                                                  //   16 KiB each: panels of 64 rows x 64 channels
+constexpr int kIOffBar = kIOffQKV + 3 * 16384;
+enum {
+    kIBGram = 0, kIBCdone = 2, kIBWU = 4, kIBFdone = 6, kIBTear = 8, kIBDrain = 9, kIBIn = 10,
+    kINumBars = 11
+};
+static_assert(kIOffMisc + 64 <= kIOffQKV, "intra shared memory layout");
 constexpr int kISmem = kIOffBar + kINumBars * 8;
+constexpr int kIThreads = 512;                    // 16 warps
 constexpr int kSmem = kCSmem > kISmem ? kCSmem : kISmem;
 static_assert(kSmem <= 227 * 1024, "shared memory");
 
 // tensor memory columns
 constexpr uint32_t kCTmemCols = 512;   // S^T [0,128), O^T [128,192), U^T [192,256),
                                        // bf16 S^T x2 [256,384), bf16 U^T [384,416)
-constexpr uint32_t kITmemCols = 256;   // Gram [0,64), W [64,192), Ut^T [192,256)
+constexpr uint32_t kITmemCols = 512;   // Gram x2 [0,128); per buffer b: W [128+192b, +128),
+                                       // Ut^T [256+192b, +64)
 
 constexpr uint32_t kIdFull = tc::idesc(128, 64, 1);    // M=128, N=64
 constexpr uint32_t kIdW = tc::idesc(64, 128, 1);       // M=64, N=128
@@ -208,7 +217,9 @@ __device__ __forceinline__ bool wait_counter(const long long *p, long long targe
 
 // ------------------------------------------------------------------ parameters
 struct Params {
-    CUtensorMap tm_q, tm_k, tm_v, tm_g;   // (128 channels, H, tokens), box (128, 1, 64)
+    CUtensorMap tm_q, tm_k, tm_v, tm_g;   // (128 channels, H, tokens), swizzled 128-byte boxes
+    const void *q, *k, *v;                // bf16 [tokens, H, 128]
+    const float *g;                       // [tokens, H, 128]
     const float *beta;                    // [tokens, H]
     const float *s0;                      // [N, H, 128, 128] or nullptr
     void *out;                            // bf16 [tokens, H, 128]
@@ -294,6 +305,19 @@ __device__ __forceinline__ void ldsm_x4_addr(uint32_t addr, uint32_t (&r)[4]) {
                  : "r"(addr));
 }
 
+__device__ __forceinline__ void stsm_x4_addr(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                             uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+__device__ __forceinline__ void stsm_x4_trans(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                              uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(addr),
+                 "r"(r0), "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
 __device__ __forceinline__ void st_global_u32(void *ptr, uint32_t v) {
     asm volatile("st.global.b32 [%0], %1;\n" ::"l"(ptr), "r"(v) : "memory");
 }
@@ -336,8 +360,19 @@ __device__ __forceinline__ void ta_put(uint8_t *ta, int r, int i, float x) {
     *reinterpret_cast<__nv_bfloat16 *>(ta + kmaj(r, i, 64)) = __float2bfloat16_rn(x);
 }
 
+// The fp32 A / T buffer (64 x 64, row stride kATStride): A (strictly lower)
+// is stored transposed in the strict upper triangle, A[R][C] at [C][R]; T
+// (unit lower triangular) in place in the lower triangle incl. the diagonal.
+// Element (r, c) of 16 x 16 block (I, J):
+__device__ __forceinline__ float a_blk(const float *at, int I, int J, int r, int c) {
+    return at[(16 * J + c) * kATStride + 16 * I + r];
+}
+__device__ __forceinline__ float t_blk(const float *at, int I, int J, int r, int c) {
+    return (I > J || r >= c) ? at[(16 * I + r) * kATStride + 16 * J + c] : 0.f;
+}
+
 // Forward substitution of one 16 x 16 diagonal block (warp w, lanes 0-15
-// each solve one column), in place in the fp32 A/T buffer, and in bf16 to TA.
+// each solve one column): T to the lower part of the block and in bf16 to TA.
 __device__ __forceinline__ void invert_diag(float *at, uint8_t *ta, int w, int lane) {
     const int j = lane & 15, b = 16 * w;
     float t[16];
@@ -346,29 +381,19 @@ __device__ __forceinline__ void invert_diag(float *at, uint8_t *ta, int w, int l
         // four independent partial sums keep the dependent chain short
         float s4[4] = {(r == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < r; ++i) s4[i & 3] = fmaf(-at[(b + r) * kATStride + b + i], t[i], s4[i & 3]);
+        for (int i = 0; i < r; ++i)
+            s4[i & 3] = fmaf(-at[(b + i) * kATStride + b + r], t[i], s4[i & 3]);
         t[r] = (s4[0] + s4[1]) + (s4[2] + s4[3]);
     }
     __syncwarp();
     if (lane < 16) {
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-            at[(b + r) * kATStride + b + j] = t[r];
+            if (r >= j) at[(b + r) * kATStride + b + j] = t[r];
             ta_put(ta, b + r, b + j, t[r]);
         }
     }
     __syncwarp();
-}
-
-// Element (r, c) of block (I, J) of A or T in the shared fp32 buffer: A's
-// strictly lower blocks in place, T's diagonal blocks in place of A's, T's
-// blocks below the diagonal stored transposed in the upper triangle.
-__device__ __forceinline__ float a_blk(const float *at, int I, int J, int r, int c) {
-    return at[(16 * I + r) * kATStride + 16 * J + c];
-}
-__device__ __forceinline__ float t_blk(const float *at, int I, int J, int r, int c) {
-    return I == J ? at[(16 * I + r) * kATStride + 16 * J + c]
-                  : at[(16 * J + c) * kATStride + 16 * I + r];
 }
 
 // acc (16 x 16, two m16n8 fragments) += A(I,K) * T(K,J)
@@ -390,8 +415,8 @@ __device__ __forceinline__ void blk_mma(float (&acc)[2][4], const float *at, int
     }
 }
 
-// T(I,J) = -T(I,I) * X where X (16 x 16, fragments) is staged in scratch;
-// to the fp32 buffer (transposed) and in bf16 to TA.
+// T(I,J) = -T(I,I) * X where X (16 x 16, fragments) is staged in scratch; to
+// the lower part of the fp32 buffer and in bf16 to TA.
 __device__ __forceinline__ void finish_blk(float *at, uint8_t *ta, float *scratch,
                                            const float (&x)[2][4], int I, int J, int lane) {
     const int g = lane >> 2, t = lane & 3;
@@ -420,10 +445,12 @@ __device__ __forceinline__ void finish_blk(float *at, uint8_t *ta, float *scratc
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
         const int c0 = 8 * nt + 2 * t;
-        at[(16 * J + c0) * kATStride + 16 * I + g] = -acc[nt][0];
-        at[(16 * J + c0 + 1) * kATStride + 16 * I + g] = -acc[nt][1];
-        at[(16 * J + c0) * kATStride + 16 * I + g + 8] = -acc[nt][2];
-        at[(16 * J + c0 + 1) * kATStride + 16 * I + g + 8] = -acc[nt][3];
+        float *row0 = at + (16 * I + g) * kATStride + 16 * J + c0;
+        float *row1 = at + (16 * I + g + 8) * kATStride + 16 * J + c0;
+        row0[0] = -acc[nt][0];
+        row0[1] = -acc[nt][1];
+        row1[0] = -acc[nt][2];
+        row1[1] = -acc[nt][3];
         *reinterpret_cast<uint32_t *>(ta + kmaj(16 * I + g, 16 * J + c0, 64)) =
             pack_bf16(-acc[nt][0], -acc[nt][1]);
         *reinterpret_cast<uint32_t *>(ta + kmaj(16 * I + g + 8, 16 * J + c0, 64)) =
@@ -432,41 +459,40 @@ __device__ __forceinline__ void finish_blk(float *at, uint8_t *ta, float *scratc
     __syncwarp();
 }
 
-// T = (I + A)^{-1} for the 64 x 64 strictly lower A in `at` (warps 0-3 of
-// the compute group; the caller synchronises the group before and after).
-// T goes to `at` (fp32, blocks below the diagonal transposed) and to TA (bf16,
-// blocks above the diagonal are zero).
-__device__ __forceinline__ void invert64(float *at, uint8_t *ta, float *scratch, int warp,
-                                         int lane) {
-    // zero TA's blocks above the diagonal: (I, J) with J > I, 6 blocks of 16 x 16
-    for (int x = threadIdx.x; x < 6 * 32; x += 128) {
+// T = (I + A)^{-1} for the 64 x 64 strictly lower A held transposed in `at`
+// (four warps; named barrier `bar_id` over their 128 threads; the caller
+// synchronises them before and after). T goes to the lower part of `at`
+// (fp32) and to TA (bf16; the blocks above the diagonal are zero).
+__device__ __forceinline__ void invert64(float *at, uint8_t *ta, float *scratch, int w, int lane,
+                                         int bar_id) {
+    for (int x = 32 * w + lane; x < 6 * 32; x += 128) {
         const int blk = x >> 5, piece = x & 31;           // 32 pieces of 16 bytes per block
         const int I = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
         const int J = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
         const int r = 16 * I + (piece >> 1), c8 = 16 * J + 8 * (piece & 1);
         *reinterpret_cast<uint4 *>(ta + kmaj(r, c8, 64)) = make_uint4(0, 0, 0, 0);
     }
-    invert_diag(at, ta, warp, lane);
-    named_sync(2, 128);
+    invert_diag(at, ta, w, lane);
+    named_sync(bar_id, 128);
     // level 1: T(I, I-1) for I = 1..3 on warps 0..2
-    if (warp < 3) {
-        const int I = warp + 1;
+    if (w < 3) {
+        const int I = w + 1;
         float x[2][4] = {};
         blk_mma(x, at, I, I - 1, I - 1, lane);
-        finish_blk(at, ta, scratch + warp * 16 * 17, x, I, I - 1, lane);
+        finish_blk(at, ta, scratch + w * 16 * 17, x, I, I - 1, lane);
     }
-    named_sync(2, 128);
+    named_sync(bar_id, 128);
     // level 2: T(I, I-2) for I = 2, 3 on warps 0, 1
-    if (warp < 2) {
-        const int I = warp + 2;
+    if (w < 2) {
+        const int I = w + 2;
         float x[2][4] = {};
         blk_mma(x, at, I, I - 2, I - 2, lane);
         blk_mma(x, at, I, I - 1, I - 2, lane);
-        finish_blk(at, ta, scratch + warp * 16 * 17, x, I, I - 2, lane);
+        finish_blk(at, ta, scratch + w * 16 * 17, x, I, I - 2, lane);
     }
-    named_sync(2, 128);
+    named_sync(bar_id, 128);
     // level 3: T(3, 0) on warp 0
-    if (warp == 0) {
+    if (w == 0) {
         float x[2][4] = {};
         blk_mma(x, at, 3, 0, 0, lane);
         blk_mma(x, at, 3, 1, 0, lane);
@@ -475,6 +501,26 @@ __device__ __forceinline__ void invert64(float *at, uint8_t *ta, float *scratch,
     }
 }
 
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+
+// Intra-chunk role, a three-stage pipeline over this CTA's items (16 warps):
+//   warps 0-7  (builders): cumulative log decay and the gated operand tiles of
+//              item n + 1 (inputs read from L2, prefetched by TMA one item
+//              ahead), the record's Q e^G, Kd, gamma, then the Gram MMA; the
+//              exact per-pair A and P of strongly decaying chunks instead go
+//              straight to the Gram's tensor memory;
+//   warps 8-11 (solvers): A and P of item n out of tensor memory, P to the
+//              record, T = (I + A)^{-1}, then the W and Ut MMAs; TMEM owner;
+//   warps 12-15 (writers): Ut^T and -W of item n - 1 to the record.
+// Double-buffered (by item parity): the Gram's tensor memory, the W / Ut
+// accumulators and the WB / UA operand tiles. One elected lane of warp 0
+// (Gram) and of warp 8 (W, Ut) issues the MMAs.
 template <bool PRE>
 __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nworkers) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -484,15 +530,16 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
     auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kIOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + kIOffMisc + 4);
-    volatile int *item_exact = reinterpret_cast<volatile int *>(smem + kIOffMisc + 8);
     if (tid == 0) {
-        mbar_init(bar(kIBIn), 1);
-        mbar_init(bar(kIBA), 8);
-        mbar_init(bar(kIBGram), 1);
-        mbar_init(bar(kIBInv), 8);
-        mbar_init(bar(kIBWU), 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(kIBGram + b), 1);
+            mbar_init(bar(kIBCdone + b), 4);
+            mbar_init(bar(kIBWU + b), 1);
+            mbar_init(bar(kIBFdone + b), 4);
+        }
         mbar_init(bar(kIBTear), blockDim.x / 32);
-        mbar_init(bar(kIBDrain), 1);
+        mbar_init(bar(kIBDrain), 2);
+        mbar_init(bar(kIBIn), 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -506,6 +553,7 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
     const uint32_t tmem = *tmem_slot;
     const bool skip = p.cu != nullptr && (*p.call_flags & kErrBadCu);
     const int64_t items = skip ? 0 : p.max_chunks * H;
+    const int64_t rowe = static_cast<int64_t>(H) * 128;   // elements between tokens
 
     // next item of this worker at or after `item` that holds a real chunk
     auto next_real = [&](int64_t item) {
@@ -517,79 +565,54 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
         }
         return item;
     };
+    // per-buffer barrier parity of item m (phases complete every second item)
+    auto pb = [](int m) { return static_cast<uint32_t>((m >> 1) & 1); };
 
-    if (warp == 8) {
-        // ================================================ TMA loads and MMA issue (whole warp,
-        // one elected lane issues)
-        int it = 0, loads = 0;
-        auto issue_loads = [&](int64_t itm) {
-            const int64_t c = itm / H;
-            const int h = static_cast<int>(itm - c * H);
-            int n, L;
-            int64_t t0;
-            locate(p, c, n, t0, L);
-            arrive_tx_e(bar(kIBIn), 3 * 16384 + 32768);
-            const int z = static_cast<int>(t0);
+    // TMA prefetch of an item's gate boxes into L2 (one lane)
+    auto prefetch = [&](int64_t itm) {
+        if (itm >= items) return;
+        int n, L;
+        int64_t t0;
+        const int64_t c = itm / H;
+        const int h = static_cast<int>(itm - c * H);
+        locate(p, c, n, t0, L);
+        const int z = static_cast<int>(t0);
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                tma_load_3d_e(sb + kIOffQ + 8192 * x, &p.tm_q, 64 * x, h, z, bar(kIBIn));
-                tma_load_3d_e(sb + kIOffK + 8192 * x, &p.tm_k, 64 * x, h, z, bar(kIBIn));
-                tma_load_3d_e(sb + kIOffV + 8192 * x, &p.tm_v, 64 * x, h, z, bar(kIBIn));
-            }
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-                tma_load_3d_e(sb + kIOffG + 8192 * x, &p.tm_g, 32 * x, h, z, bar(kIBIn));
-            ++loads;
-        };
-        const uint64_t dGA = tc::sdesc(sb + kIOffGA, 128, 2048), dGB = tc::sdesc(sb + kIOffGB, 128, 2048);
-        const uint64_t dTA = tc::sdesc(sb + kIOffTA, 128, 1024), dWB = tc::sdesc(sb + kIOffWB, 128, 1024);
-        const uint64_t dUA = tc::sdesc(sb + kIOffUA, 128, 1024);
-        int64_t item = next_real(worker);
-        if (item < items) issue_loads(item);
-        for (; item < items; ++it) {
-            // phase A done: operand tiles written, input tiles free
-            if (!wait_bar(bar(kIBA), it & 1, abort_flag, p.err)) break;
-            __syncwarp();
-            const bool exact = *item_exact != 0;
-            const int64_t next = next_real(item + nworkers);
-            if (!exact) {
-                tc::fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss_e(tmem + 0, dGA + 16 * kk, dGB + 16 * kk, kIdFull, kk > 0);
-                commit_e(bar(kIBGram));
-                if (next < items) issue_loads(next);
-            }
-            // T ready (the exact form also read the input tiles until now)
-            if (!wait_bar(bar(kIBInv), it & 1, abort_flag, p.err)) break;
-            __syncwarp();
-            if (exact && next < items) issue_loads(next);
-            tc::fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)   // W = T (beta K e^G): M = 64, N = 128 keys, K = 64 tokens
-                mma_ss_e(tmem + 64, dTA + 16 * kk, dWB + 16 * kk, kIdW, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)   // Ut^T = (beta V)^T T^T: M = 128 v, N = 64, K = 64
-                mma_ss_e(tmem + 192, dUA + 16 * kk, dTA + 16 * kk, kIdFull, kk > 0);
-            commit_e(bar(kIBWU));
-            item = next;
-        }
-        // drain: the last input load and every MMA issued have completed
-        if (loads > 0) wait_bar(bar(kIBIn), (loads - 1) & 1, abort_flag, p.err);
-        commit_e(bar(kIBDrain));
-        wait_bar(bar(kIBDrain), 0, abort_flag, p.err);
-    } else if (warp < 8) {
-        // ================================================ compute warps (256 threads)
+        for (int x = 0; x < 4; ++x) tma_prefetch_3d(&p.tm_g, 32 * x, h, z);
+    };
+
+    if (warp < 8) {
+        // ================================================ builders (256 threads)
         const int ct = tid;                 // 0..255
         const int gq = lane >> 2, tq = lane & 3;   // fragment row / column pair
         float *tot = reinterpret_cast<float *>(smem + kIOffTot);   // [2][128] half sums
         int *red = reinterpret_cast<int *>(smem + kIOffRed);
-        float *at = reinterpret_cast<float *>(smem + kIOffAT);
-        uint8_t *ta = smem + kIOffTA;
         float *betas = reinterpret_cast<float *>(smem + kIOffBeta);
         float *gs = reinterpret_cast<float *>(smem + kIOffG);
-        int it = 0;
-        for (int64_t item = next_real(worker); item < items; item = next_real(item + nworkers)) {
+        const __nv_bfloat16 *qg_ = static_cast<const __nv_bfloat16 *>(p.q);
+        const __nv_bfloat16 *kg_ = static_cast<const __nv_bfloat16 *>(p.k);
+        int it = 0, issued = 0;   // issued: input loads started (warp 0)
+        if (warp == 0) {
+            const int64_t first = next_real(worker);
+            if (first < items) {
+                int n2, L2;
+                int64_t t02;
+                const int64_t c2 = first / H;
+                const int h2 = static_cast<int>(first - c2 * H);
+                locate(p, c2, n2, t02, L2);
+                arrive_tx_e(bar(kIBIn), 3 * 16384);
+                const int z = static_cast<int>(t02);
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    tma_load_3d_e(sb + kIOffQKV + 8192 * x, &p.tm_q, 64 * x, h2, z, bar(kIBIn));
+                    tma_load_3d_e(sb + kIOffQKV + 16384 + 8192 * x, &p.tm_k, 64 * x, h2, z, bar(kIBIn));
+                    tma_load_3d_e(sb + kIOffQKV + 32768 + 8192 * x, &p.tm_v, 64 * x, h2, z, bar(kIBIn));
+                }
+                ++issued;
+            }
+        }
+        for (int64_t item = next_real(worker); item < items; item = next_real(item + nworkers), ++it) {
+            const int b = it & 1;
             const int64_t c = item / H;
             const int h = static_cast<int>(item - c * H);
             int n, L;
@@ -597,33 +620,85 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
             locate(p, c, n, t0, L);
             (void)n;
             uint8_t *rec = record_of(p, c, h);
+            const int64_t base = t0 * rowe + static_cast<int64_t>(h) * 128;   // element of (t0, h, 0)
+            if (ct == 0) {
+                if (it == 0) prefetch(item);
+                prefetch(next_real(item + nworkers));
+            }
             // ring form: the slot's previous record must have been copied out
             if (p.ring_depth > 0 && ct == 0 && c >= p.ring_depth)
                 wait_counter(p.consumed + h, c - p.ring_depth + 1, abort_flag, p.err);
             if (ct < kC) betas[ct] = ct < L ? __ldg(p.beta + (t0 + ct) * H + h) : 0.f;
-            wait_bar(bar(kIBIn), it & 1, abort_flag, p.err);
 
-            // ---- cumulative log decay (base 2), in place in the g tile: thread =
-            //      channel ct % 128, tokens [32 half, 32 half + 32); the second half
-            //      adds the first half's sum
+            // ---- q, k, v fragments (thread (gq, tq) of warp w: rows 8 tb + gq, channels
+            //      16 w + 8 cw + 2 tq and + 1) from the TMA tiles; the tiles are then
+            //      free for the next item's loads
+            uint32_t qf[8][2], kf[8][2], vf[8][2];
+            wait_bar(bar(kIBIn), it & 1, abort_flag, p.err);
+            {
+                // ldmatrix x4: matrices (tb, cw) for tb = 2 tbp + (lane >> 4), cw = (lane >> 3) & 1
+                const uint32_t lm = sb + kIOffQKV + sw_bf16(lane & 7, 16 * warp + 8 * ((lane >> 3) & 1)) +
+                                    1024 * (lane >> 4);
+#pragma unroll
+                for (int tbp = 0; tbp < 4; ++tbp) {
+                    uint32_t r[4];
+                    ldsm_x4_addr(lm + 2048 * tbp, r);
+                    qf[2 * tbp][0] = r[0]; qf[2 * tbp][1] = r[1];
+                    qf[2 * tbp + 1][0] = r[2]; qf[2 * tbp + 1][1] = r[3];
+                    ldsm_x4_addr(lm + 16384 + 2048 * tbp, r);
+                    kf[2 * tbp][0] = r[0]; kf[2 * tbp][1] = r[1];
+                    kf[2 * tbp + 1][0] = r[2]; kf[2 * tbp + 1][1] = r[3];
+                    ldsm_x4_addr(lm + 32768 + 2048 * tbp, r);
+                    vf[2 * tbp][0] = r[0]; vf[2 * tbp][1] = r[1];
+                    vf[2 * tbp + 1][0] = r[2]; vf[2 * tbp + 1][1] = r[3];
+                }
+                // rows past the sequence end count as zero
+#pragma unroll
+                for (int tb = 0; tb < 8; ++tb)
+                    if (8 * tb + gq >= L) {
+                        qf[tb][0] = qf[tb][1] = kf[tb][0] = kf[tb][1] = vf[tb][0] = vf[tb][1] = 0u;
+                    }
+            }
+            named_sync(1, 256);
+            if (warp == 0) {
+                const int64_t nxt = next_real(item + nworkers);
+                if (nxt < items) {
+                    int n2, L2;
+                    int64_t t02;
+                    const int64_t c2 = nxt / H;
+                    const int h2 = static_cast<int>(nxt - c2 * H);
+                    locate(p, c2, n2, t02, L2);
+                    arrive_tx_e(bar(kIBIn), 3 * 16384);
+                    const int z = static_cast<int>(t02);
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        tma_load_3d_e(sb + kIOffQKV + 8192 * x, &p.tm_q, 64 * x, h2, z, bar(kIBIn));
+                        tma_load_3d_e(sb + kIOffQKV + 16384 + 8192 * x, &p.tm_k, 64 * x, h2, z, bar(kIBIn));
+                        tma_load_3d_e(sb + kIOffQKV + 32768 + 8192 * x, &p.tm_v, 64 * x, h2, z, bar(kIBIn));
+                    }
+                    ++issued;
+                }
+            }
+
+            // ---- cumulative log decay (base 2) into the G tile: thread = channel
+            //      ct % 128, tokens [32 half, 32 half + 32); the second half adds the
+            //      first half's sum
             float gmax = 0.f;
             bool anypos = false;
             {
                 const int ch = ct & 127, th = ct >> 7;
-                // rows 8 k + j of this half: the swizzle term depends on j only
                 const uint32_t o0 = sw_f32(32 * th, ch);
                 float x[32];
 #pragma unroll
                 for (int r = 0; r < 32; ++r) {
-                    const uint32_t o = o0 + (r >> 3) * 1024 + (r & 7) * 128 +
-                                       ((((ch & 31) >> 2) ^ (r & 7)) - ((ch & 31) >> 2)) * 16;
-                    x[r] = *reinterpret_cast<const float *>(reinterpret_cast<const uint8_t *>(gs) + o);
+                    const int t = 32 * th + r;
+                    x[r] = t < L ? __ldg(p.g + base + t * rowe + ch) : 0.f;
                 }
                 float run = 0.f;
 #pragma unroll
                 for (int r = 0; r < 32; ++r) {
                     const int t = 32 * th + r;
-                    float xv = t < L ? x[r] : 0.f;
+                    float xv = x[r];
                     if (PRE && (p.pre & kPreGateLogits) && t < L) xv = log_sigmoid(xv);
                     anypos |= xv > 0.f;
                     run = fmaf(xv, kLog2e, run);
@@ -646,16 +721,19 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
                 const bool pos = __any_sync(0xffffffffu, anypos);
                 const float lim = pos ? 0.5f * kFactorRange * kLog2e : kFactorRange * kLog2e;
                 const unsigned any_bad = __ballot_sync(0xffffffffu, !(gmax <= lim));
-                if (lane == 0) red[warp] = (any_bad != 0) | (pos ? 2 : 0);
+                if (lane == 0) red[warp] = any_bad != 0;
             }
+            // the operand tiles are free: GA / GB once the Gram of item it - 1 is
+            // done, WB / UA of buffer b once the W / Ut MMAs of item it - 2 are
+            if (it >= 1) wait_bar(bar(kIBGram + (b ^ 1)), pb(it - 1), abort_flag, p.err);
+            if (it >= 2) wait_bar(bar(kIBWU + b), pb(it - 2), abort_flag, p.err);
+            tc::fence_after();
             named_sync(1, 256);
             bool exact = false;
 #pragma unroll
-            for (int w = 0; w < 8; ++w) exact |= (red[w] & 1) != 0;
+            for (int w = 0; w < 8; ++w) exact |= red[w] != 0;
 
-            // ---- gated operand tiles and the record's Qg, Kd, gamma (fragment layout:
-            //      warp w owns channels [16 w, 16 w + 16), thread (gq, tq) the rows
-            //      8 tb + gq and channel pairs 2 tq of each 8 x 8 core matrix)
+            // ---- gated operand tiles and the record's Qg, Kd, gamma
             const bool norm = PRE && (p.pre & kPreNormQK);
             float glast[2][2], egl[2][2];
 #pragma unroll
@@ -673,32 +751,29 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
                     *reinterpret_cast<float2 *>(rec + kRecGam + ch * 4) = make_float2(egl[cw][0], egl[cw][1]);
                 }
             }
-            // row norms (over the 128 channels) for in-kernel q / k normalisation
-            // need the whole row: done per row by the 32 threads... only when asked
             float rq[8], rk[8];
 #pragma unroll
             for (int tb = 0; tb < 8; ++tb) { rq[tb] = 1.f; rk[tb] = 1.f; }
             if (norm) {
-                // each warp sums its 16 channels of every row; the 8 partials of a row
-                // meet in shared memory (the half-sum area is free again)
-                float *part = tot + 256;   // [2][64][8]
+                // row norms over the 128 channels: each warp's 16-channel partial
+                // sums meet in the GB tile (written only after this)
+                float *part = reinterpret_cast<float *>(smem + kIOffGB);   // [2][64][8]
 #pragma unroll
                 for (int tb = 0; tb < 8; ++tb) {
-                    if (lane < 16) {
-                        const int r = 8 * tb + (lane & 7), which = lane >> 3;   // 0: q, 1: k
-                        const uint8_t *tile = smem + (which ? kIOffK : kIOffQ);
-                        float ss = 0.f;
+                    float sq = 0.f, sk = 0.f;
 #pragma unroll
-                        for (int c8 = 0; c8 < 2; ++c8) {
-                            const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw_bf16(r, 16 * warp + 8 * c8));
-                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = unpack_bf16(w4[e]);
-                                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
-                            }
-                        }
-                        part[(which * 64 + r) * 8 + warp] = ss;
+                    for (int cw = 0; cw < 2; ++cw) {
+                        const float2 q2 = unpack_bf16(qf[tb][cw]), k2 = unpack_bf16(kf[tb][cw]);
+                        sq = fmaf(q2.x, q2.x, fmaf(q2.y, q2.y, sq));
+                        sk = fmaf(k2.x, k2.x, fmaf(k2.y, k2.y, sk));
+                    }
+                    sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+                    sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+                    sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+                    sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+                    if (tq == 0) {
+                        part[(8 * tb + gq) * 8 + warp] = sq;
+                        part[(64 + 8 * tb + gq) * 8 + warp] = sk;
                     }
                 }
                 named_sync(1, 256);
@@ -714,36 +789,33 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
                     rq[tb] = rsqrtf(sq + kNormEps);
                     rk[tb] = rsqrtf(sk + kNormEps);
                 }
+                named_sync(1, 256);
             }
-            // loop-invariant parts of the addresses: row 8 tb + gq of a tile sits
+            // loop-invariant parts of the addresses: row 8 tb + gq of the G tile sits
             // tb * 1024 bytes after row gq (the swizzle depends on the row mod 8)
             const uint32_t g_off0 = sw_f32(gq, 16 * warp + 2 * tq);
             const uint32_t g_off1 = sw_f32(gq, 16 * warp + 8 + 2 * tq);
-            const uint32_t lm_off = sw_bf16(lane & 7, 16 * warp + 8 * ((lane >> 3) & 1)) +
-                                    1024 * (lane >> 4);
             const uint32_t o_tk0 = kmaj(0, 16 * warp, 128) + gq * 16 + tq * 4;   // + tb 2048 + cw 128
             const uint32_t o_kt0 = kmaj(16 * warp, 0, 64) + gq * 16 + tq * 4;    // + cw 1024 + tb 128
-            uint8_t *const sGA = smem + kIOffGA + o_tk0, *const sGB = smem + kIOffGB + o_tk0;
-            uint8_t *const sWB = smem + kIOffWB + o_kt0, *const sUA = smem + kIOffUA + o_kt0;
             uint8_t *const gB1 = rec + kRecB1 + o_tk0, *const gB2 = rec + kRecB2 + o_kt0;
             const float *const beta_r = betas + gq;
             const float sc = p.scale;
+            // stmatrix row addresses: matrix m = lane >> 3 of a group of four is
+            // (tb = 2 tbp + (m >> 1), cw = m & 1), row j = lane & 7
+            const int mq = lane >> 3, jr = lane & 7;
+            const uint32_t st_tk = sb + kmaj(0, 16 * warp, 128) + 2048 * (mq >> 1) + 128 * (mq & 1) + 16 * jr;
+            const uint32_t st_kt = sb + kmaj(16 * warp, 0, 64) + 128 * (mq >> 1) + 1024 * (mq & 1) + 16 * jr;
 #pragma unroll
             for (int tbp = 0; tbp < 4; ++tbp) {
-                // ldmatrix x4: matrices (tb, cw) for tb = 2 tbp, 2 tbp + 1 and cw = 0, 1
-                uint32_t qf[4], kf[4], vf[4];
-                ldsm_x4_addr(sb + kIOffQ + lm_off + 2048 * tbp, qf);
-                ldsm_x4_addr(sb + kIOffK + lm_off + 2048 * tbp, kf);
-                ldsm_x4_addr(sb + kIOffV + lm_off + 2048 * tbp, vf);
+                uint32_t ukb4[4], uqg4[4], ukn4[4], ubv4[4];
 #pragma unroll
                 for (int m = 0; m < 4; ++m) {
                     const int tb = 2 * tbp + (m >> 1), cw = m & 1;
-                    const bool real = 8 * tb + gq < L;
                     const float2 g2 = *reinterpret_cast<const float2 *>(
                         reinterpret_cast<const uint8_t *>(gs) + (cw ? g_off1 : g_off0) + 1024 * tb);
                     const float br = beta_r[8 * tb];
-                    float2 q2 = unpack_bf16(qf[m]), k2 = unpack_bf16(kf[m]), v2 = unpack_bf16(vf[m]);
-                    if (!real) { q2 = make_float2(0.f, 0.f); k2 = q2; }
+                    float2 q2 = unpack_bf16(qf[tb][cw]), k2 = unpack_bf16(kf[tb][cw]);
+                    float2 v2 = unpack_bf16(vf[tb][cw]);
                     if (norm) {
                         q2.x *= rq[tb]; q2.y *= rq[tb];
                         k2.x *= rk[tb]; k2.y *= rk[tb];
@@ -761,83 +833,44 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
                         kd = make_float2(k2.x * ex2f(glast[cw][0] - g2.x), k2.y * ex2f(glast[cw][1] - g2.y));
                     }
                     mul2(bv.x, bv.y, br, br);
-                    const uint32_t uqg = pack_bf16(qg.x, qg.y), ukb = pack_bf16(kb.x, kb.y);
-                    const uint32_t ukn = pack_bf16(kn.x, kn.y), ukd = pack_bf16(kd.x, kd.y);
-                    const uint32_t ubv = pack_bf16(bv.x, bv.y);
-                    // [tok][key] core matrices: GA rows 0-63 (beta K e^G) and 64-127
-                    // (scale Q e^G), GB (K e^-G); record B1 rows 0-63 (scale Q e^G)
-                    const int otk = 2048 * tb + 128 * cw;
-                    *reinterpret_cast<uint32_t *>(sGA + otk) = ukb;
-                    *reinterpret_cast<uint32_t *>(sGA + 16384 + otk) = uqg;
-                    *reinterpret_cast<uint32_t *>(sGB + otk) = ukn;
-                    st_global_u32(gB1 + otk, uqg);
-                    // [key][tok] core matrices (transposed): WB, UA; record B2 (Kd^T)
-                    const int okt = 1024 * cw + 128 * tb;
-                    *reinterpret_cast<uint32_t *>(sWB + okt) = movt(ukb);
-                    *reinterpret_cast<uint32_t *>(sUA + okt) = movt(ubv);
-                    st_global_u32(gB2 + okt, movt(ukd));
+                    uqg4[m] = pack_bf16(qg.x, qg.y);
+                    ukb4[m] = pack_bf16(kb.x, kb.y);
+                    ukn4[m] = pack_bf16(kn.x, kn.y);
+                    ubv4[m] = pack_bf16(bv.x, bv.y);
+                    const uint32_t ukd = pack_bf16(kd.x, kd.y);
+                    // record B1 rows 0-63 (scale Q e^G) and B2 (Kd^T), straight from the fragments
+                    st_global_u32(gB1 + 2048 * tb + 128 * cw, uqg4[m]);
+                    st_global_u32(gB2 + 1024 * cw + 128 * tb, movt(ukd));
                 }
+                // [tok][key] core matrices: GA rows 0-63 (beta K e^G) and 64-127
+                // (scale Q e^G), GB (K e^-G); transposed: WB, UA
+                stsm_x4_addr(st_tk + kIOffGA + 4096 * tbp, ukb4[0], ukb4[1], ukb4[2], ukb4[3]);
+                stsm_x4_addr(st_tk + kIOffGA + 16384 + 4096 * tbp, uqg4[0], uqg4[1], uqg4[2], uqg4[3]);
+                stsm_x4_addr(st_tk + kIOffGB + 4096 * tbp, ukn4[0], ukn4[1], ukn4[2], ukn4[3]);
+                stsm_x4_trans(st_kt + kIOffWB + 16384 * b + 256 * tbp, ukb4[0], ukb4[1], ukb4[2], ukb4[3]);
+                stsm_x4_trans(st_kt + kIOffUA + 16384 * b + 256 * tbp, ubv4[0], ubv4[1], ubv4[2], ubv4[3]);
             }
-            if (ct == 0) *item_exact = exact ? 1 : 0;
-            fence_async_smem();
-            tc::fence_before();
-            named_sync(1, 256);
-            if (lane == 0) mbar_arrive(bar(kIBA));
-
-            // ---- A (fp32, for the inversion) and P (to the record)
-            if (!exact) {
-                wait_bar(bar(kIBGram), it & 1, abort_flag, p.err);
-                tc::fence_after();
-                const int q4 = warp & 3, half = warp >> 2;
-                const int row = 32 * q4 + lane;    // Gram row: 0-63 A rows, 64-127 P rows
-                uint32_t d[32];
-                tld32(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 32 * half, d);
-                tc::ld_wait();
-                if (row < 64) {
-                    const int r = row;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int i = 32 * half + j;
-                        at[r * kATStride + i] = (i < r) ? __uint_as_float(d[j]) : 0.f;
-                    }
-                } else {
-                    const int r = row - 64;
-#pragma unroll
-                    for (int g8 = 0; g8 < 4; ++g8) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int i0 = 32 * half + 8 * g8 + 2 * e;
-                            const float v0 = (i0 <= r) ? __uint_as_float(d[8 * g8 + 2 * e]) : 0.f;
-                            const float v1 =
-                                (i0 + 1 <= r) ? __uint_as_float(d[8 * g8 + 2 * e + 1]) : 0.f;
-                            w4[e] = pack_bf16(v0, v1);
-                        }
-                        st_global_v4(rec + kRecB3 + kmaj(r, 32 * half + 8 * g8, 64),
-                                     make_uint4(w4[0], w4[1], w4[2], w4[3]));
-                    }
-                }
-                tc::fence_before();
-            } else {
-                // exact per-pair exponentials: 8 threads per row pair (rp, 63 - rp),
-                // pairs (r, i <= r) with i = sub (mod 8)
-                const uint8_t *qs = smem + kIOffQ, *ks = smem + kIOffK;
-                float *pf = reinterpret_cast<float *>(smem + kIOffGB);   // P fp32 [64][64]
-                // inverse row norms of q (0..63) and k (64..127) when normalising
-                float *rn = tot;
+            if (exact) {
+                // exact per-pair exponentials into the fp32 staging (the GA tile,
+                // [128][64]: rows 0-63 A, 64-127 P), then into the Gram's tensor
+                // memory (buffer b, free once the solvers read item it - 2)
+                named_sync(1, 256);
+                float *stg = reinterpret_cast<float *>(smem + kIOffGA);
+                float *rn = tot;   // inverse row norms: q 0..63, k 64..127
                 if (ct < 128) {
                     float x = 1.f;
                     if (norm) {
-                        const uint8_t *tile = ct < 64 ? qs : ks;
-                        const int r = ct & 63;
+                        const __nv_bfloat16 *src = (ct < 64 ? qg_ : kg_) + base + (ct & 63) * rowe;
                         float ss = 0.f;
-                        for (int c8 = 0; c8 < 16; ++c8) {
-                            const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw_bf16(r, 8 * c8));
-                            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+                        if ((ct & 63) < L) {
+                            for (int c8 = 0; c8 < 16; ++c8) {
+                                const uint4 u = __ldg(reinterpret_cast<const uint4 *>(src + 8 * c8));
+                                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = unpack_bf16(w4[e]);
-                                ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 f = unpack_bf16(w4[e]);
+                                    ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+                                }
                             }
                         }
                         x = rsqrtf(ss + kNormEps);
@@ -851,125 +884,225 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
                     const int r = side == 0 ? rp : 63 - rp;
                     for (int i = sub; i <= r; i += 8) {
                         float sa = 0.f, sp = 0.f;
-                        for (int c8 = 0; c8 < 16; ++c8) {
-                            const uint4 kr = *reinterpret_cast<const uint4 *>(ks + sw_bf16(r, 8 * c8));
-                            const uint4 qr = *reinterpret_cast<const uint4 *>(qs + sw_bf16(r, 8 * c8));
-                            const uint4 ki = *reinterpret_cast<const uint4 *>(ks + sw_bf16(i, 8 * c8));
-                            const uint32_t krw[4] = {kr.x, kr.y, kr.z, kr.w};
-                            const uint32_t qrw[4] = {qr.x, qr.y, qr.z, qr.w};
-                            const uint32_t kiw[4] = {ki.x, ki.y, ki.z, ki.w};
+                        if (r < L) {
+                            for (int c8 = 0; c8 < 16; ++c8) {
+                                const uint4 kr = __ldg(reinterpret_cast<const uint4 *>(kg_ + base + r * rowe + 8 * c8));
+                                const uint4 qr = __ldg(reinterpret_cast<const uint4 *>(qg_ + base + r * rowe + 8 * c8));
+                                const uint4 ki = __ldg(reinterpret_cast<const uint4 *>(kg_ + base + i * rowe + 8 * c8));
+                                const uint32_t krw[4] = {kr.x, kr.y, kr.z, kr.w};
+                                const uint32_t qrw[4] = {qr.x, qr.y, qr.z, qr.w};
+                                const uint32_t kiw[4] = {ki.x, ki.y, ki.z, ki.w};
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 a = unpack_bf16(krw[e]), bq = unpack_bf16(qrw[e]),
-                                             cc = unpack_bf16(kiw[e]);
-                                const int ch = 8 * c8 + 2 * e;
-                                const float2 gr = *reinterpret_cast<const float2 *>(
-                                    reinterpret_cast<const uint8_t *>(gs) + sw_f32(r, ch));
-                                const float2 gi = *reinterpret_cast<const float2 *>(
-                                    reinterpret_cast<const uint8_t *>(gs) + sw_f32(i, ch));
-                                const float x0 = gr.x - gi.x, x1 = gr.y - gi.y;
-                                overflow |= x0 > kFactorRange * kLog2e || x1 > kFactorRange * kLog2e;
-                                const float e0 = ex2f(x0), e1 = ex2f(x1);
-                                sa = fmaf(a.x * cc.x, e0, sa);
-                                sa = fmaf(a.y * cc.y, e1, sa);
-                                sp = fmaf(bq.x * cc.x, e0, sp);
-                                sp = fmaf(bq.y * cc.y, e1, sp);
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 a = unpack_bf16(krw[e]), bq = unpack_bf16(qrw[e]),
+                                                 cc = unpack_bf16(kiw[e]);
+                                    const int ch = 8 * c8 + 2 * e;
+                                    const float2 gr = *reinterpret_cast<const float2 *>(
+                                        reinterpret_cast<const uint8_t *>(gs) + sw_f32(r, ch));
+                                    const float2 gi = *reinterpret_cast<const float2 *>(
+                                        reinterpret_cast<const uint8_t *>(gs) + sw_f32(i, ch));
+                                    const float x0 = gr.x - gi.x, x1 = gr.y - gi.y;
+                                    overflow |= x0 > kFactorRange * kLog2e || x1 > kFactorRange * kLog2e;
+                                    const float e0 = ex2f(x0), e1 = ex2f(x1);
+                                    sa = fmaf(a.x * cc.x, e0, sa);
+                                    sa = fmaf(a.y * cc.y, e1, sa);
+                                    sp = fmaf(bq.x * cc.x, e0, sp);
+                                    sp = fmaf(bq.y * cc.y, e1, sp);
+                                }
                             }
                         }
                         const bool real = r < L && i < L;
                         const float rki = rn[64 + i];
-                        at[r * kATStride + i] = (i < r && real) ? betas[r] * rn[64 + r] * rki * sa : 0.f;
-                        pf[r * 64 + i] = real ? p.scale * rn[r] * rki * sp : 0.f;
+                        stg[r * 64 + i] = (i < r && real) ? betas[r] * rn[64 + r] * rki * sa : 0.f;
+                        stg[(64 + r) * 64 + i] = real ? p.scale * rn[r] * rki * sp : 0.f;
                     }
                 }
                 if (overflow) atomicOr(p.err, kErrGate);
+                if (it >= 2) wait_bar(bar(kIBCdone + b), pb(it - 2), abort_flag, p.err);
                 named_sync(1, 256);
-                // zeros above the diagonal of A; P to the record
-                for (int x = ct; x < 64 * 64; x += 256) {
-                    const int r = x >> 6, i = x & 63;
-                    if (i >= r) at[r * kATStride + i] = 0.f;
-                }
-                for (int gidx = ct; gidx < 64 * 8; gidx += 256) {
-                    const int r = gidx >> 3, g8 = gidx & 7;
-                    uint32_t w4[4];
+                tc::fence_after();
+                {
+                    // thread: Gram row 32 (warp % 4) + lane, columns [32 (warp / 4), +32);
+                    // entries above the row's range are never read
+                    const int q4 = warp & 3, half = warp >> 2, R = 32 * q4 + lane;
+                    uint32_t d[32];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i0 = 8 * g8 + 2 * e;
-                        w4[e] = pack_bf16(i0 <= r ? pf[r * 64 + i0] : 0.f,
-                                          i0 + 1 <= r ? pf[r * 64 + i0 + 1] : 0.f);
+                    for (int j = 0; j < 32; ++j) {
+                        const int i = 32 * half + j;
+                        const bool keep = R < 64 ? (i < R) : (i <= R - 64);
+                        d[j] = __float_as_uint(keep ? stg[R * 64 + i] : 0.f);
                     }
-                    st_global_v4(rec + kRecB3 + kmaj(r, 8 * g8, 64),
-                                 make_uint4(w4[0], w4[1], w4[2], w4[3]));
+                    tst32(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 * b + 32 * half, d);
+                    tc::st_wait();
                 }
-            }
-            if (named_sync_or(1, 256, *abort_flag != 0)) break;
-
-            // ---- T = (I + A)^{-1} (warps 0-3), straight to bf16 TA for the MMAs
-            if (warp < 4) {
-                // scratch for the off-diagonal blocks: the Gram operand tile is free now
-                float *scratch = reinterpret_cast<float *>(smem + kIOffGA);
-                invert64(at, ta, scratch, warp, lane);
             }
             fence_async_smem();
             tc::fence_before();
-            named_sync(1, 256);
-            if (lane == 0) mbar_arrive(bar(kIBInv));
-
-            // ---- Ut^T and -W to the record
-            wait_bar(bar(kIBWU), it & 1, abort_flag, p.err);
+            const bool stop = named_sync_or(1, 256, *abort_flag != 0);
+            if (warp == 0) {
+                // the Gram (or, for the exact form, the tensor-memory stores above)
+                if (!exact && it >= 2) wait_bar(bar(kIBCdone + b), pb(it - 2), abort_flag, p.err);
+                __syncwarp();
+                tc::fence_after();
+                if (!exact && !stop) {
+                    const uint64_t dGA = tc::sdesc(sb + kIOffGA, 128, 2048);
+                    const uint64_t dGB = tc::sdesc(sb + kIOffGB, 128, 2048);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss_e(tmem + 64 * b, dGA + 16 * kk, dGB + 16 * kk, kIdFull, kk > 0);
+                }
+                commit_e(bar(kIBGram + b));
+            }
+            if (stop) break;
+        }
+        if (warp == 0) {
+            // no input load of this CTA is in flight when it exits (early exit
+            // after an abort); every MMA this warp issued completes before the
+            // teardown
+            if (issued > 0) wait_bar(bar(kIBIn), (issued - 1) & 1, abort_flag, p.err);
+            commit_e(bar(kIBDrain));
+        }
+    } else if (warp < 12) {
+        // ================================================ solvers (warps 8-11)
+        const int w = warp - 8, q4 = warp & 3;
+        float *at = reinterpret_cast<float *>(smem + kIOffAT);
+        uint8_t *ta = smem + kIOffTA;
+        float *scratch = reinterpret_cast<float *>(smem + kIOffScr);
+        int it = 0;
+        for (int64_t item = next_real(worker); item < items; item = next_real(item + nworkers), ++it) {
+            const int b = it & 1;
+            const int64_t c = item / H;
+            const int h = static_cast<int>(item - c * H);
+            uint8_t *rec = record_of(p, c, h);
+            wait_bar(bar(kIBGram + b), pb(it), abort_flag, p.err);
+            // TA is free once the W / Ut MMAs of item it - 1 are done
+            if (it >= 1) wait_bar(bar(kIBWU + (b ^ 1)), pb(it - 1), abort_flag, p.err);
             tc::fence_after();
             {
-                const int q4 = warp & 3, half = warp >> 2;
-                const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-                // Ut^T row v = 32 q4 + lane, tokens [32 half, 32 half + 32)
-                uint32_t d[32];
-                tld32(tmem + lane_base + 192 + 32 * half, d);
-                // W (M = 64): rows 16 q4 + (0..15) in lanes 32 q4 + (0..15); the
-                // 16-lane shape gives thread (gq, tq) rows gq, gq + 8 and the column
-                // pair 2 tq of each 8-column block
-                uint32_t w[8][4];
-#pragma unroll
-                for (int b8 = 0; b8 < 8; ++b8)
-                    tc::ld_16x256b(tmem + lane_base + 64 + 64 * half + 8 * b8, w[b8][0], w[b8][1],
-                                   w[b8][2], w[b8][3]);
+                // Gram row R = 32 q4 + lane: 0-63 A (to A^T in the strict upper
+                // triangle), 64-127 P (to the record)
+                const int R = 32 * q4 + lane;
+                uint32_t d0[32], d1[32];
+                tld32(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 * b, d0);
+                tld32(tmem + (static_cast<uint32_t>(32 * q4) << 16) + 64 * b + 32, d1);
                 tc::ld_wait();
-                const int v = 32 * q4 + lane;
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(kIBCdone + b));
+                if (R < 64) {
 #pragma unroll
-                for (int j4 = 0; j4 < 4; ++j4) {
-                    const int j = 4 * half + j4;
-                    st_global_v4(rec + kRecUt + ut_off(v, j),
-                                 make_uint4(pack_bf16(__uint_as_float(d[8 * j4]), __uint_as_float(d[8 * j4 + 1])),
-                                            pack_bf16(__uint_as_float(d[8 * j4 + 2]), __uint_as_float(d[8 * j4 + 3])),
-                                            pack_bf16(__uint_as_float(d[8 * j4 + 4]), __uint_as_float(d[8 * j4 + 5])),
-                                            pack_bf16(__uint_as_float(d[8 * j4 + 6]), __uint_as_float(d[8 * j4 + 7]))));
-                }
+                    for (int i = 0; i < 32; ++i)
+                        if (i < R) at[i * kATStride + R] = __uint_as_float(d0[i]);
 #pragma unroll
-                for (int b8 = 0; b8 < 8; ++b8) {
-                    const int key = 64 * half + 8 * b8 + 2 * tq;
-                    const int r0 = 16 * q4 + gq;
-                    st_global_u32(rec + kRecB1 + kmaj(64 + r0, key, 128),
-                                  pack_bf16(-__uint_as_float(w[b8][0]), -__uint_as_float(w[b8][1])));
-                    st_global_u32(rec + kRecB1 + kmaj(64 + r0 + 8, key, 128),
-                                  pack_bf16(-__uint_as_float(w[b8][2]), -__uint_as_float(w[b8][3])));
+                    for (int i = 0; i < 32; ++i)
+                        if (32 + i < R) at[(32 + i) * kATStride + R] = __uint_as_float(d1[i]);
+                } else {
+                    const int r = R - 64;
+#pragma unroll
+                    for (int g8 = 0; g8 < 8; ++g8) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i0 = 8 * g8 + 2 * e;
+                            const uint32_t x0 = g8 < 4 ? d0[i0] : d1[i0 - 32];
+                            const uint32_t x1 = g8 < 4 ? d0[i0 + 1] : d1[i0 + 1 - 32];
+                            w4[e] = pack_bf16(i0 <= r ? __uint_as_float(x0) : 0.f,
+                                              i0 + 1 <= r ? __uint_as_float(x1) : 0.f);
+                        }
+                        st_global_v4(rec + kRecB3 + kmaj(r, 8 * g8, 64),
+                                     make_uint4(w4[0], w4[1], w4[2], w4[3]));
+                    }
                 }
             }
+            if (named_sync_or(2, 128, *abort_flag != 0)) break;
+            invert64(at, ta, scratch, w, lane, 2);
+            fence_async_smem();
             tc::fence_before();
-            const bool stop = named_sync_or(1, 256, *abort_flag != 0);
-            if (p.ring_depth > 0 && ct == 0 && !stop) {
+            named_sync(2, 128);
+            if (w == 0) {
+                // W and Ut^T into buffer b once the writers have read item it - 2's
+                if (it >= 2) wait_bar(bar(kIBFdone + b), pb(it - 2), abort_flag, p.err);
+                __syncwarp();
+                tc::fence_after();
+                const uint64_t dTA = tc::sdesc(sb + kIOffTA, 128, 1024);
+                const uint64_t dWB = tc::sdesc(sb + kIOffWB + 16384 * b, 128, 1024);
+                const uint64_t dUA = tc::sdesc(sb + kIOffUA + 16384 * b, 128, 1024);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)   // W = T (beta K e^G): M = 64, N = 128 keys, K = 64
+                    mma_ss_e(tmem + 128 + 192 * b, dTA + 16 * kk, dWB + 16 * kk, kIdW, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)   // Ut^T = (beta V)^T T^T: M = 128 v, N = 64, K = 64
+                    mma_ss_e(tmem + 256 + 192 * b, dUA + 16 * kk, dTA + 16 * kk, kIdFull, kk > 0);
+                commit_e(bar(kIBWU + b));
+            }
+        }
+        if (w == 0) commit_e(bar(kIBDrain));
+    } else if (warp < 16) {
+        // ================================================ writers (warps 12-15)
+        const int q4 = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
+        const int gq = lane >> 2, tq = lane & 3;
+        int it = 0;
+        for (int64_t item = next_real(worker); item < items; item = next_real(item + nworkers), ++it) {
+            const int b = it & 1;
+            const int64_t c = item / H;
+            const int h = static_cast<int>(item - c * H);
+            uint8_t *rec = record_of(p, c, h);
+            wait_bar(bar(kIBWU + b), pb(it), abort_flag, p.err);
+            tc::fence_after();
+            // Ut^T row v = 32 q4 + lane, all 64 tokens
+            uint32_t d0[32], d1[32];
+            tld32(tmem + lane_base + 256 + 192 * b, d0);
+            tld32(tmem + lane_base + 256 + 192 * b + 32, d1);
+            // W (M = 64): rows 16 q4 + (0..15); thread (gq, tq) rows gq, gq + 8 and
+            // the column pair 2 tq of each 8-column block
+            uint32_t wr[16][4];
+#pragma unroll
+            for (int b8 = 0; b8 < 16; ++b8)
+                tc::ld_16x256b(tmem + lane_base + 128 + 192 * b + 8 * b8, wr[b8][0], wr[b8][1],
+                               wr[b8][2], wr[b8][3]);
+            tc::ld_wait();
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kIBFdone + b));
+            const int v = 32 * q4 + lane;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t *dd = j < 4 ? d0 + 8 * j : d1 + 8 * (j - 4);
+                st_global_v4(rec + kRecUt + ut_off(v, j),
+                             make_uint4(pack_bf16(__uint_as_float(dd[0]), __uint_as_float(dd[1])),
+                                        pack_bf16(__uint_as_float(dd[2]), __uint_as_float(dd[3])),
+                                        pack_bf16(__uint_as_float(dd[4]), __uint_as_float(dd[5])),
+                                        pack_bf16(__uint_as_float(dd[6]), __uint_as_float(dd[7]))));
+            }
+            const int r0 = 16 * q4 + gq;
+#pragma unroll
+            for (int b8 = 0; b8 < 16; ++b8) {
+                const int key = 8 * b8 + 2 * tq;
+                st_global_u32(rec + kRecB1 + kmaj(64 + r0, key, 128),
+                              pack_bf16(-__uint_as_float(wr[b8][0]), -__uint_as_float(wr[b8][1])));
+                st_global_u32(rec + kRecB1 + kmaj(64 + r0 + 8, key, 128),
+                              pack_bf16(-__uint_as_float(wr[b8][2]), -__uint_as_float(wr[b8][3])));
+            }
+            // the whole record is written once the writers are done (the builders'
+            // and solvers' parts came earlier in the item's chain of barriers)
+            const bool stop = named_sync_or(3, 128, *abort_flag != 0);
+            if (p.ring_depth > 0 && warp == 12 && lane == 0 && !stop) {
                 __threadfence();
                 st_release(p.ready + (c % p.ring_depth) * H + h, c + 1);
             }
-            ++it;
             if (stop) break;
         }
     }
 
-    // ---- teardown: every warp, then TMEM is freed by warp 8
+    // ---- teardown: every warp, then TMEM is freed by warp 8 once every MMA
+    //      of the two issuing warps has completed
     tc::fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(kIBTear));
     if (warp == 8) {
         wait_bar(bar(kIBTear), 0, abort_flag, p.err);
+        wait_bar(bar(kIBDrain), 0, abort_flag, p.err);
         tc::fence_after();
         tc::dealloc(tmem, kITmemCols);
     }
@@ -1025,7 +1158,7 @@ __device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, i
         mbar_init(bar(kCBSdone), 1);
         mbar_init(bar(kCBOdone), 1);
         mbar_init(bar(kCBOfree), 4);
-        mbar_init(bar(kCBTear), kChainThreads / 32);
+        mbar_init(bar(kCBTear), blockDim.x / 32);
         mbar_init(bar(kCBDrain), 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -1179,7 +1312,7 @@ __device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, i
             }
             tc::fence_before();
         }
-    } else if (warp >= 10) {
+    } else if (warp >= 10 && warp < 14) {
         // ===================================================== o epilogue
         // O accumulates U^T P^T (MMA-B) and S^T Qg^T (MMA-O) from zero: these
         // warps clear it once at the start and again after each read
@@ -1286,7 +1419,7 @@ __device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, i
                 mbar_wait(bar(kCBFull + ps), (g2 / kCStages) & 1);
             }
         }
-    } else {
+    } else if (warp == 9) {
         // ===================================================== MMA issue (warp 9, one elected lane)
         int64_t gi = 0;
         bool ok = true;
@@ -1356,7 +1489,7 @@ __device__ void chain_role(const Params &p, uint8_t *smem, int h, int n_first, i
 
 // ------------------------------------------------------------------ kernels
 template <bool PRE>
-__global__ void __launch_bounds__(kThreads, 1) kda_c64_intra_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kIThreads, 1) kda_c64_intra_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     intra_role<PRE>(p, smem, blockIdx.x, gridDim.x);
 }
@@ -1371,7 +1504,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) kda_c64_chain_kernel(const _
 // all sequences, the others build the records into the ring. The last CTA to
 // finish clears the ring counters for the next call.
 template <bool PRE>
-__global__ void __launch_bounds__(kChainThreads, 1) kda_c64_fused_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kIThreads, 1) kda_c64_fused_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     if (static_cast<int>(blockIdx.x) < p.n_chain)
         chain_role(p, smem, blockIdx.x, 0, 1);
@@ -1445,6 +1578,10 @@ bool make_params(const C64Args &a, c64::Params *p) {
         !encode_rows(&p->tm_v, a.v, false, a.n_heads, a.tokens) ||
         !encode_rows(&p->tm_g, a.g, true, a.n_heads, a.tokens))
         return false;
+    p->q = a.q;
+    p->k = a.k;
+    p->v = a.v;
+    p->g = a.g;
     p->beta = a.beta;
     p->s0 = a.s0;
     p->out = a.out;
@@ -1495,10 +1632,10 @@ cudaError_t launch_c64_intra(const C64Args &a, int intra_ctas, cudaStream_t stre
     int64_t grid = intra_ctas < items ? intra_ctas : items;
     if (grid < 1) grid = 1;
     if (a.pre != 0)
-        c64::kda_c64_intra_kernel<true><<<static_cast<unsigned>(grid), c64::kThreads, c64::kSmem,
+        c64::kda_c64_intra_kernel<true><<<static_cast<unsigned>(grid), c64::kIThreads, c64::kSmem,
                                           stream>>>(p);
     else
-        c64::kda_c64_intra_kernel<false><<<static_cast<unsigned>(grid), c64::kThreads, c64::kSmem,
+        c64::kda_c64_intra_kernel<false><<<static_cast<unsigned>(grid), c64::kIThreads, c64::kSmem,
                                            stream>>>(p);
     return cudaGetLastError();
 }
@@ -1533,7 +1670,7 @@ cudaError_t launch_c64_fused(const C64Args &a, int grid, cudaStream_t stream) {
     if (!make_params(a, &p)) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(c64::kChainThreads);
+    cfg.blockDim = dim3(c64::kIThreads);
     cfg.dynamicSmemBytes = static_cast<size_t>(c64::kSmem);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
