@@ -49,8 +49,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--recurrent-impl", type=int, default=None,
-                    help="0 = tcgen05 recurrent kernel, 1 = warp-MMA kernel, 2 = hybrid "
-                         "(library default if unset)")
+                    help="1 = 16-token chunks, 3 = 64-token chunks on tcgen05 (two kernels), "
+                         "4 = 64-token chunks in one cooperative launch (library default if unset)")
     ap.add_argument("--decode", default=None, metavar="NxH",
                     help="time the one-token decode step instead (e.g. 256x64) and print its line")
     ap.add_argument("--preprocess", action="store_true",
@@ -58,8 +58,6 @@ def parse():
                          "normalisation, g read as gate logits): the same inputs, for timing")
     ap.add_argument("--no-decode", action="store_true",
                     help="leave the decode measurement out of the default line")
-    ap.add_argument("--ring-slot-mb", type=float, default=None,
-                    help="ring-slot size for segmented calls (library default if unset; <0 off)")
     ap.add_argument("--backward", action="store_true",
                     help="time the gradient call (kda_chunk_prefill_backward) on the workload "
                          "instead of the prefill; prints its own line")
@@ -402,8 +400,6 @@ def main():
     K.lib()
     if args.recurrent_impl is not None:
         K.kda_set_recurrent_impl(args.recurrent_impl)
-    if args.ring_slot_mb is not None:
-        K.kda_set_ring_slot_bytes(int(args.ring_slot_mb * (1 << 20)) if args.ring_slot_mb >= 0 else -1)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if args.decode:

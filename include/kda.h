@@ -114,9 +114,7 @@ enum { KDA_PRE_NORM_QK = 1, KDA_PRE_GATE_LOGITS = 2 };
  *
  * Workspace: the library keeps one scratch buffer per (device, stream),
  * grown stream-ordered (cudaMallocAsync / cudaFreeAsync) when a call needs
- * more (17,412 B per chunk-head: its record and one list entry; or two ring
- * slots plus the carried states for a segmented call, see
- * kda_set_ring_slot_bytes). A fixed-length call
+ * more (17,412 B per chunk-head: its record and one list entry). A fixed-length call
  * with at least 64 chunks per sequence and 4*N*H <= (SM count - 4) also reserves
  * N*H*64 KiB of midpoint states: the warp-MMA recurrent kernel then carries
  * the state to the middle of every sequence first and replays both halves
@@ -298,26 +296,16 @@ KDA_API kda_status kda_stage_timing_begin(int max_calls);
 KDA_API kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *calls);
 
 /*
- * Tuning (process-wide, host only). Fixed-length calls whose chunk records
- * (17,408 B per chunk-head) exceed `bytes` are split into segments of chunk
- * positions: the intra-chunk kernel of segment j+1 runs on an internal
- * low-priority stream while the recurrent kernel of segment j runs on an
- * internal high-priority stream, and the records live in two ring slots of
- * about `bytes` each, small enough to stay in L2 between the two kernels.
- * 0 restores the default, which is no segmentation; a negative value also
- * disables it.
- * Takes effect for later calls (the workspace grows if needed).
- */
-KDA_API kda_status kda_set_ring_slot_bytes(int64_t bytes);
-
-/*
- * Selects the recurrent kernel for later calls (process-wide, host only):
- * 0 = the 5th-generation tensor-core kernel (state in tensor memory,
- * tcgen05 MMAs, one CTA per (sequence, head)), 1 = the warp-level MMA kernel
- * (state in registers, one CTA per (sequence, head, 64 value channels)),
- * 2 = hybrid: the warp-level MMA chain with the output product Qg S on
- * tcgen05 (bf16 state handed over in tensor memory). All three compute the
- * same result to rounding. Other values: KDA_ERR_BAD_SHAPE.
+ * Selects the chunk size and kernels for later calls (process-wide, host
+ * only): 1 (default) = 16-token chunks, the intra-chunk kernel and then the
+ * warp-level MMA recurrent kernel (state in registers, one CTA per
+ * (sequence, head, 64 value channels)); 3 = 64-token chunks on the
+ * 5th-generation tensor core, an intra-chunk kernel (tcgen05 Gram, W and U
+ * products) and then a recurrent kernel (state in tensor memory, one CTA per
+ * (sequence, head)); 4 = the 64-token kernels in one cooperative launch,
+ * records passed through an L2-resident ring (3 when the heads leave fewer
+ * than 16 SMs to the record builders). All compute the same result to
+ * rounding. Other values: KDA_ERR_BAD_SHAPE.
  */
 KDA_API kda_status kda_set_recurrent_impl(int impl);
 

@@ -77,8 +77,6 @@ def lib() -> ctypes.CDLL:
                                                ctypes.POINTER(ctypes.c_int)]
             L.kda_set_recurrent_impl.restype = ctypes.c_int
             L.kda_set_recurrent_impl.argtypes = [ctypes.c_int]
-            L.kda_set_ring_slot_bytes.restype = ctypes.c_int
-            L.kda_set_ring_slot_bytes.argtypes = [i64]
             L.kda_build_info.restype = ctypes.c_char_p
             L.kda_build_info.argtypes = []
             _lib = L
@@ -158,13 +156,9 @@ def kda_stage_timing_end():
 
 
 def kda_set_recurrent_impl(impl: int) -> int:
-    """0 = tcgen05 / tensor-memory recurrent kernel, 1 = warp-MMA kernel."""
+    """1 = 16-token chunks (default), 3 = 64-token chunks on tcgen05 (two
+    kernels), 4 = 64-token chunks in one cooperative launch."""
     return lib().kda_set_recurrent_impl(int(impl))
-
-
-def kda_set_ring_slot_bytes(nbytes: int) -> int:
-    """Ring-slot size for segmented calls (0 = default, < 0 = never segment)."""
-    return lib().kda_set_ring_slot_bytes(int(nbytes))
 
 
 def kda_build_info() -> str:

@@ -15,9 +15,7 @@
 
 namespace {
 
-// Per caller stream: the scratch buffer and, for segmented calls, two
-// internal streams (intra-chunk work at the lowest priority, recurrent work
-// at the highest) with the events that order them.
+// Per caller stream: the scratch buffer.
 struct StreamWorkspace {
     void *ptr = nullptr;
     size_t bytes = 0;
@@ -25,8 +23,6 @@ struct StreamWorkspace {
     // (a fused launch leaves its counters zero; any other use of the buffer
     // may overwrite them)
     int64_t ring_clean = 0;
-    cudaStream_t s_intra = nullptr, s_recur = nullptr;
-    std::vector<cudaEvent_t> ev;
 };
 
 struct DeviceState {
@@ -45,30 +41,15 @@ struct StageTiming {
 };
 thread_local StageTiming t_timing;
 
-// Bytes of one ring slot of chunk records for segmented fixed-length calls
-// (0: default, < 0: never segment). Segmentation is off by default: on GB300
-// the recurrent kernel is latency-bound and loses more from sharing SMs with
-// the intra-chunk kernel than the L2-resident records gain (T=8192, H=64:
-// 590 us unsegmented against 685-1107 us with 96-12 MiB slots).
-std::atomic<int64_t> g_slot_bytes{0};
-constexpr int64_t kDefaultSlotBytes = -1;
-constexpr int64_t kMinSegChunks = 8;
-
-// Recurrent kernel: 0 = tcgen05 / tensor memory, 1 = warp-level MMA,
-// 2 = hybrid (warp-MMA chain, output product on tcgen05); 3 = 64-token chunks
-// on tcgen05, intra-chunk kernel then recurrent kernel; 4 = 64-token chunks,
-// both in one cooperative launch with the records in an L2-resident ring
-// (3 when the heads leave too few SMs for the record builders).
+// Path: 1 = 16-token chunks (intra-chunk kernel, then the warp-MMA recurrent
+// kernel); 3 = 64-token chunks on tcgen05, intra-chunk kernel then recurrent
+// kernel; 4 = 64-token chunks, both in one cooperative launch with the
+// records in an L2-resident ring (3 when the heads leave too few SMs for the
+// record builders).
 std::atomic<int> g_recur_impl{1};
-constexpr int kImplC64Split = 3, kImplC64Fused = 4;
+constexpr int kImplC16 = 1, kImplC64Split = 3, kImplC64Fused = 4;
 constexpr int64_t kC64Ring = 4;          // ring slots per head (fused launch)
 constexpr int kC64MinBuilders = 16;      // SMs left for record builders in a fused launch
-
-cudaError_t launch_recur(int impl, const kda::RecurParams &p, cudaStream_t s) {
-    if (impl == 0) return kda::launch_recurrent_tc(p, s);
-    if (impl == 2) return kda::launch_recurrent_hybrid(p, s);
-    return kda::launch_recurrent(p, s);
-}
 
 constexpr int64_t kMaxElems = int64_t(1) << 40;
 
@@ -104,13 +85,7 @@ struct Plan {
     int64_t max_chunks = 0;  // chunk records of one launch (upper bound when packed)
     int64_t off_bytes = 0;   // chunk offset table
     int64_t ws_bytes = 0;
-    // Segmented fixed-length calls: nseg launches of each kernel over seg_len
-    // chunk positions each, records in two ring slots of slot_bytes, the state
-    // carried between segments in carry_bytes.
-    int nseg = 1;
-    int64_t seg_len = 0;
-    int64_t slot_bytes = 0;
-    int64_t carry_bytes = 0;
+    int64_t seg_len = 0;     // fixed-length: chunks per sequence
     // Split replay of long fixed-length sequences (see kSplit*): the first
     // split_chunks chunks of every sequence are run once to carry the state to
     // the midpoint (mid_bytes of states), then both halves are replayed at once.
@@ -155,32 +130,11 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, i
     if (N * H * 2 >= (int64_t(1) << 31)) return KDA_ERR_BAD_SHAPE;
     pl->off_bytes = packed ? align256((N + 1) * 4) : 0;
     pl->ws_bytes = 256 + pl->off_bytes + pl->max_chunks * H * kda::kRecBytes;
-    pl->nseg = 1;
     pl->seg_len = (T + 15) / 16;
     if (!packed && pl->seg_len >= kSplitMinChunks && 2 * (N * H * 2) <= sm_count - kSplitSpareSms) {
         pl->split_chunks = pl->seg_len / 2;
         pl->mid_bytes = align256(N * H * 128 * 128 * 4);
         pl->ws_bytes += pl->mid_bytes;
-    }
-    if (!packed) {
-        const int64_t cps = (T + 15) / 16;
-        const int64_t per_pos = B * H * int64_t(kda::kRecBytes);
-        int64_t slot = g_slot_bytes.load();
-        if (slot == 0) slot = kDefaultSlotBytes;
-        if (slot > 0 && cps * per_pos > slot) {
-            int64_t seg = slot / per_pos;
-            if (seg < kMinSegChunks) seg = kMinSegChunks;
-            if (seg < cps) {
-                pl->nseg = static_cast<int>((cps + seg - 1) / seg);
-                pl->seg_len = seg;
-                pl->slot_bytes = align256(seg * per_pos);
-                pl->carry_bytes = align256(B * H * 128 * 128 * 4);
-                pl->max_chunks = B * seg;
-                pl->ws_bytes = 256 + 2 * pl->slot_bytes + pl->carry_bytes;
-                pl->split_chunks = 0;
-                pl->mid_bytes = 0;
-            }
-        }
     }
     pl->list_bytes = align256(pl->max_chunks * H * 4);
     pl->ws_bytes += pl->list_bytes;
@@ -192,7 +146,6 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, i
         if (pl->tokens >= (int64_t(1) << 31)) return KDA_ERR_BAD_SHAPE;
         pl->c64_chunks = packed ? (T + 63 * N) / 64 : B * ((T + 63) / 64);
         if (impl == kImplC64Fused && H + kC64MinBuilders > sm_count) pl->impl = kImplC64Split;
-        pl->nseg = 1;
         pl->split_chunks = 0;
         pl->mid_bytes = 0;
         pl->list_bytes = 0;
@@ -217,8 +170,6 @@ kda_status init_device(int dev, DeviceState &st) {
     if (cudaMemset(st.err, 0, 256) != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_intra() != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_recurrent() != cudaSuccess) return KDA_ERR_CUDA;
-    if (kda::configure_recurrent_tc() != cudaSuccess) return KDA_ERR_CUDA;
-    if (kda::configure_recurrent_hybrid() != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_c64() != cudaSuccess) return KDA_ERR_CUDA;
     st.ready = true;
     return KDA_OK;
@@ -328,10 +279,10 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
 }
 
 const char *kda_build_info(void) {
-    return "prefill_kda_chunk_gb300 0.3 (sm_103a; intra-chunk mma.sync with an exact form for "
-           "strong decay; recurrent warp-MMA chain with bulk-async staged records and split "
-           "replay, tcgen05 and hybrid kernels opt-in; decode step; in-kernel q/k normalisation "
-           "and gate logits; token-serial gradients)";
+    return "prefill_kda_chunk_gb300 0.4 (sm_103a; 16-token chunks: intra-chunk mma.sync with an "
+           "exact form for strong decay, recurrent warp-MMA chain with bulk-async staged records "
+           "and split replay; 64-token chunks on tcgen05 opt-in; decode step; in-kernel q/k "
+           "normalisation and gate logits; token-serial gradients)";
 }
 
 int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, int has_cu_seqlens) {
@@ -518,84 +469,26 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
         return e != cudaSuccess ? e : kda::launch_intra_exact(ip, s);
     };
 
-    if (pl.nseg == 1) {
-        kda::IntraParams ip{q, k, v, g, beta, rec, scale, impl == 2 ? 1 : 0, flags, st.err, geo,
-                            exact_list, exact_ctr};
-        rc = timed_launch(true, stream, [&] { return intra(ip, pl.max_chunks, stream); });
-        if (rc != KDA_OK) return rc;
-        kda::RecurParams rp{rec, initial_state, out, final_state, st.err, geo};
-        // (an in-place state would be read by one half while the other writes it)
-        if (pl.split_chunks > 0 && impl == 1 &&
-            (initial_state == nullptr || initial_state != final_state)) {
-            // state to the midpoint of every sequence, then both halves at once
-            float *mid = reinterpret_cast<float *>(rec + pl.max_chunks * H * kda::kRecBytes);
-            kda::RecurParams rl = rp;
-            rl.out = nullptr;
-            rl.s_final = mid;
-            rl.geo.seg_len = static_cast<int32_t>(pl.split_chunks);
-            rp.split_chunks = static_cast<int32_t>(pl.split_chunks);
-            rp.s_mid = mid;
-            return timed_launch(false, stream, [&] {
-                const cudaError_t e = kda::launch_recurrent_state_only(rl, stream);
-                return e != cudaSuccess ? e : kda::launch_recurrent(rp, stream);
-            });
-        }
-        return timed_launch(false, stream, [&] { return launch_recur(impl, rp, stream); });
+    kda::IntraParams ip{q, k, v, g, beta, rec, scale, flags, st.err, geo, exact_list, exact_ctr};
+    rc = timed_launch(true, stream, [&] { return intra(ip, pl.max_chunks, stream); });
+    if (rc != KDA_OK) return rc;
+    kda::RecurParams rp{rec, initial_state, out, final_state, st.err, geo};
+    // (an in-place state would be read by one half while the other writes it)
+    if (pl.split_chunks > 0 && (initial_state == nullptr || initial_state != final_state)) {
+        // state to the midpoint of every sequence, then both halves at once
+        float *mid = reinterpret_cast<float *>(rec + pl.max_chunks * H * kda::kRecBytes);
+        kda::RecurParams rl = rp;
+        rl.out = nullptr;
+        rl.s_final = mid;
+        rl.geo.seg_len = static_cast<int32_t>(pl.split_chunks);
+        rp.split_chunks = static_cast<int32_t>(pl.split_chunks);
+        rp.s_mid = mid;
+        return timed_launch(false, stream, [&] {
+            const cudaError_t e = kda::launch_recurrent_state_only(rl, stream);
+            return e != cudaSuccess ? e : kda::launch_recurrent(rp, stream);
+        });
     }
-
-    // ---- segmented: intra-chunk work of segment j+1 overlaps the recurrent
-    //      work of segment j; records alternate between two ring slots
-    if (ws.s_intra == nullptr) {
-        if (capturing) return KDA_ERR_CAPTURE;
-        int lo = 0, hi = 0;
-        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return KDA_ERR_CUDA;
-        if (cudaStreamCreateWithPriority(&ws.s_intra, cudaStreamNonBlocking, lo) != cudaSuccess ||
-            cudaStreamCreateWithPriority(&ws.s_recur, cudaStreamNonBlocking, hi) != cudaSuccess)
-            return KDA_ERR_CUDA;
-    }
-    const size_t nev = 1 + 2 * static_cast<size_t>(pl.nseg);
-    if (ws.ev.size() < nev) {
-        if (capturing) return KDA_ERR_CAPTURE;
-        while (ws.ev.size() < nev) {
-            cudaEvent_t e;
-            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return KDA_ERR_CUDA;
-            ws.ev.push_back(e);
-        }
-    }
-    cudaEvent_t ev_in = ws.ev[0];
-    cudaEvent_t *ev_intra = &ws.ev[1], *ev_recur = &ws.ev[1 + pl.nseg];
-    float *carry = reinterpret_cast<float *>(rec + 2 * pl.slot_bytes);
-    if (cudaEventRecord(ev_in, stream) != cudaSuccess ||
-        cudaStreamWaitEvent(ws.s_intra, ev_in, 0) != cudaSuccess ||
-        cudaStreamWaitEvent(ws.s_recur, ev_in, 0) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    const int64_t cps = geo.chunks_per_seq;
-    for (int j = 0; j < pl.nseg; ++j) {
-        kda::ChunkGeometry gj = geo;
-        gj.pos_begin = static_cast<int32_t>(j * pl.seg_len);
-        const int64_t left = cps - j * pl.seg_len;
-        gj.seg_len = static_cast<int32_t>(left < pl.seg_len ? left : pl.seg_len);
-        gj.slot_stride = static_cast<int32_t>(pl.seg_len);
-        uint8_t *slot = rec + (j & 1) * pl.slot_bytes;
-        if (j >= 2 && cudaStreamWaitEvent(ws.s_intra, ev_recur[j - 2], 0) != cudaSuccess)
-            return KDA_ERR_CUDA;
-        kda::IntraParams ip{q, k, v, g, beta, slot, scale, impl == 2 ? 1 : 0, flags, st.err, gj,
-                            exact_list, exact_ctr};
-        const int64_t items = B * static_cast<int64_t>(gj.seg_len);
-        rc = timed_launch(true, ws.s_intra, [&] { return intra(ip, items, ws.s_intra); });
-        if (rc != KDA_OK) return rc;
-        if (cudaEventRecord(ev_intra[j], ws.s_intra) != cudaSuccess ||
-            cudaStreamWaitEvent(ws.s_recur, ev_intra[j], 0) != cudaSuccess)
-            return KDA_ERR_CUDA;
-        const float *s_in = j == 0 ? initial_state : carry;
-        float *s_out = j == pl.nseg - 1 ? final_state : carry;
-        kda::RecurParams rp{slot, s_in, out, s_out, st.err, gj};
-        rc = timed_launch(false, ws.s_recur, [&] { return launch_recur(impl, rp, ws.s_recur); });
-        if (rc != KDA_OK) return rc;
-        if (cudaEventRecord(ev_recur[j], ws.s_recur) != cudaSuccess) return KDA_ERR_CUDA;
-    }
-    if (cudaStreamWaitEvent(stream, ev_recur[pl.nseg - 1], 0) != cudaSuccess) return KDA_ERR_CUDA;
-    return KDA_OK;
+    return timed_launch(false, stream, [&] { return kda::launch_recurrent(rp, stream); });
 }
 
 // Gradient workspace: flag block, chunk offsets (packed), one checkpoint state
@@ -771,13 +664,8 @@ kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *cal
 }
 
 kda_status kda_set_recurrent_impl(int impl) {
-    if (impl < 0 || impl > kImplC64Fused) return KDA_ERR_BAD_SHAPE;
+    if (impl != kImplC16 && impl != kImplC64Split && impl != kImplC64Fused) return KDA_ERR_BAD_SHAPE;
     g_recur_impl.store(impl);
-    return KDA_OK;
-}
-
-kda_status kda_set_ring_slot_bytes(int64_t bytes) {
-    g_slot_bytes.store(bytes);
     return KDA_OK;
 }
 
@@ -818,9 +706,6 @@ kda_status kda_workspace_release(void) {
     for (auto &kv : it->second.ws) {
         StreamWorkspace &w = kv.second;
         if (w.ptr != nullptr && cudaFree(w.ptr) != cudaSuccess) return KDA_ERR_CUDA;
-        for (cudaEvent_t e : w.ev) cudaEventDestroy(e);
-        if (w.s_intra) cudaStreamDestroy(w.s_intra);
-        if (w.s_recur) cudaStreamDestroy(w.s_recur);
     }
     it->second.ws.clear();
     return KDA_OK;

@@ -36,8 +36,6 @@ struct IntraParams {
     const float *beta;         // [tokens, H]
     uint8_t *rec;              // chunk records [chunks, H, kRecBytes]
     float scale;               // output scale, folded into the record's Q e^G and P
-    int qg_tc;                 // 1: Q e^G in the tcgen05 operand layout of the hybrid
-                               //    recurrent kernel; 0: swizzled rows for ldmatrix
     int pre;                   // kPreNormQK | kPreGateLogits (input preprocessing)
     int *err;                  // sticky per-device error word
     ChunkGeometry geo;
@@ -99,8 +97,6 @@ struct BackParams {
 // Per-device, once: raise the dynamic shared-memory limits of the kernels.
 cudaError_t configure_intra();
 cudaError_t configure_recurrent();
-cudaError_t configure_recurrent_tc();
-cudaError_t configure_recurrent_hybrid();
 
 // chunk_off[n] = first chunk of sequence n for chunks of 2^chunk_shift tokens
 cudaError_t launch_varlen_prologue(const int32_t *cu, int32_t n_seqs, int64_t total_tokens,
@@ -113,9 +109,6 @@ cudaError_t launch_intra_exact(const IntraParams &p, cudaStream_t stream);
 cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream);     // warp MMA
 // warp MMA without outputs: only carries the state (to s_final)
 cudaError_t launch_recurrent_state_only(const RecurParams &p, cudaStream_t stream);
-cudaError_t launch_recurrent_tc(const RecurParams &p, cudaStream_t stream);  // tcgen05 / TMEM
-// warp-MMA chain with the output product on tcgen05; needs IntraParams::qg_tc = 1
-cudaError_t launch_recurrent_hybrid(const RecurParams &p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int64_t units, cudaStream_t stream);
 // The gradient kernel is persistent: at most one CTA per resident slot and
 // never more than kBackwardMaxRings, each owning one 16-state ring of the

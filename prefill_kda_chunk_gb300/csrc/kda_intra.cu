@@ -131,15 +131,6 @@ __device__ __forceinline__ void load_chunk(const IntraParams &p, IntraWarpSmem &
 }
 
 // Byte offset of key pair pr (keys 2 pr, 2 pr + 1) within a token row of the
-// tcgen05 operand layout of Q e^G that the hybrid recurrent kernel reads:
-// K-major core matrices of 8 tokens x 8 keys; within a 16-key block key pair
-// j goes to pair position 2 (j & 3) + (j >> 2).
-__device__ __forceinline__ int qg_tc_pair_off(int pr) {
-    const int j = pr & 7, kidx = 16 * (pr >> 3) + 2 * (2 * (j & 3) + (j >> 2));
-    return (kidx >> 3) * 128 + (kidx & 7) * 2;
-}
-__device__ __forceinline__ int qg_tc_row_off(int r) { return (r >> 3) * 2048 + (r & 7) * 16; }
-
 // The chunk's gating, A and P without factoring exp(G_r - G_i) as
 // exp(G_r) exp(-G_i) about the chunk start, for chunks whose cumulative log
 // decay leaves [-80, 80] in some channel (strong decay: exp(-G) would
@@ -167,7 +158,7 @@ __device__ __forceinline__ int qg_tc_row_off(int r) { return (r >> 3) * 2048 + (
 // L2 norms first when pre asks). Scratch while it runs: the level's row tile
 // in sm.kg, its column tile in sm.a / sm.t (2 KB of their 2176 B).
 __device__ __forceinline__ void intra_exact_chunk(const float *gp, int64_t rowe, int L, int pre,
-                                               float scale, int qg_tc, float beta_l,
+                                               float scale, float beta_l,
                                                IntraWarpSmem *smp, uint8_t *rec, int *err) {
     IntraWarpSmem &sm = *smp;
     const int lane = threadIdx.x & 31;
@@ -199,7 +190,6 @@ __device__ __forceinline__ void intra_exact_chunk(const float *gp, int64_t rowe,
 
     // ---- per row: (normalised) q to sm.qg and k to sm.kn as bf16; scale
     //      Q e^G and K e^(G_last - G) to the record
-    const int qg_tc_off0 = qg_tc_pair_off(2 * lane), qg_tc_off1 = qg_tc_pair_off(2 * lane + 1);
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
         const int off = swz(r, 4 * lane);
@@ -232,13 +222,7 @@ __device__ __forceinline__ void intra_exact_chunk(const float *gp, int64_t rowe,
             kd[e] = k[e] * ex2(G[15][e] - G[r][e]);
         }
         const uint2 uqg = make_uint2(pack_bf16(qg[0], qg[1]), pack_bf16(qg[2], qg[3]));
-        if (qg_tc) {
-            const int rowoff = qg_tc_row_off(r);
-            __stcs(reinterpret_cast<unsigned int *>(rec + kRecQg + qg_tc_off0 + rowoff), uqg.x);
-            __stcs(reinterpret_cast<unsigned int *>(rec + kRecQg + qg_tc_off1 + rowoff), uqg.y);
-        } else {
-            __stcs(reinterpret_cast<uint2 *>(rec + kRecQg + off), uqg);
-        }
+        __stcs(reinterpret_cast<uint2 *>(rec + kRecQg + off), uqg);
         __stcs(reinterpret_cast<uint2 *>(rec + kRecKd + off),
                make_uint2(pack_bf16(kd[0], kd[1]), pack_bf16(kd[2], kd[3])));
     }
@@ -514,8 +498,6 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     cp_async_wait_all();
     __syncwarp();
 
-    // byte offsets of this lane's two key pairs in the tcgen05 layout of Q e^G
-    const int qg_tc_off0 = qg_tc_pair_off(2 * lane), qg_tc_off1 = qg_tc_pair_off(2 * lane + 1);
     // ---- gated operand tiles (in place for K e^G and scale Q e^G)
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -560,13 +542,7 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
         *reinterpret_cast<uint2 *>(sm.kg + off) = ukg;
         *reinterpret_cast<uint2 *>(sm.kn + off) = ukn;
         *reinterpret_cast<uint2 *>(sm.qg + off) = uqg;
-        if (p.qg_tc) {
-            const int rowoff = qg_tc_row_off(r);
-            __stcs(reinterpret_cast<unsigned int *>(rec + kRecQg + qg_tc_off0 + rowoff), uqg.x);
-            __stcs(reinterpret_cast<unsigned int *>(rec + kRecQg + qg_tc_off1 + rowoff), uqg.y);
-        } else {
-            __stcs(reinterpret_cast<uint2 *>(rec + kRecQg + off), uqg);
-        }
+        __stcs(reinterpret_cast<uint2 *>(rec + kRecQg + off), uqg);
         __stcs(reinterpret_cast<uint2 *>(rec + kRecKd + off), ukd);
     }
     __stcs(reinterpret_cast<float4 *>(rec + kRecGamma + 16 * lane),
@@ -650,7 +626,7 @@ kda_intra_exact_kernel(IntraParams p) {
         cp_async_wait_all();
         __syncwarp();
         intra_exact_chunk(p.g + (t0 * H + h) * kDim + 4 * lane, static_cast<int64_t>(H) * kDim, L,
-                          PRE ? p.pre : 0, p.scale, p.qg_tc, beta_l, &sm, rec, p.err);
+                          PRE ? p.pre : 0, p.scale, beta_l, &sm, rec, p.err);
         __syncwarp();
         intra_tail(sm, rec, beta_l, lane);
     }

@@ -193,7 +193,7 @@ extern "C" kda_status kda_chunk_prefill_noalloc(
     // the exact-form list after the records, its counters in the flag block
     int32_t *exact_list = reinterpret_cast<int32_t *>(rec + max_chunks * H * kda::kRecBytes);
     int *exact_ctr = reinterpret_cast<int *>(base + 64);
-    kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, 0, err, geo, exact_list, exact_ctr};
+    kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, err, geo, exact_list, exact_ctr};
     if (kda::launch_intra_chunk(ip, max_chunks, stream) != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::launch_intra_exact(ip, stream) != cudaSuccess) return KDA_ERR_CUDA;
     kda::RecurParams rp{rec, initial_state, out, final_state, err, geo};

@@ -46,21 +46,10 @@ def test_workspace_bytes(lib):
     def lst(items):                            # exact-form list: one int32 per chunk-head
         return -(-(items * 4) // 256) * 256
 
-    try:
-        K.kda_set_ring_slot_bytes(-1)          # one launch of each kernel
-        # 512 chunks x 64 heads x 17408 B + the flag block + the list
-        assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 512 * 64 * REC + lst(512 * 64)
-        K.kda_set_ring_slot_bytes(24 << 20)    # segmented when records exceed a slot
-        seg = (24 << 20) // (64 * REC)         # chunk positions per segment
-        slot = -(-(seg * 64 * REC) // 256) * 256
-        carry = 64 * 128 * 128 * 4
-        assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 2 * slot + carry + lst(seg * 64)
-        assert K.kda_workspace_bytes(1, 256, 2, 1, 0) == 256 + 16 * 2 * REC + lst(32)  # small
-        K.kda_set_ring_slot_bytes(0)           # default: one launch of each kernel
-        assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 512 * 64 * REC + lst(512 * 64)
-    finally:
-        K.kda_set_ring_slot_bytes(0)
-    # packed batches are never segmented
+    # 512 chunks x 64 heads x 17408 B + the flag block + the list
+    assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 512 * 64 * REC + lst(512 * 64)
+    assert K.kda_workspace_bytes(1, 256, 2, 1, 0) == 256 + 16 * 2 * REC + lst(32)  # small
+    # packed batches: the chunk offsets after the flag block
     pc = (8192 + 15 * 16) // 16
     assert K.kda_workspace_bytes(1, 8192, 64, 16, 1) == 256 + 256 + pc * 64 * REC + lst(pc * 64)
     # long sequences with few heads: records plus the midpoint states of the split replay

@@ -45,7 +45,7 @@ def test_launches_per_call():
     assert n["varlen16_T8192_H64"] == 4            # + the cu_seqlens prologue
     assert n["long_T131072_H32"] == 4              # + the split replay's state-only pass
     args = _Args()
-    args.recurrent_impl = 0                        # the split replay is warp-MMA only
+    args.recurrent_impl = 3                        # the split replay is 16-token only
     assert b.launches_per_call(KI.WORKLOADS["long_T131072_H32"], args) == 3
 
 

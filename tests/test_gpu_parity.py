@@ -27,9 +27,10 @@ def built():
     K.lib()
 
 
-# every test runs with each recurrent kernel: 0 = tcgen05 / tensor memory, 1 = warp MMA,
-# 2 = hybrid (warp-MMA chain, output product on tcgen05)
-@pytest.fixture(autouse=True, params=[0, 1, 2], ids=["tcgen05", "warp_mma", "hybrid"])
+# every test runs on each path: 1 = 16-token chunks (warp-MMA recurrent kernel),
+# 3 = 64-token chunks on tcgen05 (two kernels), 4 = 64-token chunks in one
+# cooperative launch with an L2 ring of records
+@pytest.fixture(autouse=True, params=[1, 3, 4], ids=["c16", "c64_split", "c64_fused"])
 def recurrent_impl(request, built):
     assert K.kda_set_recurrent_impl(request.param) == 0
     yield request.param
@@ -190,54 +191,6 @@ def test_in_place_state_and_no_final_state():
                              scale=d["scale"])
     K.check_device_error()
     assert f2 is None and torch.equal(o2, o)
-
-
-@pytest.mark.parametrize("T,Bn", [(300, 1), (129, 3), (256, 2)])
-def test_segmented_calls(T, Bn):
-    """Small ring slots force several segments (overlapped intra/recurrent
-    launches on internal streams, state carried between segments)."""
-    H = 2
-    d = KI.make_case([T] * Bn, H=H, seed=40 + T, init_state=True)
-    x = to_dev(d)
-    q, k, v, g = (x[n].view(Bn, T, H, 128) for n in ("q", "k", "v", "g"))
-    beta = x["beta"].view(Bn, T, H)
-    try:
-        K.kda_set_ring_slot_bytes(8 * Bn * H * 17408)       # 8 chunk positions per segment
-        o, f = K.chunk_prefill(q, k, v, g, beta, initial_state=x["initial_state"],
-                               scale=d["scale"])
-        st = x["initial_state"].clone()                     # in place, and no final state
-        o2, _ = K.chunk_prefill(q, k, v, g, beta, initial_state=st, final_state=st,
-                                scale=d["scale"])
-        o3, f3 = K.chunk_prefill(q, k, v, g, beta, initial_state=x["initial_state"],
-                                 output_final_state=False, scale=d["scale"])
-        K.check_device_error()
-    finally:
-        K.kda_set_ring_slot_bytes(0)
-    o_ref, f_ref = run_oracle(d)
-    assert_parity(o.view(Bn * T, H, 128), f, o_ref, f_ref, "segmented")
-    assert torch.equal(o2, o) and torch.equal(st, f)
-    assert f3 is None and torch.equal(o3, o)
-
-
-def test_segmented_calls_strong_decay():
-    """The exact form in a segmented call: every segment's intra-chunk launch
-    lists its own out-of-range chunk-heads (one list, reused per segment on
-    the internal stream). Head 1 decays at -7 per token."""
-    T, Bn, H = 300, 2, 2
-    d = KI.make_case([T] * Bn, H=H, seed=45, init_state=True)
-    d["g"][:, 1, :] = -7.0
-    x = to_dev(d)
-    q, k, v, g = (x[n].view(Bn, T, H, 128) for n in ("q", "k", "v", "g"))
-    beta = x["beta"].view(Bn, T, H)
-    try:
-        K.kda_set_ring_slot_bytes(8 * Bn * H * 17408)       # 8 chunk positions per segment
-        o, f = K.chunk_prefill(q, k, v, g, beta, initial_state=x["initial_state"],
-                               scale=d["scale"])
-        K.check_device_error()
-    finally:
-        K.kda_set_ring_slot_bytes(0)
-    o_ref, f_ref = run_oracle(d)
-    assert_parity(o.view(Bn * T, H, 128), f, o_ref, f_ref, "segmented, strong decay")
 
 
 def test_split_replay_strong_decay():

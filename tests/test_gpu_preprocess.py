@@ -120,11 +120,10 @@ def test_preprocessing_equals_preprocessed_inputs():
     assert rel_o < 1e-2 and rel_f < 1e-2, (float(rel_o), float(rel_f))
 
 
-@pytest.mark.parametrize("impl", [0, 1, 2], ids=["tcgen05", "warp_mma", "hybrid"])
+@pytest.mark.parametrize("impl", [1, 3, 4], ids=["c16", "c64_split", "c64_fused"])
 def test_preprocessing_with_each_recurrent_kernel(impl):
-    """The preprocessing lives in the intra-chunk kernel, whose record layout
-    depends on the recurrent kernel (the hybrid one takes Q e^G in its
-    tcgen05 operand layout): check every combination."""
+    """The preprocessing lives in the intra-chunk kernel of each path (the
+    16-token one and the 64-token tcgen05 one): check every path."""
     d = KI.make_raw_case([150, 33], H=2, seed=60 + impl, init_state=True)
     x = {n: d[n].cuda().contiguous() for n in ("q", "k", "v", "g", "beta")}
     assert K.kda_set_recurrent_impl(impl) == 0
@@ -141,7 +140,7 @@ def test_preprocessing_with_each_recurrent_kernel(impl):
     check(f, f_ref, "final_state")
 
 
-@pytest.mark.parametrize("impl", [0, 1, 2], ids=["tcgen05", "warp_mma", "hybrid"])
+@pytest.mark.parametrize("impl", [1, 3, 4], ids=["c16", "c64_split", "c64_fused"])
 def test_preprocessing_strong_decay(impl):
     """Gate logits far below 0 (log decays down to about -25 per token) make
     the intra-chunk kernel take its exact form, which does the q/k
