@@ -181,18 +181,37 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def scan_segments(n_units, chunks, sms):
+    """Segments of the 16-token path's segment-parallel scan for fixed-length
+    calls, as the library picks them (automatic setting)."""
+    if chunks < 64 or 4 * n_units > sms - 4:
+        return 1
+    P = min(3 * (sms - 4) // (2 * n_units), 16, chunks // 16)
+    if P < 2:
+        return 1
+    L = -(-chunks // P)
+    return -(-chunks // L)
+
+
 def launches_per_call(w, args):
-    """Kernels one unsegmented prefill call launches: the cu_seqlens prologue
-    (packed batches), the intra-chunk kernel, its exact-form companion, the
-    recurrent kernel, and the state-only pass of the split replay (warp-MMA
-    recurrent kernel, fixed-length sequences of >= 64 chunks, 4 N H <= SMs - 4)."""
+    """Kernels one prefill call launches. 16-token path: the cu_seqlens
+    prologue (packed batches), the intra-chunk kernel, its exact-form
+    companion, the recurrent kernel, and for long fixed-length sequences with
+    few heads the segment scan's maps launch and (P > 2) its combine.
+    64-token paths: the prologue (packed), then the intra-chunk and recurrent
+    kernels (split) or the one cooperative kernel (fused)."""
+    impl = 1 if args.recurrent_impl is None else args.recurrent_impl
+    if impl == 3:
+        return 2 + int(w.varlen)
+    if impl == 4:
+        return 1 + int(w.varlen)
     n = 3 + int(w.varlen)
     chunks = -(-(w.T // w.n_seqs) // 16)
-    impl = 1 if args.recurrent_impl is None else args.recurrent_impl
     sms = (torch.cuda.get_device_properties(0).multi_processor_count
            if torch.cuda.is_available() else 152)
-    if not w.varlen and impl == 1 and chunks >= 64 and 4 * w.n_seqs * w.H <= sms - 4:
-        n += 1
+    if not w.varlen:
+        P = scan_segments(w.n_seqs * w.H, chunks, sms)
+        n += (P >= 2) + (P > 2)
     return n
 
 

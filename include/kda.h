@@ -114,14 +114,16 @@ enum { KDA_PRE_NORM_QK = 1, KDA_PRE_GATE_LOGITS = 2 };
  *
  * Workspace: the library keeps one scratch buffer per (device, stream),
  * grown stream-ordered (cudaMallocAsync / cudaFreeAsync) when a call needs
- * more (17,412 B per chunk-head: its record and one list entry). A fixed-length call
- * with at least 64 chunks per sequence and 4*N*H <= (SM count - 4) also reserves
- * N*H*64 KiB of midpoint states: the warp-MMA recurrent kernel then carries
- * the state to the middle of every sequence first and replays both halves
- * side by side (same results to rounding; not with an in-place state). A segmented call also
- * forks onto two internal streams of that workspace and joins back to
- * `stream` before returning. Concurrent calls on different streams
- * therefore never share scratch. Growing is refused with KDA_ERR_CAPTURE
+ * more (17,412 B per chunk-head: its record and one list entry). A
+ * fixed-length call on the 16-token path whose sequences have at least 64
+ * chunks and with 4*N*H <= (SM count - 4) runs a segment-parallel scan with
+ * P = 3*(SM count - 4) / (2*N*H) segments (at most 16, at least 16 chunks per
+ * segment; or the P set by kda_set_scan_segments): every sequence is cut
+ * into P segments whose affine state maps are built in parallel, a short
+ * serial combine gives each segment's entry state, and all segments are
+ * replayed side by side (same results to rounding; not with an in-place
+ * state). It reserves (3P - 5) * N*H*64 KiB more. Concurrent calls on
+ * different streams never share scratch. Growing is refused with KDA_ERR_CAPTURE
  * while the stream is being captured into a graph: make one call of the
  * largest size before capturing. kda_workspace_release() frees them.
  *
@@ -294,6 +296,17 @@ KDA_API int64_t kda_backward_workspace_bytes(int64_t B, int64_t T, int64_t H, in
  */
 KDA_API kda_status kda_stage_timing_begin(int max_calls);
 KDA_API kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *calls);
+
+/*
+ * Segments of the segment-parallel scan for later fixed-length calls on the
+ * 16-token path (process-wide, host only): 0 (default) = chosen from the SM
+ * count as described for kda_chunk_prefill, 1 = off (one chain per
+ * sequence), P >= 2 = P segments (fewer when the sequence has fewer chunks
+ * than P, or when that leaves a segment empty). Values outside [0, 4096]:
+ * KDA_ERR_BAD_SHAPE. Takes effect for later calls (the workspace grows if
+ * needed).
+ */
+KDA_API kda_status kda_set_scan_segments(int segments);
 
 /*
  * Selects the chunk size and kernels for later calls (process-wide, host

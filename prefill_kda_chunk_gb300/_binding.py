@@ -77,6 +77,8 @@ def lib() -> ctypes.CDLL:
                                                ctypes.POINTER(ctypes.c_int)]
             L.kda_set_recurrent_impl.restype = ctypes.c_int
             L.kda_set_recurrent_impl.argtypes = [ctypes.c_int]
+            L.kda_set_scan_segments.restype = ctypes.c_int
+            L.kda_set_scan_segments.argtypes = [ctypes.c_int]
             L.kda_build_info.restype = ctypes.c_char_p
             L.kda_build_info.argtypes = []
             _lib = L
@@ -159,6 +161,12 @@ def kda_set_recurrent_impl(impl: int) -> int:
     """1 = 16-token chunks (default), 3 = 64-token chunks on tcgen05 (two
     kernels), 4 = 64-token chunks in one cooperative launch."""
     return lib().kda_set_recurrent_impl(int(impl))
+
+
+def kda_set_scan_segments(segments: int) -> int:
+    """Segment-parallel scan for fixed-length calls: 0 = automatic, 1 = off,
+    P >= 2 = P segments per sequence."""
+    return lib().kda_set_scan_segments(int(segments))
 
 
 def kda_build_info() -> str:

@@ -53,14 +53,40 @@ constexpr int kC64MinBuilders = 16;      // SMs left for record builders in a fu
 
 constexpr int64_t kMaxElems = int64_t(1) << 40;
 
-// Split replay (fixed-length calls, warp-MMA recurrent kernel). A recurrent
+// Segment-parallel scan (fixed-length calls, 16-token path). A recurrent
 // step is a serial chain, so with few (sequence, head) units most SMs idle
-// through T/16 steps. When twice the recurrent CTAs (2 per head) still fit one
-// per SM, a state-only pass over the first half of each sequence gives the
-// midpoint state, and one launch then replays both halves side by side: about
-// T/32 (light) + T/32 (full) steps on the chain instead of T/16 full ones.
-constexpr int64_t kSplitMinChunks = 64;    // per sequence
-constexpr int64_t kSplitSpareSms = 4;      // SMs left free beside the doubled recurrent grid
+// through T/16 steps. Cutting every sequence into P segments, the maps launch
+// builds each segment's affine state map (M, c) in parallel (the first
+// segment's end state directly), a short serial combine gives the entry
+// states, and one launch replays all segments side by side: about
+// (P - 1)/P light + 1/P full chain lengths instead of one full one.
+// A CTA's chain step costs about the same SM time whether it runs alone on an
+// SM or beside others (T=131072, H=32 on GB300: 1.1 k cycles alone, 2.7 k
+// with 2.5 CTAs per SM), so the scan pays only while the plain chains (2 N H
+// CTAs) leave more than half of the SMs idle; then P fills about three replay
+// CTAs per SM (measured there: P = 1, 2, 6, 8 -> 4.25, 3.78, 3.36, 3.42 ms).
+// kda_set_scan_segments forces P.
+constexpr int64_t kScanMinChunks = 64;     // per sequence
+constexpr int64_t kScanMinSegChunks = 16;  // per segment
+constexpr int64_t kScanMaxSegs = 16;
+constexpr int64_t kScanSpareSms = 4;
+std::atomic<int> g_scan_segs{0};           // 0: automatic, 1: off, >= 2: forced
+
+int64_t scan_segments(int64_t NH, int64_t cps, int sm_count) {
+    const int forced = g_scan_segs.load();
+    int64_t P;
+    if (forced == 1) return 1;
+    if (forced >= 2) {
+        P = forced;
+    } else {
+        if (cps < kScanMinChunks || 4 * NH > sm_count - kScanSpareSms) return 1;
+        P = 3 * (sm_count - kScanSpareSms) / (2 * NH);
+        if (P > kScanMaxSegs) P = kScanMaxSegs;
+        if (P > cps / kScanMinSegChunks) P = cps / kScanMinSegChunks;
+    }
+    if (P > cps) P = cps;
+    return P >= 2 ? P : 1;
+}
 
 // SM count of the current device; the sizing-only entry point kda_workspace_bytes
 // may run without a device, and then sizes for GB300's 152 SMs.
@@ -86,11 +112,12 @@ struct Plan {
     int64_t off_bytes = 0;   // chunk offset table
     int64_t ws_bytes = 0;
     int64_t seg_len = 0;     // fixed-length: chunks per sequence
-    // Split replay of long fixed-length sequences (see kSplit*): the first
-    // split_chunks chunks of every sequence are run once to carry the state to
-    // the midpoint (mid_bytes of states), then both halves are replayed at once.
-    int64_t split_chunks = 0;
-    int64_t mid_bytes = 0;
+    // Segment-parallel scan of fixed-length sequences (see kScan*): scan_segs
+    // segments of scan_len chunks; scan_bytes of entry states (P - 1), offsets
+    // and maps (P - 2 each): planes of N H 128 x 128 fp32 after the records.
+    int64_t scan_segs = 1;
+    int64_t scan_len = 0;
+    int64_t scan_bytes = 0;
     // list of chunk-heads for the exact form (one int32 per item of a launch)
     // at the end of the workspace; its two counters sit in the flag block
     int64_t list_bytes = 0;
@@ -131,10 +158,16 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, i
     pl->off_bytes = packed ? align256((N + 1) * 4) : 0;
     pl->ws_bytes = 256 + pl->off_bytes + pl->max_chunks * H * kda::kRecBytes;
     pl->seg_len = (T + 15) / 16;
-    if (!packed && pl->seg_len >= kSplitMinChunks && 2 * (N * H * 2) <= sm_count - kSplitSpareSms) {
-        pl->split_chunks = pl->seg_len / 2;
-        pl->mid_bytes = align256(N * H * 128 * 128 * 4);
-        pl->ws_bytes += pl->mid_bytes;
+    if (!packed) {
+        pl->scan_segs = scan_segments(N * H, pl->seg_len, sm_count);
+        if (pl->scan_segs >= 2) {
+            pl->scan_len = (pl->seg_len + pl->scan_segs - 1) / pl->scan_segs;
+            pl->scan_segs = (pl->seg_len + pl->scan_len - 1) / pl->scan_len;   // none empty
+        }
+        if (pl->scan_segs >= 2) {
+            pl->scan_bytes = (3 * pl->scan_segs - 5) * align256(N * H * 128 * 128 * 4);
+            pl->ws_bytes += pl->scan_bytes;
+        }
     }
     pl->list_bytes = align256(pl->max_chunks * H * 4);
     pl->ws_bytes += pl->list_bytes;
@@ -146,8 +179,8 @@ kda_status plan_sizes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed, i
         if (pl->tokens >= (int64_t(1) << 31)) return KDA_ERR_BAD_SHAPE;
         pl->c64_chunks = packed ? (T + 63 * N) / 64 : B * ((T + 63) / 64);
         if (impl == kImplC64Fused && H + kC64MinBuilders > sm_count) pl->impl = kImplC64Split;
-        pl->split_chunks = 0;
-        pl->mid_bytes = 0;
+        pl->scan_segs = 1;
+        pl->scan_bytes = 0;
         pl->list_bytes = 0;
         if (pl->impl == kImplC64Split) {
             pl->ws_bytes = 256 + pl->off_bytes + pl->c64_chunks * H * kda::kC64RecBytes;
@@ -281,7 +314,7 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const fl
 const char *kda_build_info(void) {
     return "prefill_kda_chunk_gb300 0.4 (sm_103a; 16-token chunks: intra-chunk mma.sync with an "
            "exact form for strong decay, recurrent warp-MMA chain with bulk-async staged records "
-           "and split replay; 64-token chunks on tcgen05 opt-in; decode step; in-kernel q/k "
+           "and a segment-parallel scan for long sequences; 64-token chunks on tcgen05 opt-in; decode step; in-kernel q/k "
            "normalisation and gate logits; token-serial gradients)";
 }
 
@@ -473,18 +506,20 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
     rc = timed_launch(true, stream, [&] { return intra(ip, pl.max_chunks, stream); });
     if (rc != KDA_OK) return rc;
     kda::RecurParams rp{rec, initial_state, out, final_state, st.err, geo};
-    // (an in-place state would be read by one half while the other writes it)
-    if (pl.split_chunks > 0 && (initial_state == nullptr || initial_state != final_state)) {
-        // state to the midpoint of every sequence, then both halves at once
-        float *mid = reinterpret_cast<float *>(rec + pl.max_chunks * H * kda::kRecBytes);
-        kda::RecurParams rl = rp;
-        rl.out = nullptr;
-        rl.s_final = mid;
-        rl.geo.seg_len = static_cast<int32_t>(pl.split_chunks);
-        rp.split_chunks = static_cast<int32_t>(pl.split_chunks);
-        rp.s_mid = mid;
+    // (an in-place state would be read by the first segment while the last
+    // one writes it)
+    if (pl.scan_segs >= 2 && (initial_state == nullptr || initial_state != final_state)) {
+        // segment maps, their serial combine, then every segment at once
+        const int64_t plane = align256(N * H * 128 * 128 * 4);
+        uint8_t *sc = rec + pl.max_chunks * H * kda::kRecBytes;
+        rp.scan_segs = static_cast<int32_t>(pl.scan_segs);
+        rp.scan_len = static_cast<int32_t>(pl.scan_len);
+        rp.seg_entry = reinterpret_cast<float *>(sc);
+        rp.seg_c = reinterpret_cast<float *>(sc + (pl.scan_segs - 1) * plane);
+        rp.seg_m = reinterpret_cast<float *>(sc + (2 * pl.scan_segs - 3) * plane);
         return timed_launch(false, stream, [&] {
-            const cudaError_t e = kda::launch_recurrent_state_only(rl, stream);
+            cudaError_t e = kda::launch_recurrent_scan_maps(rp, stream);
+            if (e == cudaSuccess) e = kda::launch_scan_combine(rp, stream);
             return e != cudaSuccess ? e : kda::launch_recurrent(rp, stream);
         });
     }
@@ -660,6 +695,12 @@ kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *cal
     if (intra_ms) *intra_ms = n ? sum[0] / n : 0.0;
     if (recurrent_ms) *recurrent_ms = n ? sum[1] / n : 0.0;
     if (calls) *calls = n;
+    return KDA_OK;
+}
+
+kda_status kda_set_scan_segments(int segments) {
+    if (segments < 0 || segments > 4096) return KDA_ERR_BAD_SHAPE;
+    g_scan_segs.store(segments);
     return KDA_OK;
 }
 

@@ -55,12 +55,23 @@ struct RecurParams {
     float *s_final;            // [N, H, 128, 128] or nullptr
     int *err;
     ChunkGeometry geo;
-    // Split replay of fixed-length sequences (warp-MMA kernel only): with
-    // split_chunks = c > 0 the launch covers 2N (sequence, half) units; half 0
-    // is chunks [0, c) from s0, half 1 chunks [c, end) from s_mid, and only
-    // half 1 writes s_final.
-    int32_t split_chunks = 0;
-    const float *s_mid = nullptr;  // [N, H, 128, 128]
+    // Segment-parallel scan of fixed-length sequences (cu == nullptr): with
+    // scan_segs = P >= 2 every sequence's chunks are cut into segments of
+    // scan_len chunks (the last one takes the rest). Over a segment the state
+    // map is affine, S_end = M S_begin + c, and M (K x K) evolves like the
+    // state with Ut taken as zero, starting from the identity.
+    //   maps launch (launch_recurrent_scan_maps): units (sequence, segment
+    //     j < P-1) x 4 slices of 64 columns; slices 0-1 carry the state
+    //     columns (from s0 for j = 0, else from zero), slices 2-3 the columns
+    //     of M (j > 0 only). j = 0 writes its end state to seg_entry[0], j > 0
+    //     writes c to seg_c[j-1] and M to seg_m[j-1].
+    //   replay launch (launch_recurrent): units (sequence, segment), segment
+    //     j > 0 starting from seg_entry[j-1]; only the last one writes s_final.
+    int32_t scan_segs = 0;
+    int32_t scan_len = 0;
+    float *seg_entry = nullptr;    // [P-1][N][H][128][128]: entry states of segments 1..P-1
+    float *seg_c = nullptr;        // [P-2][N][H][128][128]
+    float *seg_m = nullptr;        // [P-2][N][H][128][128]
 };
 
 // One-token decode step for N*H independent (sequence, head) units.
@@ -107,8 +118,11 @@ cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStr
 // after every launch_intra_chunk, on the same stream
 cudaError_t launch_intra_exact(const IntraParams &p, cudaStream_t stream);
 cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream);     // warp MMA
-// warp MMA without outputs: only carries the state (to s_final)
-cudaError_t launch_recurrent_state_only(const RecurParams &p, cudaStream_t stream);
+// the maps launch of the segment-parallel scan (RecurParams::scan_segs >= 2)
+cudaError_t launch_recurrent_scan_maps(const RecurParams &p, cudaStream_t stream);
+// its serial combine: seg_entry[j] = seg_m[j-1] seg_entry[j-1] + seg_c[j-1]
+// for j = 1 .. P-2, per (sequence, head); a no-op for P = 2
+cudaError_t launch_scan_combine(const RecurParams &p, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &p, int64_t units, cudaStream_t stream);
 // The gradient kernel is persistent: at most one CTA per resident slot and
 // never more than kBackwardMaxRings, each owning one 16-state ring of the

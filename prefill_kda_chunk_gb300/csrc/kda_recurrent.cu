@@ -45,7 +45,8 @@ struct RecurLayout {
     static constexpr int kSmem = kBars + 2 * kStages * 8;
 };
 
-// OUT = false carries only the state (no output products, no o stores).
+// OUT = false carries only the state (no output products, no o stores): the
+// maps launch of the segment-parallel scan.
 template <int BV, bool OUT>
 __global__ void __launch_bounds__((BV / 16 + 1) * 32)
 kda_recurrent_kernel(RecurParams p) {
@@ -55,9 +56,15 @@ kda_recurrent_kernel(RecurParams p) {
     const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
     const ChunkGeometry &geo = p.geo;
     const int H = geo.n_heads;
-    const int s = blockIdx.x % Lay::kSlices;
-    const int h = (blockIdx.x / Lay::kSlices) % H;
-    const int n = blockIdx.x / (Lay::kSlices * H);   // unit: sequence, or (half, sequence)
+    const bool scan = geo.cu == nullptr && p.scan_segs >= 2;
+    // slices per unit: 2 (value columns), or 4 in the maps launch (value
+    // columns, then the columns of the segment's transition map)
+    const int nsl = scan && !OUT ? 2 * Lay::kSlices : Lay::kSlices;
+    const int sl = blockIdx.x % nsl;
+    const int s = sl % Lay::kSlices;
+    const bool virt = sl >= Lay::kSlices;   // a column slice of the map M
+    const int h = (blockIdx.x / nsl) % H;
+    const int n = blockIdx.x / (nsl * H);   // unit: sequence, or (sequence, segment)
 
     const uint32_t bar_full = smem_u32(smem + Lay::kBars);
     const uint32_t bar_empty = bar_full + kStages * 8;
@@ -76,18 +83,28 @@ kda_recurrent_kernel(RecurParams p) {
     int seq = n;                       // the sequence whose states this CTA reads and writes
     const float *s_in = p.s0;
     float *s_out = p.s_final;
-    if (geo.cu == nullptr && p.split_chunks > 0) {
-        // split replay: half 0 = chunks [0, c) from s0, half 1 = [c, end) from s_mid
-        const int half = n / geo.n_seqs;
-        seq = n % geo.n_seqs;
-        const int64_t c = p.split_chunks;
+    if (scan) {
+        // segment j of sequence seq: chunks [j L, min((j + 1) L, chunks))
+        const int P = p.scan_segs;
+        const int per = OUT ? P : P - 1;   // segments of a sequence in this launch
+        const int j = n % per;
+        seq = n / per;
+        if (virt && j == 0) return;        // the first segment starts from s0: no map
+        const int64_t L = p.scan_len, cps = (geo.seq_len + 15) / 16;
+        const int64_t c0 = j * L, c1 = (j + 1) * L < cps ? (j + 1) * L : cps;
         const int64_t base = static_cast<int64_t>(seq) * geo.seq_len;
-        tb = base + (half ? 16 * c : 0);
-        te = half ? base + geo.seq_len : base + 16 * c;
-        chunk0 = static_cast<int64_t>(seq) * geo.slot_stride + (half ? c : 0);
-        nck = static_cast<int>(half ? (geo.seq_len + 15) / 16 - c : c);
-        s_in = half ? p.s_mid : p.s0;
-        s_out = half ? p.s_final : nullptr;
+        tb = base + 16 * c0;
+        te = base + (16 * c1 < geo.seq_len ? 16 * c1 : geo.seq_len);
+        chunk0 = static_cast<int64_t>(seq) * geo.slot_stride + c0;
+        nck = static_cast<int>(c1 - c0);
+        const int64_t plane = static_cast<int64_t>(geo.n_seqs) * H * kDim * kDim;
+        if (OUT) {
+            s_in = j == 0 ? p.s0 : p.seg_entry + (j - 1) * plane;
+            s_out = j == P - 1 ? p.s_final : nullptr;
+        } else {
+            s_in = j == 0 ? p.s0 : nullptr;
+            s_out = j == 0 ? p.seg_entry : (virt ? p.seg_m : p.seg_c) + (j - 1) * plane;
+        }
     } else if (geo.cu == nullptr) {
         tb = static_cast<int64_t>(n) * geo.seq_len + 16 * static_cast<int64_t>(geo.pos_begin);
         te = static_cast<int64_t>(n) * geo.seq_len + geo.seq_len;
@@ -128,7 +145,17 @@ kda_recurrent_kernel(RecurParams p) {
     const int v0 = s * BV + vw;        // ... within the head
     float acc[16][4];                  // S^T fragments: rows = value, cols = key
     const int64_t sbase = (static_cast<int64_t>(seq) * H + h) * kDim * kDim;
-    if (s_in != nullptr) {
+    if (virt) {
+        // the identity: column v0 + gid (+ 8) of M starts as the unit vector
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const int key = 8 * j + 2 * tig, c = v0 + gid;
+            acc[j][0] = key == c ? 1.f : 0.f;
+            acc[j][1] = key + 1 == c ? 1.f : 0.f;
+            acc[j][2] = key == c + 8 ? 1.f : 0.f;
+            acc[j][3] = key + 1 == c + 8 ? 1.f : 0.f;
+        }
+    } else if (s_in != nullptr) {
         const float *S0 = s_in + sbase;
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -173,9 +200,10 @@ kda_recurrent_kernel(RecurParams p) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
             const int tk = 8 * nt + 2 * tig;
-            const float2 u01 = unpack_bf16(
+            // (a column of the map M has no input term)
+            const float2 u01 = virt ? make_float2(0.f, 0.f) : unpack_bf16(
                 *reinterpret_cast<const uint32_t *>(stg + kRecUt + ((vw + gid) * 16 + tk) * 2));
-            const float2 u23 = unpack_bf16(*reinterpret_cast<const uint32_t *>(
+            const float2 u23 = virt ? make_float2(0.f, 0.f) : unpack_bf16(*reinterpret_cast<const uint32_t *>(
                 stg + kRecUt + ((vw + gid + 8) * 16 + tk) * 2));
             uT[nt][0][0] = u01.x; uT[nt][0][1] = u01.y; uT[nt][0][2] = u23.x; uT[nt][0][3] = u23.y;
 #pragma unroll
@@ -281,13 +309,69 @@ kda_recurrent_kernel(RecurParams p) {
     }
 }
 
+// Serial combine of the segment-parallel scan, one CTA per (sequence, head,
+// block of 32 value columns): E_{j+1} = M_j E_j + c_j in fp32 for the entry
+// states E of segments 2 .. P-1, the column block of E kept in shared memory
+// and M_j staged there whole.
+constexpr int kCombineCols = 32;
+constexpr int kCombineSmem = (kDim * kDim + 2 * kDim * kCombineCols) * 4;
+
+__global__ void __launch_bounds__(256) kda_scan_combine_kernel(RecurParams p) {
+    extern __shared__ __align__(16) float csm[];
+    float *Ms = csm;                              // [128][128]
+    float *E = csm + kDim * kDim;                 // [2][128][32]
+    const int tid = threadIdx.x;
+    const int nblk = kDim / kCombineCols;
+    const int cb = blockIdx.x % nblk;
+    const int64_t unit = blockIdx.x / nblk;       // sequence * H + head
+    const int64_t plane = static_cast<int64_t>(p.geo.n_seqs) * p.geo.n_heads * kDim * kDim;
+    const int64_t ub = unit * kDim * kDim;
+    // thread: row r = tid / 2, columns 16 (tid % 2) .. + 15 of the block
+    const int r = tid >> 1, c0 = 16 * (tid & 1);
+    for (int i = tid; i < kDim * kCombineCols; i += 256)
+        E[i] = p.seg_entry[ub + (i / kCombineCols) * kDim + cb * kCombineCols + i % kCombineCols];
+    for (int j = 1; j + 1 < p.scan_segs; ++j) {
+        const float *Mg = p.seg_m + (j - 1) * plane + ub;
+        const float *Cg = p.seg_c + (j - 1) * plane + ub;
+        float *Eo = p.seg_entry + j * plane + ub;
+        const float *Ein = E + ((j - 1) & 1) * kDim * kCombineCols;
+        float *Eout = E + (j & 1) * kDim * kCombineCols;
+        __syncthreads();   // the previous step's E is complete and Ms is free
+        for (int i = tid; i < kDim * kDim / 4; i += 256)
+            reinterpret_cast<float4 *>(Ms)[i] = reinterpret_cast<const float4 *>(Mg)[i];
+        __syncthreads();
+        float acc[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) acc[c] = Cg[r * kDim + cb * kCombineCols + c0 + c];
+        for (int m = 0; m < kDim; ++m) {
+            const float a = Ms[r * kDim + m];
+            const float4 *e4 = reinterpret_cast<const float4 *>(Ein + m * kCombineCols + c0);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 e = e4[q4];
+                acc[4 * q4] = fmaf(a, e.x, acc[4 * q4]);
+                acc[4 * q4 + 1] = fmaf(a, e.y, acc[4 * q4 + 1]);
+                acc[4 * q4 + 2] = fmaf(a, e.z, acc[4 * q4 + 2]);
+                acc[4 * q4 + 3] = fmaf(a, e.w, acc[4 * q4 + 3]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            Eout[r * kCombineCols + c0 + c] = acc[c];
+            Eo[r * kDim + cb * kCombineCols + c0 + c] = acc[c];
+        }
+    }
+}
+
 constexpr int kBV = 64;
 
 template <bool OUT>
 cudaError_t launch(const RecurParams &p, cudaStream_t stream) {
     using Lay = RecurLayout<kBV>;
-    const int64_t units = static_cast<int64_t>(p.geo.n_seqs) * (p.split_chunks > 0 ? 2 : 1);
-    const int64_t ctas = units * p.geo.n_heads * Lay::kSlices;
+    const bool scan = p.geo.cu == nullptr && p.scan_segs >= 2;
+    const int64_t per = scan ? (OUT ? p.scan_segs : p.scan_segs - 1) : 1;
+    const int64_t units = static_cast<int64_t>(p.geo.n_seqs) * per;
+    const int64_t ctas = units * p.geo.n_heads * Lay::kSlices * (scan && !OUT ? 2 : 1);
     if (ctas <= 0) return cudaSuccess;
     kda_recurrent_kernel<kBV, OUT><<<static_cast<unsigned>(ctas), (Lay::kWarps + 1) * 32,
                                      Lay::kSmem, stream>>>(p);
@@ -301,17 +385,27 @@ cudaError_t configure_recurrent() {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          RecurLayout<kBV>::kSmem);
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(kda_recurrent_kernel<kBV, false>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                RecurLayout<kBV>::kSmem);
+    e = cudaFuncSetAttribute(kda_recurrent_kernel<kBV, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, RecurLayout<kBV>::kSmem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(kda_scan_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kCombineSmem);
 }
 
 cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream) {
     return launch<true>(p, stream);
 }
 
-cudaError_t launch_recurrent_state_only(const RecurParams &p, cudaStream_t stream) {
+cudaError_t launch_recurrent_scan_maps(const RecurParams &p, cudaStream_t stream) {
     return launch<false>(p, stream);
+}
+
+cudaError_t launch_scan_combine(const RecurParams &p, cudaStream_t stream) {
+    if (p.scan_segs <= 2) return cudaSuccess;
+    const int64_t ctas = static_cast<int64_t>(p.geo.n_seqs) * p.geo.n_heads * (kDim / kCombineCols);
+    if (ctas <= 0) return cudaSuccess;
+    kda_scan_combine_kernel<<<static_cast<unsigned>(ctas), 256, kCombineSmem, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

@@ -52,11 +52,42 @@ def test_workspace_bytes(lib):
     # packed batches: the chunk offsets after the flag block
     pc = (8192 + 15 * 16) // 16
     assert K.kda_workspace_bytes(1, 8192, 64, 16, 1) == 256 + 256 + pc * 64 * REC + lst(pc * 64)
-    # long sequences with few heads: records plus the midpoint states of the split replay
-    assert K.kda_workspace_bytes(1, 131072, 32, 1, 0) == (256 + 8192 * 32 * REC + 32 * 65536
+    # long sequences with few heads: records plus the segment scan's entry
+    # states, offsets and maps (3 P - 5 planes of N H 64 KiB); without a GPU
+    # the library sizes for 152 SMs: with 4 N H <= 148, P = 3 (152 - 4) // (2 N H),
+    # at most 16 and at least 16 chunks per segment, then no segment left empty
+    def planes(nh, cps):
+        if cps < 64 or 4 * nh > 148:
+            return 0
+        P = min(3 * (152 - 4) // (2 * nh), 16, cps // 16)
+        if P < 2:
+            return 0
+        L = -(-cps // P)
+        P = -(-cps // L)
+        return 3 * P - 5 if P >= 2 else 0
+
+    assert planes(32, 8192) == 13                    # P = 6
+    assert K.kda_workspace_bytes(1, 131072, 32, 1, 0) == (256 + 8192 * 32 * REC + 13 * 32 * 65536
                                                          + lst(8192 * 32))
-    assert K.kda_workspace_bytes(2, 2000, 3, 2, 0) == (256 + 2 * 125 * 3 * REC + 6 * 65536
+    assert planes(64, 512) == 0                      # T8192 H64: the plain chains fill the SMs
+    assert K.kda_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 512 * 64 * REC + lst(512 * 64)
+    assert planes(6, 125) == 16                      # P = 7
+    assert K.kda_workspace_bytes(2, 2000, 3, 2, 0) == (256 + 2 * 125 * 3 * REC + 16 * 6 * 65536
                                                       + lst(2 * 125 * 3))
+    # forced segment counts, and off
+    try:
+        for P, expect in ((3, 4), (8, 19), (1, 0)):
+            assert K.kda_set_scan_segments(P) == 0
+            assert K.kda_workspace_bytes(1, 131072, 32, 1, 0) == (256 + 8192 * 32 * REC
+                                                                 + expect * 32 * 65536
+                                                                 + lst(8192 * 32))
+        assert K.kda_set_scan_segments(200) == 0     # more segments than 125 chunks allow
+        assert K.kda_workspace_bytes(2, 2000, 3, 2, 0) == (256 + 2 * 125 * 3 * REC
+                                                          + (3 * 125 - 5) * 6 * 65536
+                                                          + lst(2 * 125 * 3))
+        assert K.kda_set_scan_segments(-1) != 0 and K.kda_set_scan_segments(5000) != 0
+    finally:
+        K.kda_set_scan_segments(0)
     assert K.kda_workspace_bytes(1, 1008, 3, 1, 0) == 256 + 63 * 3 * REC + lst(63 * 3)  # < 64 chunks
     assert K.kda_workspace_bytes(1, 8192, 38, 1, 0) == 256 + 512 * 38 * REC + lst(512 * 38)  # 4*38 > 152 - 4 (no device here: sized for 152 SMs)
     assert K.kda_workspace_bytes(1, 8192, 64, 2, 0) == 0      # N != B without cu_seqlens

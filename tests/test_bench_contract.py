@@ -43,10 +43,13 @@ def test_launches_per_call():
     # intra-chunk kernel, its exact-form companion, recurrent kernel
     assert n["fixed_T8192_H64"] == 3 and n["fixed_T8192_H96"] == 3
     assert n["varlen16_T8192_H64"] == 4            # + the cu_seqlens prologue
-    assert n["long_T131072_H32"] == 4              # + the split replay's state-only pass
+    assert n["long_T131072_H32"] == 5              # + the segment scan's maps and combine (P = 6)
+    assert b.scan_segments(32, 8192, 152) == 6 and b.scan_segments(64, 512, 152) == 1
     args = _Args()
-    args.recurrent_impl = 3                        # the split replay is 16-token only
-    assert b.launches_per_call(KI.WORKLOADS["long_T131072_H32"], args) == 3
+    args.recurrent_impl = 3                        # 64-token split: intra-chunk + recurrent
+    assert b.launches_per_call(KI.WORKLOADS["long_T131072_H32"], args) == 2
+    args.recurrent_impl = 4                        # 64-token fused: one cooperative kernel
+    assert b.launches_per_call(KI.WORKLOADS["varlen16_T8192_H64"], args) == 2
 
 
 def test_backward_byte_counts():

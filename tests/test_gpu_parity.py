@@ -193,21 +193,21 @@ def test_in_place_state_and_no_final_state():
     assert f2 is None and torch.equal(o2, o)
 
 
-def test_split_replay_strong_decay():
-    """The exact form ahead of the split replay (state-only pass to the
-    midpoint, then both halves), every other channel at -6 per token."""
+def test_segment_scan_strong_decay():
+    """The exact form ahead of the segment-parallel scan (segment maps, their
+    combine, then every segment at once), every other channel at -6 per token."""
     d = KI.make_case([1100], H=2, seed=46, init_state=True)
     d["g"][:, :, ::2] = -6.0
     o, f = run_gpu(d, packed=False)
-    assert_parity(o, f, *run_oracle(d), "split replay, strong decay")
+    assert_parity(o, f, *run_oracle(d), "segment scan, strong decay")
 
 
 @pytest.mark.parametrize("T,B,init", [(1024, 1, False), (2003, 1, True), (1040, 3, True),
                                       (4096, 2, False)])
-def test_split_replay_lengths(T, B, init):
-    """Long fixed-length sequences with few heads take the split replay on the
-    warp-MMA kernel (state to the midpoint, then both halves at once): odd
-    chunk counts, a partial last chunk, several sequences."""
+def test_segment_scan_lengths(T, B, init):
+    """Long fixed-length sequences with few heads take the segment-parallel
+    scan on the 16-token path (here 4 to 16 segments, chosen from the SM
+    count): odd chunk counts, a partial last chunk, several sequences."""
     H = 2
     d = KI.make_case([T] * B, H=H, seed=T + B, init_state=init)
     x = to_dev(d)
@@ -219,8 +219,8 @@ def test_split_replay_lengths(T, B, init):
     assert_parity(o.view(B * T, H, 128), f, o_ref, f_ref)
 
 
-def test_split_replay_in_place_state():
-    """An in-place state never takes the split replay, and gives the same
+def test_segment_scan_in_place_state():
+    """An in-place state never takes the segment scan, and gives the same
     result as an out-of-place call."""
     T, H = 2048, 2
     d = KI.make_case([T], H=H, seed=8, init_state=True)
@@ -234,6 +234,57 @@ def test_split_replay_in_place_state():
     o_ref, f_ref = run_oracle(d)
     assert_parity(o2, st, o_ref, f_ref)
     assert_parity(o1, f1, o_ref, f_ref)
+
+
+def scan_case(d, segments):
+    """One fixed-length call with the segment count forced."""
+    x = to_dev(d)
+    B = len(d["seqlens"])
+    T = d["seqlens"][0]
+    q4 = {n: x[n].view(B, T, *x[n].shape[1:]) for n in ("q", "k", "v", "g", "beta")}
+    try:
+        assert K.kda_set_scan_segments(segments) == 0
+        o, f = K.chunk_prefill(q4["q"], q4["k"], q4["v"], q4["g"], q4["beta"],
+                               initial_state=x["initial_state"], scale=d["scale"])
+        K.check_device_error()
+    finally:
+        K.kda_set_scan_segments(0)
+    return o.view(B * T, *o.shape[2:]), f
+
+
+@pytest.mark.parametrize("mu", [3.0, 7.0], ids=["decay", "weak_decay"])
+@pytest.mark.parametrize("P", [2, 3, 8, 40])
+def test_segment_scan_segments(P, mu, recurrent_impl):
+    """P segments per sequence (segment maps built from the identity, the
+    serial combine for P > 2, the replay): against the token recurrence and
+    against the oracle's own segment-parallel form with P segments. 40
+    segments of 3 or 4 chunks each on 126 chunks. With weak decay (log decay
+    about -1e-3 per token) the entry states, hence the maps, carry over whole
+    segments."""
+    if recurrent_impl != 1:
+        pytest.skip("the segment scan is on the 16-token path")
+    import oracle
+    d = KI.make_case([2003] * 2, H=2, seed=90 + P, init_state=True, mu=mu)
+    o, f = scan_case(d, P)
+    o_ref, f_ref = run_oracle(d)
+    assert_parity(o, f, o_ref, f_ref, f"scan P={P}")
+    o_s, f_s = oracle.segment_scan(d["q"], d["k"], d["v"], d["g"], d["beta"],
+                                   initial_state=d["initial_state"], cu_seqlens=d["cu_seqlens"],
+                                   scale=d["scale"], segments=P)
+    assert_parity(o, f, o_s, f_s, f"scan P={P} vs oracle segments")
+
+
+def test_segment_scan_long_all_outputs(recurrent_impl):
+    """T = 32768, H = 4, 8 segments of 256 chunks: every output token of
+    every segment against the token recurrence, with a strongly decaying head
+    (the exact form inside the segment maps) and a weakly decaying one."""
+    if recurrent_impl != 1:
+        pytest.skip("the segment scan is on the 16-token path")
+    d = KI.make_case([32768], H=4, seed=97, init_state=True)
+    d["g"][:, 3, ::3] = -6.0
+    d["g"][:, 2, :] *= 0.02          # weak decay: the state carries across segments
+    o, f = scan_case(d, 8)
+    assert_parity(o, f, *run_oracle(d), "scan P=8 long")
 
 
 def test_deterministic():
