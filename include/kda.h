@@ -298,6 +298,20 @@ KDA_API kda_status kda_stage_timing_begin(int max_calls);
 KDA_API kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *calls);
 
 /*
+ * Test hook for the device-timeout report (process-wide, host only; not for
+ * production use). For later calls on the 16-token path, the record producer
+ * of every recurrent CTA issues no copy for chunk `chunk` of its sequence or
+ * any later one, and both roles of that kernel give up a wait after `wait_ns`
+ * nanoseconds (0: the default of 2 s). The consumers' wait for that chunk
+ * then runs out: they record KDA_ERR_DEVICE_TIMEOUT in the device error word
+ * and leave (outputs from that chunk on and the final state are then
+ * unspecified). Every copy the producer did issue is waited for, so none is
+ * in flight when a CTA exits. chunk = -1 turns the hook off (the default).
+ * chunk < -1 or wait_ns < 0: KDA_ERR_BAD_SHAPE.
+ */
+KDA_API kda_status kda_test_stall_recurrent(int chunk, int64_t wait_ns);
+
+/*
  * Segments of the segment-parallel scan for later fixed-length calls on the
  * 16-token path (process-wide, host only): 0 (default) = chosen from the SM
  * count as described for kda_chunk_prefill, 1 = off (one chain per

@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     kda_last_device_error,
     kda_set_recurrent_impl,
     kda_set_scan_segments,
+    kda_test_stall_recurrent,
     kda_stage_timing_begin,
     kda_stage_timing_end,
     kda_status_string,

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.kda_set_recurrent_impl.argtypes = [ctypes.c_int]
             L.kda_set_scan_segments.restype = ctypes.c_int
             L.kda_set_scan_segments.argtypes = [ctypes.c_int]
+            L.kda_test_stall_recurrent.restype = ctypes.c_int
+            L.kda_test_stall_recurrent.argtypes = [ctypes.c_int, i64]
             L.kda_build_info.restype = ctypes.c_char_p
             L.kda_build_info.argtypes = []
             _lib = L
@@ -167,6 +169,12 @@ def kda_set_scan_segments(segments: int) -> int:
     """Segment-parallel scan for fixed-length calls: 0 = automatic, 1 = off,
     P >= 2 = P segments per sequence."""
     return lib().kda_set_scan_segments(int(segments))
+
+
+def kda_test_stall_recurrent(chunk: int, wait_ns: int = 0) -> int:
+    """Test hook: the recurrent kernel's record producer stops before `chunk`
+    and its waits give up after `wait_ns` (-1: off)."""
+    return lib().kda_test_stall_recurrent(int(chunk), int(wait_ns))
 
 
 def kda_build_info() -> str:

@@ -71,6 +71,9 @@ constexpr int64_t kScanMinSegChunks = 16;  // per segment
 constexpr int64_t kScanMaxSegs = 16;
 constexpr int64_t kScanSpareSms = 4;
 std::atomic<int> g_scan_segs{0};           // 0: automatic, 1: off, >= 2: forced
+// test hook of the recurrent kernel (kda_test_stall_recurrent)
+std::atomic<int> g_stall_chunk{-1};
+std::atomic<long long> g_stall_wait_ns{0};
 
 int64_t scan_segments(int64_t NH, int64_t cps, int sm_count) {
     const int forced = g_scan_segs.load();
@@ -506,6 +509,8 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
     rc = timed_launch(true, stream, [&] { return intra(ip, pl.max_chunks, stream); });
     if (rc != KDA_OK) return rc;
     kda::RecurParams rp{rec, initial_state, out, final_state, st.err, geo};
+    rp.stall_chunk = g_stall_chunk.load();
+    rp.wait_ns = static_cast<unsigned long long>(g_stall_wait_ns.load());
     // (an in-place state would be read by the first segment while the last
     // one writes it)
     if (pl.scan_segs >= 2 && (initial_state == nullptr || initial_state != final_state)) {
@@ -695,6 +700,13 @@ kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, int *cal
     if (intra_ms) *intra_ms = n ? sum[0] / n : 0.0;
     if (recurrent_ms) *recurrent_ms = n ? sum[1] / n : 0.0;
     if (calls) *calls = n;
+    return KDA_OK;
+}
+
+kda_status kda_test_stall_recurrent(int chunk, int64_t wait_ns) {
+    if (chunk < -1 || wait_ns < 0) return KDA_ERR_BAD_SHAPE;
+    g_stall_chunk.store(chunk);
+    g_stall_wait_ns.store(chunk < 0 ? 0 : wait_ns);
     return KDA_OK;
 }
 

@@ -72,6 +72,12 @@ struct RecurParams {
     float *seg_entry = nullptr;    // [P-1][N][H][128][128]: entry states of segments 1..P-1
     float *seg_c = nullptr;        // [P-2][N][H][128][128]
     float *seg_m = nullptr;        // [P-2][N][H][128][128]
+    // Test hook (kda_test_stall_recurrent): the record producer of every CTA
+    // issues no copy for chunk stall_chunk and later ones (-1: off), and both
+    // roles give up a wait after wait_ns (0: the default limit). A copy that
+    // was issued is always waited for, so none is in flight at exit.
+    int32_t stall_chunk = -1;
+    unsigned long long wait_ns = 0;
 };
 
 // One-token decode step for N*H independent (sequence, head) units.

@@ -119,14 +119,16 @@ kda_recurrent_kernel(RecurParams p) {
     }
     const uint8_t *rec0 = p.rec + (chunk0 * H + h) * static_cast<int64_t>(kRecBytes);
     const uint32_t stage0 = smem_u32(smem);
+    const unsigned long long wait_ns = p.wait_ns ? p.wait_ns : kWaitLimitNs;
 
     if (warp == Lay::kWarps) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
             for (int i = 0; i < nck; ++i) {
+                if (i == p.stall_chunk) break;   // test hook: the consumers' wait runs out
                 const int st = i % kStages;
                 if (i >= kStages &&
-                    !mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1)) {
+                    !mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1, wait_ns)) {
                     atomicOr(p.err, kErrTimeout);
                     break;
                 }
@@ -178,7 +180,7 @@ kda_recurrent_kernel(RecurParams p) {
     const int64_t ostep = 16 * static_cast<int64_t>(H) * kDim;
     for (int i = 0; i < nck; ++i) {
         const int st = i % kStages;
-        if (!ready && !mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
+        if (!ready && !mbar_wait(bar_full + 8 * st, (i / kStages) & 1, wait_ns)) {
             atomicOr(p.err, kErrTimeout);
             break;
         }
