@@ -65,6 +65,12 @@ def parse():
                     help="mean of the gate pre-activation (g = logsigmoid(N(mu, 1))) instead of "
                          "the workload's; about -6 or below puts every chunk-head outside the "
                          "factored range (the exact form)")
+    ap.add_argument("--scan-segments", type=int, default=None,
+                    help="segments of the 16-token path's segment-parallel scan (0 = automatic, "
+                         "1 = off; library default if unset)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="run the workload with this many heads instead (a smaller case for "
+                         "profiler captures; the line's config then says so)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 2000 if args.impl == "ours" else 50
@@ -240,6 +246,8 @@ def run_reference(args, rank, world):
     w = KI.WORKLOADS[args.workload]
     if args.gate_mu is not None:
         w = dataclasses.replace(w, mu=args.gate_mu)
+    if args.heads is not None:
+        w = dataclasses.replace(w, H=args.heads)
     d = KI.make_inputs(w)
     cores = len(os.sched_getaffinity(0))
     # one head per host core (the oracle runs one (sequence, head) per thread);
@@ -419,6 +427,8 @@ def main():
     K.lib()
     if args.recurrent_impl is not None:
         K.kda_set_recurrent_impl(args.recurrent_impl)
+    if args.scan_segments is not None:
+        K.kda_set_scan_segments(args.scan_segments)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     if args.decode:
@@ -436,6 +446,8 @@ def main():
     w = KI.WORKLOADS[args.workload]
     if args.gate_mu is not None:
         w = dataclasses.replace(w, mu=args.gate_mu)
+    if args.heads is not None:
+        w = dataclasses.replace(w, H=args.heads)
     if args.backward:
         hbm, _, _ = load_peaks()
         line = bench_backward(K, dev, w, args, hbm)
