@@ -19,9 +19,9 @@ namespace {
 struct StreamWorkspace {
     void *ptr = nullptr;
     size_t bytes = 0;
-    // bytes at offset 256 known to hold zeros for the 64-token ring counters
-    // (a fused launch leaves its counters zero; any other use of the buffer
-    // may overwrite them)
+    // bytes at offset 256 known to hold zeros for the fused launch's ring
+    // counters (a fused launch leaves its own counters zero and writes past
+    // them; any other use of the buffer may overwrite them)
     int64_t ring_clean = 0;
 };
 
@@ -109,7 +109,7 @@ int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 struct Plan {
     int impl = 1;            // recurrent kernel / path actually used (see g_recur_impl)
     int64_t c64_chunks = 0;  // 64-token paths: chunks of the call (upper bound when packed)
-    int64_t c64_sync = 0;    // fused 64-token path: byte offset of the ring counters
+    int64_t c64_sync = 0;    // fused 64-token path: bytes of the ring counters after the flag block
     int64_t tokens = 0;      // total tokens
     int64_t max_chunks = 0;  // chunk records of one launch (upper bound when packed)
     int64_t off_bytes = 0;   // chunk offset table
@@ -465,10 +465,12 @@ kda_status kda_chunk_prefill_ex(const void *q, const void *k, const void *v, con
         if (pl.tokens == 0)   // nothing for the builders: the chains alone carry the states
             return timed_launch(false, stream, [&] { return kda::launch_c64_chain(a, stream); });
         long long *sync = reinterpret_cast<long long *>(wsb + 256);
-        if (ws.ring_clean < pl.c64_sync) {
-            if (cudaMemsetAsync(sync, 0, pl.c64_sync, stream) != cudaSuccess) return KDA_ERR_CUDA;
-            ws.ring_clean = pl.c64_sync;   // each fused launch leaves its counters zero again
-        }
+        if (ws.ring_clean < pl.c64_sync &&
+            cudaMemsetAsync(sync, 0, pl.c64_sync, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        // the launch leaves its own counters zero again; what lies past them
+        // (chunk offsets, ring) is not, whatever a larger layout needs there
+        ws.ring_clean = pl.c64_sync;
         a.ring_depth = static_cast<int>(kC64Ring);
         a.n_chain = static_cast<int>(H);
         a.ready = sync;

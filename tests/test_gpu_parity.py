@@ -287,6 +287,17 @@ def test_segment_scan_long_all_outputs(recurrent_impl):
     assert_parity(o, f, *run_oracle(d), "scan P=8 long")
 
 
+def test_head_count_changes_between_calls():
+    """7 heads, then 2, then 7 again on one stream (one workspace, never
+    regrown): on the fused 64-token path the 2-head call puts its chunk
+    offsets where the 7-head layout keeps ring counters, which the third call
+    must find zeroed again."""
+    for H, seqlens, seed in ((7, [150, 50], 120), (2, [100, 90], 121), (7, [150, 50], 122)):
+        d = KI.make_case(seqlens, H=H, seed=seed, init_state=True)
+        o, f = run_gpu(d)
+        assert_parity(o, f, *run_oracle(d), f"H={H}")
+
+
 def test_deterministic():
     d = KI.make_case([300], H=4, seed=13, init_state=True)
     o1, f1 = run_gpu(d, packed=False)
