@@ -32,6 +32,13 @@ UNIT = "tokens/s"
 # Counted work of the chunked algorithm (dense 16-token tiles, 2 FLOP/MAC).
 FLOPS_INTRA_PER_CHUNK_HEAD = 262144 + 2731     # gated Gram + scores, W, Ut; inversion
 FLOPS_RECUR_PER_CHUNK_HEAD = 1638400           # W S, Qg S, P U, Kd^T U
+# 64-token path, per (64-token chunk, head): the chain's W S, Qg S, P U and
+# Kd^T U (2 x 64 x 128 x 128 each, P U 2 x 64 x 64 x 128); the record
+# builder's Gram and scores (2 x 128 x 64 x 128), W and Ut (2 x 64 x 64 x 128
+# each) and the 64 x 64 inversion (64^3 / 3)
+FLOPS_C64_CHAIN_PER_CHUNK_HEAD = 3 * 2097152 + 1048576
+FLOPS_C64_INTRA_PER_CHUNK_HEAD = 2097152 + 2 * 1048576 + 87381
+FLOPS_C64_PER_CHUNK_HEAD = FLOPS_C64_CHAIN_PER_CHUNK_HEAD + FLOPS_C64_INTRA_PER_CHUNK_HEAD
 BYTES_IN_PER_TOKEN_HEAD = 3 * 256 + 512 + 4    # q, k, v bf16; g fp32; beta fp32
 BYTES_OUT_PER_TOKEN_HEAD = 256                 # o bf16
 STATE_BYTES = 128 * 128 * 4
@@ -122,7 +129,8 @@ def workload_counts(d, H):
     init = d["initial_state"] is not None
     intra_bytes = tokens * H * BYTES_IN_PER_TOKEN_HEAD
     recur_bytes = tokens * H * BYTES_OUT_PER_TOKEN_HEAD + n * H * STATE_BYTES * (1 + int(init))
-    return dict(tokens=tokens, chunk_heads=chunks * H, n_seqs=n,
+    c64 = sum((L + 63) // 64 for L in lens)
+    return dict(tokens=tokens, chunk_heads=chunks * H, n_seqs=n, c64_chunk_heads=c64 * H,
                 intra_bytes=intra_bytes, recur_bytes=recur_bytes,
                 path_bytes=intra_bytes + recur_bytes,
                 intra_flops=chunks * H * FLOPS_INTRA_PER_CHUNK_HEAD,
@@ -596,18 +604,33 @@ def main():
     sec = ms / 1e3 / args.steps
     value = world * cnt["tokens"] * args.steps / (ms / 1e3)
 
-    kernels = {
-        "kda_intra_chunk_kernel": {
-            "ms": intra_ms, "bound": "hbm", "alg_bytes": cnt["intra_bytes"],
-            "alg_flops": cnt["intra_flops"],
-            "achieved_gbs": cnt["intra_bytes"] / (intra_ms / 1e3) / 1e9,
-            "frac": cnt["intra_bytes"] / (intra_ms / 1e3) / 1e9 / hbm},
-        "kda_recurrent_kernel": {
-            "ms": recur_ms, "bound": "tensor", "alg_bytes": cnt["recur_bytes"],
-            "alg_flops": cnt["recur_flops"],
-            "achieved_tflops": cnt["recur_flops"] / (recur_ms / 1e3) / 1e12,
-            "frac": cnt["recur_flops"] / (recur_ms / 1e3) / 1e12 / tf},
-    }
+    impl = 1 if args.recurrent_impl is None else args.recurrent_impl
+
+    def hbm_kernel(ms_, nbytes, flops):
+        gbs = nbytes / (ms_ / 1e3) / 1e9
+        return {"ms": ms_, "bound": "hbm", "alg_bytes": nbytes, "alg_flops": flops,
+                "achieved_gbs": gbs, "frac": gbs / hbm}
+
+    def tc_kernel(ms_, nbytes, flops):
+        tfs = flops / (ms_ / 1e3) / 1e12
+        return {"ms": ms_, "bound": "tensor", "alg_bytes": nbytes, "alg_flops": flops,
+                "achieved_tflops": tfs, "frac": tfs / tf}
+
+    c64_chunk_heads = cnt["c64_chunk_heads"]
+    if impl == 4:
+        # one cooperative kernel: the whole path's bytes
+        kernels = {"kda_c64_fused_kernel": hbm_kernel(recur_ms, cnt["path_bytes"],
+                                                      c64_chunk_heads * FLOPS_C64_PER_CHUNK_HEAD)}
+    elif impl == 3:
+        kernels = {
+            "kda_c64_intra_kernel": hbm_kernel(intra_ms, cnt["intra_bytes"],
+                                               c64_chunk_heads * FLOPS_C64_INTRA_PER_CHUNK_HEAD),
+            "kda_c64_chain_kernel": tc_kernel(recur_ms, cnt["recur_bytes"],
+                                              c64_chunk_heads * FLOPS_C64_CHAIN_PER_CHUNK_HEAD)}
+    else:
+        kernels = {
+            "kda_intra_chunk_kernel": hbm_kernel(intra_ms, cnt["intra_bytes"], cnt["intra_flops"]),
+            "kda_recurrent_kernel": tc_kernel(recur_ms, cnt["recur_bytes"], cnt["recur_flops"])}
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     kd = kernels[dom]
     if kd["bound"] == "hbm":
