@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     kda_chunk_prefill_ex,
     kda_chunk_prefill_noalloc,
     kda_last_device_error,
+    kda_set_backward_impl,
     kda_set_recurrent_impl,
     kda_set_scan_segments,
     kda_test_stall_recurrent,

@@ -79,6 +79,8 @@ def lib() -> ctypes.CDLL:
             L.kda_set_recurrent_impl.argtypes = [ctypes.c_int]
             L.kda_set_scan_segments.restype = ctypes.c_int
             L.kda_set_scan_segments.argtypes = [ctypes.c_int]
+            L.kda_set_backward_impl.restype = ctypes.c_int
+            L.kda_set_backward_impl.argtypes = [ctypes.c_int]
             L.kda_test_stall_recurrent.restype = ctypes.c_int
             L.kda_test_stall_recurrent.argtypes = [ctypes.c_int, i64]
             L.kda_build_info.restype = ctypes.c_char_p
@@ -169,6 +171,11 @@ def kda_set_scan_segments(segments: int) -> int:
     """Segment-parallel scan for fixed-length calls: 0 = automatic, 1 = off,
     P >= 2 = P segments per sequence."""
     return lib().kda_set_scan_segments(int(segments))
+
+
+def kda_set_backward_impl(impl: int) -> int:
+    """Gradients: 0 = chunked (default), 1 = token-serial."""
+    return lib().kda_set_backward_impl(int(impl))
 
 
 def kda_test_stall_recurrent(chunk: int, wait_ns: int = 0) -> int:

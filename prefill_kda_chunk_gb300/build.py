@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libkda_gb300.so")
 SOURCES = ["kda_api.cu", "kda_intra.cu", "kda_recurrent.cu", "kda_noalloc.cu", "kda_decode.cu",
-           "kda_backward.cu", "kda_c64.cu"]
+           "kda_backward.cu", "kda_backward_chunk.cu", "kda_c64.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}", f"-I{CSRC}"]

@@ -71,6 +71,7 @@ constexpr int64_t kScanMinSegChunks = 16;  // per segment
 constexpr int64_t kScanMaxSegs = 16;
 constexpr int64_t kScanSpareSms = 4;
 std::atomic<int> g_scan_segs{0};           // 0: automatic, 1: off, >= 2: forced
+std::atomic<int> g_bwd_impl{0};            // gradients: 0 chunked, 1 token-serial
 // test hook of the recurrent kernel (kda_test_stall_recurrent)
 std::atomic<int> g_stall_chunk{-1};
 std::atomic<long long> g_stall_wait_ns{0};
@@ -207,6 +208,7 @@ kda_status init_device(int dev, DeviceState &st) {
     if (kda::configure_intra() != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_recurrent() != cudaSuccess) return KDA_ERR_CUDA;
     if (kda::configure_c64() != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::configure_backward_chunk() != cudaSuccess) return KDA_ERR_CUDA;
     st.ready = true;
     return KDA_OK;
 }
@@ -542,8 +544,16 @@ static int64_t backward_ckpt_bytes(int64_t B, int64_t T, int64_t H, int64_t N, b
     return chunks * H * 128 * 128 * 4;
 }
 
+// Chunked gradients: flag block, chunk offsets (packed), the records, the
+// exact-form list, then S^T and dS_next^T of every chunk-head in bf16.
+static int64_t backward_chunk_ws_bytes(int64_t H, const Plan &pl) {
+    const int64_t ch = pl.max_chunks * H;
+    return 256 + pl.off_bytes + ch * kda::kRecBytes + align256(ch * 4) + 2 * ch * kda::kDim * kda::kDim * 2;
+}
+
 static int64_t backward_ws_bytes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed,
                                  const Plan &pl) {
+    if (g_bwd_impl.load() == 0) return backward_chunk_ws_bytes(H, pl);
     const int64_t rings = N * H < kda::kBackwardMaxRings ? N * H : kda::kBackwardMaxRings;
     return 256 + pl.off_bytes + backward_ckpt_bytes(B, T, H, N, packed, pl) +
            rings * 16 * 128 * 128 * 4;
@@ -655,11 +665,59 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
                                     reinterpret_cast<int32_t *>(wsb + 256),
                                     reinterpret_cast<int *>(wsb), st.err, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
+    if (g_bwd_impl.load() == 0) {
+        // chunked: records, the forward chain keeping chunk-entry states, the
+        // reverse chain keeping dS_next, then the chunk-parallel gradients
+        if (pl.tokens == 0) {
+            // no chunks: dL/d(initial state) = dL/d(final state)
+            if (d_initial_state != nullptr) {
+                const size_t ns = static_cast<size_t>(N * H) * 128 * 128 * 4;
+                const cudaError_t e = d_final_state != nullptr
+                    ? cudaMemcpyAsync(d_initial_state, d_final_state, ns, cudaMemcpyDeviceToDevice, stream)
+                    : cudaMemsetAsync(d_initial_state, 0, ns, stream);
+                if (e != cudaSuccess) return KDA_ERR_CUDA;
+            }
+            return KDA_OK;
+        }
+        const int64_t ch = pl.max_chunks * H;
+        uint8_t *rec = wsb + 256 + pl.off_bytes;
+        int32_t *exact_list = reinterpret_cast<int32_t *>(rec + ch * kda::kRecBytes);
+        uint8_t *ck = rec + ch * kda::kRecBytes + align256(ch * 4);
+        uint8_t *dsn = ck + ch * kda::kDim * kda::kDim * 2;
+        int *exact_ctr = reinterpret_cast<int *>(wsb + kExactCtrOff);
+        const kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, st.err, geo, exact_list, exact_ctr};
+        if (kda::launch_intra_chunk(ip, pl.max_chunks, stream) != cudaSuccess ||
+            kda::launch_intra_exact(ip, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        kda::RecurParams rp{rec, initial_state, nullptr, nullptr, st.err, geo};
+        rp.ckpt = ck;
+        if (kda::launch_recurrent_states(rp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        kda::BwdChunkParams bp{};
+        bp.ip = ip;
+        bp.rec = rec;
+        bp.dout = d_out;
+        bp.dsf = d_final_state;
+        bp.ds0 = d_initial_state;
+        bp.ckpt = ck;
+        bp.dsn = dsn;
+        bp.dq = dq; bp.dk = dk; bp.dv = dv; bp.dg = dg; bp.dbeta = dbeta;
+        bp.err = st.err;
+        bp.geo = geo;
+        bp.max_chunks = pl.max_chunks;
+        if (kda::launch_bwd_chain(bp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        return kda::launch_bwd_grad(bp, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    }
     float *ckpt = reinterpret_cast<float *>(wsb + 256 + pl.off_bytes);
     float *ring = reinterpret_cast<float *>(wsb + 256 + pl.off_bytes + ckpt_bytes);
     const kda::BackParams p{q, k, v, g, beta, initial_state, d_out, d_final_state, scale,
                             dq, dk, dv, dg, dbeta, d_initial_state, ckpt, ring, geo};
     return kda::launch_backward(p, N * H, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_set_backward_impl(int impl) {
+    if (impl != 0 && impl != 1) return KDA_ERR_BAD_SHAPE;
+    g_bwd_impl.store(impl);
+    return KDA_OK;
 }
 
 static void free_timing() {

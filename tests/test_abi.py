@@ -196,6 +196,29 @@ def test_backward_argument_checks(lib):
 
 
 def test_backward_workspace_bytes(lib):
+    # chunked (default): per chunk-head a record, a list entry (rounded up in
+    # all) and two bf16 states
+    REC, ST2 = 17408, 2 * 32768
+
+    def lst(items):
+        return -(-(items * 4) // 256) * 256
+
+    ch = 512 * 64
+    assert K.kda_backward_workspace_bytes(1, 8192, 64, 1, 0) == 256 + ch * REC + lst(ch) + ch * ST2
+    pc = (8192 + 15 * 16) // 16
+    assert K.kda_backward_workspace_bytes(1, 8192, 64, 16, 1) == (256 + 256 + pc * 64 * REC
+                                                                 + lst(pc * 64) + pc * 64 * ST2)
+    assert K.kda_backward_workspace_bytes(1, 8192, 64, 2, 0) == 0   # N != B
+    # token-serial
+    assert K.kda_set_backward_impl(1) == 0
+    try:
+        _token_serial_workspace_bytes()
+    finally:
+        K.kda_set_backward_impl(0)
+    assert K.kda_set_backward_impl(2) != 0
+
+
+def _token_serial_workspace_bytes():
     st, mib = 65536, 1 << 20
     assert K.kda_backward_workspace_bytes(1, 8192, 64, 1, 0) == 256 + 512 * 64 * st + 64 * mib
     assert K.kda_backward_workspace_bytes(2, 17, 3, 2, 0) == 256 + 2 * 2 * 3 * st + 6 * mib
