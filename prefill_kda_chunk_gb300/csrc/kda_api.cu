@@ -545,10 +545,12 @@ static int64_t backward_ckpt_bytes(int64_t B, int64_t T, int64_t H, int64_t N, b
 }
 
 // Chunked gradients: flag block, chunk offsets (packed), the records, the
-// exact-form list, then S^T and dS_next^T of every chunk-head in bf16.
+// exact-form list, (I + A)^{-1} of every chunk-head (fp32), then S^T and
+// dS_next^T of every chunk-head in bf16.
 static int64_t backward_chunk_ws_bytes(int64_t H, const Plan &pl) {
     const int64_t ch = pl.max_chunks * H;
-    return 256 + pl.off_bytes + ch * kda::kRecBytes + align256(ch * 4) + 2 * ch * kda::kDim * kda::kDim * 2;
+    return 256 + pl.off_bytes + ch * kda::kRecBytes + align256(ch * 4) + ch * 1024 +
+           2 * ch * kda::kDim * kda::kDim * 2;
 }
 
 static int64_t backward_ws_bytes(int64_t B, int64_t T, int64_t H, int64_t N, bool packed,
@@ -682,10 +684,11 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
         const int64_t ch = pl.max_chunks * H;
         uint8_t *rec = wsb + 256 + pl.off_bytes;
         int32_t *exact_list = reinterpret_cast<int32_t *>(rec + ch * kda::kRecBytes);
-        uint8_t *ck = rec + ch * kda::kRecBytes + align256(ch * 4);
+        float *tinv = reinterpret_cast<float *>(rec + ch * kda::kRecBytes + align256(ch * 4));
+        uint8_t *ck = reinterpret_cast<uint8_t *>(tinv + ch * 256);
         uint8_t *dsn = ck + ch * kda::kDim * kda::kDim * 2;
         int *exact_ctr = reinterpret_cast<int *>(wsb + kExactCtrOff);
-        const kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, st.err, geo, exact_list, exact_ctr};
+        const kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, st.err, geo, exact_list, exact_ctr, tinv};
         if (kda::launch_intra_chunk(ip, pl.max_chunks, stream) != cudaSuccess ||
             kda::launch_intra_exact(ip, stream) != cudaSuccess)
             return KDA_ERR_CUDA;

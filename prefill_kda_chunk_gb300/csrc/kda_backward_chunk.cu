@@ -27,8 +27,10 @@
 // dS_next^T in bf16 and writing dL/d(initial state); and kda_bwd_grad_kernel,
 // chunk-parallel, one CTA per (chunk, head), for everything else. The WY
 // reverse takes exact per-pair exponentials exp(G_r - G_i) (r >= i), so it
-// holds for any decay; the record it starts from is rebuilt by the
-// forward's own per-chunk code, factored or exact form as the forward chose.
+// holds for any decay; it reads the records and T = (I + A)^-1 as the
+// forward's intra-chunk kernels left them (factored or exact form).
+
+#include <cuda.h>
 
 #include "kda_device.cuh"
 #include "kda_internal.h"
@@ -220,23 +222,66 @@ __global__ void __launch_bounds__((kCWarps + 1) * 32) kda_bwd_chain_kernel(BwdCh
 // ---------------------------------------------------------------------------
 // Chunk-parallel gradients: one 128-thread CTA per (chunk, head) at a time
 // (persistent, two CTAs per SM). Shared memory:
-constexpr int kGOffST = 0;                  // S^T bf16 [128 v][128 k], swizzled; later
-                                            //   dW, dQg, dKd, dU fp32 [16][128] each
-constexpr int kGOffDT = 32768;              // dS_next^T bf16, swizzled; later small fp32
-                                            //   tiles: dP, dgamma, dM, dA, Y, dbeta parts
-constexpr int kGOffRec = 65536;             // the chunk's record, rebuilt
-constexpr int kGOffWS = kGOffRec + kRecBytes;            // warp 0's per-chunk scratch
-constexpr int kGOffDO = kGOffWS + static_cast<int>(sizeof(IntraWarpSmem));   // dO bf16
-                                            //   [16 t][128 v], swizzled; later dW bf16
-constexpr int kGOffUB = kGOffDO + 4096;     // U bf16 [16 t][128 v], swizzled
+constexpr int kGOffST = 0;                  // S^T bf16 [128 v][128 k] as two 64-key halves
+                                            //   (128-byte swizzle, by TMA); later fp32
+                                            //   [16][kFS] tiles Z, dKd, T1
+constexpr int kGOffDT = 32768;              // dS_next^T bf16, the same; later small fp32
+                                            //   tiles and the Yc tile
+constexpr int kGOffRec = 65536;             // the chunk's record
+constexpr int kTStride = 20;                // floats per row of T in shared memory
+constexpr int kGOffT = kGOffRec + kRecBytes;             // T = (I + A)^{-1} fp32 [16][20]
+constexpr int kGOffV = kGOffT + 16 * kTStride * 4;       // V bf16 [16 t][128 v], swizzled
+constexpr int kGOffKg = kGOffV + 4096;      // K e^G bf16 [16 t][128 k], swizzled
+constexpr int kGOffKn = kGOffKg + 4096;     // K e^-G bf16 [16 t][128 k], swizzled; in phase 1
+                                            //   first k as loaded (bf16 [16][128], row-major)
+constexpr int kGOffDO = kGOffKn + 4096;     // dO bf16 [16 t][128 v], swizzled; later dW bf16
+constexpr int kGOffUB = kGOffDO + 4096;     // U bf16 [16 t][128 v], swizzled; in phase 1, with
+                                            //   the next 4 KiB, g fp32 [16][128] row-major
 constexpr int kGOffDUB = kGOffUB + 4096;    // dU bf16 [16 t][128 v], swizzled
-constexpr int kGSmem = kGOffDUB + 4096;
-static_assert(kGOffWS % 16 == 0 && kGOffDO % 16 == 0, "alignment");
+constexpr int kGOffMisc = kGOffDUB + 4096;  // beta [16], dbeta from M [16], dbeta parts [4][16],
+                                            //   the copy barrier
+constexpr int kGBar = kGOffMisc + 384;
+constexpr int kGSmem = kGOffMisc + 512;
+constexpr uint32_t kGTxBytes = 2 * 32768 + kRecBytes + 1024 + 8192 + 4096;   // TMA bytes per item
+static_assert(kGOffT % 16 == 0 && kGOffV % 16 == 0 && kGOffDO % 16 == 0, "alignment");
+// fp32 [16 rows][128 channels] tiles, rows kFS floats apart: the fragment
+// stores of eight rows then fall on distinct banks in two wavefronts
+constexpr int kFS = 136;
+constexpr int kFT = 16 * kFS * 4;
+constexpr int kGZ = kGOffST, kGK = kGZ + kFT, kGT1 = kGK + kFT;
 // small tiles in the dS_next^T region once it is read
-constexpr int kSdP = kGOffDT, kSdG = kSdP + 1024, kSdM = kSdG + 512, kSdA = kSdM + 1024,
-              kSY = kSdA + 1024, kSdB = kSY + 1024;
+constexpr int kSdP = kGOffDT;               // dP (w.r.t. the record's scale P) [16][16]
+constexpr int kSdG = kSdP + 1024;           // dgamma parts [4 warps][128]
+constexpr int kSdMp = kSdG + 2048;          // dM parts [4 warps][16][16]
+constexpr int kSdM = kSdMp + 4096;          // dM [16][16]
+constexpr int kSdT = kSdM + 1024;           // dT = dM diag(beta)
+constexpr int kSY = kSdT + 1024;            // Y = T^T dT
+constexpr int kSdA = kSY + 1024;            // dA, strict lower
+constexpr int kGYc = kSdA + 1024;           // Yc fp32 [16][kFS]
+static_assert(kGT1 + kFT <= kGOffDT && kGYc + kFT <= kGOffRec, "tiles overlap");
 constexpr int kGThreads = 128;
-constexpr float kLn2 = 0.6931471805599453f;
+
+// Byte offset of (row, col) in a [128][128] bf16 tile stored as two
+// [128][64] halves, 16-byte chunks swizzled within each 128-byte row (the
+// layout of a TMA box with 128-byte swizzling)
+__device__ __forceinline__ int sw2(int row, int col) {
+    return ((col >> 6) << 14) + row * 128 + ((((col >> 3) & 7) ^ (row & 7)) << 4) + ((col & 7) << 1);
+}
+
+struct GradMaps {
+    CUtensorMap st, dst;   // S^T and dS_next^T: [items][128 v][128 k] bf16, boxes of 128 v x 64 k
+    CUtensorMap g, k;      // g fp32, k bf16: [tokens][H][128], boxes of 16 tokens x 1 head x 128
+};
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 constexpr float kLog2eG = 1.4426950408889634f;
 
 __device__ __forceinline__ float ex2g(float x) {
@@ -245,20 +290,72 @@ __device__ __forceinline__ float ex2g(float x) {
     return y;
 }
 
-__global__ void __launch_bounds__(kGThreads, 2) kda_bwd_grad_kernel(BwdChunkParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
+// The A fragment (m16n8k16, row-major 16 x 16) of the matrix el(m, k).
+template <typename F>
+__device__ __forceinline__ void frag_a(uint32_t (&a)[4], int gid, int tig, F el) {
+    const int c0 = 2 * tig, c1 = c0 + 8;
+    a[0] = pack_bf16(el(gid, c0), el(gid, c0 + 1));
+    a[1] = pack_bf16(el(gid + 8, c0), el(gid + 8, c0 + 1));
+    a[2] = pack_bf16(el(gid, c1), el(gid, c1 + 1));
+    a[3] = pack_bf16(el(gid + 8, c1), el(gid + 8, c1 + 1));
+}
+
+// Per item: phase 1 copies in S^T, dS_next^T, the record, T, V and dO and
+// builds K e^G and K e^-G; phase 2 forms U and dU; phase 3 the contractions
+// over the values (dW, dQg, dKd, dP, dgamma); phase 4 the WY reverse (dM, dT,
+// dbeta, dA), the gated products as MMAs and the per-channel combination.
+//
+// In the factored range (|G| <= 80 in every channel of the chunk, the same
+// test as the forward) the gated products of the reverse factor like the
+// forward's: with dY = scale dP, Kn = K e^-G, Qg = scale Q e^G, Kg = K e^G,
+//   dq = e^G o (dY Kn + scale dQg)
+//   dk = e^G o beta (dA Kn + T^T dW) + e^-G o (dP^T Qg + (diag(beta) dA)^T Kg)
+//        + e^(G_last - G) o dKd
+// and dG picks the same terms times q or k (with signs + for e^G, - for
+// e^-G and e^(G_last - G)). The diagonal of P (exp(0) = 1) stays out of the
+// products: its dq and dk terms are added directly and its two dG terms,
+// equal and opposite, are left out. Outside the factored range the A and P
+// terms take exact per-pair exponentials, one channel per thread.
+__global__ void __launch_bounds__(kGThreads, 2)
+kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_constant__ GradMaps tm) {
+    extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
     const ChunkGeometry &geo = p.geo;
     const int H = geo.n_heads;
     if (geo.cu != nullptr && (*geo.call_flags & kErrBadCu)) return;
     const uint32_t sb = smem_u32(smem);
+    if (sb & 1023u) {   // the swizzled TMA boxes need 1024-byte alignment
+        if (tid == 0) atomicOr(p.err, kErrTimeout);
+        return;
+    }
+    const uint32_t bar = sb + kGBar;
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    uint32_t parity = 0;
     const uint32_t sST = sb + kGOffST, sDT = sb + kGOffDT, sRec = sb + kGOffRec, sDO = sb + kGOffDO,
-                   sUB = sb + kGOffUB, sDUB = sb + kGOffDUB;
-    IntraWarpSmem &ws = *reinterpret_cast<IntraWarpSmem *>(smem + kGOffWS);
+                   sUB = sb + kGOffUB, sDUB = sb + kGOffDUB, sT = sb + kGOffT, sV = sb + kGOffV,
+                   sKg = sb + kGOffKg, sKn = sb + kGOffKn;
     const int64_t rowe = static_cast<int64_t>(H) * kDim;
     const float scale = p.ip.scale;
     const int64_t items = p.max_chunks * H;
+    float *sBeta = reinterpret_cast<float *>(smem + kGOffMisc);
+    float *sBM = sBeta + 16, *sPB = sBeta + 32;
+    const float *T = reinterpret_cast<const float *>(smem + kGOffT);   // T[r * kTStride + i]
+    float *gZ = reinterpret_cast<float *>(smem + kGZ);
+    float *gK = reinterpret_cast<float *>(smem + kGK);
+    float *gT1 = reinterpret_cast<float *>(smem + kGT1);
+    float *gYc = reinterpret_cast<float *>(smem + kGYc);
+    float *gP = reinterpret_cast<float *>(smem + kSdP);
+    float *sdG = reinterpret_cast<float *>(smem + kSdG);
+    float *sdMp = reinterpret_cast<float *>(smem + kSdMp);
+    float *sdM = reinterpret_cast<float *>(smem + kSdM);
+    float *sdT = reinterpret_cast<float *>(smem + kSdT);
+    float *sY = reinterpret_cast<float *>(smem + kSY);
+    float *sdA = reinterpret_cast<float *>(smem + kSdA);
 
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
         const int64_t c = item / H;
@@ -268,38 +365,81 @@ __global__ void __launch_bounds__(kGThreads, 2) kda_bwd_grad_kernel(BwdChunkPara
         if (!locate_chunk(geo, c, n, t0, L, rec_idx)) continue;
         (void)n;
         __syncthreads();   // the previous item is done with every tile
+        const int64_t qoff = (t0 * H + h) * kDim;
 
-        // ---- phase 1: warp 0 rebuilds the record (and T, K e^G, V in its
-        //      scratch); warps 1-3 stage S^T, dS_next^T and dO
-        if (warp == 0) {
-            uint8_t *rec = smem + kGOffRec;
-            if (intra_item<false, true>(p.ip, ws, t0, L, h, rec))
-                intra_exact_item<false, true>(p.ip, ws, t0, L, h, rec);
-        } else {
-            const int64_t off = (rec_idx * H + h) * static_cast<int64_t>(kDim * kDim);
-            const __nv_bfloat16 *cs = static_cast<const __nv_bfloat16 *>(p.ckpt) + off;
-            const __nv_bfloat16 *ds = static_cast<const __nv_bfloat16 *>(p.dsn) + off;
-            for (int i = tid - 32; i < 2048; i += 96) {
-                const int r = i >> 4, cc = i & 15;
-                const uint32_t dst = r * 256 + ((cc ^ (r & 7)) << 4);
-                cp_async16(sST + dst, cs + r * kDim + cc * 8, 16u);
-                cp_async16(sDT + dst, ds + r * kDim + cc * 8, 16u);
+        // ---- phase 1: S^T, dS_next^T, g and k (TMA boxes), the record and T
+        //      (bulk copies), V and dO (16-byte copies, rows past the end
+        //      zero); thread = channel for G (kept in registers) and the
+        //      K e^G and K e^-G tiles
+        bool exact;
+        float Gc[16];   // this channel's G in base-2 units
+        {
+            const int64_t ri = rec_idx * H + h;
+            if (warp == 0) {
+                if (lane == 0) {
+                    // the previous item wrote these tiles through the generic proxy
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive_expect_tx(bar, kGTxBytes);
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    const int z = static_cast<int>(ri);
+                    tma_load_3d(sST, &tm.st, 0, 0, z, bar);
+                    tma_load_3d(sST + 16384, &tm.st, 64, 0, z, bar);
+                    tma_load_3d(sDT, &tm.dst, 0, 0, z, bar);
+                    tma_load_3d(sDT + 16384, &tm.dst, 64, 0, z, bar);
+                    tma_load_3d(sUB, &tm.g, 0, h, static_cast<int>(t0), bar);
+                    tma_load_3d(sKn, &tm.k, 0, h, static_cast<int>(t0), bar);
+                    bulk_g2s(sRec, p.rec + ri * static_cast<int64_t>(kRecBytes), kRecBytes, bar);
+                }
+                if (lane < 16)
+                    bulk_g2s(sT + lane * (kTStride * 4), p.ip.tinv + ri * 256 + 16 * lane, 64, bar);
             }
-            const __nv_bfloat16 *dop = static_cast<const __nv_bfloat16 *>(p.dout) + (t0 * H + h) * kDim;
-            for (int i = tid - 32; i < 256; i += 96) {
+            const __nv_bfloat16 *dop = static_cast<const __nv_bfloat16 *>(p.dout) + qoff;
+            const __nv_bfloat16 *vp = static_cast<const __nv_bfloat16 *>(p.ip.v) + qoff;
+            for (int i = tid; i < 256; i += kGThreads) {
                 const int r = i >> 4, cc = i & 15;
                 const bool ok = r < L;
-                cp_async16(sDO + r * 256 + ((cc ^ (r & 7)) << 4), dop + (ok ? r : 0) * rowe + cc * 8,
-                           ok ? 16u : 0u);
+                const uint32_t dst = r * 256 + ((cc ^ (r & 7)) << 4);
+                cp_async16(sDO + dst, dop + (ok ? r : 0) * rowe + cc * 8, ok ? 16u : 0u);
+                cp_async16(sV + dst, vp + (ok ? r : 0) * rowe + cc * 8, ok ? 16u : 0u);
             }
             cp_async_commit();
+            if (tid < 16) sBeta[tid] = tid < L ? __ldg(p.ip.beta + (t0 + tid) * H + h) : 0.f;
             cp_async_wait_all();
+            const bool got = mbar_wait(bar, parity);
+            if (__syncthreads_or(!got)) {
+                // give the copies in flight another bounded wait, then stop
+                if (tid == 0) atomicOr(p.err, kErrTimeout);
+                if (!got) mbar_wait(bar, parity);
+                break;
+            }
+            parity ^= 1u;
+            // G = running sum of g (rows past the end: zero), and its largest |G|
+            const float *gs = reinterpret_cast<const float *>(smem + kGOffUB) + tid;
+            const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(smem + kGOffKn) + tid;
+            float run = 0.f, gmax = 0.f, kr[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const bool ok = r < L;
+                run += ok ? gs[r * kDim] : 0.f;
+                gmax = fmaxf(gmax, fabsf(run));
+                kr[r] = ok ? __bfloat162float(ks[r * kDim]) : 0.f;
+                Gc[r] = run * kLog2eG;
+            }
+            __syncthreads();   // k as loaded is read; its space takes K e^-G
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                *reinterpret_cast<__nv_bfloat16 *>(smem + kGOffKg + swz(r, tid)) =
+                    __float2bfloat16_rn(kr[r] * ex2g(Gc[r]));
+                *reinterpret_cast<__nv_bfloat16 *>(smem + kGOffKn + swz(r, tid)) =
+                    __float2bfloat16_rn(kr[r] * ex2g(-Gc[r]));
+            }
+            exact = __syncthreads_or(!(gmax <= 80.f)) != 0;
         }
-        __syncthreads();
 
         // ---- phase 2: U^T = Ut^T + S^T (-W)^T and dU^T = dS_next^T Kd^T + dO^T P,
         //      value rows 32 warp + 16 mt, all 16 tokens
-        float dUf[2][2][4];   // dU^T fragments kept in fp32
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
             const int vb = 32 * warp + 16 * mt;
@@ -329,8 +469,8 @@ __global__ void __launch_bounds__(kGThreads, 2) kda_bwd_grad_kernel(BwdChunkPara
             for (int kk = 0; kk < 8; ++kk) {
                 uint32_t aS[4], aD[4], bw[4], bk[4];
                 const int ra = vb + (lane & 7) + 8 * ((lane >> 3) & 1), ca = 16 * kk + 8 * (lane >> 4);
-                ldsm_x4(sST + swz(ra, ca), aS[0], aS[1], aS[2], aS[3]);
-                ldsm_x4(sDT + swz(ra, ca), aD[0], aD[1], aD[2], aD[3]);
+                ldsm_x4(sST + sw2(ra, ca), aS[0], aS[1], aS[2], aS[3]);
+                ldsm_x4(sDT + sw2(ra, ca), aD[0], aD[1], aD[2], aD[3]);
                 const int rb = (quad >> 1) * 8 + (lane & 7), cb = 16 * kk + (quad & 1) * 8;
                 ldsm_x4(sRec + kRecW + swz(rb, cb), bw[0], bw[1], bw[2], bw[3]);
                 ldsm_x4(sRec + kRecKd + swz(rb, cb), bk[0], bk[1], bk[2], bk[3]);
@@ -346,7 +486,6 @@ __global__ void __launch_bounds__(kGThreads, 2) kda_bwd_grad_kernel(BwdChunkPara
                 for (int e = 0; e < 4; ++e) {
                     u[nt][e] = uT[nt][0][e] + uT[nt][1][e];
                     du[nt][e] = dT[nt][0][e] + dT[nt][1][e];
-                    dUf[mt][nt][e] = du[nt][e];
                 }
             // U and dU to their [t][v] tiles (bf16), transposed by stmatrix
             const int m = lane >> 3;
@@ -360,7 +499,7 @@ __global__ void __launch_bounds__(kGThreads, 2) kda_bwd_grad_kernel(BwdChunkPara
 
         // ---- phase 3: contractions over the 128 values. Warp w: keys 32 w .. + 31.
         //      dW = -dU S^T, dQg = dO S^T, dKd = U dS_next^T; warp 0 also dP = dO U^T;
-        //      thread = key for dgamma = rowsum(dS_next o S)
+        //      dgamma = rowsum(dS_next o S): thread = 8 keys x 16 of the 128 values
         float cW[4][4], cQ[4][4], cK[4][4], cP[2][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -381,8 +520,8 @@ __global__ void __launch_bounds__(kGThreads, 2) kda_bwd_grad_kernel(BwdChunkPara
             for (int jp = 0; jp < 2; ++jp) {
                 uint32_t bs[4], bd[4];
                 const int rk = 16 * kk + (quad & 1) * 8 + (lane & 7), ck = 32 * warp + 16 * jp + (quad >> 1) * 8;
-                ldsm_x4_t(sST + swz(rk, ck), bs[0], bs[1], bs[2], bs[3]);
-                ldsm_x4_t(sDT + swz(rk, ck), bd[0], bd[1], bd[2], bd[3]);
+                ldsm_x4_t(sST + sw2(rk, ck), bs[0], bs[1], bs[2], bs[3]);
+                ldsm_x4_t(sDT + sw2(rk, ck), bd[0], bd[1], bd[2], bd[3]);
                 mma_r(cW[2 * jp], aDU, bs[0], bs[1]);
                 mma_r(cW[2 * jp + 1], aDU, bs[2], bs[3]);
                 mma_r(cQ[2 * jp], aO_, bs[0], bs[1]);
@@ -398,45 +537,43 @@ __global__ void __launch_bounds__(kGThreads, 2) kda_bwd_grad_kernel(BwdChunkPara
                 mma_r(cP[1], aO_, bu[2], bu[3]);
             }
         }
-        float dgam = 0.f;
+        float dg8[8];
         {
-            const int k = tid;
-            for (int v = 0; v < kDim; ++v) {
-                const uint32_t o = v * 256 + ((((k >> 3) ^ (v & 7))) << 4) + (k & 7) * 2;
-                dgam = fmaf(__bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + kGOffST + o)),
-                            __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + kGOffDT + o)),
-                            dgam);
+            // rows v = vg + 8 j (so v & 7 = vg), 16-byte chunk kc of keys 8 kc .. + 7
+            const int kc = tid & 15, vg = tid >> 4;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dg8[e] = 0.f;
+#pragma unroll 4
+            for (int j = 0; j < 16; ++j) {
+                const uint32_t o = sw2(vg + 8 * j, 8 * kc);
+                const uint4 s4 = *reinterpret_cast<const uint4 *>(smem + kGOffST + o);
+                const uint4 d4 = *reinterpret_cast<const uint4 *>(smem + kGOffDT + o);
+                const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    dg8[2 * w] = fmaf(__uint_as_float(sw[w] << 16), __uint_as_float(dw[w] << 16), dg8[2 * w]);
+                    dg8[2 * w + 1] = fmaf(__uint_as_float(sw[w] & 0xffff0000u),
+                                          __uint_as_float(dw[w] & 0xffff0000u), dg8[2 * w + 1]);
+                }
             }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dg8[e] += __shfl_xor_sync(0xffffffffu, dg8[e], 16);
         }
         __syncthreads();
-        // results: dW, dQg, dKd, dU fp32 [16][128] over S^T; dW bf16 over dO;
-        // dP, dgamma over dS_next^T
-        float *gW = reinterpret_cast<float *>(smem + kGOffST);
-        float *gQ = gW + 16 * kDim, *gK = gQ + 16 * kDim, *gU = gK + 16 * kDim;
+        // results: dQg, dKd fp32 over S^T; dW bf16 over dO; dP and the dgamma
+        // parts over dS_next^T
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int key = 32 * warp + 8 * j + 2 * tig;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
                 const int t = gid + 8 * hf;
-                *reinterpret_cast<float2 *>(gW + t * kDim + key) = make_float2(-cW[j][2 * hf], -cW[j][2 * hf + 1]);
-                *reinterpret_cast<float2 *>(gQ + t * kDim + key) = make_float2(cQ[j][2 * hf], cQ[j][2 * hf + 1]);
-                *reinterpret_cast<float2 *>(gK + t * kDim + key) = make_float2(cK[j][2 * hf], cK[j][2 * hf + 1]);
+                *reinterpret_cast<float2 *>(gZ + t * kFS + key) = make_float2(cQ[j][2 * hf], cQ[j][2 * hf + 1]);
+                *reinterpret_cast<float2 *>(gK + t * kFS + key) = make_float2(cK[j][2 * hf], cK[j][2 * hf + 1]);
                 *reinterpret_cast<uint32_t *>(smem + kGOffDO + swz(t, key)) =
                     pack_bf16(-cW[j][2 * hf], -cW[j][2 * hf + 1]);
             }
         }
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int v = 32 * warp + 16 * mt + gid, t = 8 * nt + 2 * tig;
-                gU[t * kDim + v] = dUf[mt][nt][0];
-                gU[(t + 1) * kDim + v] = dUf[mt][nt][1];
-                gU[t * kDim + v + 8] = dUf[mt][nt][2];
-                gU[(t + 1) * kDim + v + 8] = dUf[mt][nt][3];
-            }
-        float *gP = reinterpret_cast<float *>(smem + kSdP);
         if (warp == 0) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -447,20 +584,19 @@ __global__ void __launch_bounds__(kGThreads, 2) kda_bwd_grad_kernel(BwdChunkPara
                     gP[r * 16 + i + 1] = i + 1 <= r ? cP[nt][2 * hf + 1] : 0.f;
                 }
         }
-        reinterpret_cast<float *>(smem + kSdG)[tid] = dgam;
+        if (lane < 16) {
+            float4 *dst = reinterpret_cast<float4 *>(sdG + warp * kDim + 8 * lane);
+            dst[0] = make_float4(dg8[0], dg8[1], dg8[2], dg8[3]);
+            dst[1] = make_float4(dg8[4], dg8[5], dg8[6], dg8[7]);
+        }
         __syncthreads();
 
-        // ---- phase 4a (warp 0): dM = dU V^T + dW Kg^T (16 x 16), then dT = dM diag(beta),
-        //      dbeta from M = T diag(beta), dA = -(T^T dT T^T) on the strict lower triangle
-        float *sM = reinterpret_cast<float *>(smem + kSdM);
-        float *sA = reinterpret_cast<float *>(smem + kSdA);
-        float *sY = reinterpret_cast<float *>(smem + kSY);
-        float *sB = reinterpret_cast<float *>(smem + kSdB);   // [0,16): dbeta from dM; [16,80): parts
-        if (warp == 0) {
+        // ---- phase 4a: dM = dU V^T + dW Kg^T (16 x 16), warp w over channels 32 w .. + 31
+        {
             float m2[2][4] = {};
-            const uint32_t sV = smem_u32(ws.v), sKg = smem_u32(ws.kg);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int kk = 2 * warp + q2;
                 uint32_t aD[4], aW[4], bv[4], bg[4];
                 const int ra = (lane & 7) + 8 * ((lane >> 3) & 1), ca = 16 * kk + 8 * (lane >> 4);
                 ldsm_x4(sDUB + swz(ra, ca), aD[0], aD[1], aD[2], aD[3]);
@@ -473,152 +609,246 @@ __global__ void __launch_bounds__(kGThreads, 2) kda_bwd_grad_kernel(BwdChunkPara
                 mma_r(m2[0], aW, bg[0], bg[1]);
                 mma_r(m2[1], aW, bg[2], bg[3]);
             }
+            float *part = sdMp + warp * 256;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int r = gid + 8 * hf, i = 8 * nt + 2 * tig;
-                    sM[r * 16 + i] = m2[nt][2 * hf];
-                    sM[r * 16 + i + 1] = m2[nt][2 * hf + 1];
+                    *reinterpret_cast<float2 *>(part + r * 16 + i) = make_float2(m2[nt][2 * hf], m2[nt][2 * hf + 1]);
                 }
-            __syncwarp();
-            const float *T = ws.t;   // T[r * 17 + i]
-            const float *bet = p.ip.beta;
-            // lane j < 16: dbeta_j (from M) = sum_r dM[r][j] T[r][j]; dT[r][j] = dM[r][j] beta_j
-            if (lane < 16) {
-                const float bj = lane < L ? __ldg(bet + (t0 + lane) * H + h) : 0.f;
-                float sbj = 0.f;
-                for (int r = 0; r < 16; ++r) {
-                    sbj = fmaf(sM[r * 16 + lane], T[r * 17 + lane], sbj);
-                    sM[r * 16 + lane] *= bj;                  // now dT
+        }
+        __syncthreads();
+        // ---- phase 4b: dM and dT = dM diag(beta) (M = T diag(beta)); two entries per thread
+#pragma unroll
+        for (int e = tid; e < 256; e += kGThreads) {
+            const float m = sdMp[e] + sdMp[256 + e] + sdMp[512 + e] + sdMp[768 + e];
+            sdM[e] = m;
+            sdT[e] = m * sBeta[e & 15];
+        }
+        __syncthreads();
+        // ---- phase 4c: Y = T^T dT; dbeta_j (from M) = sum_r dM[r][j] T[r][j]
+#pragma unroll
+        for (int e = tid; e < 256; e += kGThreads) {
+            const int r = e >> 4, b = e & 15;
+            float y = 0.f;
+#pragma unroll
+            for (int a = 0; a < 16; ++a) y = fmaf(T[a * kTStride + r], sdT[a * 16 + b], y);
+            sY[e] = y;
+        }
+        if (tid < 16) {
+            float sbj = 0.f;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sbj = fmaf(sdM[r * 16 + tid], T[r * kTStride + tid], sbj);
+            sBM[tid] = sbj;
+        }
+        __syncthreads();
+        // ---- phase 4d: dA = -(Y T^T) on the strict lower triangle
+#pragma unroll
+        for (int e = tid; e < 256; e += kGThreads) {
+            const int r = e >> 4, i = e & 15;
+            float a = 0.f;
+#pragma unroll
+            for (int b = 0; b < 16; ++b) a = fmaf(sY[r * 16 + b], T[i * kTStride + b], a);
+            sdA[e] = i < r ? -a : 0.f;
+        }
+        __syncthreads();
+
+        // ---- phase 4e: the products over the chunk's tokens, warp w: channels 32 w .. + 31
+        {
+            uint32_t aTt[4];
+            frag_a(aTt, gid, tig, [&](int m, int k) { return T[k * kTStride + m]; });
+            float zc[4][4], xc[4][4], dc[4][4], uc[4][4], yc[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) zc[j][e] = xc[j][e] = dc[j][e] = uc[j][e] = yc[j][e] = 0.f;
+            const int rk = (quad & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int jp = 0; jp < 2; ++jp) {
+                const int ck = 32 * warp + 16 * jp + (quad >> 1) * 8;
+                uint32_t b[4];
+                ldsm_x4_t(sDO + swz(rk, ck), b[0], b[1], b[2], b[3]);    // dW
+                mma_r(dc[2 * jp], aTt, b[0], b[1]);
+                mma_r(dc[2 * jp + 1], aTt, b[2], b[3]);
+                ldsm_x4_t(sDUB + swz(rk, ck), b[0], b[1], b[2], b[3]);   // dU
+                mma_r(uc[2 * jp], aTt, b[0], b[1]);
+                mma_r(uc[2 * jp + 1], aTt, b[2], b[3]);
+            }
+            if (!exact) {
+                uint32_t aY[4], aA[4], aYt[4], aAt[4];
+                // the diagonal of P (exp(0) = 1) is left to the combination below
+                frag_a(aY, gid, tig, [&](int m, int k) { return m == k ? 0.f : scale * gP[m * 16 + k]; });
+                frag_a(aA, gid, tig, [&](int m, int k) { return sdA[m * 16 + k]; });
+                frag_a(aYt, gid, tig, [&](int m, int k) { return m == k ? 0.f : gP[k * 16 + m]; });
+                frag_a(aAt, gid, tig, [&](int m, int k) { return sBeta[k] * sdA[k * 16 + m]; });
+#pragma unroll
+                for (int jp = 0; jp < 2; ++jp) {
+                    const int ck = 32 * warp + 16 * jp + (quad >> 1) * 8;
+                    uint32_t b[4];
+                    ldsm_x4_t(sKn + swz(rk, ck), b[0], b[1], b[2], b[3]);
+                    mma_r(zc[2 * jp], aY, b[0], b[1]);
+                    mma_r(zc[2 * jp + 1], aY, b[2], b[3]);
+                    mma_r(xc[2 * jp], aA, b[0], b[1]);
+                    mma_r(xc[2 * jp + 1], aA, b[2], b[3]);
+                    ldsm_x4_t(sRec + kRecQg + swz(rk, ck), b[0], b[1], b[2], b[3]);
+                    mma_r(yc[2 * jp], aYt, b[0], b[1]);
+                    mma_r(yc[2 * jp + 1], aYt, b[2], b[3]);
+                    ldsm_x4_t(sKg + swz(rk, ck), b[0], b[1], b[2], b[3]);
+                    mma_r(yc[2 * jp], aAt, b[0], b[1]);
+                    mma_r(yc[2 * jp + 1], aAt, b[2], b[3]);
                 }
-                sB[lane] = sbj;
             }
-            __syncwarp();
-            // Y = T^T dT: Y[r][b] = sum_a T[a][r] dT[a][b]; lane: 8 entries
-            for (int e = lane; e < 256; e += 32) {
-                const int r = e >> 4, b = e & 15;
-                float y = 0.f;
-                for (int a = 0; a < 16; ++a) y = fmaf(T[a * 17 + r], sM[a * 16 + b], y);
-                sY[e] = y;
+            // epilogue: Z = dY Kn + scale dQg, T1 = beta (dA Kn + T^T dW), Yc,
+            // dv = beta T^T dU; dbeta parts sum_c Kg (dA Kn)
+            float pb0 = 0.f, pb1 = 0.f;
+            const float b0 = sBeta[gid], b1 = sBeta[gid + 8];
+            float *dvp = p.dv + qoff;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int col = 32 * warp + 8 * j + 2 * tig;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int r = gid + 8 * hf;
+                    const float br = hf ? b1 : b0;
+                    const float x0 = xc[j][2 * hf], x1 = xc[j][2 * hf + 1];
+                    float2 *zp = reinterpret_cast<float2 *>(gZ + r * kFS + col);
+                    const float2 q2 = *zp;
+                    *zp = make_float2(fmaf(scale, q2.x, zc[j][2 * hf]), fmaf(scale, q2.y, zc[j][2 * hf + 1]));
+                    *reinterpret_cast<float2 *>(gT1 + r * kFS + col) =
+                        make_float2(br * (x0 + dc[j][2 * hf]), br * (x1 + dc[j][2 * hf + 1]));
+                    *reinterpret_cast<float2 *>(gYc + r * kFS + col) = make_float2(yc[j][2 * hf], yc[j][2 * hf + 1]);
+                    const float2 kg = unpack_bf16(*reinterpret_cast<const uint32_t *>(smem + kGOffKg + swz(r, col)));
+                    const float pb = fmaf(kg.x, x0, kg.y * x1);
+                    if (hf) pb1 += pb; else pb0 += pb;
+                    if (r < L)
+                        *reinterpret_cast<float2 *>(dvp + r * rowe + col) =
+                            make_float2(br * uc[j][2 * hf], br * uc[j][2 * hf + 1]);
+                }
             }
-            __syncwarp();
-            // dA[r][i] = -sum_b Y[r][b] T[i][b], strict lower
-            for (int e = lane; e < 256; e += 32) {
-                const int r = e >> 4, i = e & 15;
-                float a = 0.f;
-                for (int b = 0; b < 16; ++b) a = fmaf(sY[r * 16 + b], T[i * 17 + b], a);
-                sA[e] = i < r ? -a : 0.f;
+            if (!exact) {
+#pragma unroll
+                for (int o = 1; o < 4; o <<= 1) {
+                    pb0 += __shfl_xor_sync(0xffffffffu, pb0, o);
+                    pb1 += __shfl_xor_sync(0xffffffffu, pb1, o);
+                }
+                if (tig == 0) {
+                    sPB[warp * 16 + gid] = pb0;
+                    sPB[warp * 16 + gid + 8] = pb1;
+                }
             }
         }
         __syncthreads();
 
-        // ---- phase 4b: thread = channel ch, all 16 rows
+        // ---- phase 4f: thread = channel ch, all 16 rows
         {
             const int ch = tid;
-            const int64_t base = (t0 * H + h) * kDim + ch;
-            const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.ip.q);
-            const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.ip.k);
-            float kk_[16], qq[16], G2[16], bet[16];
-            float run = 0.f;
+            const int64_t base = qoff + ch;
+            float dG[16];
+            const float G2L = Gc[15];
+            float dGL = (sdG[ch] + sdG[kDim + ch] + sdG[2 * kDim + ch] + sdG[3 * kDim + ch]) * ex2g(G2L);
+            if (!exact) {
+                // q and k enter through the record's scale Q e^G and K e^(G_last - G)
+                // and the K e^G, K e^-G tiles
+                const float inv_scale = scale != 0.f ? 1.f / scale : 0.f;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const bool ok = r < L;
-                kk_[r] = ok ? __bfloat162float(kg[base + r * rowe]) : 0.f;
-                qq[r] = ok ? __bfloat162float(qg[base + r * rowe]) : 0.f;
-                run += ok ? __ldg(p.ip.g + base + r * rowe) * kLog2eG : 0.f;
-                G2[r] = run;
-                bet[r] = ok ? __ldg(p.ip.beta + (t0 + r) * H + h) : 0.f;
-            }
-            const float *T = ws.t;
-            float dk[16], dq[16], dG[16], pb[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) { dk[r] = 0.f; dq[r] = 0.f; dG[r] = 0.f; pb[r] = 0.f; }
-            // the gated Gram products, exact per-pair exponentials
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-#pragma unroll
-                for (int i = 0; i <= r; ++i) {
-                    const float E = ex2g(G2[r] - G2[i]);
-                    const float dY = scale * gP[r * 16 + i];
-                    const float wP = dY * E;
-                    dq[r] = fmaf(wP, kk_[i], dq[r]);
-                    dk[i] = fmaf(wP, qq[r], dk[i]);
-                    const float tP = wP * qq[r] * kk_[i];
-                    dG[r] += tP;
-                    dG[i] -= tP;
-                    if (i < r) {
-                        const float dAr = sA[r * 16 + i];
-                        const float kkE = kk_[r] * kk_[i] * E;
-                        pb[r] = fmaf(dAr, kkE, pb[r]);
-                        const float wA = bet[r] * dAr * E;
-                        dk[r] = fmaf(wA, kk_[i], dk[r]);
-                        dk[i] = fmaf(wA, kk_[r], dk[i]);
-                        const float tA = bet[r] * dAr * kkE;
-                        dG[r] += tA;
-                        dG[i] -= tA;
+                for (int r = 0; r < 16; ++r) {
+                    const float eG = ex2g(Gc[r]), eN = ex2g(-Gc[r]), eD = ex2g(G2L - Gc[r]);
+                    const int o16 = swz(r, ch);
+                    const float qgs = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                                          smem + kGOffRec + kRecQg + o16)) * inv_scale;
+                    const float kd = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
+                        smem + kGOffRec + kRecKd + o16));
+                    const float kgv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + kGOffKg + o16));
+                    const float knv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + kGOffKn + o16));
+                    const float z = gZ[r * kFS + ch], t1 = gT1[r * kFS + ch];
+                    const float yc = gYc[r * kFS + ch], dkd = gK[r * kFS + ch];
+                    // q dq = (q e^G) Z, k a = (k e^G) T1, k b = (k e^-G) Yc, k d = Kd dKd
+                    const float kdd = kd * dkd;
+                    dG[r] = fmaf(qgs, z, fmaf(kgv, t1, -fmaf(knv, yc, kdd)));
+                    dGL += kdd;
+                    if (r < L) {
+                        // the diagonal pair: its two dG terms cancel exactly
+                        const float yd = scale * gP[r * 17];
+                        const int64_t o = base + r * rowe;
+                        p.dq[o] = fmaf(yd, knv * eG, eG * z);
+                        p.dk[o] = fmaf(yd, qgs * eN, fmaf(eG, t1, fmaf(eN, yc, eD * dkd)));
                     }
                 }
-            }
-            // Qg = scale q e^G, Kd = k e^(G_last - G), gamma = e^(G_last), Kg = k e^G
-            const float G2L = G2[15];
-            float dGL = reinterpret_cast<const float *>(smem + kSdG)[ch] * ex2g(G2L);
-            float dv[16];
+            } else {
+                // exact per-pair exponentials for the P and A terms
+                const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.ip.q);
+                const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.ip.k);
+                float kk_[16], qq[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const float eG = ex2g(G2[r]);
-                const float dQg = gQ[r * kDim + ch];
-                dq[r] = fmaf(scale * dQg, eG, dq[r]);
-                dG[r] = fmaf(dQg, scale * qq[r] * eG, dG[r]);
-                const float eD = ex2g(G2L - G2[r]);
-                const float dKd = gK[r * kDim + ch];
-                dk[r] = fmaf(dKd, eD, dk[r]);
-                const float kdv = dKd * kk_[r] * eD;
-                dG[r] -= kdv;
-                dGL += kdv;
-                // dKg = M^T dW and dv = M^T dUt, M[u][r] = T[u][r] beta_r
-                float sW = 0.f, sU = 0.f;
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float tr = T[u * 17 + r];
-                    sW = fmaf(tr, gW[u * kDim + ch], sW);
-                    sU = fmaf(tr, gU[u * kDim + ch], sU);
+                for (int r = 0; r < 16; ++r) {
+                    const bool ok = r < L;
+                    kk_[r] = ok ? __bfloat162float(kg[base + r * rowe]) : 0.f;
+                    qq[r] = ok ? __bfloat162float(qg[base + r * rowe]) : 0.f;
                 }
-                const float dKg = bet[r] * sW;
-                dv[r] = bet[r] * sU;
-                dk[r] = fmaf(dKg, eG, dk[r]);
-                dG[r] = fmaf(dKg, kk_[r] * eG, dG[r]);
+                float dk[16], dq[16], pb[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) { dk[r] = 0.f; dq[r] = 0.f; dG[r] = 0.f; pb[r] = 0.f; }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const float br = sBeta[r];
+#pragma unroll
+                    for (int i = 0; i <= r; ++i) {
+                        const float E = ex2g(Gc[r] - Gc[i]);
+                        const float wP = scale * gP[r * 16 + i] * E;
+                        dq[r] = fmaf(wP, kk_[i], dq[r]);
+                        dk[i] = fmaf(wP, qq[r], dk[i]);
+                        const float tP = wP * qq[r] * kk_[i];
+                        dG[r] += tP;
+                        dG[i] -= tP;
+                        if (i < r) {
+                            const float dAr = sdA[r * 16 + i];
+                            const float kkE = kk_[r] * kk_[i] * E;
+                            pb[r] = fmaf(dAr, kkE, pb[r]);
+                            const float wA = br * dAr * E;
+                            dk[r] = fmaf(wA, kk_[i], dk[r]);
+                            dk[i] = fmaf(wA, kk_[r], dk[i]);
+                            const float tA = br * dAr * kkE;
+                            dG[r] += tA;
+                            dG[i] -= tA;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const float eG = ex2g(Gc[r]), eD = ex2g(G2L - Gc[r]);
+                    const float q1 = eG * gZ[r * kFS + ch];
+                    const float a = eG * gT1[r * kFS + ch];
+                    const float d = eD * gK[r * kFS + ch];
+                    dG[r] = fmaf(qq[r], q1, fmaf(kk_[r], a - d, dG[r]));
+                    dGL = fmaf(kk_[r], d, dGL);
+                    if (r < L) {
+                        const int64_t o = base + r * rowe;
+                        p.dq[o] = dq[r] + q1;
+                        p.dk[o] = dk[r] + a + d;
+                    }
+                }
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float x = pb[r];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                    if (lane == 0) sPB[warp * 16 + r] = x;
+                }
             }
             dG[15] += dGL;
-            // dbeta partials of this channel (A part), summed over the channels below
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float x = pb[r];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-                if (lane == 0) sB[16 + warp * 16 + r] = x;
-            }
-            // dg = reverse cumulative sum of dG; outputs for rows < L
+            // dg = reverse cumulative sum of dG over the rows
             float acc = 0.f;
 #pragma unroll
             for (int r = 15; r >= 0; --r) {
                 acc += dG[r];
-                if (r < L) {
-                    const int64_t o = base + r * rowe;
-                    p.dq[o] = dq[r];
-                    p.dk[o] = dk[r];
-                    p.dv[o] = dv[r];
-                    p.dg[o] = acc;
-                }
+                if (r < L) p.dg[base + r * rowe] = acc;
             }
         }
         __syncthreads();
-        if (tid < 16 && tid < L) {
-            const float bA = sB[16 + tid] + sB[32 + tid] + sB[48 + tid] + sB[64 + tid];
-            p.dbeta[(t0 + tid) * H + h] = sB[tid] + bA;
-        }
+        if (tid < 16 && tid < L)
+            p.dbeta[(t0 + tid) * H + h] = sBM[tid] + sPB[tid] + sPB[16 + tid] + sPB[32 + tid] + sPB[48 + tid];
     }
-    (void)kLn2;
 }
 
 }  // namespace
@@ -640,13 +870,49 @@ cudaError_t launch_bwd_chain(const BwdChunkParams &p, cudaStream_t stream) {
 cudaError_t launch_bwd_grad(const BwdChunkParams &p, cudaStream_t stream) {
     const int64_t items = p.max_chunks * p.geo.n_heads;
     if (items <= 0) return cudaSuccess;
+    using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+    const EncodeFn enc = reinterpret_cast<EncodeFn>(tensor_map_encoder());
+    if (enc == nullptr) return cudaErrorNotSupported;
+    GradMaps tm;
+    {
+        // g and k: [tokens][H][128], a box is 16 tokens of one head
+        const int64_t tokens = p.geo.cu != nullptr ? p.geo.seq_len
+                                                   : static_cast<int64_t>(p.geo.n_seqs) * p.geo.seq_len;
+        const cuuint64_t H = static_cast<cuuint64_t>(p.geo.n_heads);
+        const cuuint64_t gd[3] = {static_cast<cuuint64_t>(kDim), H, static_cast<cuuint64_t>(tokens)};
+        const cuuint64_t gs4[2] = {kDim * 4, H * kDim * 4}, gs2[2] = {kDim * 2, H * kDim * 2};
+        const cuuint32_t gb[3] = {128, 1, 16};
+        const cuuint32_t e1[3] = {1, 1, 1};
+        if (enc(&tm.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(p.ip.g), gd, gs4, gb, e1,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+            enc(&tm.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.ip.k), gd, gs2, gb, e1,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kDim),
+                                static_cast<cuuint64_t>(items)};
+    const cuuint64_t strides[2] = {kDim * 2, kDim * kDim * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const void *bases[2] = {p.ckpt, p.dsn};
+    CUtensorMap *maps[2] = {&tm.st, &tm.dst};
+    for (int i = 0; i < 2; ++i)
+        if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(bases[i]), dims, strides, box,
+                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
     int dev = 0, sms = 0, nb = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kda_bwd_grad_kernel, kGThreads, kGSmem);
     int64_t grid = static_cast<int64_t>(sms > 0 ? sms : 152) * (nb > 0 ? nb : 1);
     if (grid > items) grid = items;
-    kda_bwd_grad_kernel<<<static_cast<unsigned>(grid), kGThreads, kGSmem, stream>>>(p);
+    kda_bwd_grad_kernel<<<static_cast<unsigned>(grid), kGThreads, kGSmem, stream>>>(p, tm);
     return cudaGetLastError();
 }
 

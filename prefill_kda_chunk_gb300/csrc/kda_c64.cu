@@ -1532,6 +1532,21 @@ __global__ void __launch_bounds__(kIThreads, 1) kda_c64_fused_kernel(const __gri
 // ============================================================================
 namespace kda {
 
+void *tensor_map_encoder() {
+    static void *fn = [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<void *>(nullptr);
+        }
+        return f;
+    }();
+    return fn;
+}
+
 namespace {
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -1539,20 +1554,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_
                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                             &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess) {
-            cudaGetLastError();
-            return static_cast<EncodeTiledFn>(nullptr);
-        }
-        return reinterpret_cast<EncodeTiledFn>(f);
-    }();
-    return fn;
-}
+EncodeTiledFn encode_fn() { return reinterpret_cast<EncodeTiledFn>(tensor_map_encoder()); }
 
 // [tokens, H, 128] row-major as a 3D tiled map (channel, head, token); a box
 // is 64 tokens x 1 head x 128 bytes of channels (64 bf16 or 32 fp32), stored

@@ -46,6 +46,9 @@ struct IntraParams {
     // counters are 0 between calls; exact_list holds one entry per item.
     int32_t *exact_list = nullptr;
     int *exact_ctr = nullptr;
+    // When not null, (I + A)^{-1} of every chunk-head, fp32 [16][16] row-major
+    // at item index (record index * H + head) * 256 (the gradients read it)
+    float *tinv = nullptr;
 };
 
 struct RecurParams {
@@ -132,6 +135,9 @@ struct BwdChunkParams {
     ChunkGeometry geo;
     int64_t max_chunks;
 };
+// cuTensorMapEncodeTiled from the driver (cast to its signature), or null.
+void *tensor_map_encoder();
+
 cudaError_t configure_backward_chunk();
 cudaError_t launch_bwd_chain(const BwdChunkParams &p, cudaStream_t stream);
 cudaError_t launch_bwd_grad(const BwdChunkParams &p, cudaStream_t stream);

@@ -48,8 +48,10 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     int64_t t0, rec_idx;
     if (!locate_chunk(geo, chunk, n, t0, L, rec_idx)) continue;
     (void)n;
-    uint8_t *rec = p.rec + (rec_idx * H + h) * kRecBytes;
-    if (intra_item<PRE, false>(p, sm, t0, L, h, rec) && lane == 0)
+    const int64_t ri = rec_idx * H + h;
+    uint8_t *rec = p.rec + ri * kRecBytes;
+    if (intra_item<PRE, false>(p, sm, t0, L, h, rec, p.tinv != nullptr ? p.tinv + ri * 256 : nullptr) &&
+        lane == 0)
         p.exact_list[atomicAdd(p.exact_ctr, 1)] = static_cast<int32_t>(item);
     }  // items
 }
@@ -83,7 +85,9 @@ kda_intra_exact_kernel(IntraParams p) {
         int64_t t0, rec_idx;
         if (!locate_chunk(geo, chunk, n, t0, L, rec_idx)) continue;
         (void)n;
-        intra_exact_item<PRE, false>(p, sm, t0, L, h, p.rec + (rec_idx * H + h) * kRecBytes);
+        const int64_t ri = rec_idx * H + h;
+        intra_exact_item<PRE, false>(p, sm, t0, L, h, p.rec + ri * kRecBytes,
+                                     p.tinv != nullptr ? p.tinv + ri * 256 : nullptr);
     }
     if (count == 0) return;   // the same count in every CTA: nothing to reset
     __syncthreads();

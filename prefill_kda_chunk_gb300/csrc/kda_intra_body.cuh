@@ -347,10 +347,11 @@ __device__ __forceinline__ void intra_exact_chunk(const float *gp, int64_t rowe,
 
 // The part of an item common to both forms: Tm = (I + A)^{-1} from sm.a,
 // then W = Tm diag(beta) (K e^G) from sm.kg and Ut^T = (Tm diag(beta) V)^T
-// from sm.v, both to the record.
+// from sm.v, both to the record; Tm itself to tout ([16][16] fp32) when that
+// is not null.
 template <bool KEEP>
-__device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, float beta_l,
-                                           int lane) {
+__device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, float *tout,
+                                           float beta_l, int lane) {
     const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
     const uint32_t s_kg = smem_u32(sm.kg), s_v = smem_u32(sm.v);
 
@@ -371,6 +372,13 @@ __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, floa
         }
     }
     __syncwarp();
+    if (tout != nullptr) {
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+            const int e = lane + 32 * it;
+            __stcs(tout + e, sm.t[(e >> 4) * 17 + (e & 15)]);
+        }
+    }
 
     // ---- A fragments of Tm diag(beta) (bf16)
     uint32_t aT[4];
@@ -429,13 +437,14 @@ __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, floa
     __syncwarp();
 }
 // One (chunk, head) item in the factored form, by one warp: sm is the warp's
-// shared memory, rec its record, rows [t0, t0 + L) of head h its tokens.
+// shared memory, rec its record, tout where (I + A)^{-1} goes (or null),
+// rows [t0, t0 + L) of head h its tokens.
 // Returns whether the chunk leaves the factored range (|G| > 80 in some
 // channel): its record then holds wrong numbers until intra_exact_item
 // rewrites it.
 template <bool PRE, bool KEEP>
 __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &sm, int64_t t0,
-                                           int L, int h, uint8_t *rec) {
+                                           int L, int h, uint8_t *rec, float *tout) {
     const int lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
     const int H = p.geo.n_heads;
@@ -568,14 +577,14 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
         }
     }
     __syncwarp();
-    intra_tail<KEEP>(sm, rec, beta_l, lane);
+    intra_tail<KEEP>(sm, rec, tout, beta_l, lane);
     return exact;
 }
 
 // The same item in the exact per-pair form (the whole record rewritten).
 template <bool PRE, bool KEEP>
 __device__ __forceinline__ void intra_exact_item(const IntraParams &p, IntraWarpSmem &sm, int64_t t0,
-                                                 int L, int h, uint8_t *rec) {
+                                                 int L, int h, uint8_t *rec, float *tout) {
     const int lane = threadIdx.x & 31;
     const int H = p.geo.n_heads;
     load_chunk(p, sm, t0, L, h, lane);
@@ -585,7 +594,7 @@ __device__ __forceinline__ void intra_exact_item(const IntraParams &p, IntraWarp
     intra_exact_chunk<KEEP>(p.g + (t0 * H + h) * kDim + 4 * lane, static_cast<int64_t>(H) * kDim, L,
                             PRE ? p.pre : 0, p.scale, beta_l, &sm, rec, p.err);
     __syncwarp();
-    intra_tail<KEEP>(sm, rec, beta_l, lane);
+    intra_tail<KEEP>(sm, rec, tout, beta_l, lane);
 }
 
 }  // namespace
