@@ -692,12 +692,10 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
         if (kda::launch_intra_chunk(ip, pl.max_chunks, stream) != cudaSuccess ||
             kda::launch_intra_exact(ip, stream) != cudaSuccess)
             return KDA_ERR_CUDA;
-        kda::RecurParams rp{rec, initial_state, nullptr, nullptr, st.err, geo};
-        rp.ckpt = ck;
-        if (kda::launch_recurrent_states(rp, stream) != cudaSuccess) return KDA_ERR_CUDA;
         kda::BwdChunkParams bp{};
         bp.ip = ip;
         bp.rec = rec;
+        bp.s0 = initial_state;
         bp.dout = d_out;
         bp.dsf = d_final_state;
         bp.ds0 = d_initial_state;
@@ -707,7 +705,9 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
         bp.err = st.err;
         bp.geo = geo;
         bp.max_chunks = pl.max_chunks;
-        if (kda::launch_bwd_chain(bp, stream) != cudaSuccess) return KDA_ERR_CUDA;
+        if (kda::launch_bwd_states(bp, stream) != cudaSuccess ||
+            kda::launch_bwd_chain(bp, stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
         return kda::launch_bwd_grad(bp, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     }
     float *ckpt = reinterpret_cast<float *>(wsb + 256 + pl.off_bytes);

@@ -41,41 +41,78 @@ namespace kda {
 
 namespace {
 
-constexpr int kChainStageBytes = kRecUt;   // W, Qg, Kd, P, gamma (the reverse needs no Ut)
-constexpr int kCBV = 64;                   // value channels per reverse-chain CTA
-constexpr int kCWarps = kCBV / 16;
-constexpr int kChainSmem = kStages * kChainStageBytes + 2 * kStages * 8;
-
 // ---------------------------------------------------------------------------
-// Reverse chain: one CTA per (sequence, head, 64-value slice), 4 consumer
-// warps holding dS^T fragments (16 values x 128 keys each, fp32) and one
-// producer warp streaming the records (last chunk first) into a ring of
-// shared-memory stages.
-__global__ void __launch_bounds__((kCWarps + 1) * 32) kda_bwd_chain_kernel(BwdChunkParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
-    const ChunkGeometry &geo = p.geo;
-    const int H = geo.n_heads;
-    constexpr int kSlices = kDim / kCBV;
-    const int s = blockIdx.x % kSlices;
-    const int h = (blockIdx.x / kSlices) % H;
-    const int n = blockIdx.x / (kSlices * H);
-    const uint32_t stage0 = smem_u32(smem);
-    const uint32_t bar_full = stage0 + kStages * kChainStageBytes;
-    const uint32_t bar_empty = bar_full + kStages * 8;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(bar_full + 8 * i, 1);
-            mbar_init(bar_empty + 8 * i, kCWarps * 32);
-        }
-        mbar_fence_init();
-    }
-    __syncthreads();
-    if (geo.cu != nullptr && (*geo.call_flags & kErrBadCu)) return;
+// The two chains. Each CTA owns (sequence, head, 64-value slice), 4 consumer
+// warps holding 16 value rows x 128 keys of an fp32 state in MMA fragments
+// and one producer warp streaming the records into a ring of stages. Every
+// chunk, each consumer warp writes its rows of the state, in bf16, to the
+// [record index][H][128 v][128 k] array of the gradient kernel: stmatrix into
+// a shared staging half-pair ([16][64] x 2, 128-byte swizzle, double
+// buffered) and two TMA tensor stores, so the chain issues 8 shared stores
+// and 2 copies a step instead of 32 scattered global stores a thread.
+constexpr int kCBV = 64;                   // value channels per chain CTA
+constexpr int kCWarps = kCBV / 16;
+constexpr int kStageOff = kCWarps * 2 * 4096;            // after the staging buffers
+constexpr int kChainStageBytes = kRecUt + 2048;          // W, Qg, Kd, P, gamma (no Ut), then dO
+                                                         //   [16 t][64 v] bf16, 128-byte swizzle
+constexpr int kStatesStageBytes = kRecUt + kCBV * 32;    // ... and the slice of Ut^T
+constexpr int kChainSmem = kStageOff + kStages * kChainStageBytes + 2 * kStages * 8;
+constexpr int kStatesSmem = kStageOff + kStages * kStatesStageBytes + 2 * kStages * 8;
 
-    int64_t tb, te, chunk0;
-    int nck;
+struct ChainMaps {
+    CUtensorMap out;       // [items][128 v][128 k] bf16, boxes of 16 v x 64 k
+    CUtensorMap dout;      // dO [tokens][H][128] bf16, boxes of 16 tokens x 1 head x 64 v
+};
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void stsm_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(addr), "r"(r0),
+                 "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y, int z) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
+// The warp's 16 x 128 slice of the state fragments (rows v0 .. v0 + 15) to
+// row z's entry of the bf16 state array. Lane 0 owns the bulk groups: the
+// buffer written now was last read by the store of two chunks ago.
+__device__ __forceinline__ void store_state_slice(const float (&acc)[16][4], uint32_t stage_buf,
+                                                  const CUtensorMap *map, int v0, int z, int lane) {
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+    __syncwarp();
+    const int m = lane >> 3, rr = (m & 1) * 8 + (lane & 7);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+        const int c = 8 * (j + (m >> 1));   // key column of this lane's row address
+        const uint32_t addr = stage_buf + ((c >> 6) << 11) + rr * 128 + ((((c >> 3) & 7) ^ (rr & 7)) << 4);
+        stsm_x4(addr, pack_bf16(acc[j][0], acc[j][1]), pack_bf16(acc[j][2], acc[j][3]),
+                pack_bf16(acc[j + 1][0], acc[j + 1][1]), pack_bf16(acc[j + 1][2], acc[j + 1][3]));
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_3d(map, stage_buf, 0, v0, z);
+        tma_store_3d(map, stage_buf + 2048, 64, v0, z);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+}
+
+// The chunks of unit n: tokens [tb, te), records from chunk0, nck chunks.
+__device__ __forceinline__ void chain_unit(const ChunkGeometry &geo, int n, int64_t &tb, int64_t &te,
+                                           int64_t &chunk0, int &nck) {
     if (geo.cu == nullptr) {
         tb = static_cast<int64_t>(n) * geo.seq_len;
         te = tb + geo.seq_len;
@@ -87,6 +124,123 @@ __global__ void __launch_bounds__((kCWarps + 1) * 32) kda_bwd_chain_kernel(BwdCh
         chunk0 = geo.chunk_off[n];
         nck = static_cast<int>((te - tb + 15) / 16);
     }
+}
+
+// ---------------------------------------------------------------------------
+// Forward chain keeping the states: the recurrent step without outputs, the
+// state entering every chunk stored as S^T.
+__global__ void __launch_bounds__((kCWarps + 1) * 32)
+kda_bwd_states_kernel(const __grid_constant__ BwdChunkParams p, const __grid_constant__ ChainMaps tm) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const ChunkGeometry &geo = p.geo;
+    const int H = geo.n_heads;
+    constexpr int kSlices = kDim / kCBV;
+    const int s = blockIdx.x % kSlices;
+    const int h = (blockIdx.x / kSlices) % H;
+    const int n = blockIdx.x / (kSlices * H);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t stage0 = sb + kStageOff;
+    const uint32_t bar_full = stage0 + kStages * kStatesStageBytes;
+    const uint32_t bar_empty = bar_full + kStages * 8;
+    if (sb & 1023u) {   // the swizzled staging halves need 1024-byte alignment
+        if (threadIdx.x == 0) atomicOr(p.err, kErrTimeout);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, kCWarps * 32);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (geo.cu != nullptr && (*geo.call_flags & kErrBadCu)) return;
+    int64_t tb, te, chunk0;
+    int nck;
+    chain_unit(geo, n, tb, te, chunk0, nck);
+    const uint8_t *rec0 = p.rec + (chunk0 * H + h) * static_cast<int64_t>(kRecBytes);
+
+    if (warp == kCWarps) {
+        // ------------------------------------------------------ producer
+        if (lane == 0) {
+            for (int i = 0; i < nck; ++i) {
+                const int st = i % kStages;
+                if (i >= kStages && !mbar_wait(bar_empty + 8 * st, ((i / kStages) - 1) & 1)) {
+                    atomicOr(p.err, kErrTimeout);
+                    break;
+                }
+                const uint8_t *src = rec0 + static_cast<int64_t>(i) * H * kRecBytes;
+                const uint32_t dst = stage0 + st * kStatesStageBytes;
+                mbar_arrive_expect_tx(bar_full + 8 * st, kStatesStageBytes);
+                bulk_g2s(dst, src, kRecUt, bar_full + 8 * st);
+                bulk_g2s(dst + kRecUt, src + kRecUt + s * kCBV * 32, kCBV * 32, bar_full + 8 * st);
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    const int vw = 16 * warp;
+    const int v0 = s * kCBV + vw;
+    float acc[16][4];   // S^T fragments: rows = value, cols = key
+    recur_load_state(acc, p.s0 != nullptr ? p.s0 + (static_cast<int64_t>(n) * H + h) * kDim * kDim : nullptr, v0);
+    const uint32_t buf0 = sb + warp * 8192;
+    bool ready = false;
+    for (int i = 0; i < nck; ++i) {
+        const int st = i % kStages;
+        store_state_slice(acc, buf0 + (i & 1) * 4096, &tm.out, v0, static_cast<int>((chunk0 + i) * H + h), lane);
+        if (!ready && !mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
+            atomicOr(p.err, kErrTimeout);
+            break;
+        }
+        const int64_t t0 = tb + 16 * static_cast<int64_t>(i);
+        ready = recur_step<false>(acc, smem + kStageOff + st * kStatesStageBytes, stage0 + st * kStatesStageBytes,
+                                  vw, false, nullptr, nullptr, static_cast<int>(te - t0 < 16 ? te - t0 : 16), H,
+                                  [&] {
+                                      return i + 1 < nck &&
+                                             mbar_test(bar_full + 8 * ((i + 1) % kStages), ((i + 1) / kStages) & 1);
+                                  });
+        mbar_arrive(bar_empty + 8 * st);
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Reverse chain: the records last chunk first, each with its 16 rows of dO
+// for the CTA's 64 values, dS^T in the fragments, dS_next^T of every chunk
+// stored, dL/d(initial state) at the end.
+__global__ void __launch_bounds__((kCWarps + 1) * 32)
+kda_bwd_chain_kernel(const __grid_constant__ BwdChunkParams p, const __grid_constant__ ChainMaps tm) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
+    const ChunkGeometry &geo = p.geo;
+    const int H = geo.n_heads;
+    constexpr int kSlices = kDim / kCBV;
+    const int s = blockIdx.x % kSlices;
+    const int h = (blockIdx.x / kSlices) % H;
+    const int n = blockIdx.x / (kSlices * H);
+    const uint32_t sb = smem_u32(smem);
+    const uint32_t stage0 = sb + kStageOff;
+    const uint32_t bar_full = stage0 + kStages * kChainStageBytes;
+    const uint32_t bar_empty = bar_full + kStages * 8;
+    if (sb & 1023u) {
+        if (threadIdx.x == 0) atomicOr(p.err, kErrTimeout);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, kCWarps * 32);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (geo.cu != nullptr && (*geo.call_flags & kErrBadCu)) return;
+    int64_t tb, te, chunk0;
+    int nck;
+    chain_unit(geo, n, tb, te, chunk0, nck);
     const uint8_t *rec0 = p.rec + (chunk0 * H + h) * static_cast<int64_t>(kRecBytes);
 
     if (warp == kCWarps) {
@@ -100,8 +254,10 @@ __global__ void __launch_bounds__((kCWarps + 1) * 32) kda_bwd_chain_kernel(BwdCh
                 }
                 mbar_arrive_expect_tx(bar_full + 8 * st, kChainStageBytes);
                 bulk_g2s(stage0 + st * kChainStageBytes,
-                         rec0 + static_cast<int64_t>(nck - 1 - i) * H * kRecBytes, kChainStageBytes,
+                         rec0 + static_cast<int64_t>(nck - 1 - i) * H * kRecBytes, kRecUt,
                          bar_full + 8 * st);
+                tma_load_3d(stage0 + st * kChainStageBytes + kRecUt, &tm.dout, s * kCBV, h,
+                            static_cast<int>(tb + 16 * static_cast<int64_t>(nck - 1 - i)), bar_full + 8 * st);
             }
         }
         return;
@@ -113,43 +269,37 @@ __global__ void __launch_bounds__((kCWarps + 1) * 32) kda_bwd_chain_kernel(BwdCh
     const int64_t sbase = (static_cast<int64_t>(n) * H + h) * kDim * kDim;
     float acc[16][4];   // dS^T fragments: rows = value, cols = key
     recur_load_state(acc, p.dsf != nullptr ? p.dsf + sbase : nullptr, v0);
-    const __nv_bfloat16 *dout = static_cast<const __nv_bfloat16 *>(p.dout);
-    const int64_t rowe = static_cast<int64_t>(H) * kDim;
+    const uint32_t buf0 = sb + warp * 8192;
 
     for (int i = 0; i < nck; ++i) {
         const int c = nck - 1 - i;                   // chunk of the sequence
         const int st = i % kStages;
-        const int64_t t0 = tb + 16 * static_cast<int64_t>(c);
-        const int L = static_cast<int>(te - t0 < 16 ? te - t0 : 16);
-        // dO^T as the A operand: rows v0 + gid (+ 8), tokens 2 tig (+ 1), + 8
-        uint32_t aO[4];
-        {
-            auto ld = [&](int t, int v) -> float {
-                return t < L ? __bfloat162float(dout[(t0 + t) * rowe + h * kDim + v]) : 0.f;
-            };
-            const int va = v0 + gid, vb = va + 8, ta = 2 * tig, tc = ta + 8;
-            aO[0] = pack_bf16(ld(ta, va), ld(ta + 1, va));
-            aO[1] = pack_bf16(ld(ta, vb), ld(ta + 1, vb));
-            aO[2] = pack_bf16(ld(tc, va), ld(tc + 1, va));
-            aO[3] = pack_bf16(ld(tc, vb), ld(tc + 1, vb));
-        }
         // dS_next^T of this chunk (bf16, [v][k]) for the gradient kernel
-        {
-            __nv_bfloat16 *dp = static_cast<__nv_bfloat16 *>(p.dsn) +
-                                ((chunk0 + c) * H + h) * static_cast<int64_t>(kDim * kDim) +
-                                static_cast<int64_t>(v0 + gid) * kDim + 2 * tig;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                *reinterpret_cast<uint32_t *>(dp + 8 * j) = pack_bf16(acc[j][0], acc[j][1]);
-                *reinterpret_cast<uint32_t *>(dp + 8 * kDim + 8 * j) = pack_bf16(acc[j][2], acc[j][3]);
-            }
-        }
+        store_state_slice(acc, buf0 + (i & 1) * 4096, &tm.out, v0, static_cast<int>((chunk0 + c) * H + h), lane);
         if (!mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
             atomicOr(p.err, kErrTimeout);
             break;
         }
-        const uint8_t *stg = smem + st * kChainStageBytes;
+        const uint8_t *stg = smem + kStageOff + st * kChainStageBytes;
         const uint32_t sw = stage0 + st * kChainStageBytes;
+        // dO^T as the A operand (rows vw + gid (+ 8), tokens 2 tig (+ 1), + 8) from
+        // the [t][v] tile; tokens past the end of the sequence are zero
+        uint32_t aO[4];
+        {
+            const int m = lane >> 3, t = (m >> 1) * 8 + (lane & 7), vc = vw + (m & 1) * 8;
+            ldsm_x4_t(sw + kRecUt + t * 128 + ((((vc >> 3) & 7) ^ (t & 7)) << 4), aO[0], aO[1], aO[2], aO[3]);
+            const int64_t t0 = tb + 16 * static_cast<int64_t>(c);
+            const int L = static_cast<int>(te - t0 < 16 ? te - t0 : 16);
+            if (L < 16) {
+                const int ta = 2 * tig;
+                const uint32_t lo = (ta < L ? 0x0000ffffu : 0u) | (ta + 1 < L ? 0xffff0000u : 0u);
+                const uint32_t hi = (ta + 8 < L ? 0x0000ffffu : 0u) | (ta + 9 < L ? 0xffff0000u : 0u);
+                aO[0] &= lo;
+                aO[1] &= lo;
+                aO[2] &= hi;
+                aO[3] &= hi;
+            }
+        }
 
         // dS_next^T as bf16 A fragments, one per 16-key step
         uint32_t aD[8][4];
@@ -217,6 +367,7 @@ __global__ void __launch_bounds__((kCWarps + 1) * 32) kda_bwd_chain_kernel(BwdCh
         mbar_arrive(bar_empty + 8 * st);
     }
     if (p.ds0 != nullptr) recur_store_state(acc, p.ds0 + sbase, v0);
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -272,15 +423,6 @@ struct GradMaps {
     CUtensorMap st, dst;   // S^T and dS_next^T: [items][128 v][128 k] bf16, boxes of 128 v x 64 k
     CUtensorMap g, k;      // g fp32, k bf16: [tokens][H][128], boxes of 16 tokens x 1 head x 128
 };
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int x, int y, int z,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
 
 constexpr float kLog2eG = 1.4426950408889634f;
 
@@ -853,59 +995,89 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
 
 }  // namespace
 
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// [items][128 v][128 k] bf16 with boxes of `rows` values x 64 keys, 128-byte swizzle
+bool encode_states(EncodeFn enc, CUtensorMap *m, const void *base, int64_t items, uint32_t rows) {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kDim),
+                                static_cast<cuuint64_t>(items)};
+    const cuuint64_t strides[2] = {kDim * 2, kDim * kDim * 2};
+    const cuuint32_t box[3] = {64, rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// [tokens][H][128] rows with boxes of 16 tokens x 1 head x `width` channels: 128
+// without swizzle, or 64 bf16 (128 bytes) with 128-byte swizzle
+bool encode_rows16(EncodeFn enc, CUtensorMap *m, const void *base, bool f32, int64_t H, int64_t tokens,
+                   uint32_t width = 128) {
+    const cuuint64_t es = f32 ? 4 : 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(tokens)};
+    const cuuint64_t strides[2] = {kDim * es, static_cast<cuuint64_t>(H) * kDim * es};
+    const cuuint32_t box[3] = {width, 1, 16};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               width == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t configure_backward_chunk() {
     cudaError_t e = cudaFuncSetAttribute(kda_bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kChainSmem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kda_bwd_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStatesSmem);
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(kda_bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
+}
+
+cudaError_t launch_bwd_states(const BwdChunkParams &p, cudaStream_t stream) {
+    const int64_t ctas = static_cast<int64_t>(p.geo.n_seqs) * p.geo.n_heads * (kDim / kCBV);
+    if (ctas <= 0) return cudaSuccess;
+    const EncodeFn enc = reinterpret_cast<EncodeFn>(tensor_map_encoder());
+    if (enc == nullptr) return cudaErrorNotSupported;
+    ChainMaps tm;
+    if (!encode_states(enc, &tm.out, p.ckpt, p.max_chunks * p.geo.n_heads, 16)) return cudaErrorInvalidValue;
+    kda_bwd_states_kernel<<<static_cast<unsigned>(ctas), (kCWarps + 1) * 32, kStatesSmem, stream>>>(p, tm);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_chain(const BwdChunkParams &p, cudaStream_t stream) {
     const int64_t ctas = static_cast<int64_t>(p.geo.n_seqs) * p.geo.n_heads * (kDim / kCBV);
     if (ctas <= 0) return cudaSuccess;
-    kda_bwd_chain_kernel<<<static_cast<unsigned>(ctas), (kCWarps + 1) * 32, kChainSmem, stream>>>(p);
+    const EncodeFn enc = reinterpret_cast<EncodeFn>(tensor_map_encoder());
+    if (enc == nullptr) return cudaErrorNotSupported;
+    ChainMaps tm;
+    const int64_t tokens =
+        p.geo.cu != nullptr ? p.geo.seq_len : static_cast<int64_t>(p.geo.n_seqs) * p.geo.seq_len;
+    if (!encode_states(enc, &tm.out, p.dsn, p.max_chunks * p.geo.n_heads, 16) ||
+        !encode_rows16(enc, &tm.dout, p.dout, false, p.geo.n_heads, tokens, 64))
+        return cudaErrorInvalidValue;
+    kda_bwd_chain_kernel<<<static_cast<unsigned>(ctas), (kCWarps + 1) * 32, kChainSmem, stream>>>(p, tm);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_grad(const BwdChunkParams &p, cudaStream_t stream) {
     const int64_t items = p.max_chunks * p.geo.n_heads;
     if (items <= 0) return cudaSuccess;
-    using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
     const EncodeFn enc = reinterpret_cast<EncodeFn>(tensor_map_encoder());
     if (enc == nullptr) return cudaErrorNotSupported;
+    const int64_t tokens =
+        p.geo.cu != nullptr ? p.geo.seq_len : static_cast<int64_t>(p.geo.n_seqs) * p.geo.seq_len;
     GradMaps tm;
-    {
-        // g and k: [tokens][H][128], a box is 16 tokens of one head
-        const int64_t tokens = p.geo.cu != nullptr ? p.geo.seq_len
-                                                   : static_cast<int64_t>(p.geo.n_seqs) * p.geo.seq_len;
-        const cuuint64_t H = static_cast<cuuint64_t>(p.geo.n_heads);
-        const cuuint64_t gd[3] = {static_cast<cuuint64_t>(kDim), H, static_cast<cuuint64_t>(tokens)};
-        const cuuint64_t gs4[2] = {kDim * 4, H * kDim * 4}, gs2[2] = {kDim * 2, H * kDim * 2};
-        const cuuint32_t gb[3] = {128, 1, 16};
-        const cuuint32_t e1[3] = {1, 1, 1};
-        if (enc(&tm.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(p.ip.g), gd, gs4, gb, e1,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-            enc(&tm.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(p.ip.k), gd, gs2, gb, e1,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
-    }
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(kDim),
-                                static_cast<cuuint64_t>(items)};
-    const cuuint64_t strides[2] = {kDim * 2, kDim * kDim * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const void *bases[2] = {p.ckpt, p.dsn};
-    CUtensorMap *maps[2] = {&tm.st, &tm.dst};
-    for (int i = 0; i < 2; ++i)
-        if (enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(bases[i]), dims, strides, box,
-                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return cudaErrorInvalidValue;
+    if (!encode_states(enc, &tm.st, p.ckpt, items, 128) || !encode_states(enc, &tm.dst, p.dsn, items, 128) ||
+        !encode_rows16(enc, &tm.g, p.ip.g, true, p.geo.n_heads, tokens) ||
+        !encode_rows16(enc, &tm.k, p.ip.k, false, p.geo.n_heads, tokens))
+        return cudaErrorInvalidValue;
     int dev = 0, sms = 0, nb = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -81,9 +81,6 @@ struct RecurParams {
     // was issued is always waited for, so none is in flight at exit.
     int32_t stall_chunk = -1;
     unsigned long long wait_ns = 0;
-    // Chunked gradients: when set, the state entering every chunk is stored
-    // as S^T in bf16, [record index][H][128 values][128 keys].
-    void *ckpt = nullptr;
 };
 
 // One-token decode step for N*H independent (sequence, head) units.
@@ -124,10 +121,11 @@ struct BackParams {
 struct BwdChunkParams {
     IntraParams ip;
     const uint8_t *rec;
+    const float *s0;           // [N, H, 128, 128] or nullptr (zero initial state)
     const void *dout;          // bf16 [tokens, H, 128]: dL/do
     const float *dsf;          // [N, H, 128, 128] or nullptr: dL/d(final state)
     float *ds0;                // [N, H, 128, 128] or nullptr: dL/d(initial state)
-    const void *ckpt;
+    void *ckpt;
     void *dsn;
     float *dq, *dk, *dv, *dg;  // fp32 [tokens, H, 128]
     float *dbeta;              // fp32 [tokens, H]
@@ -139,6 +137,7 @@ struct BwdChunkParams {
 void *tensor_map_encoder();
 
 cudaError_t configure_backward_chunk();
+cudaError_t launch_bwd_states(const BwdChunkParams &p, cudaStream_t stream);
 cudaError_t launch_bwd_chain(const BwdChunkParams &p, cudaStream_t stream);
 cudaError_t launch_bwd_grad(const BwdChunkParams &p, cudaStream_t stream);
 
@@ -155,9 +154,6 @@ cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStr
 // after every launch_intra_chunk, on the same stream
 cudaError_t launch_intra_exact(const IntraParams &p, cudaStream_t stream);
 cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream);     // warp MMA
-// the recurrent kernel without outputs over whole sequences (no scan): the
-// chunk-entry states for the gradients (RecurParams::ckpt)
-cudaError_t launch_recurrent_states(const RecurParams &p, cudaStream_t stream);
 // the maps launch of the segment-parallel scan (RecurParams::scan_segs >= 2)
 cudaError_t launch_recurrent_scan_maps(const RecurParams &p, cudaStream_t stream);
 // its serial combine: seg_entry[j] = seg_m[j-1] seg_entry[j-1] + seg_c[j-1]

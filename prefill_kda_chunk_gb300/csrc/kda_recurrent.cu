@@ -164,18 +164,6 @@ kda_recurrent_kernel(RecurParams p) {
         }
         const uint8_t *stg = smem + st * Lay::kStageBytes;
         const uint32_t sw = stage0 + st * Lay::kStageBytes;
-        if (p.ckpt != nullptr) {
-            // the state entering this chunk, S^T in bf16 (rows v0 + gid and + 8)
-            __nv_bfloat16 *cp = static_cast<__nv_bfloat16 *>(p.ckpt) +
-                                ((chunk0 + i) * H + h) * static_cast<int64_t>(kDim * kDim) +
-                                static_cast<int64_t>(v0 + gid) * kDim + 2 * tig;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                *reinterpret_cast<uint32_t *>(cp + 8 * j) = pack_bf16(acc[j][0], acc[j][1]);
-                *reinterpret_cast<uint32_t *>(cp + 8 * kDim + 8 * j) = pack_bf16(acc[j][2], acc[j][3]);
-            }
-        }
-
         ready = recur_step<OUT>(acc, stg, sw, vw, virt, so, orow,
                                 static_cast<int>((te - (tb + 16 * i)) < 16 ? (te - (tb + 16 * i)) : 16), H,
                                 [&] {
@@ -278,12 +266,6 @@ cudaError_t launch_recurrent(const RecurParams &p, cudaStream_t stream) {
 
 cudaError_t launch_recurrent_scan_maps(const RecurParams &p, cudaStream_t stream) {
     return launch<false>(p, stream);
-}
-
-cudaError_t launch_recurrent_states(const RecurParams &p, cudaStream_t stream) {
-    RecurParams q = p;
-    q.scan_segs = 0;
-    return launch<false>(q, stream);
 }
 
 cudaError_t launch_scan_combine(const RecurParams &p, cudaStream_t stream) {
