@@ -705,9 +705,7 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
         bp.err = st.err;
         bp.geo = geo;
         bp.max_chunks = pl.max_chunks;
-        if (kda::launch_bwd_states(bp, stream) != cudaSuccess ||
-            kda::launch_bwd_chain(bp, stream) != cudaSuccess)
-            return KDA_ERR_CUDA;
+        if (kda::launch_bwd_chains(bp, stream) != cudaSuccess) return KDA_ERR_CUDA;
         return kda::launch_bwd_grad(bp, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     }
     float *ckpt = reinterpret_cast<float *>(wsb + 256 + pl.off_bytes);

@@ -56,11 +56,12 @@ constexpr int kStageOff = kCWarps * 2 * 4096;            // after the staging bu
 constexpr int kChainStageBytes = kRecUt + 2048;          // W, Qg, Kd, P, gamma (no Ut), then dO
                                                          //   [16 t][64 v] bf16, 128-byte swizzle
 constexpr int kStatesStageBytes = kRecUt + kCBV * 32;    // ... and the slice of Ut^T
+static_assert(kChainStageBytes == kStatesStageBytes, "one stage size for both chains");
 constexpr int kChainSmem = kStageOff + kStages * kChainStageBytes + 2 * kStages * 8;
-constexpr int kStatesSmem = kStageOff + kStages * kStatesStageBytes + 2 * kStages * 8;
 
 struct ChainMaps {
-    CUtensorMap out;       // [items][128 v][128 k] bf16, boxes of 16 v x 64 k
+    CUtensorMap ckpt;      // S^T per chunk: [items][128 v][128 k] bf16, boxes of 16 v x 64 k
+    CUtensorMap dsn;       // dS_next^T per chunk, the same
     CUtensorMap dout;      // dO [tokens][H][128] bf16, boxes of 16 tokens x 1 head x 64 v
 };
 
@@ -128,17 +129,16 @@ __device__ __forceinline__ void chain_unit(const ChunkGeometry &geo, int n, int6
 
 // ---------------------------------------------------------------------------
 // Forward chain keeping the states: the recurrent step without outputs, the
-// state entering every chunk stored as S^T.
-__global__ void __launch_bounds__((kCWarps + 1) * 32)
-kda_bwd_states_kernel(const __grid_constant__ BwdChunkParams p, const __grid_constant__ ChainMaps tm) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+// state entering every chunk stored as S^T. unit = (sequence, head, slice).
+__device__ __forceinline__ void states_cta(const BwdChunkParams &p, const CUtensorMap *out, int unit,
+                                           uint8_t *smem) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const ChunkGeometry &geo = p.geo;
     const int H = geo.n_heads;
     constexpr int kSlices = kDim / kCBV;
-    const int s = blockIdx.x % kSlices;
-    const int h = (blockIdx.x / kSlices) % H;
-    const int n = blockIdx.x / (kSlices * H);
+    const int s = unit % kSlices;
+    const int h = (unit / kSlices) % H;
+    const int n = unit / (kSlices * H);
     const uint32_t sb = smem_u32(smem);
     const uint32_t stage0 = sb + kStageOff;
     const uint32_t bar_full = stage0 + kStages * kStatesStageBytes;
@@ -189,7 +189,7 @@ kda_bwd_states_kernel(const __grid_constant__ BwdChunkParams p, const __grid_con
     bool ready = false;
     for (int i = 0; i < nck; ++i) {
         const int st = i % kStages;
-        store_state_slice(acc, buf0 + (i & 1) * 4096, &tm.out, v0, static_cast<int>((chunk0 + i) * H + h), lane);
+        store_state_slice(acc, buf0 + (i & 1) * 4096, out, v0, static_cast<int>((chunk0 + i) * H + h), lane);
         if (!ready && !mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
             atomicOr(p.err, kErrTimeout);
             break;
@@ -210,17 +210,16 @@ kda_bwd_states_kernel(const __grid_constant__ BwdChunkParams p, const __grid_con
 // Reverse chain: the records last chunk first, each with its 16 rows of dO
 // for the CTA's 64 values, dS^T in the fragments, dS_next^T of every chunk
 // stored, dL/d(initial state) at the end.
-__global__ void __launch_bounds__((kCWarps + 1) * 32)
-kda_bwd_chain_kernel(const __grid_constant__ BwdChunkParams p, const __grid_constant__ ChainMaps tm) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+__device__ __forceinline__ void chain_cta(const BwdChunkParams &p, const CUtensorMap *out,
+                                          const CUtensorMap *dout_map, int unit, uint8_t *smem) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
     const ChunkGeometry &geo = p.geo;
     const int H = geo.n_heads;
     constexpr int kSlices = kDim / kCBV;
-    const int s = blockIdx.x % kSlices;
-    const int h = (blockIdx.x / kSlices) % H;
-    const int n = blockIdx.x / (kSlices * H);
+    const int s = unit % kSlices;
+    const int h = (unit / kSlices) % H;
+    const int n = unit / (kSlices * H);
     const uint32_t sb = smem_u32(smem);
     const uint32_t stage0 = sb + kStageOff;
     const uint32_t bar_full = stage0 + kStages * kChainStageBytes;
@@ -256,7 +255,7 @@ kda_bwd_chain_kernel(const __grid_constant__ BwdChunkParams p, const __grid_cons
                 bulk_g2s(stage0 + st * kChainStageBytes,
                          rec0 + static_cast<int64_t>(nck - 1 - i) * H * kRecBytes, kRecUt,
                          bar_full + 8 * st);
-                tma_load_3d(stage0 + st * kChainStageBytes + kRecUt, &tm.dout, s * kCBV, h,
+                tma_load_3d(stage0 + st * kChainStageBytes + kRecUt, dout_map, s * kCBV, h,
                             static_cast<int>(tb + 16 * static_cast<int64_t>(nck - 1 - i)), bar_full + 8 * st);
             }
         }
@@ -275,7 +274,7 @@ kda_bwd_chain_kernel(const __grid_constant__ BwdChunkParams p, const __grid_cons
         const int c = nck - 1 - i;                   // chunk of the sequence
         const int st = i % kStages;
         // dS_next^T of this chunk (bf16, [v][k]) for the gradient kernel
-        store_state_slice(acc, buf0 + (i & 1) * 4096, &tm.out, v0, static_cast<int>((chunk0 + c) * H + h), lane);
+        store_state_slice(acc, buf0 + (i & 1) * 4096, out, v0, static_cast<int>((chunk0 + c) * H + h), lane);
         if (!mbar_wait(bar_full + 8 * st, (i / kStages) & 1)) {
             atomicOr(p.err, kErrTimeout);
             break;
@@ -368,6 +367,19 @@ kda_bwd_chain_kernel(const __grid_constant__ BwdChunkParams p, const __grid_cons
     }
     if (p.ds0 != nullptr) recur_store_state(acc, p.ds0 + sbase, v0);
     if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Both chains in one launch: CTAs [0, units) keep the forward states, the
+// rest run the reverse chain. Neither waits on the other, so they need not be
+// resident together; sharing the launch lets them share the SMs.
+__global__ void __launch_bounds__((kCWarps + 1) * 32)
+kda_bwd_chains_kernel(const __grid_constant__ BwdChunkParams p, const __grid_constant__ ChainMaps tm,
+                      int units) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    if (static_cast<int>(blockIdx.x) < units)
+        states_cta(p, &tm.ckpt, blockIdx.x, smem);
+    else
+        chain_cta(p, &tm.dsn, &tm.dout, blockIdx.x - units, smem);
 }
 
 // ---------------------------------------------------------------------------
@@ -1032,37 +1044,26 @@ bool encode_rows16(EncodeFn enc, CUtensorMap *m, const void *base, bool f32, int
 }  // namespace
 
 cudaError_t configure_backward_chunk() {
-    cudaError_t e = cudaFuncSetAttribute(kda_bwd_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(kda_bwd_chains_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kChainSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kda_bwd_states_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStatesSmem);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(kda_bwd_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem);
 }
 
-cudaError_t launch_bwd_states(const BwdChunkParams &p, cudaStream_t stream) {
-    const int64_t ctas = static_cast<int64_t>(p.geo.n_seqs) * p.geo.n_heads * (kDim / kCBV);
-    if (ctas <= 0) return cudaSuccess;
+cudaError_t launch_bwd_chains(const BwdChunkParams &p, cudaStream_t stream) {
+    const int64_t units = static_cast<int64_t>(p.geo.n_seqs) * p.geo.n_heads * (kDim / kCBV);
+    if (units <= 0) return cudaSuccess;
     const EncodeFn enc = reinterpret_cast<EncodeFn>(tensor_map_encoder());
     if (enc == nullptr) return cudaErrorNotSupported;
     ChainMaps tm;
-    if (!encode_states(enc, &tm.out, p.ckpt, p.max_chunks * p.geo.n_heads, 16)) return cudaErrorInvalidValue;
-    kda_bwd_states_kernel<<<static_cast<unsigned>(ctas), (kCWarps + 1) * 32, kStatesSmem, stream>>>(p, tm);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_bwd_chain(const BwdChunkParams &p, cudaStream_t stream) {
-    const int64_t ctas = static_cast<int64_t>(p.geo.n_seqs) * p.geo.n_heads * (kDim / kCBV);
-    if (ctas <= 0) return cudaSuccess;
-    const EncodeFn enc = reinterpret_cast<EncodeFn>(tensor_map_encoder());
-    if (enc == nullptr) return cudaErrorNotSupported;
-    ChainMaps tm;
+    const int64_t items = p.max_chunks * p.geo.n_heads;
     const int64_t tokens =
         p.geo.cu != nullptr ? p.geo.seq_len : static_cast<int64_t>(p.geo.n_seqs) * p.geo.seq_len;
-    if (!encode_states(enc, &tm.out, p.dsn, p.max_chunks * p.geo.n_heads, 16) ||
+    if (!encode_states(enc, &tm.ckpt, p.ckpt, items, 16) || !encode_states(enc, &tm.dsn, p.dsn, items, 16) ||
         !encode_rows16(enc, &tm.dout, p.dout, false, p.geo.n_heads, tokens, 64))
         return cudaErrorInvalidValue;
-    kda_bwd_chain_kernel<<<static_cast<unsigned>(ctas), (kCWarps + 1) * 32, kChainSmem, stream>>>(p, tm);
+    kda_bwd_chains_kernel<<<static_cast<unsigned>(2 * units), (kCWarps + 1) * 32, kChainSmem, stream>>>(
+        p, tm, static_cast<int>(units));
     return cudaGetLastError();
 }
 

@@ -137,8 +137,8 @@ struct BwdChunkParams {
 void *tensor_map_encoder();
 
 cudaError_t configure_backward_chunk();
-cudaError_t launch_bwd_states(const BwdChunkParams &p, cudaStream_t stream);
-cudaError_t launch_bwd_chain(const BwdChunkParams &p, cudaStream_t stream);
+// the forward chain keeping chunk-entry states and the reverse chain, one launch
+cudaError_t launch_bwd_chains(const BwdChunkParams &p, cudaStream_t stream);
 cudaError_t launch_bwd_grad(const BwdChunkParams &p, cudaStream_t stream);
 
 // Per-device, once: raise the dynamic shared-memory limits of the kernels.
