@@ -65,6 +65,8 @@ def parse():
                          "normalisation, g read as gate logits): the same inputs, for timing")
     ap.add_argument("--no-decode", action="store_true",
                     help="leave the decode measurement out of the default line")
+    ap.add_argument("--backward-impl", type=int, default=0, choices=[0, 1],
+                    help="gradient form for --backward: 0 chunked (default), 1 token-serial")
     ap.add_argument("--backward", action="store_true",
                     help="time the gradient call (kda_chunk_prefill_backward) on the workload "
                          "instead of the prefill; prints its own line")
@@ -373,6 +375,8 @@ def bench_backward(K, dev, w, args, hbm):
     do_d, dsf_d = dout.to(dev).view(x["v"].shape), dsf.to(dev)
     stream = torch.cuda.current_stream(dev)
 
+    K.kda_set_backward_impl(args.backward_impl)
+
     def call():
         return K.chunk_prefill_backward(x["q"], x["k"], x["v"], x["g"], x["beta"], do_d,
                                         initial_state=s0, cu_seqlens=cu, scale=d["scale"],
@@ -399,9 +403,13 @@ def bench_backward(K, dev, w, args, hbm):
             "dtype": "fp32 (bf16 q, k, v, dO)", "data": "synthetic",
             "config": dict(config_of(w, d), backward=True),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                         "frac": gbs / hbm, "traffic": None, "kernel": "kda_backward_kernel",
+                         "frac": gbs / hbm, "traffic": None,
+                         "kernel": ("the whole call: intra-chunk, exact form, both chains, gradients"
+                                    if args.backward_impl == 0 else "kda_backward_kernel"),
                          "bytes_per_call": nbytes},
-            "gpu_launches": steps * (1 + int(w.varlen))}
+            "backward_impl": "chunked" if args.backward_impl == 0 else "token-serial",
+            # chunked: intra-chunk, exact form, the chains, the gradient kernel
+            "gpu_launches": steps * ((4 if args.backward_impl == 0 else 1) + int(w.varlen))}
     if not args.no_cpu_baseline:
         import oracle
         oracle.build()
