@@ -351,7 +351,7 @@ __device__ __forceinline__ void intra_exact_chunk(const float *gp, int64_t rowe,
 // is not null.
 template <bool KEEP>
 __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, float *tout,
-                                           float beta_l, int lane) {
+                                           float beta_l, int lane, float wscale = 1.f) {
     const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
     const uint32_t s_kg = smem_u32(sm.kg), s_v = smem_u32(sm.v);
 
@@ -404,6 +404,10 @@ __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, floa
         mma16816(w0, aT, b[0], b[1]);
         mma16816(w1, aT, b[2], b[3]);
         const int c0 = 16 * jp + 2 * tig, c1 = c0 + 8;
+        if (wscale != 1.f) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) { w0[e] *= wscale; w1[e] *= wscale; }
+        }
         *reinterpret_cast<uint32_t *>(sm.kn + swz(gid, c0)) = pack_bf16(-w0[0], -w0[1]);
         *reinterpret_cast<uint32_t *>(sm.kn + swz(gid + 8, c0)) = pack_bf16(-w0[2], -w0[3]);
         *reinterpret_cast<uint32_t *>(sm.kn + swz(gid, c1)) = pack_bf16(-w1[0], -w1[1]);
@@ -461,9 +465,9 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
             graw[r] = (r < L) ? __ldcs(reinterpret_cast<const float4 *>(gp + r * rowe))
                               : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float G[16][4];   // cumulative log decay in base-2 units (G * log2 e)
+    float G[16][4];   // cumulative log decay in base 2 (g log2 e summed), then about G_ref
     float run[4] = {0.f, 0.f, 0.f, 0.f};
-    float gmax = 0.f;
+    float gmax = 0.f;   // largest |G| (base 2)
     const bool gate_logits = PRE && (p.pre & kPreGateLogits) != 0;
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -472,17 +476,59 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
             gg.x = log_sigmoid(gg.x); gg.y = log_sigmoid(gg.y);
             gg.z = log_sigmoid(gg.z); gg.w = log_sigmoid(gg.w);
         }
-        run[0] += gg.x; run[1] += gg.y; run[2] += gg.z; run[3] += gg.w;
-        G[r][0] = run[0] * kLog2e; G[r][1] = run[1] * kLog2e;
-        G[r][2] = run[2] * kLog2e; G[r][3] = run[3] * kLog2e;
+        run[0] = fmaf(gg.x, kLog2e, run[0]); run[1] = fmaf(gg.y, kLog2e, run[1]);
+        run[2] = fmaf(gg.z, kLog2e, run[2]); run[3] = fmaf(gg.w, kLog2e, run[3]);
+        G[r][0] = run[0]; G[r][1] = run[1]; G[r][2] = run[2]; G[r][3] = run[3];
         gmax = fmaxf(gmax, fmaxf(fmaxf(fabsf(run[0]), fabsf(run[1])),
                                  fmaxf(fabsf(run[2]), fabsf(run[3]))));
     }
-    // Chunks with |G| > 80 in some channel go through the code below all the
-    // same (the factored numbers are then wrong); the caller has their record
-    // rewritten by the exact form
-    const bool exact = __any_sync(0xffffffffu, !(gmax <= 80.f));
-    float eL[4];
+    // The gated products factor about a reference G_ref: exp(G_r - G_i) =
+    // exp(G_r - G_ref) exp(G_ref - G_i). G_ref = 0 (the chunk start) while
+    // |G| <= 80 everywhere; otherwise the middle of the chunk's range of G,
+    // which keeps both factors within exp(+-80) as long as that range is at
+    // most 160 and G rises by at most 80 anywhere (the record's exp(G) and
+    // exp(G_last - G) stay representable). In base 2: 80 nats = 115.42,
+    // 160 nats = 230.84 (with room for the rounding of the sums).
+    float gref = 0.f;   // G_ref in base 2
+    float eref = 1.f;   // exp(G_ref): rescales the record's gamma, scale Q e^G and W
+    bool exact = false;
+    const bool wide = __any_sync(0xffffffffu, !(gmax <= 115.42f));
+    // A loop the compiler cannot see through keeps this a branch: the work
+    // inside, predicated into the straight-line code, measured 4 % slower on
+    // chunks that never need it.
+    int wide_trips;
+    asm volatile("mov.b32 %0, %1;" : "=r"(wide_trips) : "r"(static_cast<int>(wide)));
+#pragma unroll 1
+    for (int once = 0; once < wide_trips; ++once) {
+        // range of G from the chunk start (0) on, and its largest rise
+        float hi = 0.f, low = 0.f, rise = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float m = 0.f;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                rise = fmaxf(rise, G[r][e] - m);
+                m = fminf(m, G[r][e]);
+                hi = fmaxf(hi, G[r][e]);
+            }
+            low = fminf(low, m);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+            low = fminf(low, __shfl_xor_sync(0xffffffffu, low, o));
+        }
+        exact = !(hi - low <= 230.84f) || __any_sync(0xffffffffu, !(rise <= 115.42f));
+        if (!exact) {
+            gref = 0.5f * (hi + low);
+            eref = ex2(gref);
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) G[r][e] -= gref;
+        }
+    }
+    float eL[4];       // exp(G_last - G_ref): K e^(G_last - G) = (K e^(G_ref - G)) eL; gamma = eL eref
 #pragma unroll
     for (int e = 0; e < 4; ++e) eL[e] = ex2(G[15][e]);
     cp_async_wait_all();
@@ -536,7 +582,18 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
         st_rec<KEEP>(reinterpret_cast<uint2 *>(rec + kRecKd + off), ukd);
     }
     st_rec<KEEP>(reinterpret_cast<float4 *>(rec + kRecGamma + 16 * lane),
-           make_float4(eL[0], eL[1], eL[2], eL[3]));
+           make_float4(eL[0] * eref, eL[1] * eref, eL[2] * eref, eL[3] * eref));
+    if (!exact && eref != 1.f) {
+        // the record's scale Q e^G = (scale Q e^(G - G_ref)) exp(G_ref), from the tile
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const int off = swz(r, 4 * lane);
+            const uint2 qq = *reinterpret_cast<const uint2 *>(sm.qg + off);
+            const float2 a = unpack_bf16(qq.x), b = unpack_bf16(qq.y);
+            st_rec<KEEP>(reinterpret_cast<uint2 *>(rec + kRecQg + off),
+                         make_uint2(pack_bf16(a.x * eref, a.y * eref), pack_bf16(b.x * eref, b.y * eref)));
+        }
+    }
     __syncwarp();
 
     // ---- A_raw = (K e^G)(K e^-G)^T and P_raw = scale (Q e^G)(K e^-G)^T, 16x16 each
@@ -577,7 +634,7 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
         }
     }
     __syncwarp();
-    intra_tail<KEEP>(sm, rec, tout, beta_l, lane);
+    intra_tail<KEEP>(sm, rec, tout, beta_l, lane, eref);
     return exact;
 }
 

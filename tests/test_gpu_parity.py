@@ -352,27 +352,45 @@ def test_gate_growth_flagged():
     assert rc == K.STATUS_CODE["KDA_ERR_GATE_RANGE"]
 
 
-def out_of_range_chunk_heads(d):
-    """(chunk-heads whose cumulative log decay leaves [-80, 80], all chunk-heads)."""
+def chunk_head_forms(d):
+    """How many chunk-heads take each form of the gated products, by the
+    intra-chunk kernel's rule on the cumulative log decay G of a chunk (nats,
+    from 0 at the chunk start): factored about the chunk start when |G| <= 80
+    everywhere; factored about the middle of G's range when that range
+    (including the start) is at most 160 and G rises by at most 80; the exact
+    per-pair form otherwise. The bounds are the kernel's, in base 2 (80 and
+    160 nats with room for rounding: 115.42 and 230.84). Returns (start,
+    middle, exact)."""
+    log2e = 1.4426950408889634
     cu = d["cu_seqlens"].tolist()
-    n_out = n_all = 0
+    counts = [0, 0, 0]
     for n in range(len(cu) - 1):
         for t0 in range(cu[n], cu[n + 1], 16):
-            G = d["g"][t0:min(t0 + 16, cu[n + 1])].double().cumsum(0)
-            per_head = G.abs().amax(dim=(0, 2))
-            n_out += int((per_head > 80).sum())
-            n_all += per_head.numel()
-    return n_out, n_all
+            G = d["g"][t0:min(t0 + 16, cu[n + 1])].double().cumsum(0)   # [L, H, 128]
+            for h in range(G.shape[1]):
+                g = G[:, h, :]
+                if float(g.abs().max()) * log2e <= 115.42:
+                    counts[0] += 1
+                    continue
+                hi, lo = max(0.0, float(g.max())), min(0.0, float(g.min()))
+                low_so_far = torch.minimum(torch.cummin(g, 0).values, torch.zeros_like(g))
+                before = torch.cat([torch.zeros_like(g[:1]), low_so_far[:-1]], 0)
+                rise = float((g - before).max())
+                counts[1 if ((hi - lo) * log2e <= 230.84 and rise * log2e <= 115.42) else 2] += 1
+    return tuple(counts)
 
 
-@pytest.mark.parametrize("gval", [-5.0, -5.001, -6.0, -10.0, -60.0])
+@pytest.mark.parametrize("gval", [-5.0, -5.001, -6.0, -10.0, -10.01, -60.0])
 def test_strong_uniform_decay(gval):
-    """A chunk whose cumulative log decay passes -80 in some channel takes the
-    exact (unfactored) form of A, P and the gated rows; -5 per token stays
-    just inside the factored form (16 * 5 = 80), -5.001 just outside. The
-    5-token tail chunk of the 37-token sequence stays factored. No flag."""
+    """The three forms of the gated products at their edges: -5 per token
+    keeps |G| <= 80 (16 * 5 = 80) and factors about the chunk start; -5.001
+    to -10 factor about the middle of the chunk's range (at most 160, which
+    -10 reaches); -10.01 and -60 take the exact form. The 5-token tail chunk
+    of the 37-token sequence stays in the first form. No flag."""
     d = KI.make_case([37, 16, 100], H=2, seed=31, init_state=True)
     d["g"] = torch.full_like(d["g"], gval)
+    form = 0 if gval >= -5.0 else 1 if gval >= -10.0 else 2
+    assert chunk_head_forms(d)[form] > 0
     o, f = run_gpu(d)
     assert_parity(o, f, *run_oracle(d), f"g={gval}")
 
@@ -385,17 +403,20 @@ def test_strong_mixed_decay_per_channel():
     gen = torch.Generator().manual_seed(33)
     x = torch.randn(d["g"].shape, generator=gen) * 4.0 - 2.0
     d["g"] = torch.nn.functional.logsigmoid(x)
-    n_exact, n_all = out_of_range_chunk_heads(d)
-    assert 0 < n_exact < n_all, (n_exact, n_all)   # 30 of 84: both forms present
+    start, middle, exact = chunk_head_forms(d)
+    assert start > 0 and middle > 0, (start, middle, exact)   # 54 and 30 of 84
     o, f = run_gpu(d)
     assert_parity(o, f, *run_oracle(d), "mixed")
 
 
 def test_strong_decay_in_some_heads_only():
-    """One head decays strongly (exact form), the others not (factored):
-    the two forms side by side in one launch."""
+    """Two heads decay strongly, -9 per token (factored about the middle of
+    the range) and -12 (exact form), the others not (factored about the
+    chunk start): the three forms side by side in one launch."""
     d = KI.make_case([300], H=4, seed=34, init_state=True)
     d["g"][:, 2, :] = -9.0
+    d["g"][:, 3, :] = -12.0
+    assert all(n > 0 for n in chunk_head_forms(d))
     o, f = run_gpu(d)
     assert_parity(o, f, *run_oracle(d), "head 2 strong")
 
