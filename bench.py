@@ -240,8 +240,11 @@ def traffic_for(kernel, workload):
     rec = json.load(open(p)).get(kernel)
     if not rec:
         return None
-    src = os.path.join(ROOT, "prefill_kda_chunk_gb300", "csrc", rec["source"])
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    srcs = rec["source"] if isinstance(rec["source"], list) else [rec["source"]]
+    h = hashlib.sha256()
+    for f in srcs:   # the kernel's file and the headers holding its body
+        h.update(open(os.path.join(ROOT, "prefill_kda_chunk_gb300", "csrc", f), "rb").read())
+    sha = h.hexdigest()[:16]
     if sha != rec.get("source_sha") or workload not in rec.get("per_launch_bytes", {}):
         return None
     return rec["per_launch_bytes"][workload]
