@@ -231,6 +231,14 @@ def launches_per_call(w, args):
     return n
 
 
+def stock_workload(args):
+    """Whether the run is the named workload with no size, gate, input
+    preprocessing or scan override (the traffic records are per workload as
+    named)."""
+    return (args.heads is None and args.gate_mu is None and not args.preprocess
+            and args.scan_segments is None)
+
+
 def traffic_for(kernel, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on this kernel source (else None)."""
@@ -652,7 +660,8 @@ def main():
                 "unit": "TFLOP/s", "frac": kd["frac"]}
     roof.update({"kernel": dom, "peak_source": f"{peak_src} (MEASURED_PEAKS.json burst)"
                  if peak_src == "measured" else "fallback",
-                 "traffic": traffic_for(dom, w.name)})
+                 # a record holds for the workload it was captured on, as it is
+                 "traffic": traffic_for(dom, w.name) if stock_workload(args) else None})
     # the whole call against the slower of the two bounds of the counted work
     t_hbm = cnt["path_bytes"] / (hbm * 1e9)
     t_tc = (cnt["intra_flops"] + cnt["recur_flops"]) / (tf * 1e12)
