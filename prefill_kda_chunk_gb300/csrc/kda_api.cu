@@ -130,6 +130,9 @@ struct Plan {
 // flag block (the first 256 bytes of a workspace): per-call flag word at 0,
 // the exact-form list counters at kExactCtrOff
 constexpr int64_t kExactCtrOff = 64;
+// ... and, in a gradient call, the out-of-range flag and the gradient kernel's
+// finish count at kWideOff (both reset by that kernel)
+constexpr int64_t kWideOff = 128;
 
 bool misaligned(const void *p, uintptr_t a) {
     return p != nullptr && (reinterpret_cast<uintptr_t>(p) % a) != 0;
@@ -688,7 +691,8 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
         uint8_t *ck = reinterpret_cast<uint8_t *>(tinv + ch * 256);
         uint8_t *dsn = ck + ch * kda::kDim * kda::kDim * 2;
         int *exact_ctr = reinterpret_cast<int *>(wsb + kExactCtrOff);
-        const kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, st.err, geo, exact_list, exact_ctr, tinv};
+        int *wide = reinterpret_cast<int *>(wsb + kWideOff);
+        const kda::IntraParams ip{q, k, v, g, beta, rec, scale, 0, st.err, geo, exact_list, exact_ctr, tinv, wide};
         if (kda::launch_intra_chunk(ip, pl.max_chunks, stream) != cudaSuccess ||
             kda::launch_intra_exact(ip, stream) != cudaSuccess)
             return KDA_ERR_CUDA;
@@ -705,6 +709,7 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
         bp.err = st.err;
         bp.geo = geo;
         bp.max_chunks = pl.max_chunks;
+        bp.wide = wide;
         if (kda::launch_bwd_chains(bp, stream) != cudaSuccess) return KDA_ERR_CUDA;
         return kda::launch_bwd_grad(bp, stream) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
     }

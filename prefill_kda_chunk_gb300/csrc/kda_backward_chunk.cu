@@ -401,12 +401,18 @@ constexpr int kGOffDO = kGOffKn + 4096;     // dO bf16 [16 t][128 v], swizzled; 
 constexpr int kGOffUB = kGOffDO + 4096;     // U bf16 [16 t][128 v], swizzled; in phase 1, with
                                             //   the next 4 KiB, g fp32 [16][128] row-major
 constexpr int kGOffDUB = kGOffUB + 4096;    // dU bf16 [16 t][128 v], swizzled
-constexpr int kGOffMisc = kGOffDUB + 4096;  // beta [16], dbeta from M [16], dbeta parts [4][16],
-                                            //   the copy barrier
-constexpr int kGBar = kGOffMisc + 384;
+constexpr int kGOffQn = kGOffDUB + 4096;    // q as loaded (bf16 [16][128], row-major), then, for
+                                            //   chunks factored about the middle of their
+                                            //   range, scale Q e^(G - G_ref) bf16, swizzled
+constexpr int kGOffMisc = kGOffQn + 4096;   // beta [16], dbeta from M [16], dbeta parts [4][16],
+                                            //   the copy barrier, range partials [4][2]
+constexpr int kGBar = kGOffMisc + 384;       // the item's copies
+constexpr int kGBarQ = kGOffMisc + 392;      // a late copy of q
+constexpr int kGRed = kGOffMisc + 400;      // range partials [4][2]
 constexpr int kGSmem = kGOffMisc + 512;
-constexpr uint32_t kGTxBytes = 2 * 32768 + kRecBytes + 1024 + 8192 + 4096;   // TMA bytes per item
-static_assert(kGOffT % 16 == 0 && kGOffV % 16 == 0 && kGOffDO % 16 == 0, "alignment");
+constexpr uint32_t kGTxBytes = 2 * 32768 + kRecBytes + 1024 + 8192 + 4096;   // TMA bytes per item, q aside
+static_assert(kGOffT % 16 == 0 && kGOffV % 16 == 0 && kGOffDO % 16 == 0 && kGOffQn % 128 == 0 &&
+                  kGOffUB % 128 == 0 && kGOffKn % 128 == 0, "alignment");
 // fp32 [16 rows][128 channels] tiles, rows kFS floats apart: the fragment
 // stores of eight rows then fall on distinct banks in two wavefronts
 constexpr int kFS = 136;
@@ -433,7 +439,7 @@ __device__ __forceinline__ int sw2(int row, int col) {
 
 struct GradMaps {
     CUtensorMap st, dst;   // S^T and dS_next^T: [items][128 v][128 k] bf16, boxes of 128 v x 64 k
-    CUtensorMap g, k;      // g fp32, k bf16: [tokens][H][128], boxes of 16 tokens x 1 head x 128
+    CUtensorMap g, k, q;   // g fp32, k and q bf16: [tokens][H][128], boxes of 16 tokens x 1 head x 128
 };
 
 constexpr float kLog2eG = 1.4426950408889634f;
@@ -470,9 +476,12 @@ __device__ __forceinline__ void frag_a(uint32_t (&a)[4], int gid, int tig, F el)
 // products: its dq and dk terms are added directly and its two dG terms,
 // equal and opposite, are left out. Outside the factored range the A and P
 // terms take exact per-pair exponentials, one channel per thread.
-__global__ void __launch_bounds__(kGThreads, 2)
-kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_constant__ GradMaps tm) {
-    extern __shared__ __align__(1024) uint8_t smem[];
+// The kernel's items. kMid = false compiles out the form factored about the
+// middle of a chunk's range (its chunks then take the exact form): the kernel
+// takes it for calls whose intra-chunk kernel saw no chunk out of the
+// start-referenced range, where carrying that form measured 3 % slower.
+template <bool kMid>
+__device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMaps &tm, uint8_t *smem) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
     const ChunkGeometry &geo = p.geo;
@@ -483,13 +492,18 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
         if (tid == 0) atomicOr(p.err, kErrTimeout);
         return;
     }
-    const uint32_t bar = sb + kGBar;
+    const uint32_t bar = sb + kGBar, bar_q = sb + kGBarQ;
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(bar_q, 1);
         mbar_fence_init();
     }
     __syncthreads();
-    uint32_t parity = 0;
+    uint32_t parity = 0, parity_q = 0;
+    // q is needed only by chunks factored about the middle of their range; it
+    // comes with an item's copies when the CTA's previous item needed it (the
+    // decay of a workload changes little from chunk to chunk), else late
+    bool want_q = false;
     const uint32_t sST = sb + kGOffST, sDT = sb + kGOffDT, sRec = sb + kGOffRec, sDO = sb + kGOffDO,
                    sUB = sb + kGOffUB, sDUB = sb + kGOffDUB, sT = sb + kGOffT, sV = sb + kGOffV,
                    sKg = sb + kGOffKg, sKn = sb + kGOffKn;
@@ -521,19 +535,21 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
         __syncthreads();   // the previous item is done with every tile
         const int64_t qoff = (t0 * H + h) * kDim;
 
-        // ---- phase 1: S^T, dS_next^T, g and k (TMA boxes), the record and T
+        // ---- phase 1: S^T, dS_next^T, g, k and q (TMA boxes), the record and T
         //      (bulk copies), V and dO (16-byte copies, rows past the end
         //      zero); thread = channel for G (kept in registers) and the
         //      K e^G and K e^-G tiles
-        bool exact;
-        float Gc[16];   // this channel's G in base-2 units
+        bool exact, middle;
+        float Gc[16];       // this channel's G in base-2 units, less G_ref
+        float gref = 0.f;   // G_ref in base-2 units
+        float eref = 1.f;   // exp(G_ref)
         {
             const int64_t ri = rec_idx * H + h;
             if (warp == 0) {
                 if (lane == 0) {
                     // the previous item wrote these tiles through the generic proxy
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    mbar_arrive_expect_tx(bar, kGTxBytes);
+                    mbar_arrive_expect_tx(bar, kGTxBytes + (kMid && want_q ? 4096u : 0u));
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -544,6 +560,7 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                     tma_load_3d(sDT + 16384, &tm.dst, 64, 0, z, bar);
                     tma_load_3d(sUB, &tm.g, 0, h, static_cast<int>(t0), bar);
                     tma_load_3d(sKn, &tm.k, 0, h, static_cast<int>(t0), bar);
+                    if (kMid && want_q) tma_load_3d(sb + kGOffQn, &tm.q, 0, h, static_cast<int>(t0), bar);
                     bulk_g2s(sRec, p.rec + ri * static_cast<int64_t>(kRecBytes), kRecBytes, bar);
                 }
                 if (lane < 16)
@@ -569,19 +586,80 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                 break;
             }
             parity ^= 1u;
-            // G = running sum of g (rows past the end: zero), and its largest |G|
+            // G = running sum of g (rows past the end: zero): its largest |G|, its
+            // range from the chunk start on and its largest rise (nats)
             const float *gs = reinterpret_cast<const float *>(smem + kGOffUB) + tid;
             const __nv_bfloat16 *ks = reinterpret_cast<const __nv_bfloat16 *>(smem + kGOffKn) + tid;
-            float run = 0.f, gmax = 0.f, kr[16];
+            float run = 0.f, gmax = 0.f, kr[16], hi = 0.f, low = 0.f, rise = 0.f;
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 const bool ok = r < L;
                 run += ok ? gs[r * kDim] : 0.f;
                 gmax = fmaxf(gmax, fabsf(run));
+                if constexpr (kMid) {
+                    rise = fmaxf(rise, run - low);
+                    low = fminf(low, run);
+                    hi = fmaxf(hi, run);
+                }
                 kr[r] = ok ? __bfloat162float(ks[r * kDim]) : 0.f;
                 Gc[r] = run * kLog2eG;
             }
-            __syncthreads();   // k as loaded is read; its space takes K e^-G
+            // The chunk's form, as in the forward: the gated products factor about
+            // G_ref = 0 while |G| <= 80, else about the middle of G's range while
+            // that range is at most 160 and G rises by at most 80; beyond, exact
+            exact = false;
+            middle = false;
+            if constexpr (!kMid) {
+                exact = __syncthreads_or(!(gmax <= 80.f)) != 0;   // (also: k as loaded is read)
+            } else {
+                if (__syncthreads_or(!(gmax <= 80.f))) {   // (also: k as loaded is read)
+                    float *red = reinterpret_cast<float *>(smem + kGRed);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+                        low = fminf(low, __shfl_xor_sync(0xffffffffu, low, o));
+                    }
+                    if (lane == 0) { red[2 * warp] = hi; red[2 * warp + 1] = low; }
+                    const bool big_rise = __syncthreads_or(!(rise <= 80.f)) != 0;
+                    hi = fmaxf(fmaxf(red[0], red[2]), fmaxf(red[4], red[6]));
+                    low = fminf(fminf(red[1], red[3]), fminf(red[5], red[7]));
+                    exact = big_rise || !(hi - low <= 160.f);
+                    middle = !exact;
+                }
+                if (middle && !want_q) {
+                    // q was not among the item's copies: fetch it now
+                    if (tid == 0) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        mbar_arrive_expect_tx(bar_q, 4096u);
+                        tma_load_3d(sb + kGOffQn, &tm.q, 0, h, static_cast<int>(t0), bar_q);
+                    }
+                    const bool got_q = mbar_wait(bar_q, parity_q);
+                    parity_q ^= 1u;
+                    if (__syncthreads_or(!got_q)) {
+                        if (tid == 0) atomicOr(p.err, kErrTimeout);
+                        if (!got_q) mbar_wait(bar_q, parity_q ^ 1u);
+                        break;
+                    }
+                }
+                want_q = middle;
+                if (middle) {
+                    // G now holds G - G_ref; this channel's column of scale Q e^(G - G_ref)
+                    gref = 0.5f * (hi + low) * kLog2eG;
+                    eref = ex2g(gref);
+                    const __nv_bfloat16 *qs = reinterpret_cast<const __nv_bfloat16 *>(smem + kGOffQn) + tid;
+                    float qr[16];
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        Gc[r] -= gref;
+                        qr[r] = r < L ? __bfloat162float(qs[r * kDim]) : 0.f;
+                    }
+                    __syncthreads();   // q as loaded is read; its space takes the tile
+#pragma unroll
+                    for (int r = 0; r < 16; ++r)
+                        *reinterpret_cast<__nv_bfloat16 *>(smem + kGOffQn + swz(r, tid)) =
+                            __float2bfloat16_rn(scale * qr[r] * ex2g(Gc[r]));
+                }
+            }
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 *reinterpret_cast<__nv_bfloat16 *>(smem + kGOffKg + swz(r, tid)) =
@@ -589,8 +667,10 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                 *reinterpret_cast<__nv_bfloat16 *>(smem + kGOffKn + swz(r, tid)) =
                     __float2bfloat16_rn(kr[r] * ex2g(-Gc[r]));
             }
-            exact = __syncthreads_or(!(gmax <= 80.f)) != 0;
+            __syncthreads();
         }
+        // scale Q e^(G - G_ref): the record's scale Q e^G when G_ref = 0
+        const uint32_t sQs = kMid && middle ? sb + kGOffQn : sRec + kRecQg;
 
         // ---- phase 2: U^T = Ut^T + S^T (-W)^T and dU^T = dS_next^T Kd^T + dO^T P,
         //      value rows 32 warp + 16 mt, all 16 tokens
@@ -746,8 +826,9 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
         __syncthreads();
 
         // ---- phase 4a: dM = dU V^T + dW Kg^T (16 x 16), warp w over channels 32 w .. + 31
+        //      (the tile holds K e^(G - G_ref): its product is scaled by exp(G_ref))
         {
-            float m2[2][4] = {};
+            float m2[2][4] = {}, m3[2][4] = {};
 #pragma unroll
             for (int q2 = 0; q2 < 2; ++q2) {
                 const int kk = 2 * warp + q2;
@@ -760,8 +841,19 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                 ldsm_x4(sKg + swz(rb, cb), bg[0], bg[1], bg[2], bg[3]);
                 mma_r(m2[0], aD, bv[0], bv[1]);
                 mma_r(m2[1], aD, bv[2], bv[3]);
-                mma_r(m2[0], aW, bg[0], bg[1]);
-                mma_r(m2[1], aW, bg[2], bg[3]);
+                if constexpr (kMid) {
+                    mma_r(m3[0], aW, bg[0], bg[1]);
+                    mma_r(m3[1], aW, bg[2], bg[3]);
+                } else {
+                    mma_r(m2[0], aW, bg[0], bg[1]);
+                    mma_r(m2[1], aW, bg[2], bg[3]);
+                }
+            }
+            if constexpr (kMid) {
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) m2[nt][e] = fmaf(eref, m3[nt][e], m2[nt][e]);
             }
             float *part = sdMp + warp * 256;
 #pragma unroll
@@ -845,7 +937,7 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                     mma_r(zc[2 * jp + 1], aY, b[2], b[3]);
                     mma_r(xc[2 * jp], aA, b[0], b[1]);
                     mma_r(xc[2 * jp + 1], aA, b[2], b[3]);
-                    ldsm_x4_t(sRec + kRecQg + swz(rk, ck), b[0], b[1], b[2], b[3]);
+                    ldsm_x4_t(sQs + swz(rk, ck), b[0], b[1], b[2], b[3]);
                     mma_r(yc[2 * jp], aYt, b[0], b[1]);
                     mma_r(yc[2 * jp + 1], aYt, b[2], b[3]);
                     ldsm_x4_t(sKg + swz(rk, ck), b[0], b[1], b[2], b[3]);
@@ -853,8 +945,11 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                     mma_r(yc[2 * jp + 1], aAt, b[2], b[3]);
                 }
             }
-            // epilogue: Z = dY Kn + scale dQg, T1 = beta (dA Kn + T^T dW), Yc,
-            // dv = beta T^T dU; dbeta parts sum_c Kg (dA Kn)
+            // epilogue: Z = dY Kn + exp(G_ref) scale dQg, T1 = beta (dA Kn +
+            // exp(G_ref) T^T dW), Yc, dv = beta T^T dU; dbeta parts sum_c Kg (dA Kn)
+            // (Kn, Kg about G_ref: the terms that carry e^G itself are brought to
+            // e^(G - G_ref) here; exp(G_ref) = 1 for chunks factored about the start)
+            const float sref = scale * eref;
             float pb0 = 0.f, pb1 = 0.f;
             const float b0 = sBeta[gid], b1 = sBeta[gid + 8];
             float *dvp = p.dv + qoff;
@@ -868,9 +963,9 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                     const float x0 = xc[j][2 * hf], x1 = xc[j][2 * hf + 1];
                     float2 *zp = reinterpret_cast<float2 *>(gZ + r * kFS + col);
                     const float2 q2 = *zp;
-                    *zp = make_float2(fmaf(scale, q2.x, zc[j][2 * hf]), fmaf(scale, q2.y, zc[j][2 * hf + 1]));
+                    *zp = make_float2(fmaf(sref, q2.x, zc[j][2 * hf]), fmaf(sref, q2.y, zc[j][2 * hf + 1]));
                     *reinterpret_cast<float2 *>(gT1 + r * kFS + col) =
-                        make_float2(br * (x0 + dc[j][2 * hf]), br * (x1 + dc[j][2 * hf + 1]));
+                        make_float2(br * fmaf(eref, dc[j][2 * hf], x0), br * fmaf(eref, dc[j][2 * hf + 1], x1));
                     *reinterpret_cast<float2 *>(gYc + r * kFS + col) = make_float2(yc[j][2 * hf], yc[j][2 * hf + 1]);
                     const float2 kg = unpack_bf16(*reinterpret_cast<const uint32_t *>(smem + kGOffKg + swz(r, col)));
                     const float pb = fmaf(kg.x, x0, kg.y * x1);
@@ -898,19 +993,20 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
         {
             const int ch = tid;
             const int64_t base = qoff + ch;
-            float dG[16];
+            float dG[16];    // dG less the K e^(G_last - G) terms
+            float kdv[16];   // those terms: k e^(G_last - G) dKd per row
             const float G2L = Gc[15];
-            float dGL = (sdG[ch] + sdG[kDim + ch] + sdG[2 * kDim + ch] + sdG[3 * kDim + ch]) * ex2g(G2L);
+            float dGL = (sdG[ch] + sdG[kDim + ch] + sdG[2 * kDim + ch] + sdG[3 * kDim + ch]) * ex2g(G2L + gref);
             if (!exact) {
-                // q and k enter through the record's scale Q e^G and K e^(G_last - G)
-                // and the K e^G, K e^-G tiles
+                // q and k enter through the tiles scale Q e^(G - G_ref), K e^(G - G_ref),
+                // K e^(G_ref - G) and the record's K e^(G_last - G); G here is less G_ref
                 const float inv_scale = scale != 0.f ? 1.f / scale : 0.f;
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
                     const float eG = ex2g(Gc[r]), eN = ex2g(-Gc[r]), eD = ex2g(G2L - Gc[r]);
                     const int o16 = swz(r, ch);
                     const float qgs = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                          smem + kGOffRec + kRecQg + o16)) * inv_scale;
+                                          smem + (sQs - sb) + o16)) * inv_scale;
                     const float kd = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
                         smem + kGOffRec + kRecKd + o16));
                     const float kgv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + kGOffKg + o16));
@@ -918,9 +1014,9 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                     const float z = gZ[r * kFS + ch], t1 = gT1[r * kFS + ch];
                     const float yc = gYc[r * kFS + ch], dkd = gK[r * kFS + ch];
                     // q dq = (q e^G) Z, k a = (k e^G) T1, k b = (k e^-G) Yc, k d = Kd dKd
-                    const float kdd = kd * dkd;
-                    dG[r] = fmaf(qgs, z, fmaf(kgv, t1, -fmaf(knv, yc, kdd)));
-                    dGL += kdd;
+                    // (each e^G here is e^(G - G_ref), e^-G is e^(G_ref - G))
+                    kdv[r] = kd * dkd;
+                    dG[r] = fmaf(qgs, z, fmaf(kgv, t1, -knv * yc));
                     if (r < L) {
                         // the diagonal pair: its two dG terms cancel exactly
                         const float yd = scale * gP[r * 17];
@@ -952,10 +1048,11 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                         const float wP = scale * gP[r * 16 + i] * E;
                         dq[r] = fmaf(wP, kk_[i], dq[r]);
                         dk[i] = fmaf(wP, qq[r], dk[i]);
-                        const float tP = wP * qq[r] * kk_[i];
-                        dG[r] += tP;
-                        dG[i] -= tP;
                         if (i < r) {
+                            // (the diagonal pair's two dG terms cancel: left out)
+                            const float tP = wP * qq[r] * kk_[i];
+                            dG[r] += tP;
+                            dG[i] -= tP;
                             const float dAr = sdA[r * 16 + i];
                             const float kkE = kk_[r] * kk_[i] * E;
                             pb[r] = fmaf(dAr, kkE, pb[r]);
@@ -974,8 +1071,8 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                     const float q1 = eG * gZ[r * kFS + ch];
                     const float a = eG * gT1[r * kFS + ch];
                     const float d = eD * gK[r * kFS + ch];
-                    dG[r] = fmaf(qq[r], q1, fmaf(kk_[r], a - d, dG[r]));
-                    dGL = fmaf(kk_[r], d, dGL);
+                    dG[r] = fmaf(qq[r], q1, fmaf(kk_[r], a, dG[r]));
+                    kdv[r] = kk_[r] * d;
                     if (r < L) {
                         const int64_t o = base + r * rowe;
                         p.dq[o] = dq[r] + q1;
@@ -991,17 +1088,52 @@ kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_const
                 }
             }
             dG[15] += dGL;
-            // dg = reverse cumulative sum of dG over the rows
+            // dg = reverse cumulative sum of the full dG over the rows. Each row's
+            // K e^(G_last - G) term enters its own row with - and the last row with
+            // + (through G_last), so it cancels in dg_u for u at or before its row;
+            // summed as dg_u = sum_{r >= u} dG_r + sum_{r < u} kdv_r it cancels
+            // exactly (under strong decay dg is far below those terms)
+            float kpre = 0.f;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const float x = kdv[r];
+                kdv[r] = kpre;
+                kpre += x;
+            }
             float acc = 0.f;
 #pragma unroll
             for (int r = 15; r >= 0; --r) {
                 acc += dG[r];
-                if (r < L) p.dg[base + r * rowe] = acc;
+                if (r < L) p.dg[base + r * rowe] = acc + kdv[r];
             }
         }
         __syncthreads();
         if (tid < 16 && tid < L)
             p.dbeta[(t0 + tid) * H + h] = sBM[tid] + sPB[tid] + sPB[16 + tid] + sPB[32 + tid] + sPB[48 + tid];
+    }
+}
+
+__global__ void __launch_bounds__(kGThreads, 2)
+kda_bwd_grad_kernel(const __grid_constant__ BwdChunkParams p, const __grid_constant__ GradMaps tm) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    // p.wide[0]: raised by this call's intra-chunk kernel for a chunk out of the
+    // start-referenced range (a stale raise costs time only: the other form
+    // handles every chunk too)
+    if (p.wide != nullptr && __ldcg(p.wide) != 0)
+        grad_items<true>(p, tm, smem);
+    else
+        grad_items<false>(p, tm, smem);
+    if (p.wide != nullptr) {
+        // the last CTA to finish lowers the flag and its own counter for the next call
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(p.wide + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+                p.wide[0] = 0;
+                p.wide[1] = 0;
+                __threadfence();
+            }
+        }
     }
 }
 
@@ -1077,7 +1209,8 @@ cudaError_t launch_bwd_grad(const BwdChunkParams &p, cudaStream_t stream) {
     GradMaps tm;
     if (!encode_states(enc, &tm.st, p.ckpt, items, 128) || !encode_states(enc, &tm.dst, p.dsn, items, 128) ||
         !encode_rows16(enc, &tm.g, p.ip.g, true, p.geo.n_heads, tokens) ||
-        !encode_rows16(enc, &tm.k, p.ip.k, false, p.geo.n_heads, tokens))
+        !encode_rows16(enc, &tm.k, p.ip.k, false, p.geo.n_heads, tokens) ||
+        !encode_rows16(enc, &tm.q, p.ip.q, false, p.geo.n_heads, tokens))
         return cudaErrorInvalidValue;
     int dev = 0, sms = 0, nb = 0;
     cudaGetDevice(&dev);

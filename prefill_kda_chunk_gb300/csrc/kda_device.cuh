@@ -43,6 +43,16 @@ enum : int { kErrBadCu = 1, kErrTimeout = 2, kErrGate = 4 };
 // Bounded waits give up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
+// 1 if c else 0, through an instruction the compiler does not look into: a
+// loop of that many trips stays a branch. Work written as an if can be
+// predicated into the straight-line code around it, and then costs every
+// thread that does not need it.
+__device__ __forceinline__ int opaque_trips(bool c) {
+    int t;
+    asm volatile("mov.b32 %0, %1;" : "=r"(t) : "r"(static_cast<int>(c)));
+    return t;
+}
+
 __device__ __forceinline__ int swz(int row, int col) {
     return row * 256 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1);
 }

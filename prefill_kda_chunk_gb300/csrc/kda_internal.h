@@ -49,6 +49,9 @@ struct IntraParams {
     // When not null, (I + A)^{-1} of every chunk-head, fp32 [16][16] row-major
     // at item index (record index * H + head) * 256 (the gradients read it)
     float *tinv = nullptr;
+    // When not null, set to 1 by any chunk-head whose |G| passes 80 (the
+    // gradient kernel compiles the form for such chunks in only when it is set)
+    int *wide_flag = nullptr;
 };
 
 struct RecurParams {
@@ -132,6 +135,9 @@ struct BwdChunkParams {
     int *err;
     ChunkGeometry geo;
     int64_t max_chunks;
+    // [0]: the intra-chunk kernel's wide_flag; [1]: the gradient kernel's finish
+    // count (both 0 between calls; the gradient kernel's last CTA resets them)
+    int *wide = nullptr;
 };
 // cuTensorMapEncodeTiled from the driver (cast to its signature), or null.
 void *tensor_map_encoder();

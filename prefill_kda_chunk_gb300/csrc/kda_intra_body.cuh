@@ -493,13 +493,11 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
     float eref = 1.f;   // exp(G_ref): rescales the record's gamma, scale Q e^G and W
     bool exact = false;
     const bool wide = __any_sync(0xffffffffu, !(gmax <= 115.42f));
-    // A loop the compiler cannot see through keeps this a branch: the work
-    // inside, predicated into the straight-line code, measured 4 % slower on
-    // chunks that never need it.
-    int wide_trips;
-    asm volatile("mov.b32 %0, %1;" : "=r"(wide_trips) : "r"(static_cast<int>(wide)));
+    // (a loop of opaque trip count keeps this a branch: written as an if, it
+    //  measured 4 % slower on chunks that never need it)
 #pragma unroll 1
-    for (int once = 0; once < wide_trips; ++once) {
+    for (int once = 0, n = opaque_trips(wide); once < n; ++once) {
+        if (p.wide_flag != nullptr && lane == 0) *p.wide_flag = 1;
         // range of G from the chunk start (0) on, and its largest rise
         float hi = 0.f, low = 0.f, rise = 0.f;
 #pragma unroll

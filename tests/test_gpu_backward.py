@@ -109,10 +109,23 @@ def test_backward_without_final_state_gradient():
     check_all(d, gpu_grads(d), "dsf=None")
 
 
-def test_backward_strong_decay():
+@pytest.mark.parametrize("gval", [-6.0, -9.0, -12.0, -40.0])
+def test_backward_strong_decay(gval):
+    """Strong decay in each form of the gated products: -6 and -9 per token
+    (a chunk's range of G up to 144) factor about the middle of the range;
+    -12 and -40 (ranges of 192 and 640) take the exact per-pair form."""
     d = make([64, 9], H=2, seed=24)
-    d["g"] = torch.full_like(d["g"], -9.0)
-    check_all(d, gpu_grads(d), "g=-9")
+    d["g"] = torch.full_like(d["g"], gval)
+    check_all(d, gpu_grads(d), f"g={gval}")
+
+
+def test_backward_strong_decay_mixed_heads():
+    """Heads in all three forms in one call: ordinary gates, -9 per token
+    (middle of the range) and -12 (exact)."""
+    d = make([100, 37], H=3, seed=25)
+    d["g"][:, 1, :] = -9.0
+    d["g"][:, 2, :] = -12.0
+    check_all(d, gpu_grads(d), "mixed heads")
 
 
 def test_backward_zero_tokens_passes_state_gradient():
