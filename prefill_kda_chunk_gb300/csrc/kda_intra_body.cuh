@@ -446,7 +446,7 @@ __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, floa
 // Returns whether the chunk leaves the factored range (|G| > 80 in some
 // channel): its record then holds wrong numbers until intra_exact_item
 // rewrites it.
-template <bool PRE, bool KEEP>
+template <bool PRE, bool KEEP, bool FLAG = false>
 __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &sm, int64_t t0,
                                            int L, int h, uint8_t *rec, float *tout) {
     const int lane = threadIdx.x & 31;
@@ -497,7 +497,9 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
     //  measured 4 % slower on chunks that never need it)
 #pragma unroll 1
     for (int once = 0, n = opaque_trips(wide); once < n; ++once) {
-        if (p.wide_flag != nullptr && lane == 0) *p.wide_flag = 1;
+        if constexpr (FLAG) {
+            if (lane == 0) *p.wide_flag = 1;   // (compiled in only where a caller wants it)
+        }
         // range of G from the chunk start (0) on, and its largest rise
         float hi = 0.f, low = 0.f, rise = 0.f;
 #pragma unroll
