@@ -141,13 +141,15 @@ def test_preprocessing_with_each_recurrent_kernel(impl):
 
 
 @pytest.mark.parametrize("impl", [1, 3, 4], ids=["c16", "c64_split", "c64_fused"])
-def test_preprocessing_strong_decay(impl):
-    """Gate logits far below 0 (log decays down to about -25 per token) make
-    the intra-chunk kernel take its exact form, which does the q/k
-    normalisation and the logsigmoid itself."""
+@pytest.mark.parametrize("spread", [1.0, 4.0], ids=["middle", "exact"])
+def test_preprocessing_strong_decay(impl, spread):
+    """Gate logits far below 0. At about -6 per token the 16-token chunks'
+    decay ranges (about 96) are factored about their middle; at about -24
+    (spread 4) the intra-chunk kernel takes its exact form. Both do the q/k
+    normalisation and the logsigmoid themselves."""
     d = KI.make_raw_case([150, 33], H=2, seed=70 + impl, init_state=True, mu=-6.0)
     gen = torch.Generator().manual_seed(71)
-    d["g"] = d["g"] * 4.0 + 0.5 * torch.randn(d["g"].shape, generator=gen)
+    d["g"] = d["g"] * spread + 0.5 * torch.randn(d["g"].shape, generator=gen)
     x = {n: d[n].cuda().contiguous() for n in ("q", "k", "v", "g", "beta")}
     assert K.kda_set_recurrent_impl(impl) == 0
     try:

@@ -93,10 +93,12 @@ def test_noalloc_matches_oracle_two_calls():
 
 
 def test_noalloc_strong_decay_matches_oracle():
-    """The exact form of strongly decaying chunks (its list lives in the
-    fixed scratch too): a packed batch with one head at -9 per token."""
+    """Strong decay in both of its forms: a packed batch with one head at -9
+    per token (factored about the middle of each chunk's decay range) and one
+    at -12 (the exact form, whose list lives in the fixed scratch too)."""
     d = KI.make_case([90, 40, 130], H=3, seed=33, init_state=True)
     d["g"][:, 0, :] = -9.0
+    d["g"][:, 1, :] = -12.0
     o_na, f_na = _run(K.kda_chunk_prefill_noalloc, d, True)
     o_ref, f_ref = _oracle(d)
     _close(o_na, o_ref)
