@@ -420,7 +420,7 @@ constexpr int kFT = 16 * kFS * 4;
 constexpr int kGZ = kGOffST, kGK = kGZ + kFT, kGT1 = kGK + kFT;
 // small tiles in the dS_next^T region once it is read
 constexpr int kSdP = kGOffDT;               // dP (w.r.t. the record's scale P) [16][16]
-constexpr int kSdG = kSdP + 1024;           // dgamma parts [4 warps][128]
+constexpr int kSdG = kSdP + 1024;           // dgamma [128] (2 KB kept)
 constexpr int kSdMp = kSdG + 2048;          // dM parts [4 warps][16][16]
 constexpr int kSdM = kSdMp + 4096;          // dM [16][16]
 constexpr int kSdT = kSdM + 1024;           // dT = dM diag(beta)
@@ -733,8 +733,10 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
 
         // ---- phase 3: contractions over the 128 values. Warp w: keys 32 w .. + 31.
         //      dW = -dU S^T, dQg = dO S^T, dKd = U dS_next^T; warp 0 also dP = dO U^T;
-        //      dgamma = rowsum(dS_next o S): thread = 8 keys x 16 of the 128 values
-        float cW[4][4], cQ[4][4], cK[4][4], cP[2][4];
+        //      dgamma = rowsum(dS_next o S) as the diagonal of the 16 x 16 blocks
+        //      S dS_next^T of the warp's keys (the S^T fragments loaded as B serve
+        //      as A: both hold two consecutive values of one key)
+        float cW[4][4], cQ[4][4], cK[4][4], cP[2][4], cG[2][2][4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -742,7 +744,7 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
 #pragma unroll
         for (int j = 0; j < 2; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) cP[j][e] = 0.f;
+            for (int e = 0; e < 4; ++e) cP[j][e] = cG[j][0][e] = cG[j][1][e] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             uint32_t aU_[4], aO_[4], aDU[4];
@@ -762,6 +764,9 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                 mma_r(cQ[2 * jp + 1], aO_, bs[2], bs[3]);
                 mma_r(cK[2 * jp], aU_, bd[0], bd[1]);
                 mma_r(cK[2 * jp + 1], aU_, bd[2], bd[3]);
+                const uint32_t aS[4] = {bs[0], bs[2], bs[1], bs[3]};   // S: 16 keys x 16 values
+                mma_r(cG[jp][0], aS, bd[0], bd[1]);
+                mma_r(cG[jp][1], aS, bd[2], bd[3]);
             }
             if (warp == 0) {
                 uint32_t bu[4];
@@ -771,31 +776,9 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                 mma_r(cP[1], aO_, bu[2], bu[3]);
             }
         }
-        float dg8[8];
-        {
-            // rows v = vg + 8 j (so v & 7 = vg), 16-byte chunk kc of keys 8 kc .. + 7
-            const int kc = tid & 15, vg = tid >> 4;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dg8[e] = 0.f;
-#pragma unroll 4
-            for (int j = 0; j < 16; ++j) {
-                const uint32_t o = sw2(vg + 8 * j, 8 * kc);
-                const uint4 s4 = *reinterpret_cast<const uint4 *>(smem + kGOffST + o);
-                const uint4 d4 = *reinterpret_cast<const uint4 *>(smem + kGOffDT + o);
-                const uint32_t sw[4] = {s4.x, s4.y, s4.z, s4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    dg8[2 * w] = fmaf(__uint_as_float(sw[w] << 16), __uint_as_float(dw[w] << 16), dg8[2 * w]);
-                    dg8[2 * w + 1] = fmaf(__uint_as_float(sw[w] & 0xffff0000u),
-                                          __uint_as_float(dw[w] & 0xffff0000u), dg8[2 * w + 1]);
-                }
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) dg8[e] += __shfl_xor_sync(0xffffffffu, dg8[e], 16);
-        }
         __syncthreads();
-        // results: dQg, dKd fp32 over S^T; dW bf16 over dO; dP and the dgamma
-        // parts over dS_next^T
+        // results: dQg, dKd fp32 over S^T; dW bf16 over dO; dP and dgamma over
+        // dS_next^T
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int key = 32 * warp + 8 * j + 2 * tig;
@@ -818,10 +801,15 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                     gP[r * 16 + i + 1] = i + 1 <= r ? cP[nt][2 * hf + 1] : 0.f;
                 }
         }
-        if (lane < 16) {
-            float4 *dst = reinterpret_cast<float4 *>(sdG + warp * kDim + 8 * lane);
-            dst[0] = make_float4(dg8[0], dg8[1], dg8[2], dg8[3]);
-            dst[1] = make_float4(dg8[4], dg8[5], dg8[6], dg8[7]);
+        if (tig == (gid >> 1)) {
+            // the diagonal: row gid of the first n-tile, row gid + 8 of the second
+            const bool odd = gid & 1;
+#pragma unroll
+            for (int jp = 0; jp < 2; ++jp) {
+                const int kb = 32 * warp + 16 * jp;
+                sdG[kb + gid] = odd ? cG[jp][0][1] : cG[jp][0][0];
+                sdG[kb + 8 + gid] = odd ? cG[jp][1][3] : cG[jp][1][2];
+            }
         }
         __syncthreads();
 
@@ -996,7 +984,7 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
             float dG[16];    // dG less the K e^(G_last - G) terms
             float kdv[16];   // those terms: k e^(G_last - G) dKd per row
             const float G2L = Gc[15];
-            float dGL = (sdG[ch] + sdG[kDim + ch] + sdG[2 * kDim + ch] + sdG[3 * kDim + ch]) * ex2g(G2L + gref);
+            float dGL = sdG[ch] * ex2g(G2L + gref);
             if (!exact) {
                 // q and k enter through the tiles scale Q e^(G - G_ref), K e^(G - G_ref),
                 // K e^(G_ref - G) and the record's K e^(G_last - G); G here is less G_ref
