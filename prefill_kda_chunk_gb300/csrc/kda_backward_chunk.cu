@@ -444,6 +444,16 @@ struct GradMaps {
 
 constexpr float kLog2eG = 1.4426950408889634f;
 
+// D += A * B, m16n8k8, tf32 operands, fp32 accumulate.
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ float ex2g(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -861,30 +871,56 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
             sdT[e] = m * sBeta[e & 15];
         }
         __syncthreads();
-        // ---- phase 4c: Y = T^T dT; dbeta_j (from M) = sum_r dM[r][j] T[r][j]
+        // ---- phase 4c (warp 0): Y = T^T dT and dA = -(Y T^T) on the strict lower
+        //      triangle, as tf32 MMAs (m16n8k8); dbeta_j (from M) = sum_r dM[r][j] T[r][j]
+        if (warp == 0) {
+            auto tf = [](float x) {
+                uint32_t r;
+                asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+                return r;
+            };
+            float y[2][4] = {};
 #pragma unroll
-        for (int e = tid; e < 256; e += kGThreads) {
-            const int r = e >> 4, b = e & 15;
-            float y = 0.f;
+            for (int ks = 0; ks < 2; ++ks) {
+                const int a = 8 * ks + tig;
+                const uint32_t a0 = tf(T[a * kTStride + gid]), a1 = tf(T[a * kTStride + gid + 8]);
+                const uint32_t a2 = tf(T[(a + 4) * kTStride + gid]), a3 = tf(T[(a + 4) * kTStride + gid + 8]);
 #pragma unroll
-            for (int a = 0; a < 16; ++a) y = fmaf(T[a * kTStride + r], sdT[a * 16 + b], y);
-            sY[e] = y;
-        }
-        if (tid < 16) {
-            float sbj = 0.f;
+                for (int nt = 0; nt < 2; ++nt)
+                    mma_tf32(y[nt], a0, a1, a2, a3, tf(sdT[a * 16 + 8 * nt + gid]),
+                             tf(sdT[(a + 4) * 16 + 8 * nt + gid]));
+            }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sbj = fmaf(sdM[r * 16 + tid], T[r * kTStride + tid], sbj);
-            sBM[tid] = sbj;
-        }
-        __syncthreads();
-        // ---- phase 4d: dA = -(Y T^T) on the strict lower triangle
+            for (int nt = 0; nt < 2; ++nt) {
+                *reinterpret_cast<float2 *>(sY + gid * 16 + 8 * nt + 2 * tig) = make_float2(y[nt][0], y[nt][1]);
+                *reinterpret_cast<float2 *>(sY + (gid + 8) * 16 + 8 * nt + 2 * tig) = make_float2(y[nt][2], y[nt][3]);
+            }
+            __syncwarp();
+            float da[2][4] = {};
 #pragma unroll
-        for (int e = tid; e < 256; e += kGThreads) {
-            const int r = e >> 4, i = e & 15;
-            float a = 0.f;
+            for (int ks = 0; ks < 2; ++ks) {
+                const int b = 8 * ks + tig;
+                const uint32_t a0 = tf(sY[gid * 16 + b]), a1 = tf(sY[(gid + 8) * 16 + b]);
+                const uint32_t a2 = tf(sY[gid * 16 + b + 4]), a3 = tf(sY[(gid + 8) * 16 + b + 4]);
 #pragma unroll
-            for (int b = 0; b < 16; ++b) a = fmaf(sY[r * 16 + b], T[i * kTStride + b], a);
-            sdA[e] = i < r ? -a : 0.f;
+                for (int nt = 0; nt < 2; ++nt)
+                    mma_tf32(da[nt], a0, a1, a2, a3, tf(T[(8 * nt + gid) * kTStride + b]),
+                             tf(T[(8 * nt + gid) * kTStride + b + 4]));
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int r = gid + 8 * hf, i = 8 * nt + 2 * tig;
+                    *reinterpret_cast<float2 *>(sdA + r * 16 + i) =
+                        make_float2(i < r ? -da[nt][2 * hf] : 0.f, i + 1 < r ? -da[nt][2 * hf + 1] : 0.f);
+                }
+            if (lane < 16) {
+                float sbj = 0.f;
+#pragma unroll
+                for (int r = 0; r < 16; ++r) sbj = fmaf(sdM[r * 16 + lane], T[r * kTStride + lane], sbj);
+                sBM[lane] = sbj;
+            }
         }
         __syncthreads();
 
@@ -989,9 +1025,11 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                 // q and k enter through the tiles scale Q e^(G - G_ref), K e^(G - G_ref),
                 // K e^(G_ref - G) and the record's K e^(G_last - G); G here is less G_ref
                 const float inv_scale = scale != 0.f ? 1.f / scale : 0.f;
+                // e^(G_last - G) = e^(G_last - G_ref) e^(G_ref - G): both within e^+-80 here
+                const float eLr = ex2g(G2L);
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
-                    const float eG = ex2g(Gc[r]), eN = ex2g(-Gc[r]), eD = ex2g(G2L - Gc[r]);
+                    const float eG = ex2g(Gc[r]), eN = ex2g(-Gc[r]), eD = eLr * eN;
                     const int o16 = swz(r, ch);
                     const float qgs = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
                                           smem + (sQs - sb) + o16)) * inv_scale;
