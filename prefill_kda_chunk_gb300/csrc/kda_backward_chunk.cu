@@ -427,7 +427,9 @@ constexpr int kSdT = kSdM + 1024;           // dT = dM diag(beta)
 constexpr int kSY = kSdT + 1024;            // Y = T^T dT
 constexpr int kSdA = kSY + 1024;            // dA, strict lower
 constexpr int kGYc = kSdA + 1024;           // Yc fp32 [16][kFS]
-static_assert(kGT1 + kFT <= kGOffDT && kGYc + kFT <= kGOffRec, "tiles overlap");
+constexpr int kGGt = kGYc + kFT;            // G - G_ref fp32 [16][128] (for phase 4f's layout)
+constexpr int kGTot = kGGt + 8192;          // phase 4f's row-block totals, fp32 [2][4][128]
+static_assert(kGT1 + kFT <= kGOffDT && kGTot + 4096 <= kGOffRec, "tiles overlap");
 constexpr int kGThreads = 128;
 
 // Byte offset of (row, col) in a [128][128] bf16 tile stored as two
@@ -926,6 +928,10 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
 
         // ---- phase 4e: the products over the chunk's tokens, warp w: channels 32 w .. + 31
         {
+            // (this channel's G for phase 4f, whose threads hold other channels)
+            float *sGt = reinterpret_cast<float *>(smem + kGGt);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sGt[r * kDim + tid] = Gc[r];
             uint32_t aTt[4];
             frag_a(aTt, gid, tig, [&](int m, int k) { return T[k * kTStride + m]; });
             float zc[4][4], xc[4][4], dc[4][4], uc[4][4], yc[4][4];
@@ -1013,45 +1019,114 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
         }
         __syncthreads();
 
-        // ---- phase 4f: thread = channel ch, all 16 rows
-        {
+        // ---- phase 4f: the combination. Factored forms: warp w takes rows 4 w .. + 3,
+        //      lane l channels 4 l .. + 3 (128- and 64-bit shared loads, 16-byte
+        //      stores); the exact form: thread = channel, all 16 rows
+        if (!exact) {
+            const int c0 = 4 * lane, rb = 4 * warp;
+            const float *sGt = reinterpret_cast<const float *>(smem + kGGt);
+            float *sTot = reinterpret_cast<float *>(smem + kGTot);   // [0]: dG sums, [1]: kdv sums
+            // q and k enter through the tiles scale Q e^(G - G_ref), K e^(G - G_ref),
+            // K e^(G_ref - G) and the record's K e^(G_last - G); G here is less G_ref
+            const float inv_scale = scale != 0.f ? 1.f / scale : 0.f;
+            const float4 gl4 = *reinterpret_cast<const float4 *>(sGt + 15 * kDim + c0);
+            const float gL[4] = {gl4.x, gl4.y, gl4.z, gl4.w};
+            // e^(G_last - G) = e^(G_last - G_ref) e^(G_ref - G): both within e^+-80 here
+            float eLr[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) eLr[e] = ex2g(gL[e]);
+            float dG[4][4];    // dG less the K e^(G_last - G) terms
+            float kdv[4][4];   // those terms: k e^(G_last - G) dKd
+            auto bf4 = [](uint2 u, float (&f)[4]) {
+                const float2 a = unpack_bf16(u.x), b = unpack_bf16(u.y);
+                f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+            };
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = rb + i;
+                const float4 g4 = *reinterpret_cast<const float4 *>(sGt + r * kDim + c0);
+                const float4 z4 = *reinterpret_cast<const float4 *>(gZ + r * kFS + c0);
+                const float4 t4 = *reinterpret_cast<const float4 *>(gT1 + r * kFS + c0);
+                const float4 y4 = *reinterpret_cast<const float4 *>(gYc + r * kFS + c0);
+                const float4 d4 = *reinterpret_cast<const float4 *>(gK + r * kFS + c0);
+                const int o16 = swz(r, c0);   // channels c0 .. c0 + 3: 8 bytes of one 16-byte chunk
+                float qs[4], kd[4], kgv[4], knv[4];
+                bf4(*reinterpret_cast<const uint2 *>(smem + (sQs - sb) + o16), qs);
+                bf4(*reinterpret_cast<const uint2 *>(smem + kGOffRec + kRecKd + o16), kd);
+                bf4(*reinterpret_cast<const uint2 *>(smem + kGOffKg + o16), kgv);
+                bf4(*reinterpret_cast<const uint2 *>(smem + kGOffKn + o16), knv);
+                const float G[4] = {g4.x, g4.y, g4.z, g4.w}, z[4] = {z4.x, z4.y, z4.z, z4.w};
+                const float t1[4] = {t4.x, t4.y, t4.z, t4.w}, yc[4] = {y4.x, y4.y, y4.z, y4.w};
+                const float dkd[4] = {d4.x, d4.y, d4.z, d4.w};
+                const float yd = scale * gP[r * 17];   // the diagonal pair: its dG terms cancel
+                float dq[4], dk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float eG = ex2g(G[e]), eN = ex2g(-G[e]), eD = eLr[e] * eN;
+                    const float qgs = qs[e] * inv_scale;
+                    // q dq = (q e^G) Z, k a = (k e^G) T1, k b = (k e^-G) Yc, k d = Kd dKd
+                    // (each e^G here is e^(G - G_ref), e^-G is e^(G_ref - G))
+                    kdv[i][e] = kd[e] * dkd[e];
+                    dG[i][e] = fmaf(qgs, z[e], fmaf(kgv[e], t1[e], -knv[e] * yc[e]));
+                    dq[e] = fmaf(yd, knv[e] * eG, eG * z[e]);
+                    dk[e] = fmaf(yd, qgs * eN, fmaf(eG, t1[e], fmaf(eN, yc[e], eD * dkd[e])));
+                }
+                if (r < L) {
+                    const int64_t o = qoff + r * rowe + c0;
+                    *reinterpret_cast<float4 *>(p.dq + o) = make_float4(dq[0], dq[1], dq[2], dq[3]);
+                    *reinterpret_cast<float4 *>(p.dk + o) = make_float4(dk[0], dk[1], dk[2], dk[3]);
+                }
+            }
+            if (warp == 3) {
+                // the last row also takes dgamma e^(G_last)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) dG[3][e] = fmaf(sdG[c0 + e], ex2g(gL[e] + gref), dG[3][e]);
+            }
+            // dg_u = sum_{r >= u} dG_r + sum_{r < u} kdv_r (see the exact form below):
+            // within the block, then the other blocks' totals
+            float sfx[4][4], pfx[4][4], tS[4], tK[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                float a = 0.f, b = 0.f;
+#pragma unroll
+                for (int i = 3; i >= 0; --i) { a += dG[i][e]; sfx[i][e] = a; }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) { pfx[i][e] = b; b += kdv[i][e]; }
+                tS[e] = a;
+                tK[e] = b;
+            }
+            *reinterpret_cast<float4 *>(sTot + warp * kDim + c0) = make_float4(tS[0], tS[1], tS[2], tS[3]);
+            *reinterpret_cast<float4 *>(sTot + 4 * kDim + warp * kDim + c0) = make_float4(tK[0], tK[1], tK[2], tK[3]);
+            __syncthreads();
+            float addS[4] = {0.f, 0.f, 0.f, 0.f}, addK[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w2 = 0; w2 < 4; ++w2) {
+                if (w2 > warp) {
+                    const float4 v = *reinterpret_cast<const float4 *>(sTot + w2 * kDim + c0);
+                    addS[0] += v.x; addS[1] += v.y; addS[2] += v.z; addS[3] += v.w;
+                } else if (w2 < warp) {
+                    const float4 v = *reinterpret_cast<const float4 *>(sTot + 4 * kDim + w2 * kDim + c0);
+                    addK[0] += v.x; addK[1] += v.y; addK[2] += v.z; addK[3] += v.w;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int r = rb + i;
+                if (r < L)
+                    *reinterpret_cast<float4 *>(p.dg + qoff + r * rowe + c0) =
+                        make_float4(sfx[i][0] + addS[0] + (pfx[i][0] + addK[0]),
+                                    sfx[i][1] + addS[1] + (pfx[i][1] + addK[1]),
+                                    sfx[i][2] + addS[2] + (pfx[i][2] + addK[2]),
+                                    sfx[i][3] + addS[3] + (pfx[i][3] + addK[3]));
+            }
+        } else {
             const int ch = tid;
             const int64_t base = qoff + ch;
             float dG[16];    // dG less the K e^(G_last - G) terms
             float kdv[16];   // those terms: k e^(G_last - G) dKd per row
             const float G2L = Gc[15];
             float dGL = sdG[ch] * ex2g(G2L + gref);
-            if (!exact) {
-                // q and k enter through the tiles scale Q e^(G - G_ref), K e^(G - G_ref),
-                // K e^(G_ref - G) and the record's K e^(G_last - G); G here is less G_ref
-                const float inv_scale = scale != 0.f ? 1.f / scale : 0.f;
-                // e^(G_last - G) = e^(G_last - G_ref) e^(G_ref - G): both within e^+-80 here
-                const float eLr = ex2g(G2L);
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const float eG = ex2g(Gc[r]), eN = ex2g(-Gc[r]), eD = eLr * eN;
-                    const int o16 = swz(r, ch);
-                    const float qgs = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                                          smem + (sQs - sb) + o16)) * inv_scale;
-                    const float kd = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(
-                        smem + kGOffRec + kRecKd + o16));
-                    const float kgv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + kGOffKg + o16));
-                    const float knv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(smem + kGOffKn + o16));
-                    const float z = gZ[r * kFS + ch], t1 = gT1[r * kFS + ch];
-                    const float yc = gYc[r * kFS + ch], dkd = gK[r * kFS + ch];
-                    // q dq = (q e^G) Z, k a = (k e^G) T1, k b = (k e^-G) Yc, k d = Kd dKd
-                    // (each e^G here is e^(G - G_ref), e^-G is e^(G_ref - G))
-                    kdv[r] = kd * dkd;
-                    dG[r] = fmaf(qgs, z, fmaf(kgv, t1, -knv * yc));
-                    if (r < L) {
-                        // the diagonal pair: its two dG terms cancel exactly
-                        const float yd = scale * gP[r * 17];
-                        const int64_t o = base + r * rowe;
-                        p.dq[o] = fmaf(yd, knv * eG, eG * z);
-                        p.dk[o] = fmaf(yd, qgs * eN, fmaf(eG, t1, fmaf(eN, yc, eD * dkd)));
-                    }
-                }
-            } else {
+            {
                 // exact per-pair exponentials for the P and A terms
                 const __nv_bfloat16 *qg = static_cast<const __nv_bfloat16 *>(p.ip.q);
                 const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(p.ip.k);
