@@ -24,10 +24,11 @@ int g_exact_blocks_per_sm[kMaxDev] = {};
 // Persistent: each warp walks (chunk, head) items with a grid-wide stride,
 // items ordered chunk-major so the warps of a CTA share a chunk's rows.
 // PRE = false compiles no preprocessing code at all (p.pre must be 0);
-// PRE = true reads the preprocessing flags from p.pre. FLAG = true raises
-// p.wide_flag for chunks out of the start-referenced range (gradient calls;
-// the forward's instantiation carries no code for it).
-template <bool PRE, bool FLAG = false>
+// PRE = true reads the preprocessing flags from p.pre. GRAD = true is the
+// gradient call's instantiation: it also writes (I + A)^{-1} to p.tinv and
+// raises p.wide_flag for chunks out of the start-referenced range (the
+// forward's instantiation carries no code for either).
+template <bool PRE, bool GRAD = false>
 __global__ void __launch_bounds__(kIntraWarps * 32, 3)
 kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -52,7 +53,7 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     (void)n;
     const int64_t ri = rec_idx * H + h;
     uint8_t *rec = p.rec + ri * kRecBytes;
-    if (intra_item<PRE, false, FLAG>(p, sm, t0, L, h, rec, p.tinv != nullptr ? p.tinv + ri * 256 : nullptr) &&
+    if (intra_item<PRE, false, GRAD>(p, sm, t0, L, h, rec, p.tinv != nullptr ? p.tinv + ri * 256 : nullptr) &&
         lane == 0)
         p.exact_list[atomicAdd(p.exact_ctr, 1)] = static_cast<int32_t>(item);
     }  // items
@@ -211,7 +212,7 @@ cudaError_t launch_intra_chunk(const IntraParams &p, int64_t max_chunks, cudaStr
     if (p.pre != 0)
         kda_intra_chunk_kernel<true><<<static_cast<unsigned>(blocks), kIntraWarps * 32, smem,
                                        stream>>>(p, max_chunks);
-    else if (p.wide_flag != nullptr)
+    else if (p.tinv != nullptr)   // a gradient call (p.wide_flag set too)
         kda_intra_chunk_kernel<false, true><<<static_cast<unsigned>(blocks), kIntraWarps * 32, smem,
                                               stream>>>(p, max_chunks);
     else

@@ -347,9 +347,9 @@ __device__ __forceinline__ void intra_exact_chunk(const float *gp, int64_t rowe,
 
 // The part of an item common to both forms: Tm = (I + A)^{-1} from sm.a,
 // then W = Tm diag(beta) (K e^G) from sm.kg and Ut^T = (Tm diag(beta) V)^T
-// from sm.v, both to the record; Tm itself to tout ([16][16] fp32) when that
-// is not null.
-template <bool KEEP>
+// from sm.v, both to the record; Tm itself to tout ([16][16] fp32) when TOUT
+// and tout is not null.
+template <bool KEEP, bool TOUT = true>
 __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, float *tout,
                                            float beta_l, int lane, float wscale = 1.f) {
     const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
@@ -372,7 +372,7 @@ __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, floa
         }
     }
     __syncwarp();
-    if (tout != nullptr) {
+    if (TOUT && tout != nullptr) {
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
             const int e = lane + 32 * it;
@@ -446,7 +446,7 @@ __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, floa
 // Returns whether the chunk leaves the factored range (|G| > 80 in some
 // channel): its record then holds wrong numbers until intra_exact_item
 // rewrites it.
-template <bool PRE, bool KEEP, bool FLAG = false>
+template <bool PRE, bool KEEP, bool GRAD = false>
 __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &sm, int64_t t0,
                                            int L, int h, uint8_t *rec, float *tout) {
     const int lane = threadIdx.x & 31;
@@ -497,8 +497,8 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
     //  measured 4 % slower on chunks that never need it)
 #pragma unroll 1
     for (int once = 0, n = opaque_trips(wide); once < n; ++once) {
-        if constexpr (FLAG) {
-            if (lane == 0) *p.wide_flag = 1;   // (compiled in only where a caller wants it)
+        if constexpr (GRAD) {
+            if (lane == 0) *p.wide_flag = 1;   // (only in the gradient call's instantiation)
         }
         // range of G from the chunk start (0) on, and its largest rise
         float hi = 0.f, low = 0.f, rise = 0.f;
@@ -634,7 +634,7 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
         }
     }
     __syncwarp();
-    intra_tail<KEEP>(sm, rec, tout, beta_l, lane, eref);
+    intra_tail<KEEP, GRAD>(sm, rec, tout, beta_l, lane, eref);
     return exact;
 }
 
