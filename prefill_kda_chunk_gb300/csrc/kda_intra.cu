@@ -53,9 +53,8 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     (void)n;
     const int64_t ri = rec_idx * H + h;
     uint8_t *rec = p.rec + ri * kRecBytes;
-    if (intra_item<PRE, false, GRAD>(p, sm, t0, L, h, rec, p.tinv != nullptr ? p.tinv + ri * 256 : nullptr) &&
-        lane == 0)
-        p.exact_list[atomicAdd(p.exact_ctr, 1)] = static_cast<int32_t>(item);
+    intra_item<PRE, false, GRAD>(p, sm, t0, L, h, rec, p.tinv != nullptr ? p.tinv + ri * 256 : nullptr,
+                                 static_cast<int32_t>(item));
     }  // items
 }
 

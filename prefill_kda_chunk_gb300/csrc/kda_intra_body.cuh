@@ -443,12 +443,13 @@ __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, floa
 // One (chunk, head) item in the factored form, by one warp: sm is the warp's
 // shared memory, rec its record, tout where (I + A)^{-1} goes (or null),
 // rows [t0, t0 + L) of head h its tokens.
-// Returns whether the chunk leaves the factored range (|G| > 80 in some
-// channel): its record then holds wrong numbers until intra_exact_item
-// rewrites it.
+// A chunk outside both factored ranges (see below) gets wrong numbers in its
+// record until intra_exact_item rewrites it: its item index (list_item) goes
+// on p.exact_list.
 template <bool PRE, bool KEEP, bool GRAD = false>
-__device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &sm, int64_t t0,
-                                           int L, int h, uint8_t *rec, float *tout) {
+__device__ __forceinline__ void intra_item(const IntraParams &p, IntraWarpSmem &sm, int64_t t0,
+                                           int L, int h, uint8_t *rec, float *tout,
+                                           int32_t list_item) {
     const int lane = threadIdx.x & 31;
     const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
     const int H = p.geo.n_heads;
@@ -519,6 +520,7 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
             low = fminf(low, __shfl_xor_sync(0xffffffffu, low, o));
         }
         exact = !(hi - low <= 230.84f) || __any_sync(0xffffffffu, !(rise <= 115.42f));
+        if (exact && lane == 0) p.exact_list[atomicAdd(p.exact_ctr, 1)] = list_item;
         if (!exact) {
             gref = 0.5f * (hi + low);
             eref = ex2(gref);
@@ -635,7 +637,6 @@ __device__ __forceinline__ bool intra_item(const IntraParams &p, IntraWarpSmem &
     }
     __syncwarp();
     intra_tail<KEEP, GRAD>(sm, rec, tout, beta_l, lane, eref);
-    return exact;
 }
 
 // The same item in the exact per-pair form (the whole record rewritten).
