@@ -20,15 +20,19 @@
 // Kd = K e^(G_last - G), gamma = e^(G_last)) to dq, dk, dv, dbeta and dG, and
 // dg as the reverse cumulative sum of dG within the chunk.
 //
-// Three launches after the forward's intra-chunk kernels (which build the
-// records): the forward chain again without outputs, keeping every chunk's
-// entry state S^T in bf16; kda_bwd_chain_kernel, the reverse chain over
-// the chunks (the forward step with roles swapped), keeping every chunk's
-// dS_next^T in bf16 and writing dL/d(initial state); and kda_bwd_grad_kernel,
-// chunk-parallel, one CTA per (chunk, head), for everything else. The WY
-// reverse takes exact per-pair exponentials exp(G_r - G_i) (r >= i), so it
-// holds for any decay; it reads the records and T = (I + A)^-1 as the
-// forward's intra-chunk kernels left them (factored or exact form).
+// Two launches after the forward's intra-chunk kernels (which build the
+// records and T = (I + A)^-1 per chunk-head):
+//   kda_bwd_chains_kernel: the forward chain again without outputs, keeping
+//     every chunk's entry state S^T in bf16, and the reverse chain over the
+//     chunks (the forward step with roles swapped), keeping every chunk's
+//     dS_next^T in bf16 and writing dL/d(initial state); both roles in one
+//     launch, neither waiting on the other;
+//   kda_bwd_grad_kernel: chunk-parallel, one CTA per (chunk, head) at a time,
+//     for everything else.
+// The WY reverse factors the gated products like the forward (about the chunk
+// start, or about the middle of the chunk's decay range) and takes exact
+// per-pair exponentials exp(G_r - G_i) (r >= i) beyond those ranges, so it
+// holds for any decay.
 
 #include <cuda.h>
 
