@@ -217,7 +217,7 @@ __device__ __forceinline__ void states_cta(const BwdChunkParams &p, const CUtens
 __device__ __forceinline__ void chain_cta(const BwdChunkParams &p, const CUtensorMap *out,
                                           const CUtensorMap *dout_map, int unit, uint8_t *smem) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int gid = lane >> 2, tig = lane & 3, quad = lane >> 3;
+    const int tig = lane & 3, quad = lane >> 3;
     const ChunkGeometry &geo = p.geo;
     const int H = geo.n_heads;
     constexpr int kSlices = kDim / kCBV;

@@ -32,7 +32,7 @@ template <bool PRE, bool GRAD = false>
 __global__ void __launch_bounds__(kIntraWarps * 32, 3)
 kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const ChunkGeometry &geo = p.geo;
     const int H = geo.n_heads;
     // let the exact-form kernel, launched next as a programmatic dependent, be
