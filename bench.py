@@ -414,7 +414,11 @@ def bench_backward(K, dev, w, args, hbm):
             "dtype": "fp32 (bf16 q, k, v, dO)", "data": "synthetic",
             "config": dict(config_of(w, d), backward=True),
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                         "frac": gbs / hbm, "traffic": None,
+                         "frac": gbs / hbm,
+                         # DRAM bytes of the whole chunked call (all its launches), from
+                         # the committed ncu record
+                         "traffic": (traffic_for("backward_call", w.name)
+                                     if args.backward_impl == 0 and stock_workload(args) else None),
                          "kernel": ("the whole call: intra-chunk, exact form, both chains, gradients"
                                     if args.backward_impl == 0 else "kda_backward_kernel"),
                          "bytes_per_call": nbytes},
