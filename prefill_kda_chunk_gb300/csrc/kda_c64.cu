@@ -1050,39 +1050,49 @@ __device__ void intra_role(const Params &p, uint8_t *smem, int worker, int nwork
             uint8_t *rec = record_of(p, c, h);
             wait_bar(bar(kIBWU + b), pb(it), abort_flag, p.err);
             tc::fence_after();
-            // Ut^T row v = 32 q4 + lane, all 64 tokens
-            uint32_t d0[32], d1[32];
-            tld32(tmem + lane_base + 256 + 192 * b, d0);
-            tld32(tmem + lane_base + 256 + 192 * b + 32, d1);
-            // W (M = 64): rows 16 q4 + (0..15); thread (gq, tq) rows gq, gq + 8 and
-            // the column pair 2 tq of each 8-column block
-            uint32_t wr[16][4];
-#pragma unroll
-            for (int b8 = 0; b8 < 16; ++b8)
-                tc::ld_16x256b(tmem + lane_base + 128 + 192 * b + 8 * b8, wr[b8][0], wr[b8][1],
-                               wr[b8][2], wr[b8][3]);
-            tc::ld_wait();
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(kIBFdone + b));
+            // Ut^T row v = 32 q4 + lane, 32 tokens at a time, then W (M = 64): rows
+            // 16 q4 + (0..15), thread (gq, tq) rows gq, gq + 8 and the column pair
+            // 2 tq of each 8-column block, 64 keys at a time (one half of the
+            // tensor-memory data in registers at once)
             const int v = 32 * q4 + lane;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t *dd = j < 4 ? d0 + 8 * j : d1 + 8 * (j - 4);
-                st_global_v4(rec + kRecUt + ut_off(v, j),
-                             make_uint4(pack_bf16(__uint_as_float(dd[0]), __uint_as_float(dd[1])),
-                                        pack_bf16(__uint_as_float(dd[2]), __uint_as_float(dd[3])),
-                                        pack_bf16(__uint_as_float(dd[4]), __uint_as_float(dd[5])),
-                                        pack_bf16(__uint_as_float(dd[6]), __uint_as_float(dd[7]))));
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t d[32];
+                tld32(tmem + lane_base + 256 + 192 * b + 32 * hf, d);
+                tc::ld_wait();
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t *dd = d + 8 * j;
+                    st_global_v4(rec + kRecUt + ut_off(v, 4 * hf + j),
+                                 make_uint4(pack_bf16(__uint_as_float(dd[0]), __uint_as_float(dd[1])),
+                                            pack_bf16(__uint_as_float(dd[2]), __uint_as_float(dd[3])),
+                                            pack_bf16(__uint_as_float(dd[4]), __uint_as_float(dd[5])),
+                                            pack_bf16(__uint_as_float(dd[6]), __uint_as_float(dd[7]))));
+                }
             }
             const int r0 = 16 * q4 + gq;
 #pragma unroll
-            for (int b8 = 0; b8 < 16; ++b8) {
-                const int key = 8 * b8 + 2 * tq;
-                st_global_u32(rec + kRecB1 + kmaj(64 + r0, key, 128),
-                              pack_bf16(-__uint_as_float(wr[b8][0]), -__uint_as_float(wr[b8][1])));
-                st_global_u32(rec + kRecB1 + kmaj(64 + r0 + 8, key, 128),
-                              pack_bf16(-__uint_as_float(wr[b8][2]), -__uint_as_float(wr[b8][3])));
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t wr[8][4];
+#pragma unroll
+                for (int b8 = 0; b8 < 8; ++b8)
+                    tc::ld_16x256b(tmem + lane_base + 128 + 192 * b + 8 * (8 * hf + b8), wr[b8][0],
+                                   wr[b8][1], wr[b8][2], wr[b8][3]);
+                tc::ld_wait();
+                if (hf == 1) {
+                    // the accumulators of buffer b are read: release them
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(kIBFdone + b));
+                }
+#pragma unroll
+                for (int b8 = 0; b8 < 8; ++b8) {
+                    const int key = 8 * (8 * hf + b8) + 2 * tq;
+                    st_global_u32(rec + kRecB1 + kmaj(64 + r0, key, 128),
+                                  pack_bf16(-__uint_as_float(wr[b8][0]), -__uint_as_float(wr[b8][1])));
+                    st_global_u32(rec + kRecB1 + kmaj(64 + r0 + 8, key, 128),
+                                  pack_bf16(-__uint_as_float(wr[b8][2]), -__uint_as_float(wr[b8][3])));
+                }
             }
             // the whole record is written once the writers are done (the builders'
             // and solvers' parts came earlier in the item's chain of barriers)
