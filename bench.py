@@ -393,6 +393,8 @@ def bench_backward(K, dev, w, args, hbm):
                                         initial_state=s0, cu_seqlens=cu, scale=d["scale"],
                                         d_final_state=dsf_d)
 
+    clocks = ClockSampler(dev)
+    clocks.start()
     for _ in range(max(args.warmup, 3)):
         call()
     K.check_device_error()
@@ -404,6 +406,7 @@ def bench_backward(K, dev, w, args, hbm):
         call()
     b.record(stream)
     torch.cuda.synchronize(dev)
+    clk = clocks.stop()
     K.check_device_error()
     ms = a.elapsed_time(b) / steps
     nbytes = T * H * BWD_TOKEN_HEAD_BYTES + n_seqs * H * BWD_UNIT_BYTES
@@ -423,6 +426,7 @@ def bench_backward(K, dev, w, args, hbm):
                                     if args.backward_impl == 0 else "kda_backward_kernel"),
                          "bytes_per_call": nbytes},
             "backward_impl": "chunked" if args.backward_impl == 0 else "token-serial",
+            "clocks": clk,
             # chunked: intra-chunk, exact form, the chains, the gradient kernel
             "gpu_launches": steps * ((4 if args.backward_impl == 0 else 1) + int(w.varlen))}
     if not args.no_cpu_baseline:
