@@ -410,11 +410,13 @@ constexpr int kGOffQn = kGOffDUB + 4096;    // q as loaded (bf16 [16][128], row-
                                             //   range, scale Q e^(G - G_ref) bf16, swizzled
 constexpr int kGOffMisc = kGOffQn + 4096;   // beta [16], dbeta from M [16], dbeta parts [4][16],
                                             //   the copy barrier, range partials [4][2]
-constexpr int kGBar = kGOffMisc + 384;       // the item's copies
+constexpr int kGBar = kGOffMisc + 384;       // the item's g and k (and q)
 constexpr int kGBarQ = kGOffMisc + 392;      // a late copy of q
 constexpr int kGRed = kGOffMisc + 400;      // range partials [4][2]
+constexpr int kGBarS = kGOffMisc + 432;     // the item's states, record and T
 constexpr int kGSmem = kGOffMisc + 512;
-constexpr uint32_t kGTxBytes = 2 * 32768 + kRecBytes + 1024 + 8192 + 4096;   // TMA bytes per item, q aside
+constexpr uint32_t kGTxBytes = 8192 + 4096;                       // g and k, q aside
+constexpr uint32_t kGTxBytesS = 2 * 32768 + kRecBytes + 1024;     // S^T, dS_next^T, record, T
 static_assert(kGOffT % 16 == 0 && kGOffV % 16 == 0 && kGOffDO % 16 == 0 && kGOffQn % 128 == 0 &&
                   kGOffUB % 128 == 0 && kGOffKn % 128 == 0, "alignment");
 // fp32 [16 rows][128 channels] tiles, rows kFS floats apart: the fragment
@@ -508,10 +510,11 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
         if (tid == 0) atomicOr(p.err, kErrTimeout);
         return;
     }
-    const uint32_t bar = sb + kGBar, bar_q = sb + kGBarQ;
+    const uint32_t bar = sb + kGBar, bar_q = sb + kGBarQ, bar_s = sb + kGBarS;
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(bar_q, 1);
+        mbar_init(bar_s, 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -551,10 +554,11 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
         __syncthreads();   // the previous item is done with every tile
         const int64_t qoff = (t0 * H + h) * kDim;
 
-        // ---- phase 1: S^T, dS_next^T, g, k and q (TMA boxes), the record and T
-        //      (bulk copies), V and dO (16-byte copies, rows past the end
-        //      zero); thread = channel for G (kept in registers) and the
-        //      K e^G and K e^-G tiles
+        // ---- phase 1: g, k and q (TMA boxes) first, then S^T, dS_next^T (TMA
+        //      boxes), the record and T (bulk copies) on a second barrier,
+        //      and V and dO (16-byte copies, rows past the end zero); thread =
+        //      channel for G (kept in registers) and the K e^G and K e^-G
+        //      tiles, built while the states are still arriving
         bool exact, middle;
         float Gc[16];       // this channel's G in base-2 units, less G_ref
         float gref = 0.f;   // G_ref in base-2 units
@@ -566,21 +570,22 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                     // the previous item wrote these tiles through the generic proxy
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     mbar_arrive_expect_tx(bar, kGTxBytes + (kMid && want_q ? 4096u : 0u));
+                    mbar_arrive_expect_tx(bar_s, kGTxBytesS);
                 }
                 __syncwarp();
                 if (lane == 0) {
                     const int z = static_cast<int>(ri);
-                    tma_load_3d(sST, &tm.st, 0, 0, z, bar);
-                    tma_load_3d(sST + 16384, &tm.st, 64, 0, z, bar);
-                    tma_load_3d(sDT, &tm.dst, 0, 0, z, bar);
-                    tma_load_3d(sDT + 16384, &tm.dst, 64, 0, z, bar);
                     tma_load_3d(sUB, &tm.g, 0, h, static_cast<int>(t0), bar);
                     tma_load_3d(sKn, &tm.k, 0, h, static_cast<int>(t0), bar);
                     if (kMid && want_q) tma_load_3d(sb + kGOffQn, &tm.q, 0, h, static_cast<int>(t0), bar);
-                    bulk_g2s(sRec, p.rec + ri * static_cast<int64_t>(kRecBytes), kRecBytes, bar);
+                    tma_load_3d(sST, &tm.st, 0, 0, z, bar_s);
+                    tma_load_3d(sST + 16384, &tm.st, 64, 0, z, bar_s);
+                    tma_load_3d(sDT, &tm.dst, 0, 0, z, bar_s);
+                    tma_load_3d(sDT + 16384, &tm.dst, 64, 0, z, bar_s);
+                    bulk_g2s(sRec, p.rec + ri * static_cast<int64_t>(kRecBytes), kRecBytes, bar_s);
                 }
                 if (lane < 16)
-                    bulk_g2s(sT + lane * (kTStride * 4), p.ip.tinv + ri * 256 + 16 * lane, 64, bar);
+                    bulk_g2s(sT + lane * (kTStride * 4), p.ip.tinv + ri * 256 + 16 * lane, 64, bar_s);
             }
             const __nv_bfloat16 *dop = static_cast<const __nv_bfloat16 *>(p.dout) + qoff;
             const __nv_bfloat16 *vp = static_cast<const __nv_bfloat16 *>(p.ip.v) + qoff;
@@ -593,15 +598,15 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
             }
             cp_async_commit();
             if (tid < 16) sBeta[tid] = tid < L ? __ldg(p.ip.beta + (t0 + tid) * H + h) : 0.f;
-            cp_async_wait_all();
             const bool got = mbar_wait(bar, parity);
             if (__syncthreads_or(!got)) {
                 // give the copies in flight another bounded wait, then stop
                 if (tid == 0) atomicOr(p.err, kErrTimeout);
                 if (!got) mbar_wait(bar, parity);
+                mbar_wait(bar_s, parity);
+                cp_async_wait_all();
                 break;
             }
-            parity ^= 1u;
             // G = running sum of g (rows past the end: zero): its largest |G|, its
             // range from the chunk start on and its largest rise (nats)
             const float *gs = reinterpret_cast<const float *>(smem + kGOffUB) + tid;
@@ -654,6 +659,8 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                     if (__syncthreads_or(!got_q)) {
                         if (tid == 0) atomicOr(p.err, kErrTimeout);
                         if (!got_q) mbar_wait(bar_q, parity_q ^ 1u);
+                        mbar_wait(bar_s, parity);
+                        cp_async_wait_all();
                         break;
                     }
                 }
@@ -683,7 +690,15 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                 *reinterpret_cast<__nv_bfloat16 *>(smem + kGOffKn + swz(r, tid)) =
                     __float2bfloat16_rn(kr[r] * ex2g(-Gc[r]));
             }
-            __syncthreads();
+            // the states, record and T, and V and dO
+            cp_async_wait_all();
+            const bool got_s = mbar_wait(bar_s, parity);
+            parity ^= 1u;
+            if (__syncthreads_or(!got_s)) {
+                if (tid == 0) atomicOr(p.err, kErrTimeout);
+                if (!got_s) mbar_wait(bar_s, parity ^ 1u);
+                break;
+            }
         }
         // scale Q e^(G - G_ref): the record's scale Q e^G when G_ref = 0
         const uint32_t sQs = kMid && middle ? sb + kGOffQn : sRec + kRecQg;
