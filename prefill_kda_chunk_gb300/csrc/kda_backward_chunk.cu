@@ -413,10 +413,12 @@ constexpr int kGOffMisc = kGOffQn + 4096;   // beta [16], dbeta from M [16], dbe
 constexpr int kGBar = kGOffMisc + 384;       // the item's g and k (and q)
 constexpr int kGBarQ = kGOffMisc + 392;      // a late copy of q
 constexpr int kGRed = kGOffMisc + 400;      // range partials [4][2]
-constexpr int kGBarS = kGOffMisc + 432;     // the item's states, record and T
+constexpr int kGBarS = kGOffMisc + 432;     // the item's S^T, record and T
+constexpr int kGBarD = kGOffMisc + 440;     // the item's dS_next^T
 constexpr int kGSmem = kGOffMisc + 512;
-constexpr uint32_t kGTxBytes = 8192 + 4096;                       // g and k, q aside
-constexpr uint32_t kGTxBytesS = 2 * 32768 + kRecBytes + 1024;     // S^T, dS_next^T, record, T
+constexpr uint32_t kGTxBytes = 8192 + 4096;                   // g and k, q aside
+constexpr uint32_t kGTxBytesS = 32768 + kRecBytes + 1024;     // S^T, record, T
+constexpr uint32_t kGTxBytesD = 32768;                        // dS_next^T
 static_assert(kGOffT % 16 == 0 && kGOffV % 16 == 0 && kGOffDO % 16 == 0 && kGOffQn % 128 == 0 &&
                   kGOffUB % 128 == 0 && kGOffKn % 128 == 0, "alignment");
 // fp32 [16 rows][128 channels] tiles, rows kFS floats apart: the fragment
@@ -510,11 +512,12 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
         if (tid == 0) atomicOr(p.err, kErrTimeout);
         return;
     }
-    const uint32_t bar = sb + kGBar, bar_q = sb + kGBarQ, bar_s = sb + kGBarS;
+    const uint32_t bar = sb + kGBar, bar_q = sb + kGBarQ, bar_s = sb + kGBarS, bar_d = sb + kGBarD;
     if (tid == 0) {
         mbar_init(bar, 1);
         mbar_init(bar_q, 1);
         mbar_init(bar_s, 1);
+        mbar_init(bar_d, 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -554,11 +557,11 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
         __syncthreads();   // the previous item is done with every tile
         const int64_t qoff = (t0 * H + h) * kDim;
 
-        // ---- phase 1: g, k and q (TMA boxes) first, then S^T, dS_next^T (TMA
-        //      boxes), the record and T (bulk copies) on a second barrier,
-        //      and V and dO (16-byte copies, rows past the end zero); thread =
-        //      channel for G (kept in registers) and the K e^G and K e^-G
-        //      tiles, built while the states are still arriving
+        // ---- phase 1: g, k and q (TMA boxes) first; then S^T (TMA boxes), the
+        //      record and T (bulk copies) on a second barrier and dS_next^T on
+        //      a third, and V and dO (16-byte copies, rows past the end zero);
+        //      thread = channel for G (kept in registers) and the K e^G and
+        //      K e^-G tiles, built while the rest is still arriving
         bool exact, middle;
         float Gc[16];       // this channel's G in base-2 units, less G_ref
         float gref = 0.f;   // G_ref in base-2 units
@@ -571,6 +574,7 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     mbar_arrive_expect_tx(bar, kGTxBytes + (kMid && want_q ? 4096u : 0u));
                     mbar_arrive_expect_tx(bar_s, kGTxBytesS);
+                    mbar_arrive_expect_tx(bar_d, kGTxBytesD);
                 }
                 __syncwarp();
                 if (lane == 0) {
@@ -580,12 +584,16 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                     if (kMid && want_q) tma_load_3d(sb + kGOffQn, &tm.q, 0, h, static_cast<int>(t0), bar);
                     tma_load_3d(sST, &tm.st, 0, 0, z, bar_s);
                     tma_load_3d(sST + 16384, &tm.st, 64, 0, z, bar_s);
-                    tma_load_3d(sDT, &tm.dst, 0, 0, z, bar_s);
-                    tma_load_3d(sDT + 16384, &tm.dst, 64, 0, z, bar_s);
                     bulk_g2s(sRec, p.rec + ri * static_cast<int64_t>(kRecBytes), kRecBytes, bar_s);
                 }
                 if (lane < 16)
                     bulk_g2s(sT + lane * (kTStride * 4), p.ip.tinv + ri * 256 + 16 * lane, 64, bar_s);
+                __syncwarp();
+                if (lane == 0) {
+                    const int z = static_cast<int>(ri);
+                    tma_load_3d(sDT, &tm.dst, 0, 0, z, bar_d);
+                    tma_load_3d(sDT + 16384, &tm.dst, 64, 0, z, bar_d);
+                }
             }
             const __nv_bfloat16 *dop = static_cast<const __nv_bfloat16 *>(p.dout) + qoff;
             const __nv_bfloat16 *vp = static_cast<const __nv_bfloat16 *>(p.ip.v) + qoff;
@@ -604,6 +612,7 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                 if (tid == 0) atomicOr(p.err, kErrTimeout);
                 if (!got) mbar_wait(bar, parity);
                 mbar_wait(bar_s, parity);
+                mbar_wait(bar_d, parity);
                 cp_async_wait_all();
                 break;
             }
@@ -660,6 +669,7 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                         if (tid == 0) atomicOr(p.err, kErrTimeout);
                         if (!got_q) mbar_wait(bar_q, parity_q ^ 1u);
                         mbar_wait(bar_s, parity);
+                        mbar_wait(bar_d, parity);
                         cp_async_wait_all();
                         break;
                     }
@@ -690,25 +700,26 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                 *reinterpret_cast<__nv_bfloat16 *>(smem + kGOffKn + swz(r, tid)) =
                     __float2bfloat16_rn(kr[r] * ex2g(-Gc[r]));
             }
-            // the states, record and T, and V and dO
+            // S^T, the record and T, and V and dO
             cp_async_wait_all();
             const bool got_s = mbar_wait(bar_s, parity);
-            parity ^= 1u;
             if (__syncthreads_or(!got_s)) {
                 if (tid == 0) atomicOr(p.err, kErrTimeout);
-                if (!got_s) mbar_wait(bar_s, parity ^ 1u);
+                if (!got_s) mbar_wait(bar_s, parity);
+                mbar_wait(bar_d, parity);
                 break;
             }
         }
         // scale Q e^(G - G_ref): the record's scale Q e^G when G_ref = 0
         const uint32_t sQs = kMid && middle ? sb + kGOffQn : sRec + kRecQg;
 
-        // ---- phase 2: U^T = Ut^T + S^T (-W)^T and dU^T = dS_next^T Kd^T + dO^T P,
-        //      value rows 32 warp + 16 mt, all 16 tokens
+        // ---- phase 2: U^T = Ut^T + S^T (-W)^T, value rows 32 warp + 16 mt, all 16
+        //      tokens; then, once dS_next^T is in, dU^T = dS_next^T Kd^T + dO^T P
+        const int m2 = lane >> 3;
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
             const int vb = 32 * warp + 16 * mt;
-            float uT[2][2][4], dT[2][2][4];
+            float uT[2][2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int tk = 8 * nt + 2 * tig;
@@ -718,47 +729,70 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                     smem + kGOffRec + kRecUt + ((vb + gid + 8) * 16 + tk) * 2));
                 uT[nt][0][0] = u01.x; uT[nt][0][1] = u01.y; uT[nt][0][2] = u23.x; uT[nt][0][3] = u23.y;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) { uT[nt][1][e] = 0.f; dT[nt][0][e] = 0.f; dT[nt][1][e] = 0.f; }
+                for (int e = 0; e < 4; ++e) uT[nt][1][e] = 0.f;
             }
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t aS[4], bw[4];
+                const int ra = vb + (lane & 7) + 8 * ((lane >> 3) & 1), ca = 16 * kk + 8 * (lane >> 4);
+                ldsm_x4(sST + sw2(ra, ca), aS[0], aS[1], aS[2], aS[3]);
+                const int rb = (quad >> 1) * 8 + (lane & 7), cb = 16 * kk + (quad & 1) * 8;
+                ldsm_x4(sRec + kRecW + swz(rb, cb), bw[0], bw[1], bw[2], bw[3]);
+                mma_r(uT[0][kk & 1], aS, bw[0], bw[1]);
+                mma_r(uT[1][kk & 1], aS, bw[2], bw[3]);
+            }
+            float u[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) u[nt][e] = uT[nt][0][e] + uT[nt][1][e];
+            // U to its [t][v] tile (bf16), transposed by stmatrix
+            stsm_x4_t(sUB + swz(8 * (m2 >> 1) + (lane & 7), vb + 8 * (m2 & 1)), pack_bf16(u[0][0], u[0][1]),
+                      pack_bf16(u[0][2], u[0][3]), pack_bf16(u[1][0], u[1][1]), pack_bf16(u[1][2], u[1][3]));
+        }
+        {
+            const bool got_d = mbar_wait(bar_d, parity);
+            parity ^= 1u;
+            if (__syncthreads_or(!got_d)) {
+                if (tid == 0) atomicOr(p.err, kErrTimeout);
+                if (!got_d) mbar_wait(bar_d, parity ^ 1u);
+                break;
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            const int vb = 32 * warp + 16 * mt;
+            float dT[2][2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) { dT[nt][0][e] = 0.f; dT[nt][1][e] = 0.f; }
             {
                 // dO^T (v x t) from the [t][v] tile, transposed; P as B (r x t), transposed
                 uint32_t aO[4], bp[4];
-                const int m = lane >> 3;
-                ldsm_x4_t(sDO + swz((lane & 7) + 8 * (m >> 1), vb + 8 * (m & 1)), aO[0], aO[1], aO[2], aO[3]);
-                ldsm_x4_t(sRec + kRecP + (((m & 1) * 8 + (lane & 7)) * 16 + (m >> 1) * 8) * 2, bp[0], bp[1],
+                ldsm_x4_t(sDO + swz((lane & 7) + 8 * (m2 >> 1), vb + 8 * (m2 & 1)), aO[0], aO[1], aO[2], aO[3]);
+                ldsm_x4_t(sRec + kRecP + (((m2 & 1) * 8 + (lane & 7)) * 16 + (m2 >> 1) * 8) * 2, bp[0], bp[1],
                           bp[2], bp[3]);
                 mma_r(dT[0][1], aO, bp[0], bp[1]);
                 mma_r(dT[1][1], aO, bp[2], bp[3]);
             }
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                uint32_t aS[4], aD[4], bw[4], bk[4];
+                uint32_t aD[4], bk[4];
                 const int ra = vb + (lane & 7) + 8 * ((lane >> 3) & 1), ca = 16 * kk + 8 * (lane >> 4);
-                ldsm_x4(sST + sw2(ra, ca), aS[0], aS[1], aS[2], aS[3]);
                 ldsm_x4(sDT + sw2(ra, ca), aD[0], aD[1], aD[2], aD[3]);
                 const int rb = (quad >> 1) * 8 + (lane & 7), cb = 16 * kk + (quad & 1) * 8;
-                ldsm_x4(sRec + kRecW + swz(rb, cb), bw[0], bw[1], bw[2], bw[3]);
                 ldsm_x4(sRec + kRecKd + swz(rb, cb), bk[0], bk[1], bk[2], bk[3]);
-                mma_r(uT[0][kk & 1], aS, bw[0], bw[1]);
-                mma_r(uT[1][kk & 1], aS, bw[2], bw[3]);
                 mma_r(dT[0][kk & 1], aD, bk[0], bk[1]);
                 mma_r(dT[1][kk & 1], aD, bk[2], bk[3]);
             }
-            float u[2][4], du[2][4];
+            float du[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    u[nt][e] = uT[nt][0][e] + uT[nt][1][e];
-                    du[nt][e] = dT[nt][0][e] + dT[nt][1][e];
-                }
-            // U and dU to their [t][v] tiles (bf16), transposed by stmatrix
-            const int m = lane >> 3;
-            const uint32_t so = swz(8 * (m >> 1) + (lane & 7), vb + 8 * (m & 1));
-            stsm_x4_t(sUB + so, pack_bf16(u[0][0], u[0][1]), pack_bf16(u[0][2], u[0][3]),
-                      pack_bf16(u[1][0], u[1][1]), pack_bf16(u[1][2], u[1][3]));
-            stsm_x4_t(sDUB + so, pack_bf16(du[0][0], du[0][1]), pack_bf16(du[0][2], du[0][3]),
-                      pack_bf16(du[1][0], du[1][1]), pack_bf16(du[1][2], du[1][3]));
+                for (int e = 0; e < 4; ++e) du[nt][e] = dT[nt][0][e] + dT[nt][1][e];
+            stsm_x4_t(sDUB + swz(8 * (m2 >> 1) + (lane & 7), vb + 8 * (m2 & 1)), pack_bf16(du[0][0], du[0][1]),
+                      pack_bf16(du[0][2], du[0][3]), pack_bf16(du[1][0], du[1][1]), pack_bf16(du[1][2], du[1][3]));
         }
         __syncthreads();
 
