@@ -278,7 +278,7 @@ KDA_API int64_t kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int64_t N, 
 /* The same for kda_chunk_prefill_backward with the gradient form set by
  * kda_set_backward_impl: chunked (default): 256 B of flags, the packed chunk
  * offsets, then per 16-token chunk per head 17,408 B of record, 4 B of list
- * entry (rounded up to 256 B in all), 1 KiB of (I + A)^-1 and 64 KiB of
+ * entry (rounded up to 256 B in all), 1,280 B of (I + A)^-1 and 64 KiB of
  * bf16 states;
  * token-serial: 256 B of flags, the packed chunk offsets, 64 KiB per
  * 16-token chunk per head and 1 MiB for each of min(N * H, 1024) state
@@ -309,7 +309,7 @@ KDA_API kda_status kda_stage_timing_end(double *intra_ms, double *recurrent_ms, 
  * keeping every chunk's entry state (bf16), a reverse chain over the chunks
  * keeps every chunk's dL/d(exit state) (bf16) and writes dL/d(initial
  * state), and a chunk-parallel kernel computes dq, dk, dv, dg and dbeta
- * (workspace: per chunk-head 17,408 B of record, 4 B of list entry, 1 KiB
+ * (workspace: per chunk-head 17,408 B of record, 4 B of list entry, 1,280 B
  * of (I + A)^-1 and 64 KiB of states); 1 = the token-serial first form. Both compute the same
  * gradients to rounding. Other values: KDA_ERR_BAD_SHAPE.
  */

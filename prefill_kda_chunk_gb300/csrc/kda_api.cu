@@ -552,7 +552,7 @@ static int64_t backward_ckpt_bytes(int64_t B, int64_t T, int64_t H, int64_t N, b
 // dS_next^T of every chunk-head in bf16.
 static int64_t backward_chunk_ws_bytes(int64_t H, const Plan &pl) {
     const int64_t ch = pl.max_chunks * H;
-    return 256 + pl.off_bytes + ch * kda::kRecBytes + align256(ch * 4) + ch * 1024 +
+    return 256 + pl.off_bytes + ch * kda::kRecBytes + align256(ch * 4) + ch * 1280 +
            2 * ch * kda::kDim * kda::kDim * 2;
 }
 
@@ -688,7 +688,7 @@ kda_status kda_chunk_prefill_backward(const void *q, const void *k, const void *
         uint8_t *rec = wsb + 256 + pl.off_bytes;
         int32_t *exact_list = reinterpret_cast<int32_t *>(rec + ch * kda::kRecBytes);
         float *tinv = reinterpret_cast<float *>(rec + ch * kda::kRecBytes + align256(ch * 4));
-        uint8_t *ck = reinterpret_cast<uint8_t *>(tinv + ch * 256);
+        uint8_t *ck = reinterpret_cast<uint8_t *>(tinv + ch * 320);
         uint8_t *dsn = ck + ch * kda::kDim * kda::kDim * 2;
         int *exact_ctr = reinterpret_cast<int *>(wsb + kExactCtrOff);
         int *wide = reinterpret_cast<int *>(wsb + kWideOff);

@@ -417,7 +417,7 @@ constexpr int kGBarS = kGOffMisc + 432;     // the item's S^T, record and T
 constexpr int kGBarD = kGOffMisc + 440;     // the item's dS_next^T
 constexpr int kGSmem = kGOffMisc + 512;
 constexpr uint32_t kGTxBytes = 8192 + 4096;                   // g and k, q aside
-constexpr uint32_t kGTxBytesS = 32768 + kRecBytes + 1024;     // S^T, record, T
+constexpr uint32_t kGTxBytesS = 32768 + kRecBytes + 16 * kTStride * 4;   // S^T, record, T
 constexpr uint32_t kGTxBytesD = 32768;                        // dS_next^T
 static_assert(kGOffT % 16 == 0 && kGOffV % 16 == 0 && kGOffDO % 16 == 0 && kGOffQn % 128 == 0 &&
                   kGOffUB % 128 == 0 && kGOffKn % 128 == 0, "alignment");
@@ -585,12 +585,7 @@ __device__ __forceinline__ void grad_items(const BwdChunkParams &p, const GradMa
                     tma_load_3d(sST, &tm.st, 0, 0, z, bar_s);
                     tma_load_3d(sST + 16384, &tm.st, 64, 0, z, bar_s);
                     bulk_g2s(sRec, p.rec + ri * static_cast<int64_t>(kRecBytes), kRecBytes, bar_s);
-                }
-                if (lane < 16)
-                    bulk_g2s(sT + lane * (kTStride * 4), p.ip.tinv + ri * 256 + 16 * lane, 64, bar_s);
-                __syncwarp();
-                if (lane == 0) {
-                    const int z = static_cast<int>(ri);
+                    bulk_g2s(sT, p.ip.tinv + ri * (16 * kTStride), 16 * kTStride * 4, bar_s);
                     tma_load_3d(sDT, &tm.dst, 0, 0, z, bar_d);
                     tma_load_3d(sDT + 16384, &tm.dst, 64, 0, z, bar_d);
                 }

@@ -46,8 +46,9 @@ struct IntraParams {
     // counters are 0 between calls; exact_list holds one entry per item.
     int32_t *exact_list = nullptr;
     int *exact_ctr = nullptr;
-    // When not null, (I + A)^{-1} of every chunk-head, fp32 [16][16] row-major
-    // at item index (record index * H + head) * 256 (the gradients read it)
+    // When not null, (I + A)^{-1} of every chunk-head, fp32, 16 rows of 20
+    // floats (the last 4 unused) at item index (record index * H + head) * 320
+    // (the gradient kernel copies one item's 1280 bytes in one piece)
     float *tinv = nullptr;
     // When not null, set to 1 by any chunk-head whose |G| passes 80 (the
     // gradient kernel compiles the form for such chunks in only when it is set)

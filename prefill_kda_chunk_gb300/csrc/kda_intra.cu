@@ -53,7 +53,7 @@ kda_intra_chunk_kernel(IntraParams p, int64_t max_chunks) {
     (void)n;
     const int64_t ri = rec_idx * H + h;
     uint8_t *rec = p.rec + ri * kRecBytes;
-    intra_item<PRE, false, GRAD>(p, sm, t0, L, h, rec, p.tinv != nullptr ? p.tinv + ri * 256 : nullptr,
+    intra_item<PRE, false, GRAD>(p, sm, t0, L, h, rec, p.tinv != nullptr ? p.tinv + ri * 320 : nullptr,
                                  static_cast<int32_t>(item));
     }  // items
 }
@@ -89,7 +89,7 @@ kda_intra_exact_kernel(IntraParams p) {
         (void)n;
         const int64_t ri = rec_idx * H + h;
         intra_exact_item<PRE, false>(p, sm, t0, L, h, p.rec + ri * kRecBytes,
-                                     p.tinv != nullptr ? p.tinv + ri * 256 : nullptr);
+                                     p.tinv != nullptr ? p.tinv + ri * 320 : nullptr);
     }
     if (count == 0) return;   // the same count in every CTA: nothing to reset
     __syncthreads();

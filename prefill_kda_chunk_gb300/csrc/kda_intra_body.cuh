@@ -347,8 +347,8 @@ __device__ __forceinline__ void intra_exact_chunk(const float *gp, int64_t rowe,
 
 // The part of an item common to both forms: Tm = (I + A)^{-1} from sm.a,
 // then W = Tm diag(beta) (K e^G) from sm.kg and Ut^T = (Tm diag(beta) V)^T
-// from sm.v, both to the record; Tm itself to tout ([16][16] fp32) when TOUT
-// and tout is not null.
+// from sm.v, both to the record; Tm itself to tout ([16] rows of 20 fp32, the
+// first 16 used) when TOUT and tout is not null.
 template <bool KEEP, bool TOUT = true>
 __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, float *tout,
                                            float beta_l, int lane, float wscale = 1.f) {
@@ -376,7 +376,7 @@ __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, floa
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
             const int e = lane + 32 * it;
-            __stcs(tout + e, sm.t[(e >> 4) * 17 + (e & 15)]);
+            __stcs(tout + (e >> 4) * 20 + (e & 15), sm.t[(e >> 4) * 17 + (e & 15)]);
         }
     }
 

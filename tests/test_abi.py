@@ -198,7 +198,7 @@ def test_backward_argument_checks(lib):
 def test_backward_workspace_bytes(lib):
     # chunked (default): per chunk-head a record, a list entry (rounded up in
     # all), (I + A)^-1 in fp32 and two bf16 states
-    REC, ST2 = 17408 + 1024, 2 * 32768
+    REC, ST2 = 17408 + 1280, 2 * 32768
 
     def lst(items):
         return -(-(items * 4) // 256) * 256
