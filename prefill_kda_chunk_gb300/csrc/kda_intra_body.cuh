@@ -348,7 +348,7 @@ __device__ __forceinline__ void intra_exact_chunk(const float *gp, int64_t rowe,
 // The part of an item common to both forms: Tm = (I + A)^{-1} from sm.a,
 // then W = Tm diag(beta) (K e^G) from sm.kg and Ut^T = (Tm diag(beta) V)^T
 // from sm.v, both to the record; Tm itself to tout ([16] rows of 20 fp32, the
-// first 16 used) when TOUT and tout is not null.
+// last 4 zero) when TOUT and tout is not null.
 template <bool KEEP, bool TOUT = true>
 __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, float *tout,
                                            float beta_l, int lane, float wscale = 1.f) {
@@ -373,10 +373,12 @@ __device__ __forceinline__ void intra_tail(IntraWarpSmem &sm, uint8_t *rec, floa
     }
     __syncwarp();
     if (TOUT && tout != nullptr) {
+        // whole rows, the 4 pad columns as zeros: every 32-byte sector of the
+        // item is written in full (no read of partly written sectors)
 #pragma unroll
-        for (int it = 0; it < 8; ++it) {
-            const int e = lane + 32 * it;
-            __stcs(tout + (e >> 4) * 20 + (e & 15), sm.t[(e >> 4) * 17 + (e & 15)]);
+        for (int it = 0; it < 10; ++it) {
+            const int e = lane + 32 * it, r = e / 20, col = e - 20 * r;
+            __stcs(tout + e, col < 16 ? sm.t[r * 17 + col] : 0.f);
         }
     }
 
