@@ -128,6 +128,20 @@ def test_backward_strong_decay_mixed_heads():
     check_all(d, gpu_grads(d), "mixed heads")
 
 
+def test_backward_deterministic():
+    """Two calls on the same inputs give bitwise equal gradients. Heads in all
+    three forms: the exact-form list is filled by atomic appends, in an order
+    that may differ between calls, and every output still has one writer."""
+    d = make([200, 77], H=3, seed=31)
+    d["g"][:, 1, :] = -9.0
+    d["g"][:, 2, :] = -12.0
+    a = gpu_grads(d)
+    b = gpu_grads(d)
+    torch.cuda.synchronize()
+    for name, x, y in zip(NAMES, a, b):
+        assert torch.equal(x, y), name
+
+
 def test_backward_zero_tokens_passes_state_gradient():
     d = make([0, 0], H=2, seed=25)
     got = gpu_grads(d)
