@@ -223,3 +223,34 @@ def test_backward_benchmarked_workload_sampled():
         sub["cu_seqlens"], sub["scale"] = d["cu_seqlens"], d["scale"]
         for name, x, ref in zip(NAMES, got, oracle_grads(sub)):
             check(x[:, h:h + 1], ref, f"head {h} {name}")
+
+
+def test_backward_varlen_workload_sampled():
+    """The gradient call on the packed workload varlen16_T8192_H64 (16 sequences
+    of ragged lengths, initial states), checked against the oracle on sampled
+    (sequence, head) units: each unit's slice of the inputs alone, its tokens'
+    gradients and its d_initial_state."""
+    d = KI.make_inputs(KI.WORKLOADS["varlen16_T8192_H64"])
+    T, H = d["q"].shape[0], d["q"].shape[1]
+    N = len(d["seqlens"])
+    gen = torch.Generator().manual_seed(4343)
+    d["dout"] = torch.randn(T, H, 128, generator=gen).to(torch.bfloat16)
+    d["dsf"] = torch.randn(N, H, 128, 128, generator=gen) * 0.1
+    got = gpu_grads(d)
+    torch.cuda.synchronize()
+    got = [t.cpu() for t in got]
+    cu = d["cu_seqlens"].tolist()
+    rng = np.random.default_rng(11)
+    units = [(int(n), int(h)) for n, h in zip(rng.choice(N, size=3, replace=False),
+                                               rng.choice(H, size=3, replace=False))]
+    for n, h in units:
+        a, b = cu[n], cu[n + 1]
+        sub = {k: d[k][a:b, h:h + 1].contiguous() for k in ("q", "k", "v", "g", "beta", "dout")}
+        sub["initial_state"] = d["initial_state"][n:n + 1, h:h + 1].contiguous()
+        sub["dsf"] = d["dsf"][n:n + 1, h:h + 1].contiguous()
+        sub["cu_seqlens"] = torch.tensor([0, b - a], dtype=torch.int32)
+        sub["scale"] = d["scale"]
+        refs = oracle_grads(sub)
+        for name, x, ref in zip(NAMES[:5], got[:5], refs[:5]):
+            check(x[a:b, h:h + 1], ref, f"seq {n} head {h} {name}")
+        check(got[5][n:n + 1, h:h + 1], refs[5], f"seq {n} head {h} d_initial_state")
