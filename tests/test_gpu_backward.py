@@ -200,12 +200,13 @@ def test_backward_consistent_with_forward_by_directional_derivative():
     assert abs(diff - an) <= 0.03 * max(1.0, abs(an)), (diff, an)
 
 
-def test_backward_benchmarked_workload_sampled():
-    """The gradient call at the size it is timed at (fixed_T8192_H64: one
-    sequence of 8192 tokens, 64 heads), every output checked against the
-    oracle on a sample of heads: the heads are independent units, so the
-    oracle runs on each sampled head's slice of the inputs alone."""
-    d = KI.make_inputs(KI.WORKLOADS["fixed_T8192_H64"])
+@pytest.mark.parametrize("workload", ["fixed_T8192_H64", "fixed_T8192_H96"])
+def test_backward_benchmarked_workload_sampled(workload):
+    """The gradient call at the sizes it is timed at (one sequence of 8192
+    tokens, 64 or 96 heads), every output checked against the oracle on a
+    sample of heads: the heads are independent units, so the oracle runs on
+    each sampled head's slice of the inputs alone."""
+    d = KI.make_inputs(KI.WORKLOADS[workload])
     T, H = d["q"].shape[0], d["q"].shape[1]
     gen = torch.Generator().manual_seed(4242)
     d["dout"] = torch.randn(T, H, 128, generator=gen).to(torch.bfloat16)
